@@ -1,0 +1,362 @@
+"""Benchmark of one decode step on GB300: append_paged_kv (one new token per
+sequence) + batch_decode_paged_kv (gather, RoPE, GQA attention, on-device split
+merge), on the Llama-3-8B-shaped bf16 serving load by default.
+
+Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K timed steps; the L2
+is flushed (a 2x-L2 memset) before every timed step and each step is bracketed by
+CUDA events on the launching stream.  The decode kernel is timed by its own event
+pair for the roofline.  `e2e` re-times the step through the public API from pinned
+host buffers (H2D of the step's inputs and D2H of out + lse inside the timed region).
+
+--impl reference times the fp64 oracle (the CPU baseline) on a bounded sample.
+Under torchrun every rank runs its own replica of the workload (no collective on the
+data path; weak scaling); the reported time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from paged_kv_decode_19_gb300 import workloads as W  # noqa: E402
+
+METRIC = "paged decode attention µs/call and KV-read GB/s as % of GB300 HBM peak"
+UNIT = "us/call"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _oracle_sample(wl: W.Workload, budget_s: float):
+    """Run the oracle on whole sequences (all heads) until `budget_s` of CPU time is
+    spent; returns (seconds, sequences, attended rows)."""
+    import oracle
+    s = wl.spec
+    Q = W.bits(wl.Q)
+    pages = W.bits(wl.pages)
+    ip = wl.indptr.cpu().numpy()
+    vals = wl.values.cpu().numpy()
+    li = wl.length_info.cpu().numpy()
+    kro = wl.k_rope_pos_offset.cpu().numpy()
+    qrp = wl.q_rope_position.cpu().numpy()
+    t0 = time.perf_counter()
+    nseq = rows = 0
+    for b in range(s.B):
+        mask = np.zeros((s.B, s.H_qo), bool)
+        mask[b] = True
+        oracle.batch_decode_paged_kv(
+            Q, pages, ip, vals, li, kro, qrp, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
+            H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode,
+            rope_scale=s.rope_scale, rope_theta=s.rope_theta, sm_scale=wl.sm_scale,
+            sliding_window=s.window is not None, k_scale=wl.k_scale, v_scale=wl.v_scale,
+            mask=mask)
+        nseq += 1
+        rows += int(wl.attended[b])
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return time.perf_counter() - t0, nseq, rows
+
+
+def _cpu_baseline(wl: W.Workload, budget_s: float):
+    secs, nseq, rows = _oracle_sample(wl, budget_s)
+    total_rows = int(wl.attended.sum())
+    us_per_call = secs * 1e6 * total_rows / max(rows, 1)
+    return {"value": round(us_per_call, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"fp64 oracle (single thread) on {nseq} of {wl.spec.B} sequences, all "
+                      f"{wl.spec.H_qo} heads ({rows} of {total_rows} attended rows) in "
+                      f"{secs:.1f} s, scaled to the full batch by attended rows"}
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.result = None
+        if self.proc is None:
+            return
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if sm:
+            self.result = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                           "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _append_inputs(wl: W.Workload, device):
+    """New-token K/V (one per sequence, at row len-1) for the step's append."""
+    s = wl.spec
+    if wl.k_new is not None:
+        return wl.k_new, wl.v_new, wl.slot_mapping
+    g = torch.Generator(device=device)
+    g.manual_seed(12345)
+    dt = W.TORCH_DTYPES[s.q_dtype]
+    k = torch.randn((s.B, s.H_kv, s.D), generator=g, device=device).to(dt)
+    v = torch.randn((s.B, s.H_kv, s.D), generator=g, device=device).to(dt)
+    ip = wl.indptr.cpu().numpy()
+    vals = wl.values.cpu().numpy()
+    row = np.maximum(wl.seq_len - 1, 0)
+    slots = np.where(wl.seq_len > 0,
+                     vals[ip[:-1] + row // s.page_size].astype(np.int64) * s.page_size
+                     + row % s.page_size, -1)
+    return k, v, torch.from_numpy(slots.astype(np.int64)).to(device)
+
+
+def run_ours(args, ws, rank, local):
+    import paged_kv_decode_19_gb300 as pd
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = W.make(args.config, seed=1000 + rank, device=dev)
+    s = wl.spec
+    k_new, v_new, slots = _append_inputs(wl, dev)
+    out = torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=dev)
+    lse = torch.empty((s.B, s.H_qo), dtype=torch.float32, device=dev)
+    split = dict(num_splits=1) if args.config == "tiny_fp32" else {}
+    stream = torch.cuda.current_stream(dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+
+    def step():
+        pd.append_paged_kv(wl.pages, k_new, v_new, slots, wl.k_scale, wl.v_scale)
+        pd.batch_decode_paged_kv(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info,
+                                 wl.k_rope_pos_offset, wl.q_rope_position, out, lse,
+                                 s.rotary_mode, s.rope_scale, s.rope_theta, wl.sm_scale,
+                                 k_scale=wl.k_scale, v_scale=wl.v_scale, **split)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    variant = pd.last_decode_variant()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            pd.append_paged_kv(wl.pages, k_new, v_new, slots, wl.k_scale, wl.v_scale)
+            e1.record(stream)
+            pd.batch_decode_paged_kv(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info,
+                                     wl.k_rope_pos_offset, wl.q_rope_position, out, lse,
+                                     s.rotary_mode, s.rope_scale, s.rope_theta, wl.sm_scale,
+                                     k_scale=wl.k_scale, v_scale=wl.v_scale, **split)
+            e2.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    assert pd.check_device_errors() == "PD_OK"
+    launches = 2 * args.steps
+
+    # end-to-end through the public API from pinned host buffers
+    host_in = {k: getattr(wl, k).cpu().pin_memory() for k in
+               ("Q", "indptr", "values", "length_info", "k_rope_pos_offset", "q_rope_position")}
+    host_in["k_new"], host_in["v_new"], host_in["slots"] = (k_new.cpu().pin_memory(),
+                                                            v_new.cpu().pin_memory(),
+                                                            slots.cpu().pin_memory())
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for k, v in host_in.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        pd.append_paged_kv(wl.pages, dev_in["k_new"], dev_in["v_new"], dev_in["slots"],
+                           wl.k_scale, wl.v_scale)
+        pd.batch_decode_paged_kv(dev_in["Q"], wl.pages, dev_in["indptr"], dev_in["values"],
+                                 dev_in["length_info"], dev_in["k_rope_pos_offset"],
+                                 dev_in["q_rope_position"], out, lse, s.rotary_mode,
+                                 s.rope_scale, s.rope_theta, wl.sm_scale, k_scale=wl.k_scale,
+                                 v_scale=wl.v_scale, **split)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+
+    res = dict(step=statistics.mean(step_ms), dec=statistics.mean(dec_ms),
+               dec_med=statistics.median(dec_ms), app=statistics.mean(app_ms),
+               e2e=statistics.mean(e2e_ms), launches=launches, variant=variant,
+               clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h)
+    return res
+
+
+def _max_over_ranks(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="llama3_8b_bf16", choices=list(W.SPECS))
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    ws, rank, local = _dist()
+    spec = W.spec(args.config)
+    cfg = {"workload": f"{args.config}: B={spec.B}, H_qo={spec.H_qo}, H_kv={spec.H_kv}, "
+                       f"D={spec.D}, page_size={spec.page_size}, {spec.kv_dtype} KV",
+           "B": spec.B, "H_qo": spec.H_qo, "H_kv": spec.H_kv, "D": spec.D,
+           "page_size": spec.page_size, "kv_dtype": spec.kv_dtype, "q_dtype": spec.q_dtype,
+           "rotary_mode": spec.rotary_mode, "len_dist": list(spec.len_dist),
+           "step": "append_paged_kv (1 token/seq) + batch_decode_paged_kv",
+           "l2": "flushed before every timed step (2x L2 memset)",
+           "parallelism": f"replicas x{ws} (each rank its own batch; no collective)"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        wl = W.make(args.config, seed=1000)
+        for _ in range(args.warmup):
+            _oracle_sample(wl, 0.0)
+        times = []
+        for _ in range(args.steps):
+            secs, nseq, rows = _oracle_sample(wl, 0.0)  # one sequence per step
+            times.append(secs * 1e6 * int(wl.attended.sum()) / max(rows, 1))
+        v = statistics.mean(times)
+        line = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
+                "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "config": cfg, "impl": "reference",
+                "cpu_baseline": {"value": round(v, 1), "unit": UNIT, "cores": 1,
+                                 "kind": "oracle",
+                                 "sample": "fp64 oracle, single thread: each step decodes one "
+                                           "sequence (all heads) and is scaled to the batch by "
+                                           "attended rows"},
+                "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if ws > 1:
+        torch.distributed.init_process_group("nccl")
+    res = run_ours(args, ws, rank, local)
+    step_us = _max_over_ranks(res["step"] * 1e3, ws)
+    dec_us = _max_over_ranks(res["dec"] * 1e3, ws)
+    e2e_us = _max_over_ranks(res["e2e"] * 1e3, ws)
+    if rank != 0:
+        torch.distributed.destroy_process_group() if ws > 1 else None
+        return
+    wl = res["wl"]
+    kv_bytes = wl.kv_bytes_attended()
+    alg_bytes = kv_bytes + wl.io_bytes()
+    peak, peak_kind = _peaks()
+    achieved = alg_bytes / (dec_us * 1e-6) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(step_us / ws, 2),
+        "unit": UNIT,
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_us / 1e3, 5),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": spec.kv_dtype,
+        "data": "synthetic",
+        "config": cfg,
+        "decode_us": round(dec_us, 2),
+        "append_us": round(res["app"] * 1e3, 2),
+        "kv_read_gbs": round(kv_bytes / (dec_us * 1e-6) / 1e9, 1),
+        "decode_variant": res["variant"],
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": f"decode_{res['variant']}_kernel",
+                     "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
+        "e2e": {"value": round(e2e_us / ws, 2), "unit": UNIT,
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+        "gpu_launches": res["launches"],
+        "clocks": res["clocks"],
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(wl, args.cpu_budget)
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * libpageddecode — single-token (decode) attention over a paged KV cache, for
+ * NVIDIA GB300 (sm_103a).  Plain C ABI: device pointers, sizes and a CUDA stream.
+ *
+ * The operations follow three published descriptions of the problem:
+ *   [TVM]  Apache TVM, python/tvm/relax/frontend/nn/llm/_decode_kernels.py —
+ *          `batch_decode_paged_kv` (argument list, page layout, length_info,
+ *          RoPE arguments, base-2 log-sum-exp) and `merge_state_inplace`.
+ *   [VLLM] vllm-cpu 0.8.5, vllm/attention/ops/nki_flash_attn.py — `reshape_and_cache`
+ *          (writing new tokens' K/V into their cache slots).
+ *   [NKI]  NKI Attention Block TKG Kernel API Reference — FP8 KV cache with
+ *          per-tensor `k_scale` / `v_scale`, OCP e4m3fn (max 448), and the
+ *          sentinel slot that skips a cache write.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller unless noted;
+ *     the library never frees or retains it beyond the call.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream) and
+ *     return a status; no exception or abort crosses the ABI.
+ *   - Host-side argument errors return PD_ERR_INVALID_ARG / PD_ERR_UNSUPPORTED
+ *     before anything is launched.  Problems only visible on the device (a page id
+ *     outside [0, max_pages), inconsistent lengths, a slot beyond the cache) never
+ *     trap: the offending rows/tokens are skipped and a device error word records
+ *     them; `pd_check_device_errors` reports and clears it.
+ *   - `lse` is always float32 in log2 units: lse = log2(sum_r 2^(s_r)), where
+ *     s_r = sm_scale * log2(e) * q.k_r.
+ */
+#ifndef PAGEDDECODE_H_
+#define PAGEDDECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (binary-compatible with cudaStream_t / CUstream). */
+typedef struct CUstream_st* pd_stream_t;
+
+typedef enum {
+  PD_OK = 0,
+  PD_ERR_INVALID_ARG = 1,   /* bad pointer / shape / dtype combination (host check) */
+  PD_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. odd head dim) */
+  PD_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+  PD_ERR_BAD_PAGE = 4,      /* device: a page id or sequence offset was out of range */
+  PD_ERR_BAD_LENGTH = 5,    /* device: length_info inconsistent, or more KV chunks than planned */
+  PD_ERR_BAD_SLOT = 6,      /* device: an append slot lay beyond max_pages*page_size */
+  PD_ERR_TIMEOUT = 7,       /* device: an internal pipeline wait gave up (never expected) */
+  PD_ERR_WORKSPACE = 8      /* caller workspace too small or misaligned */
+} pd_status;
+
+/* Element types.  PD_E4M3 = OCP float8 e4m3fn (bias 7, max 448, no inf); KV only. */
+typedef enum { PD_F32 = 0, PD_F16 = 1, PD_BF16 = 2, PD_E4M3 = 3 } pd_dtype;
+
+/*
+ * What [TVM] fixes when it builds a decode kernel (head counts, head dim, page
+ * size, dtype, sliding-window variant), plus the FP8 scales of [NKI] and the
+ * split controls of this library.
+ */
+typedef struct {
+  int32_t B;                 /* number of sequences (one query token each) */
+  int32_t H_qo;              /* query heads; must be a multiple of H_kv */
+  int32_t H_kv;              /* KV heads; Q head h reads KV head h / (H_qo/H_kv) */
+  int32_t D;                 /* head dim: 64, 128 or 256 */
+  int32_t page_size;         /* rows per page, P */
+  int32_t q_dtype;           /* pd_dtype of Q: F32, F16 or BF16 */
+  int32_t kv_dtype;          /* pd_dtype of pages: F32, F16, BF16 or E4M3 */
+  int32_t out_dtype;         /* pd_dtype of output: F32, F16 or BF16 */
+  int32_t sliding_window;    /* 0: length_info is [B] = last_page_len.
+                                1: length_info is [3,B] = (last_page_len,
+                                   window start offset, attention-sink length). */
+  int32_t num_splits;        /* KV chunks per sequence: 0 = automatic, 1 = never split,
+                                n > 1 = at most n chunks (needs max_kv_len_hint) */
+  int64_t max_pages;         /* pages buffer holds [max_pages,2,H_kv,P,D] */
+  int64_t nnz_pages;         /* entries in page_table_values (= indptr[B]) */
+  int32_t max_kv_len_hint;   /* optional upper bound on attended rows per sequence (0 = none);
+                                tightens split planning, must not be exceeded */
+  float k_scale;             /* E4M3 KV only: K = code * k_scale (else ignored) */
+  float v_scale;             /* E4M3 KV only: V = code * v_scale (else ignored) */
+  void* workspace;           /* optional caller workspace (device); NULL = library-managed */
+  size_t workspace_bytes;    /* size of `workspace` */
+} pd_decode_desc;
+
+/*
+ * batch_decode_paged_kv — [TVM] `batch_decode_paged_kv`.
+ * For each sequence b and query head h (KV head hk = h / (H_qo/H_kv)):
+ *   rows  r = 0 .. L_b-1, L_b from page_table_indptr and length_info:
+ *         no window: L = (npages-1)*P + last_page_len, row r at sequence offset r;
+ *         window:    L = (npages-1)*P + last_page_len - win_off + sink, row r at
+ *                    offset r (r < sink) or r - sink + win_off.
+ *   page  page_table_values[indptr[b] + off / P], slot off % P;
+ *         K row = pages[page, 0, hk, slot, :], V row = pages[page, 1, hk, slot, :].
+ *   RoPE  (rotary_mode == 1) rotate-half over the full head dim with angle
+ *         pos * rope_scale / rope_theta^(2i/D); Q at q_rope_position[b],
+ *         K row r at k_rope_pos_offset[b] + r.
+ *   s_r = sm_scale * log2(e) * q.k_r;  out = sum_r 2^(s_r) v_r / sum_r 2^(s_r);
+ *   lse = log2(sum_r 2^(s_r)).  An empty sequence gives out = 0, lse = -5e4.
+ * Arguments (all device pointers):
+ *   Q           [B, H_qo, D] desc->q_dtype, contiguous.
+ *   pages       [max_pages, 2, H_kv, P, D] desc->kv_dtype, contiguous, 16-byte aligned.
+ *   page_table_indptr [B+1] int32, non-decreasing, indptr[0] = 0.
+ *   page_table_values [nnz_pages] int32 physical page ids.
+ *   length_info [B] or [3,B] int32 (see desc->sliding_window).
+ *   k_rope_pos_offset, q_rope_position [B] int32; may be NULL when rotary_mode == 0.
+ *   output      [B, H_qo, D] desc->out_dtype.   lse [B, H_qo] float32 (log2 units).
+ * Scalars: rotary_mode (0 none, 1 RoPE), rope_scale, rope_theta, sm_scale.
+ * Long sequences are split across thread blocks and the partial (out, lse) pairs
+ * are merged on the device; the split plan uses only host-known sizes.
+ * Workspace: desc->workspace if non-NULL (at least pd_workspace_size(desc) bytes,
+ * 256-byte aligned, zero-filled before its first use — see pd_workspace_init),
+ * otherwise a per-device buffer the library allocates on first use and grows as
+ * needed (allocation happens on the calling thread; do the first call of a given
+ * size outside CUDA-graph capture).
+ * Returns PD_OK once the work is enqueued.
+ */
+pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
+                                   const int32_t* page_table_indptr,
+                                   const int32_t* page_table_values, const int32_t* length_info,
+                                   const int32_t* k_rope_pos_offset,
+                                   const int32_t* q_rope_position, void* output, float* lse,
+                                   int32_t rotary_mode, float rope_scale, float rope_theta,
+                                   float sm_scale, const pd_decode_desc* desc,
+                                   pd_stream_t stream);
+
+/*
+ * merge_state_inplace — [TVM] `merge_state_inplace`.
+ * For every (n, h):  m = max(S, S_o);  w = 2^(S - m);  w_o = 2^(S_o - m);
+ *   V[n,h,:] <- V * w/(w+w_o) + V_other * w_o/(w+w_o);  S[n,h] <- log2(w + w_o) + m.
+ * V, V_other [N, H, D] of v_dtype (F32, F16 or BF16), contiguous; S, S_other
+ * [N, H] float32 (log2 units).  V and S are updated in place; arithmetic in fp32.
+ * A partner with S_other = -5e4 and V_other = 0 leaves (V, S) unchanged.
+ */
+pd_status pd_merge_state_inplace(void* V, float* S, const void* V_other, const float* S_other,
+                                 int32_t N, int32_t H, int32_t D, int32_t v_dtype,
+                                 pd_stream_t stream);
+
+/*
+ * append_paged_kv — [VLLM] `reshape_and_cache`, on the [TVM] page layout.
+ * For token t with slot_mapping[t] = s >= 0:  page = s / P, off = s % P;
+ *   pages[page, 0, h, off, :] = conv(k_new[t, h, :]);  pages[page, 1, h, off, :] = conv(v_new[t, h, :]).
+ * conv: same dtype -> bit copy; E4M3 cache -> e4m3(x / scale) with an IEEE fp32
+ * division (scale = k_scale for K, v_scale for V), round-to-nearest-even,
+ * saturating to +-448; other conversions round to nearest even.
+ * A negative slot skips the token ([NKI] sentinel).  A slot >= max_pages*P is
+ * skipped and recorded as PD_ERR_BAD_SLOT in the device error word.
+ * k_new, v_new [T, H_kv, D] of in_dtype (F32, F16, BF16); slot_mapping [T] int64;
+ * pages [max_pages, 2, H_kv, P, D] of kv_dtype.  Two tokens with the same slot
+ * race (last writer unspecified), as in the source.
+ */
+pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
+                             const int64_t* slot_mapping, int32_t T, int32_t H_kv, int32_t D,
+                             int32_t page_size, int64_t max_pages, int32_t in_dtype,
+                             int32_t kv_dtype, float k_scale, float v_scale, pd_stream_t stream);
+
+/* Bytes of workspace pd_batch_decode_paged_kv needs for `desc` on the current device
+ * (0 on invalid desc).  Host-only apart from reading the device's SM count. */
+size_t pd_workspace_size(const pd_decode_desc* desc);
+
+/* Zero-fill a caller-provided workspace before its first use (enqueued on stream). */
+pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream);
+
+/*
+ * Host-only split planner (no CUDA calls): for `desc` on a GPU with `num_sms`
+ * multiprocessors and `ctas_per_sm` resident decode blocks, returns the KV chunk
+ * length in rows (*chunk_rows; INT32_MAX = no split), the number of work items the
+ * grid provides (*grid_items) and the workspace bytes.  Used by the library and
+ * exposed for tests.
+ */
+pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_sm,
+                  int32_t* chunk_rows, int32_t* grid_items, size_t* workspace_bytes);
+
+/* Synchronises `stream`, then reads and clears the current device's error word.
+ * Returns PD_OK, PD_ERR_BAD_PAGE, PD_ERR_BAD_LENGTH, PD_ERR_BAD_SLOT or
+ * PD_ERR_TIMEOUT (the first that is set, in that order), or PD_ERR_CUDA. */
+pd_status pd_check_device_errors(pd_stream_t stream);
+
+/* Name of the decode kernel variant the last pd_batch_decode_paged_kv call on this
+ * thread launched ("mma" or "simt"), for tests and benchmarks. */
+const char* pd_last_decode_variant(void);
+
+/* Human-readable message for the last non-OK status returned on this thread. */
+const char* pd_get_last_error_string(void);
+
+/* Library ABI version (major * 10000 + minor * 100 + patch). */
+int32_t pd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDDECODE_H_ */

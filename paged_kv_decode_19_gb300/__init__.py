@@ -1,0 +1,19 @@
+"""GB300-native paged-KV decode attention (libpageddecode).
+
+Python front of the C-ABI library ``include/pageddecode.h``: ``batch_decode_paged_kv``,
+``merge_state_inplace`` and ``append_paged_kv`` run hand-written sm_103a CUDA kernels.
+PyTorch supplies device memory and streams only.
+"""
+from ._lib import (  # noqa: F401
+    PDError,
+    append_paged_kv,
+    batch_decode_paged_kv,
+    check_device_errors,
+    last_decode_variant,
+    make_desc,
+    merge_state_inplace,
+    plan,
+    version,
+    workspace_init,
+    workspace_size,
+)

@@ -1,0 +1,225 @@
+"""ctypes binding of libpageddecode (include/pageddecode.h).
+
+Argument marshalling only: tensors are turned into device pointers, shapes and
+dtype codes, and every call goes to the C ABI.  The library must be built
+(``__graft_entry__.build()`` or ``python -m paged_kv_decode_19_gb300.build``);
+if it is missing, loading raises — there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_LIB_PATH = _build.LIB
+_lock = threading.Lock()
+_lib = None
+
+STATUS = {
+    0: "PD_OK",
+    1: "PD_ERR_INVALID_ARG",
+    2: "PD_ERR_UNSUPPORTED",
+    3: "PD_ERR_CUDA",
+    4: "PD_ERR_BAD_PAGE",
+    5: "PD_ERR_BAD_LENGTH",
+    6: "PD_ERR_BAD_SLOT",
+    7: "PD_ERR_TIMEOUT",
+    8: "PD_ERR_WORKSPACE",
+}
+DTYPE_CODES = {
+    torch.float32: 0,
+    torch.float16: 1,
+    torch.bfloat16: 2,
+    torch.float8_e4m3fn: 3,
+}
+DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
+
+# Every entry point declared in include/pageddecode.h.
+EXPORTS = (
+    "pd_batch_decode_paged_kv",
+    "pd_merge_state_inplace",
+    "pd_append_paged_kv",
+    "pd_workspace_size",
+    "pd_workspace_init",
+    "pd_plan",
+    "pd_check_device_errors",
+    "pd_last_decode_variant",
+    "pd_get_last_error_string",
+    "pd_version",
+)
+
+
+class PDError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        self.status_name = STATUS.get(status, str(status))
+        super().__init__(f"{self.status_name}: {message}")
+
+
+class DecodeDesc(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int32),
+        ("H_qo", ctypes.c_int32),
+        ("H_kv", ctypes.c_int32),
+        ("D", ctypes.c_int32),
+        ("page_size", ctypes.c_int32),
+        ("q_dtype", ctypes.c_int32),
+        ("kv_dtype", ctypes.c_int32),
+        ("out_dtype", ctypes.c_int32),
+        ("sliding_window", ctypes.c_int32),
+        ("num_splits", ctypes.c_int32),
+        ("max_pages", ctypes.c_int64),
+        ("nnz_pages", ctypes.c_int64),
+        ("max_kv_len_hint", ctypes.c_int32),
+        ("k_scale", ctypes.c_float),
+        ("v_scale", ctypes.c_float),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+def lib():
+    """Load libpageddecode.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"libpageddecode is not built ({_LIB_PATH} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(_LIB_PATH)
+            P, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+            L.pd_batch_decode_paged_kv.argtypes = [P, P, P, P, P, P, P, P, P, i32, f32, f32, f32,
+                                                   ctypes.POINTER(DecodeDesc), P]
+            L.pd_batch_decode_paged_kv.restype = i32
+            L.pd_merge_state_inplace.argtypes = [P, P, P, P, i32, i32, i32, i32, P]
+            L.pd_merge_state_inplace.restype = i32
+            L.pd_append_paged_kv.argtypes = [P, P, P, P, i32, i32, i32, i32, i64, i32, i32, f32,
+                                             f32, P]
+            L.pd_append_paged_kv.restype = i32
+            L.pd_workspace_size.argtypes = [ctypes.POINTER(DecodeDesc)]
+            L.pd_workspace_size.restype = ctypes.c_size_t
+            L.pd_workspace_init.argtypes = [P, ctypes.c_size_t, P]
+            L.pd_workspace_init.restype = i32
+            L.pd_plan.argtypes = [ctypes.POINTER(DecodeDesc), i32, i32, ctypes.POINTER(i32),
+                                  ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_size_t)]
+            L.pd_plan.restype = i32
+            L.pd_check_device_errors.argtypes = [P]
+            L.pd_check_device_errors.restype = i32
+            L.pd_last_decode_variant.restype = ctypes.c_char_p
+            L.pd_get_last_error_string.restype = ctypes.c_char_p
+            L.pd_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise PDError(status, lib().pd_get_last_error_string().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_kv_len_hint=0,
+              k_scale=1.0, v_scale=1.0, workspace=None) -> DecodeDesc:
+    B, H_qo, D = Q.shape
+    max_pages, two, H_kv, P, D2 = pages.shape
+    if two != 2 or D2 != D:
+        raise ValueError(f"pages must be [max_pages, 2, H_kv, P, {D}], got {tuple(pages.shape)}")
+    return DecodeDesc(
+        B=B, H_qo=H_qo, H_kv=H_kv, D=D, page_size=P, q_dtype=DTYPE_CODES[Q.dtype],
+        kv_dtype=DTYPE_CODES[pages.dtype], out_dtype=DTYPE_CODES[out.dtype],
+        sliding_window=int(length_info.dim() == 2), num_splits=int(num_splits),
+        max_pages=max_pages, nnz_pages=int(values.numel()) if values is not None else 0,
+        max_kv_len_hint=int(max_kv_len_hint), k_scale=float(k_scale), v_scale=float(v_scale),
+        workspace=None if workspace is None else workspace.data_ptr(),
+        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+
+
+def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length_info,
+                          k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
+                          rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
+                          v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
+                          stream=None):
+    """pd_batch_decode_paged_kv on device tensors; writes `output` and `lse`."""
+    if sm_scale is None:
+        sm_scale = Q.shape[-1] ** -0.5
+    desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
+                     num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
+                     v_scale=v_scale, workspace=workspace)
+    _check(lib().pd_batch_decode_paged_kv(
+        _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
+        _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
+        _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta), float(sm_scale),
+        ctypes.byref(desc), _stream(stream)))
+    return output, lse
+
+
+def merge_state_inplace(V, S, V_other, S_other, stream=None):
+    """pd_merge_state_inplace: V [N,H,D], S [N,H] float32 updated in place."""
+    N, H, D = V.shape
+    if V_other.shape != V.shape or V_other.dtype != V.dtype or S.shape != (N, H) or S_other.shape != (N, H):
+        raise ValueError("merge_state_inplace: shape/dtype mismatch")
+    _check(lib().pd_merge_state_inplace(_ptr(V), _ptr(S), _ptr(V_other), _ptr(S_other), N, H, D,
+                                        DTYPE_CODES[V.dtype], _stream(stream)))
+    return V, S
+
+
+def append_paged_kv(pages, k_new, v_new, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):
+    """pd_append_paged_kv: writes new tokens' K/V into their slots (in place)."""
+    T, H_kv, D = k_new.shape
+    max_pages, _, H2, P, D2 = pages.shape
+    if v_new.shape != k_new.shape or H2 != H_kv or D2 != D or slot_mapping.dtype != torch.int64:
+        raise ValueError("append_paged_kv: shape/dtype mismatch")
+    _check(lib().pd_append_paged_kv(_ptr(pages), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                    T, H_kv, D, P, max_pages, DTYPE_CODES[k_new.dtype],
+                                    DTYPE_CODES[pages.dtype], float(k_scale), float(v_scale),
+                                    _stream(stream)))
+    return pages
+
+
+def check_device_errors(stream=None) -> str:
+    """Synchronises and returns the device error status name ("PD_OK" if clean)."""
+    st = lib().pd_check_device_errors(_stream(stream))
+    return STATUS.get(st, str(st))
+
+
+def workspace_size(desc: DecodeDesc) -> int:
+    return int(lib().pd_workspace_size(ctypes.byref(desc)))
+
+
+def workspace_init(ws: torch.Tensor, stream=None):
+    _check(lib().pd_workspace_init(_ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def plan(desc: DecodeDesc, num_sms: int, ctas_per_sm: int):
+    """Host-only split plan: (chunk_rows, grid_items, workspace_bytes)."""
+    c, g, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
+    _check(lib().pd_plan(ctypes.byref(desc), num_sms, ctas_per_sm, ctypes.byref(c),
+                         ctypes.byref(g), ctypes.byref(w)))
+    return c.value, g.value, w.value
+
+
+def last_decode_variant() -> str:
+    return lib().pd_last_decode_variant().decode()
+
+
+def version() -> int:
+    return int(lib().pd_version())

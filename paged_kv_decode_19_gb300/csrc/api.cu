@@ -1,0 +1,456 @@
+// Host side of libpageddecode: argument validation, the split planner, workspace
+// and error-word management, TMA descriptor set-up and kernel dispatch.  Every
+// entry point of include/pageddecode.h is defined here.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "kernels.h"
+#include "pageddecode.h"
+
+namespace pd {
+
+// Split planner constants: aim for ~kWaves resident waves of equal-sized work items,
+// never cutting a sequence into chunks shorter than kMinChunkRows attended rows.
+constexpr int kWaves = 4;
+constexpr int kMinChunkRows = 128;
+constexpr size_t kWsAlign = 256;
+
+static thread_local std::string t_last_error;
+static thread_local const char* t_last_variant = "none";
+
+static pd_status fail(pd_status st, const std::string& msg) {
+  t_last_error = msg;
+  return st;
+}
+static pd_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Device error word: one per device that loads the library.
+static __device__ unsigned g_error_word;
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  unsigned* err = nullptr;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+constexpr int kMaxDevices = 64;
+static DeviceState g_dev[kMaxDevices];
+static std::mutex g_mu;
+
+static pd_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PD_ERR_CUDA, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& s = g_dev[dev];
+  if (!s.ready) {
+    e = cudaDeviceGetAttribute(&s.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    e = cudaGetSymbolAddress((void**)&s.err, g_error_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    s.ready = true;
+  }
+  *out = &s;
+  return PD_OK;
+}
+
+static int elem_bytes(int dt) {
+  switch (dt) {
+    case kF32: return 4;
+    case kF16: return 2;
+    case kBF16: return 2;
+    case kE4M3: return 1;
+  }
+  return 0;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------- validation
+static pd_status validate_desc(const pd_decode_desc* d) {
+  if (!d) return fail(PD_ERR_INVALID_ARG, "desc is NULL");
+  if (d->B < 0) return fail(PD_ERR_INVALID_ARG, "B < 0");
+  if (d->H_kv <= 0 || d->H_qo <= 0 || d->H_qo % d->H_kv != 0)
+    return fail(PD_ERR_INVALID_ARG, "H_qo must be a positive multiple of H_kv");
+  if (d->D != 64 && d->D != 128 && d->D != 256)
+    return fail(PD_ERR_UNSUPPORTED, "head dim must be 64, 128 or 256");
+  if (d->page_size <= 0 || d->page_size > 256) return fail(PD_ERR_INVALID_ARG, "page_size must be in [1, 256]");
+  if (d->q_dtype != kF32 && d->q_dtype != kF16 && d->q_dtype != kBF16)
+    return fail(PD_ERR_INVALID_ARG, "q_dtype must be F32, F16 or BF16");
+  if (d->kv_dtype < kF32 || d->kv_dtype > kE4M3) return fail(PD_ERR_INVALID_ARG, "bad kv_dtype");
+  if (d->out_dtype != kF32 && d->out_dtype != kF16 && d->out_dtype != kBF16)
+    return fail(PD_ERR_INVALID_ARG, "out_dtype must be F32, F16 or BF16");
+  if (d->max_pages <= 0 && d->B > 0) return fail(PD_ERR_INVALID_ARG, "max_pages must be positive");
+  if (d->nnz_pages < 0) return fail(PD_ERR_INVALID_ARG, "nnz_pages < 0");
+  if ((long long)d->max_pages * 2 * d->H_kv > INT_MAX)
+    return fail(PD_ERR_UNSUPPORTED, "max_pages * 2 * H_kv exceeds 2^31");
+  if (d->num_splits < 0) return fail(PD_ERR_INVALID_ARG, "num_splits < 0");
+  if (d->num_splits > 1 && d->max_kv_len_hint <= 0)
+    return fail(PD_ERR_INVALID_ARG, "num_splits > 1 needs max_kv_len_hint");
+  if (d->kv_dtype == kE4M3 && !(d->k_scale > 0.f && d->v_scale > 0.f && std::isfinite(d->k_scale) &&
+                                std::isfinite(d->v_scale)))
+    return fail(PD_ERR_INVALID_ARG, "E4M3 KV needs finite positive k_scale and v_scale");
+  if (d->kv_dtype != d->q_dtype && d->kv_dtype != kE4M3)
+    return fail(PD_ERR_UNSUPPORTED, "q_dtype must equal kv_dtype unless the cache is E4M3");
+  return PD_OK;
+}
+
+// ---------------------------------------------------------------------------- planner
+static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int* chunk_rows,
+                      int* grid_items, size_t* ws_bytes) {
+  const int P = d->page_size;
+  const int group = d->H_qo / d->H_kv;
+  const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
+  long long est_rows = (long long)d->nnz_pages * P;
+  if (d->max_kv_len_hint > 0) est_rows = std::min(est_rows, (long long)d->B * d->max_kv_len_hint);
+  long long chunk;
+  if (d->num_splits == 1 || d->B == 0) {
+    chunk = INT_MAX;
+  } else {
+    const long long slots = (long long)std::max(num_sms, 1) * std::max(ctas_per_sm, 1) * kWaves;
+    const long long units = est_rows * d->H_kv * n_z;
+    chunk = std::max<long long>((units + slots - 1) / slots, kMinChunkRows);
+    if (d->num_splits > 1) chunk = std::max<long long>(chunk, (d->max_kv_len_hint + d->num_splits - 1) / d->num_splits);
+    chunk = (chunk + P - 1) / P * P;
+    if (chunk >= INT_MAX) chunk = INT_MAX;
+  }
+  long long items;
+  if (chunk == INT_MAX) {
+    items = d->B;
+  } else {
+    items = ((long long)d->nnz_pages * P + chunk - 1) / chunk + d->B;
+    if (d->max_kv_len_hint > 0)
+      items = std::min(items, (long long)d->B * ((d->max_kv_len_hint + chunk - 1) / chunk));
+  }
+  items = std::max<long long>(items, 0);
+  size_t ws = 0;
+  if (chunk != INT_MAX) {
+    ws = align_up((size_t)d->B * d->H_kv * n_z * sizeof(int), kWsAlign) +
+         align_up((size_t)items * d->H_qo * sizeof(float), kWsAlign) +
+         align_up((size_t)items * d->H_qo * d->D * sizeof(float), kWsAlign);
+  }
+  *chunk_rows = (int)chunk;
+  *grid_items = (int)std::min<long long>(items, INT_MAX);
+  *ws_bytes = ws;
+}
+
+// ---------------------------------------------------------------------------- TMA map
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// pages viewed as a 3-D tensor [blocks = max_pages*2*H_kv][P][D]; box = 128 bytes of a
+// row x P rows x one block, 128B swizzle.
+static pd_status make_kv_map(const void* pages, const pd_decode_desc* d, CUtensorMap* map) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  const int eb = elem_bytes(d->kv_dtype);
+  const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  cuuint64_t dims[3] = {(cuuint64_t)d->D, (cuuint64_t)d->page_size,
+                        (cuuint64_t)d->max_pages * 2 * d->H_kv};
+  cuuint64_t strides[2] = {(cuuint64_t)d->D * eb, (cuuint64_t)d->D * eb * d->page_size};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)d->page_size, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(map, dt, 3, const_cast<void*>(pages), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+  return PD_OK;
+}
+
+// Tensor-core variant eligibility (pages == nullptr: ignore the pointer's alignment).
+static bool mma_path(const pd_decode_desc* d, const void* pages) {
+  if ((reinterpret_cast<uintptr_t>(pages) & 15) != 0) return false;
+  if (d->page_size % 16 != 0) return false;
+  if (d->kv_dtype == kBF16 || d->kv_dtype == kF16) return d->D == 64 || d->D == 128;
+  if (d->kv_dtype == kE4M3) return d->D == 128 && (d->q_dtype == kBF16 || d->q_dtype == kF16);
+  return false;
+}
+
+static cudaError_t mma_dispatch(const DecodeParams& p, const CUtensorMap& map, int q_dtype,
+                                int kv_dtype, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
+  if (kv_dtype == kBF16) return launch_mma_bf16(p, map, q_dtype, grid, st, cfg);
+  if (kv_dtype == kF16) return launch_mma_f16(p, map, q_dtype, grid, st, cfg);
+  return launch_mma_fp8(p, map, q_dtype, grid, st, cfg);
+}
+
+// Fixed-point RoPE frequencies: F_i = 2^64 * frac(rope_scale / rope_theta^(2i/D) / (2 pi)).
+static void rope_table(float rope_scale, float rope_theta, int D, unsigned long long* F) {
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < D / 2; ++i) {
+    const double x = (double)rope_scale * std::pow((double)rope_theta, -2.0 * i / D) / two_pi;
+    const double f = x - std::floor(x);
+    double s = std::ldexp(f, 64);
+    if (s >= 18446744073709551616.0) s = 0.0;
+    F[i] = (unsigned long long)s;
+  }
+}
+
+}  // namespace pd
+
+using namespace pd;
+
+extern "C" {
+
+int32_t pd_version(void) { return 10000; }
+
+const char* pd_get_last_error_string(void) { return t_last_error.c_str(); }
+
+const char* pd_last_decode_variant(void) { return t_last_variant; }
+
+pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_sm,
+                  int32_t* chunk_rows, int32_t* grid_items, size_t* workspace_bytes) {
+  pd_status st = validate_desc(desc);
+  if (st != PD_OK) return st;
+  if (!chunk_rows || !grid_items || !workspace_bytes) return fail(PD_ERR_INVALID_ARG, "NULL output");
+  plan_impl(desc, num_sms, ctas_per_sm, chunk_rows, grid_items, workspace_bytes);
+  return PD_OK;
+}
+
+static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary, int* ctas) {
+  DecodeParams p{};
+  p.D = d->D;
+  p.P = d->page_size;
+  p.rotary = rotary;
+  cudaError_t e;
+  int n = 0;
+  if (use_mma) {
+    MmaConfig cfg{};
+    CUtensorMap dummy{};
+    e = mma_dispatch(p, dummy, d->q_dtype, d->kv_dtype, dim3(1), nullptr, &cfg);
+    n = cfg.ctas_per_sm;
+  } else {
+    if (!simt_supports(d->q_dtype, d->kv_dtype, d->D)) return fail(PD_ERR_UNSUPPORTED, "dtype / head-dim combination");
+    e = launch_decode_simt(p, d->q_dtype, d->kv_dtype, dim3(1), nullptr, &n);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  *ctas = std::max(n, 1);
+  return PD_OK;
+}
+
+size_t pd_workspace_size(const pd_decode_desc* desc) {
+  if (validate_desc(desc) != PD_OK) return 0;
+  DeviceState* ds = nullptr;
+  if (device_state(&ds) != PD_OK) return 0;
+  // the largest plan over the variants a call with this desc may take
+  size_t best = 0;
+  for (int mma = 0; mma < 2; ++mma) {
+    if (mma && !mma_path(desc, nullptr)) continue;
+    for (int rot = 0; rot < 2; ++rot) {
+      int ctas = 1;
+      if (occupancy_for(desc, mma != 0, rot, &ctas) != PD_OK) continue;
+      int chunk, items;
+      size_t ws;
+      plan_impl(desc, ds->num_sms, ctas, &chunk, &items, &ws);
+      best = std::max(best, ws);
+    }
+  }
+  return best;
+}
+
+pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream) {
+  if (!workspace && bytes) return fail(PD_ERR_INVALID_ARG, "workspace is NULL");
+  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return PD_OK;
+}
+
+pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
+                                   const int32_t* page_table_indptr,
+                                   const int32_t* page_table_values, const int32_t* length_info,
+                                   const int32_t* k_rope_pos_offset,
+                                   const int32_t* q_rope_position, void* output, float* lse,
+                                   int32_t rotary_mode, float rope_scale, float rope_theta,
+                                   float sm_scale, const pd_decode_desc* desc,
+                                   pd_stream_t stream) {
+  pd_status st = validate_desc(desc);
+  if (st != PD_OK) return st;
+  const pd_decode_desc& d = *desc;
+  if (rotary_mode != 0 && rotary_mode != 1) return fail(PD_ERR_INVALID_ARG, "rotary_mode must be 0 or 1");
+  if (rotary_mode == 1 && (!k_rope_pos_offset || !q_rope_position))
+    return fail(PD_ERR_INVALID_ARG, "RoPE needs k_rope_pos_offset and q_rope_position");
+  if (rotary_mode == 1 && !(rope_theta > 0.f && std::isfinite(rope_theta) && std::isfinite(rope_scale)))
+    return fail(PD_ERR_INVALID_ARG, "rope_theta must be finite and positive");
+  if (!std::isfinite(sm_scale)) return fail(PD_ERR_INVALID_ARG, "sm_scale must be finite");
+  if (d.B == 0) return PD_OK;
+  if (!Q || !pages || !page_table_indptr || !length_info || !output || !lse)
+    return fail(PD_ERR_INVALID_ARG, "NULL device pointer");
+  if (d.nnz_pages > 0 && !page_table_values) return fail(PD_ERR_INVALID_ARG, "page_table_values is NULL");
+  if ((reinterpret_cast<uintptr_t>(pages) % elem_bytes(d.kv_dtype)) != 0 ||
+      (reinterpret_cast<uintptr_t>(Q) % 16) != 0)
+    return fail(PD_ERR_INVALID_ARG, "Q must be 16-byte aligned and pages element-aligned");
+
+  DeviceState* ds = nullptr;
+  st = device_state(&ds);
+  if (st != PD_OK) return st;
+  const bool use_mma = mma_path(desc, pages);
+  int ctas = 1;
+  st = occupancy_for(desc, use_mma, rotary_mode, &ctas);
+  if (st != PD_OK) return st;
+  int chunk = 0, items = 0;
+  size_t ws_need = 0;
+  plan_impl(desc, ds->num_sms, ctas, &chunk, &items, &ws_need);
+  if (items == 0) return PD_OK;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  void* ws = d.workspace;
+  if (ws_need) {
+    if (ws) {
+      if (d.workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(ws) % kWsAlign) != 0)
+        return fail(PD_ERR_WORKSPACE, "caller workspace smaller than pd_workspace_size() or not 256-byte aligned");
+    } else {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (ds->ws_bytes < ws_need) {
+        if (ds->ws) {
+          cudaError_t e = cudaFree(ds->ws);
+          ds->ws = nullptr;
+          ds->ws_bytes = 0;
+          if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
+        }
+        const size_t bytes = align_up(ws_need + ws_need / 4, 1 << 20);
+        cudaError_t e = cudaMalloc(&ds->ws, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+        e = cudaMemset(ds->ws, 0, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+        ds->ws_bytes = bytes;
+      }
+      ws = ds->ws;
+    }
+  }
+
+  const int group = d.H_qo / d.H_kv;
+  const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
+  DecodeParams p{};
+  p.Q = Q;
+  p.pages = pages;
+  p.indptr = page_table_indptr;
+  p.values = page_table_values;
+  p.length_info = length_info;
+  p.k_rope_pos_offset = k_rope_pos_offset;
+  p.q_rope_position = q_rope_position;
+  p.out = output;
+  p.lse = lse;
+  if (ws_need) {
+    char* w = (char*)ws;
+    p.counters = (int*)w;
+    w += align_up((size_t)d.B * d.H_kv * n_z * sizeof(int), kWsAlign);
+    p.part_lse = (float*)w;
+    w += align_up((size_t)items * d.H_qo * sizeof(float), kWsAlign);
+    p.part_o = (float*)w;
+  }
+  p.err = ds->err;
+  p.max_pages = d.max_pages;
+  p.B = d.B;
+  p.H_qo = d.H_qo;
+  p.H_kv = d.H_kv;
+  p.D = d.D;
+  p.P = d.page_size;
+  p.group = group;
+  p.n_z = n_z;
+  p.window = d.sliding_window ? 1 : 0;
+  p.rotary = rotary_mode;
+  p.chunk_rows = chunk;
+  p.out_dtype = d.out_dtype;
+  const double log2e = 1.4426950408889634073599246810019;
+  const double kdeq = d.kv_dtype == kE4M3 ? (double)d.k_scale : 1.0;
+  p.score_scale = (float)((double)sm_scale * log2e * kdeq);
+  p.q_prescale = p.score_scale;
+  p.out_scale = d.kv_dtype == kE4M3 ? d.v_scale : 1.f;
+  if (rotary_mode) rope_table(rope_scale, rope_theta, d.D, p.rope_F);
+
+  const dim3 grid((unsigned)items, (unsigned)d.H_kv, (unsigned)n_z);
+  cudaError_t e;
+  if (use_mma) {
+    CUtensorMap map;
+    st = make_kv_map(pages, desc, &map);
+    if (st != PD_OK) return st;
+    e = mma_dispatch(p, map, d.q_dtype, d.kv_dtype, grid, s, nullptr);
+    t_last_variant = "mma";
+  } else {
+    if (!simt_supports(d.q_dtype, d.kv_dtype, d.D)) return fail(PD_ERR_UNSUPPORTED, "dtype / head-dim combination");
+    e = launch_decode_simt(p, d.q_dtype, d.kv_dtype, grid, s);
+    t_last_variant = "simt";
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return PD_OK;
+}
+
+pd_status pd_merge_state_inplace(void* V, float* S, const void* V_other, const float* S_other,
+                                 int32_t N, int32_t H, int32_t D, int32_t v_dtype,
+                                 pd_stream_t stream) {
+  if (N < 0 || H < 0 || D <= 0) return fail(PD_ERR_INVALID_ARG, "bad N/H/D");
+  if (v_dtype != kF32 && v_dtype != kF16 && v_dtype != kBF16)
+    return fail(PD_ERR_INVALID_ARG, "v_dtype must be F32, F16 or BF16");
+  if ((long long)N * H == 0) return PD_OK;
+  if (!V || !S || !V_other || !S_other) return fail(PD_ERR_INVALID_ARG, "NULL device pointer");
+  cudaError_t e = launch_merge_state(V, S, V_other, S_other, N, H, D, v_dtype, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return PD_OK;
+}
+
+pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
+                             const int64_t* slot_mapping, int32_t T, int32_t H_kv, int32_t D,
+                             int32_t page_size, int64_t max_pages, int32_t in_dtype,
+                             int32_t kv_dtype, float k_scale, float v_scale, pd_stream_t stream) {
+  if (T < 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || max_pages <= 0)
+    return fail(PD_ERR_INVALID_ARG, "bad T/H_kv/D/page_size/max_pages");
+  if (in_dtype != kF32 && in_dtype != kF16 && in_dtype != kBF16)
+    return fail(PD_ERR_INVALID_ARG, "in_dtype must be F32, F16 or BF16");
+  if (kv_dtype < kF32 || kv_dtype > kE4M3) return fail(PD_ERR_INVALID_ARG, "bad kv_dtype");
+  if (kv_dtype == kE4M3 && !(k_scale > 0.f && v_scale > 0.f && std::isfinite(k_scale) && std::isfinite(v_scale)))
+    return fail(PD_ERR_INVALID_ARG, "E4M3 cache needs finite positive k_scale and v_scale");
+  if ((long long)T * H_kv > INT_MAX) return fail(PD_ERR_UNSUPPORTED, "T * H_kv too large");
+  if (T == 0) return PD_OK;
+  if (!pages || !k_new || !v_new || !slot_mapping) return fail(PD_ERR_INVALID_ARG, "NULL device pointer");
+  DeviceState* ds = nullptr;
+  pd_status st = device_state(&ds);
+  if (st != PD_OK) return st;
+  cudaError_t e = launch_append(pages, k_new, v_new, slot_mapping, T, H_kv, D, page_size, max_pages,
+                                in_dtype, kv_dtype, k_scale, v_scale, ds->err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  return PD_OK;
+}
+
+pd_status pd_check_device_errors(pd_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  DeviceState* ds = nullptr;
+  pd_status st = device_state(&ds);
+  if (st != PD_OK) return st;
+  unsigned word = 0;
+  e = cudaMemcpy(&word, ds->err, sizeof(word), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (word) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(ds->err, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  if (word & kErrBadPage) return fail(PD_ERR_BAD_PAGE, "a page id or sequence offset was out of range");
+  if (word & kErrBadLength) return fail(PD_ERR_BAD_LENGTH, "inconsistent length_info or split-plan overflow");
+  if (word & kErrBadSlot) return fail(PD_ERR_BAD_SLOT, "an append slot was beyond the cache");
+  if (word & kErrTimeout) return fail(PD_ERR_TIMEOUT, "a pipeline wait timed out");
+  return PD_OK;
+}
+
+}  // extern "C"

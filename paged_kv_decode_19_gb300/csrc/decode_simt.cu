@@ -1,0 +1,208 @@
+// SIMT decode kernel: any element type (fp32 / f16 / bf16 / e4m3 KV), head dim
+// 64/128/256, any page size, any GQA group.  Used for fp32 (where the 16-bit tensor
+// path would lose the 1e-5 accuracy the fp32 path keeps) and for shapes the MMA
+// kernel does not take.
+//
+// One block = one (work item, KV head, slice of <= 8 query heads).  Each warp walks
+// rows r0+w, r0+w+NW, ... of the item's chunk; a lane holds D/32 elements of a row:
+// D/64 from each half, so a RoPE pair (d, d + D/2) sits in one lane.  Per row: the
+// q.k dot product is a warp sum, then the base-2 online softmax update of the TVM
+// `batch_decode_paged_kv` kernel (m, d, O) and the PV accumulate; the warps' states
+// are merged at the end (same formula as `merge_state_inplace`).
+#include "decode_common.cuh"
+#include "kernels.h"
+
+namespace pd {
+
+template <typename T, int N>
+struct RowHalf {  // N consecutive elements of a row, loaded with one vector access
+  static constexpr int kBytes = N * ElemBytes<T>::v;
+  __device__ __forceinline__ static void load(const T* src, float (&dst)[N]) {
+    if constexpr (kBytes == 16) {
+      uint4 v = __ldg(reinterpret_cast<const uint4*>(src));
+      unpack(reinterpret_cast<const uint8_t*>(&v), dst);
+    } else if constexpr (kBytes == 8) {
+      uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+      unpack(reinterpret_cast<const uint8_t*>(&v), dst);
+    } else if constexpr (kBytes == 4) {
+      unsigned v = __ldg(reinterpret_cast<const unsigned*>(src));
+      unpack(reinterpret_cast<const uint8_t*>(&v), dst);
+    } else if constexpr (kBytes == 2) {
+      unsigned short v = __ldg(reinterpret_cast<const unsigned short*>(src));
+      unpack(reinterpret_cast<const uint8_t*>(&v), dst);
+    } else {
+      uint8_t v = *reinterpret_cast<const uint8_t*>(src);
+      unpack(&v, dst);
+    }
+  }
+  __device__ __forceinline__ static void unpack(const uint8_t* b, float (&dst)[N]) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) dst[i] = to_f32(reinterpret_cast<const T*>(b)[i]);
+  }
+};
+
+template <typename KT, typename QT, int D, int NW>
+__global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr int NT = NW * 32;
+  constexpr int H2 = D / 64;  // elements per lane per half
+  constexpr int E = 2 * H2;
+  __shared__ float sm_m[NW * 8], sm_d[NW * 8];
+  __shared__ float sm_o[NW * 8 * D];
+
+  const int item = blockIdx.x, hk = blockIdx.y, z = blockIdx.z;
+  Work w;
+  if (!locate_item<NT>(p, item, w)) return;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int hq0 = hk * p.group + z * kMaxGroupPerCta;
+  const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
+  const int r0 = w.chunk * p.chunk_rows;
+  const int r1 = (w.seq.L - r0 > p.chunk_rows) ? r0 + p.chunk_rows : w.seq.L;
+  const int d0 = lane * H2, d1 = D / 2 + lane * H2;  // this lane's dims: [d0,d0+H2) and [d1,d1+H2)
+
+  // rope frequencies of this lane
+  unsigned long long F[H2];
+#pragma unroll
+  for (int e = 0; e < H2; ++e) F[e] = p.rope_F[d0 + e];
+
+  // Q rows of this block's heads, roped, in log2 units
+  float q[kMaxGroupPerCta][E];
+  const int qpos = p.rotary ? p.q_rope_position[w.b] : 0;
+#pragma unroll
+  for (int j = 0; j < kMaxGroupPerCta; ++j) {
+    float a[H2], bb[H2];
+    if (j < hcount) {
+      const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)w.b * p.H_qo + hq0 + j) * D;
+      RowHalf<QT, H2>::load(qrow + d0, a);
+      RowHalf<QT, H2>::load(qrow + d1, bb);
+    } else {
+#pragma unroll
+      for (int e = 0; e < H2; ++e) a[e] = bb[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < H2; ++e) {
+      float x = a[e], y = bb[e];
+      if (p.rotary) {
+        float c, s;
+        rope_cos_sin(qpos, F[e], c, s);
+        const float xr = x * c - y * s, yr = y * c + x * s;
+        x = xr;
+        y = yr;
+      }
+      q[j][e] = x * p.score_scale;
+      q[j][H2 + e] = y * p.score_scale;
+    }
+  }
+
+  float m[kMaxGroupPerCta], dsum[kMaxGroupPerCta], o[kMaxGroupPerCta][E];
+#pragma unroll
+  for (int j = 0; j < kMaxGroupPerCta; ++j) {
+    m[j] = kEmptyM;
+    dsum[j] = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) o[j][e] = 0.f;
+  }
+
+  const int kpos0 = p.rotary ? p.k_rope_pos_offset[w.b] : 0;
+  const KT* pages = reinterpret_cast<const KT*>(p.pages);
+  const size_t kv_stride = (size_t)p.H_kv * p.P * D;  // K block -> V block of a page
+  for (int r = r0 + warp; r < r1; r += NW) {
+    const int so = r < w.seq.sink ? r : r - w.seq.sink + w.seq.win_off;
+    const int page = lookup_page(p, w.seq, so / p.P);
+    if (page < 0) continue;
+    const size_t kofs = (((size_t)page * 2 * p.H_kv + hk) * p.P + (so % p.P)) * D;
+    float k[E], v[E];
+    {
+      float ka[H2], kb[H2], va[H2], vb[H2];
+      RowHalf<KT, H2>::load(pages + kofs + d0, ka);
+      RowHalf<KT, H2>::load(pages + kofs + d1, kb);
+      RowHalf<KT, H2>::load(pages + kofs + kv_stride + d0, va);
+      RowHalf<KT, H2>::load(pages + kofs + kv_stride + d1, vb);
+#pragma unroll
+      for (int e = 0; e < H2; ++e) {
+        float x = ka[e], y = kb[e];
+        if (p.rotary) {
+          float c, s;
+          rope_cos_sin(kpos0 + r, F[e], c, s);
+          const float xr = x * c - y * s, yr = y * c + x * s;
+          x = xr;
+          y = yr;
+        }
+        k[e] = x;
+        k[H2 + e] = y;
+        v[e] = va[e];
+        v[H2 + e] = vb[e];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxGroupPerCta; ++j) {
+      if (j < hcount) {
+        float s = 0.f;
+#pragma unroll
+        for (int e = 0; e < E; ++e) s = fmaf(q[j][e], k[e], s);
+        s = warp_sum(s);
+        const float mn = fmaxf(m[j], s);
+        const float a = fast_exp2(m[j] - mn), pj = fast_exp2(s - mn);
+        dsum[j] = dsum[j] * a + pj;
+#pragma unroll
+        for (int e = 0; e < E; ++e) o[j][e] = fmaf(pj, v[e], o[j][e] * a);
+        m[j] = mn;
+      }
+    }
+  }
+
+  // warp states -> shared memory
+#pragma unroll
+  for (int j = 0; j < kMaxGroupPerCta; ++j) {
+    if (lane == 0) {
+      sm_m[warp * 8 + j] = m[j];
+      sm_d[warp * 8 + j] = dsum[j];
+    }
+#pragma unroll
+    for (int e = 0; e < H2; ++e) {
+      sm_o[(warp * 8 + j) * D + d0 + e] = o[j][e];
+      sm_o[(warp * 8 + j) * D + d1 + e] = o[j][H2 + e];
+    }
+  }
+  __syncthreads();
+  finish_block<NT, NW>(p, w, item, hk, z, hq0, hcount, sm_m, sm_d, sm_o);
+}
+
+// ------------------------------------------------------------------------- dispatch
+// Launch, or (ctas != nullptr) report how many blocks of the variant fit on one SM.
+template <typename KT, typename QT, int D>
+static cudaError_t launch_simt_d(const DecodeParams& p, dim3 grid, cudaStream_t st, int* ctas) {
+  constexpr int NW = 4;
+  auto kern = decode_simt_kernel<KT, QT, D, NW>;
+  if (ctas) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, NW * 32, 0);
+  kern<<<grid, NW * 32, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename KT, typename QT>
+static cudaError_t launch_simt_t(const DecodeParams& p, dim3 grid, cudaStream_t st, int* ctas) {
+  switch (p.D) {
+    case 64: return launch_simt_d<KT, QT, 64>(p, grid, st, ctas);
+    case 128: return launch_simt_d<KT, QT, 128>(p, grid, st, ctas);
+    case 256: return launch_simt_d<KT, QT, 256>(p, grid, st, ctas);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode_simt(const DecodeParams& p, int q_dtype, int kv_dtype, dim3 grid,
+                               cudaStream_t st, int* ctas) {
+  if (kv_dtype == kF32 && q_dtype == kF32) return launch_simt_t<float, float>(p, grid, st, ctas);
+  if (kv_dtype == kBF16 && q_dtype == kBF16) return launch_simt_t<__nv_bfloat16, __nv_bfloat16>(p, grid, st, ctas);
+  if (kv_dtype == kF16 && q_dtype == kF16) return launch_simt_t<__half, __half>(p, grid, st, ctas);
+  if (kv_dtype == kE4M3 && q_dtype == kBF16) return launch_simt_t<F8, __nv_bfloat16>(p, grid, st, ctas);
+  if (kv_dtype == kE4M3 && q_dtype == kF16) return launch_simt_t<F8, __half>(p, grid, st, ctas);
+  if (kv_dtype == kE4M3 && q_dtype == kF32) return launch_simt_t<F8, float>(p, grid, st, ctas);
+  return cudaErrorInvalidValue;
+}
+
+bool simt_supports(int q_dtype, int kv_dtype, int D) {
+  if (D != 64 && D != 128 && D != 256) return false;
+  if (kv_dtype == q_dtype && kv_dtype != kE4M3) return true;
+  return kv_dtype == kE4M3 && (q_dtype == kBF16 || q_dtype == kF16 || q_dtype == kF32);
+}
+
+}  // namespace pd

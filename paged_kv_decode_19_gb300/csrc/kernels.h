@@ -1,0 +1,39 @@
+// Internal launch interface between the host API (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "decode_common.cuh"
+
+namespace pd {
+
+// SIMT decode (any dtype / D in {64,128,256} / page size / group)
+bool simt_supports(int q_dtype, int kv_dtype, int D);
+// Launch, or (ctas != nullptr) only report resident blocks per SM.
+cudaError_t launch_decode_simt(const DecodeParams& p, int q_dtype, int kv_dtype, dim3 grid,
+                               cudaStream_t st, int* ctas = nullptr);
+
+// Tensor-core decode (TMA page staging + mma.sync); see decode_mma.cuh for limits.
+struct MmaConfig {
+  int threads;       // block size
+  int smem_bytes;    // dynamic shared memory
+  int ctas_per_sm;   // occupancy (0 until queried)
+};
+// Launch (cfg == nullptr) or just query the launch configuration (cfg != nullptr).
+cudaError_t launch_mma_bf16(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
+                            cudaStream_t st, MmaConfig* cfg);
+cudaError_t launch_mma_f16(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
+                           cudaStream_t st, MmaConfig* cfg);
+cudaError_t launch_mma_fp8(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
+                           cudaStream_t st, MmaConfig* cfg);
+
+// merge_state_inplace and append_paged_kv
+cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const float* S_other, int N,
+                               int H, int D, int v_dtype, cudaStream_t st);
+cudaError_t launch_append(void* pages, const void* k_new, const void* v_new,
+                          const int64_t* slot_mapping, int T, int H_kv, int D, int P,
+                          long long max_pages, int in_dtype, int kv_dtype, float k_scale,
+                          float v_scale, unsigned* err, cudaStream_t st);
+
+}  // namespace pd

@@ -1,0 +1,118 @@
+// merge_state_inplace and append_paged_kv kernels.
+//
+// merge: Apache TVM `_decode_kernels.py`, `merge_state_inplace` — one warp per
+//   (n, h) row: both log-sum-exps are read, the row of V is rescaled and summed in
+//   fp32, and S is written last (after the warp's reads).
+// append: vllm-cpu `nki_flash_attn.py`, `reshape_and_cache`, on the TVM page layout
+//   [max_pages, 2, H_kv, P, D]; FP8 encode per the NKI Attention Block TKG reference
+//   (per-tensor k_scale / v_scale, OCP e4m3fn): IEEE fp32 division, then the hardware
+//   round-to-nearest-even saturating conversion.  A negative slot skips the token.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pd {
+
+template <typename VT>
+__global__ void merge_state_kernel(VT* __restrict__ V, float* __restrict__ S,
+                                   const VT* __restrict__ Vo, const float* __restrict__ So,
+                                   int rows, int D) {
+  const int warps = blockDim.x >> 5;
+  const int row = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const float s = S[row], so = So[row];
+  const float smax = fmaxf(s, so);
+  const float w = exp2f(s - smax), wo = exp2f(so - smax);
+  const float a = w / (w + wo), ao = wo / (w + wo);
+  VT* v = V + (size_t)row * D;
+  const VT* vo = Vo + (size_t)row * D;
+  for (int d = lane; d < D; d += 32) v[d] = from_f32<VT>(to_f32(v[d]) * a + to_f32(vo[d]) * ao);
+  __syncwarp();
+  if (lane == 0) S[row] = log2f(w + wo) + smax;
+}
+
+cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const float* S_other, int N,
+                               int H, int D, int v_dtype, cudaStream_t st) {
+  const int rows = N * H;
+  if (rows == 0) return cudaSuccess;
+  const int threads = 256, per = threads / 32;
+  const dim3 grid((rows + per - 1) / per);
+  if (v_dtype == kF32)
+    merge_state_kernel<float><<<grid, threads, 0, st>>>((float*)V, S, (const float*)V_other, S_other, rows, D);
+  else if (v_dtype == kBF16)
+    merge_state_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
+        (__nv_bfloat16*)V, S, (const __nv_bfloat16*)V_other, S_other, rows, D);
+  else if (v_dtype == kF16)
+    merge_state_kernel<__half><<<grid, threads, 0, st>>>((__half*)V, S, (const __half*)V_other, S_other, rows, D);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+template <typename IT, typename OT>
+__device__ __forceinline__ OT convert_elem(IT x, float scale) {
+  if constexpr (std::is_same<IT, OT>::value) {
+    return x;
+  } else if constexpr (std::is_same<OT, F8>::value) {
+    F8 r;
+    r.v = f32_to_e4m3(to_f32(x) / scale);  // IEEE division (no fast-math), then RNE satfinite
+    return r;
+  } else {
+    return from_f32<OT>(to_f32(x));
+  }
+}
+
+// grid: (T * H_kv) blocks; block threads stride over D.  blockIdx.y: 0 = K, 1 = V.
+template <typename IT, typename OT>
+__global__ void append_kernel(OT* __restrict__ pages, const IT* __restrict__ k_new,
+                              const IT* __restrict__ v_new, const int64_t* __restrict__ slots,
+                              int T, int H_kv, int D, int P, long long max_pages, float k_scale,
+                              float v_scale, unsigned* err) {
+  const int th = blockIdx.x;
+  const int t = th / H_kv, h = th - t * H_kv;
+  const int kv = blockIdx.y;
+  const long long slot = slots[t];
+  if (slot < 0) return;
+  const long long page = slot / P, off = slot % P;
+  if (page >= max_pages) {
+    if (threadIdx.x == 0 && kv == 0 && h == 0) set_error(err, kErrBadSlot);
+    return;
+  }
+  const IT* src = (kv == 0 ? k_new : v_new) + ((size_t)t * H_kv + h) * D;
+  OT* dst = pages + ((((size_t)page * 2 + kv) * H_kv + h) * P + off) * D;
+  const float scale = kv == 0 ? k_scale : v_scale;
+  for (int d = threadIdx.x; d < D; d += blockDim.x) dst[d] = convert_elem<IT, OT>(src[d], scale);
+}
+
+template <typename IT>
+static cudaError_t append_in(void* pages, const void* k, const void* v, const int64_t* slots, int T,
+                             int H, int D, int P, long long max_pages, int kv_dtype, float ks,
+                             float vs, unsigned* err, cudaStream_t st) {
+  const dim3 grid((unsigned)T * H, 2);
+  const int threads = D < 128 ? D : 128;
+  const IT* kk = (const IT*)k;
+  const IT* vv = (const IT*)v;
+  switch (kv_dtype) {
+    case kF32: append_kernel<IT, float><<<grid, threads, 0, st>>>((float*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
+    case kF16: append_kernel<IT, __half><<<grid, threads, 0, st>>>((__half*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
+    case kBF16: append_kernel<IT, __nv_bfloat16><<<grid, threads, 0, st>>>((__nv_bfloat16*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
+    case kE4M3: append_kernel<IT, F8><<<grid, threads, 0, st>>>((F8*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append(void* pages, const void* k_new, const void* v_new,
+                          const int64_t* slot_mapping, int T, int H_kv, int D, int P,
+                          long long max_pages, int in_dtype, int kv_dtype, float k_scale,
+                          float v_scale, unsigned* err, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  switch (in_dtype) {
+    case kF32: return append_in<float>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, st);
+    case kF16: return append_in<__half>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, st);
+    case kBF16: return append_in<__nv_bfloat16>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace pd

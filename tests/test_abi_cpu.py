@@ -1,0 +1,114 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point that
+include/pageddecode.h declares, the struct layout matches, host-side validation
+rejects bad arguments before any CUDA call, and the split planner's arithmetic."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import __graft_entry__
+from paged_kv_decode_19_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pageddecode.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    __graft_entry__.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pd_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert L.pd_version() == 10000
+
+
+def test_desc_layout_matches_header():
+    # int32 x10, int64 x2, int32, float x2, void*, size_t
+    assert ctypes.sizeof(_lib.DecodeDesc) == 88
+    assert _lib.DecodeDesc.max_pages.offset == 40
+    assert _lib.DecodeDesc.workspace.offset == 72
+
+
+def _desc(**kw):
+    d = dict(B=4, H_qo=8, H_kv=2, D=128, page_size=16, q_dtype=2, kv_dtype=2, out_dtype=2,
+             sliding_window=0, num_splits=0, max_pages=100, nnz_pages=40, max_kv_len_hint=0,
+             k_scale=1.0, v_scale=1.0, workspace=None, workspace_bytes=0)
+    d.update(kw)
+    return _lib.DecodeDesc(**d)
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(H_qo=7), "PD_ERR_INVALID_ARG"), (dict(D=96), "PD_ERR_UNSUPPORTED"),
+    (dict(page_size=0), "PD_ERR_INVALID_ARG"), (dict(q_dtype=3), "PD_ERR_INVALID_ARG"),
+    (dict(out_dtype=3), "PD_ERR_INVALID_ARG"), (dict(kv_dtype=3, k_scale=0.0), "PD_ERR_INVALID_ARG"),
+    (dict(kv_dtype=1), "PD_ERR_UNSUPPORTED"), (dict(num_splits=4), "PD_ERR_INVALID_ARG"),
+    (dict(max_pages=0), "PD_ERR_INVALID_ARG"), (dict(B=-1), "PD_ERR_INVALID_ARG"),
+])
+def test_decode_validation_without_gpu(L, bad, status):
+    d = _desc(**bad)
+    st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 0,
+                                    1.0, 1e4, 0.1, ctypes.byref(d), None)
+    assert _lib.STATUS[st] == status, L.pd_get_last_error_string()
+
+
+def test_decode_null_pointers_rejected(L):
+    d = _desc()
+    st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 0,
+                                    1.0, 1e4, 0.1, ctypes.byref(d), None)
+    assert _lib.STATUS[st] == "PD_ERR_INVALID_ARG"
+    st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 1,
+                                    1.0, 1e4, 0.1, ctypes.byref(d), None)
+    assert _lib.STATUS[st] == "PD_ERR_INVALID_ARG"
+    assert b"RoPE" in L.pd_get_last_error_string()
+
+
+def test_merge_and_append_validation_without_gpu(L):
+    assert _lib.STATUS[L.pd_merge_state_inplace(None, None, None, None, 2, 2, 64, 3, None)] == "PD_ERR_INVALID_ARG"
+    assert _lib.STATUS[L.pd_merge_state_inplace(None, None, None, None, 2, 2, 64, 0, None)] == "PD_ERR_INVALID_ARG"
+    assert L.pd_merge_state_inplace(None, None, None, None, 0, 2, 64, 0, None) == 0
+    assert _lib.STATUS[L.pd_append_paged_kv(None, None, None, None, 3, 2, 64, 16, 10, 3, 2, 1.0, 1.0, None)] == "PD_ERR_INVALID_ARG"
+    assert _lib.STATUS[L.pd_append_paged_kv(None, None, None, None, 3, 2, 64, 16, 10, 2, 3, 0.0, 1.0, None)] == "PD_ERR_INVALID_ARG"
+    assert L.pd_append_paged_kv(None, None, None, None, 0, 2, 64, 16, 10, 2, 2, 1.0, 1.0, None) == 0
+
+
+def test_planner_arithmetic(L):
+    # llama3-8b-shaped decode: 32 sequences, 4608 pages of 16, 8 KV heads
+    d = _desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, max_pages=16384)
+    chunk, items, ws = _lib.plan(d, 148, 3)
+    assert chunk % 16 == 0 and chunk >= 128
+    # every sequence fits: items >= sum over sequences of ceil(L/chunk) for any lengths
+    assert items >= (4608 * 16 + chunk - 1) // chunk
+    assert ws >= items * 32 * (128 + 1) * 4
+    # more resident blocks -> smaller chunks
+    assert _lib.plan(d, 148, 4)[0] <= chunk
+    # num_splits = 1: no split, no workspace
+    c1, i1, w1 = _lib.plan(_desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, num_splits=1), 148, 3)
+    assert c1 == 2**31 - 1 and i1 == 32 and w1 == 0
+    # explicit split count with a length hint
+    c2, i2, _ = _lib.plan(_desc(B=8, nnz_pages=40000, num_splits=32, max_kv_len_hint=131072), 148, 3)
+    assert c2 >= 131072 // 32 and i2 <= 8 * 32 + 8
+    # a length hint caps the grid
+    c3, i3, _ = _lib.plan(_desc(B=64, H_kv=4, H_qo=32, nnz_pages=64 * 640, max_kv_len_hint=4100), 148, 3)
+    assert i3 <= 64 * ((4100 + c3 - 1) // c3)
+
+
+def test_python_binding_rejects_missing_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(_lib, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _lib.lib()

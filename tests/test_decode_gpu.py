@@ -1,0 +1,257 @@
+"""GPU parity of batch_decode_paged_kv against the fp64 oracle (called through the
+C ABI).  Reduced workloads are compared element by element; edge cases and the
+error path follow."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_19_gb300 import workloads as W
+from tests._util import compare, gpu_decode, kind_of, oracle_decode
+
+pd = pytest.importorskip("paged_kv_decode_19_gb300")
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _wl(name, seed, **kw):
+    return W.make(name, seed=seed, reduced=True, **kw).to(DEV)
+
+
+def _check(wl, expect_variant=None, **kw):
+    out, lse = gpu_decode(wl, **kw)
+    assert pd.check_device_errors() == "PD_OK"
+    if expect_variant:
+        assert pd.last_decode_variant() == expect_variant
+    ro, rl, st = oracle_decode(wl)
+    assert st == 0
+    return compare(kind_of(wl), out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+@pytest.mark.parametrize("splits", [1, 0])
+def test_tiny_fp32(seed, splits):
+    wl = W.make("tiny_fp32", seed=seed).to(DEV)
+    _check(wl, "simt", num_splits=splits)
+
+
+@pytest.mark.parametrize("seed", [0, 3])
+def test_llama3_bf16_rope_mma(seed):
+    _check(_wl("llama3_8b_bf16", seed), "mma")
+
+
+def test_llama3_bf16_rope_simt_page8():
+    """Page size 8 is outside the tensor-core variant: the SIMT kernel serves it."""
+    _check(_wl("llama3_8b_bf16", 4, page_size=8, pool=1200), "simt")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_long_context_internal_split(seed):
+    wl = _wl("long_ctx_bf16", seed)
+    _check(wl, "mma")
+    # force many chunks per sequence
+    _check(wl, "mma", num_splits=32, max_kv_len_hint=int(wl.attended.max()))
+
+
+def test_long_context_external_split_merge_tree():
+    """Config-3 flow: decode each page-aligned chunk as a pseudo-sequence (fp32
+    partials), then merge pairwise with merge_state_inplace in a tree."""
+    wl = _wl("long_ctx_bf16", 2)
+    s = wl.spec
+    ipc, valc, lastc, koff, owner = W.split_chunks(wl.indptr.cpu().numpy(), wl.values.cpu().numpy(),
+                                                   wl.seq_len, s.page_size, 32)
+    nchunk = np.bincount(owner, minlength=s.B)
+    assert nchunk.max() == 32
+    Bc = len(owner)
+    Qc = wl.Q[torch.from_numpy(owner).to(DEV)].contiguous()
+    out = torch.empty((Bc, s.H_qo, s.D), dtype=torch.float32, device=DEV)
+    lse = torch.empty((Bc, s.H_qo), dtype=torch.float32, device=DEV)
+    t = lambda a: torch.from_numpy(a).to(DEV)
+    pd.batch_decode_paged_kv(Qc, wl.pages, t(ipc), t(valc), t(lastc), t(koff), t(koff), out, lse,
+                             0, 1.0, 1e4, wl.sm_scale, num_splits=1)
+    # tree: level by level, merge chunk 2i+1 into chunk 2i of each sequence
+    idx = [list(np.nonzero(owner == b)[0]) for b in range(s.B)]
+    while max(len(x) for x in idx) > 1:
+        dst, src = [], []
+        for b in range(s.B):
+            x = idx[b]
+            dst += x[0:len(x) - 1:2]
+            src += x[1:len(x):2]
+            idx[b] = x[0::2]
+        di, si = t(np.array(dst)), t(np.array(src))
+        V, S = out[di].contiguous(), lse[di].contiguous()
+        pd.merge_state_inplace(V, S, out[si].contiguous(), lse[si].contiguous())
+        out[di], lse[di] = V, S
+    first = [x[0] for x in idx]
+    assert pd.check_device_errors() == "PD_OK"
+    ro, rl, _ = oracle_decode(wl)
+    compare("bf16", out[first], lse[first], ro, rl)
+
+
+@pytest.mark.parametrize("seed", [0, 5])
+def test_window_sink_f16(seed):
+    _check(_wl("window_sink_f16", seed), "mma")
+
+
+def test_window_sink_f16_split():
+    wl = _wl("window_sink_f16", 6)
+    _check(wl, "mma", num_splits=7, max_kv_len_hint=int(wl.attended.max()))
+
+
+@pytest.mark.parametrize("seed", [0, 7])
+def test_fp8_append_then_decode(seed):
+    wl = _wl("fp8_kv_highconc", seed)
+    s = wl.spec
+    ref_pages, bad = oracle.append_paged_kv(
+        W.bits(wl.pages), W.bits(wl.k_new), W.bits(wl.v_new), wl.slot_mapping.cpu().numpy(),
+        in_dtype=s.q_dtype, kv_dtype="e4m3", page_size=s.page_size, k_scale=wl.k_scale,
+        v_scale=wl.v_scale)
+    assert bad == 0
+    pd.append_paged_kv(wl.pages, wl.k_new, wl.v_new, wl.slot_mapping, wl.k_scale, wl.v_scale)
+    assert pd.check_device_errors() == "PD_OK"
+    assert np.array_equal(W.bits(wl.pages), ref_pages), "append not bit-exact"
+    out, lse = gpu_decode(wl)
+    assert pd.last_decode_variant() == "mma"
+    ro, rl, _ = oracle_decode(wl, pages=ref_pages)
+    compare("e4m3", out, lse, ro, rl)
+
+
+def test_fp8_f16_query_and_simt_variant():
+    wl = _wl("fp8_kv_highconc", 8, q_dtype="f16", out_dtype="f16")
+    _check(wl, "mma")
+    wl2 = _wl("fp8_kv_highconc", 9, page_size=8)
+    _check(wl2, "simt")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
+def test_shape_sweep(kv, D, group):
+    rope = group % 2 == 0
+    wl = _wl("llama3_8b_bf16", 10 + group, q_dtype=kv, kv_dtype=kv, out_dtype=kv, D=D,
+             H_kv=2, H_qo=2 * group, B=3, len_dist=("uniform", 1, 300), pool=200,
+             rotary_mode=int(rope))
+    _check(wl, "mma")
+    _check(wl, "mma", num_splits=4, max_kv_len_hint=300)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_fp32_dims(D):
+    wl = W.make("tiny_fp32", seed=D, D=D, rotary_mode=1, rope_theta=1e4).to(DEV)
+    _check(wl, "simt")
+
+
+def test_out_dtype_f32_for_bf16_cache():
+    wl = _wl("llama3_8b_bf16", 11)
+    _check(wl, "mma", out_dtype="f32")
+
+
+# ----------------------------------------------------------------------------- edge cases
+
+def _custom(lens, P=16, window=None, sink=0, H_qo=8, H_kv=2, D=128, dt="bf16", seed=0, rope=0):
+    """Workload with explicit lengths (0 allowed)."""
+    wl = W.make("llama3_8b_bf16", seed=seed, reduced=True, B=len(lens), H_qo=H_qo, H_kv=H_kv,
+                D=D, page_size=P, q_dtype=dt, kv_dtype=dt, out_dtype=dt, pool=64,
+                rotary_mode=rope, len_dist=("uniform", 1, 1))
+    lens = np.array(lens, np.int64)
+    npages = (lens + P - 1) // P
+    rng = np.random.default_rng(seed + 100)
+    vals = rng.permutation(wl.max_pages)[: npages.sum()].astype(np.int32)
+    indptr = np.concatenate([[0], np.cumsum(npages)]).astype(np.int32)
+    last = np.where(npages > 0, lens - (npages - 1) * P, 0).astype(np.int32)
+    if window is None:
+        li = last
+        att = lens
+    else:
+        win_off = np.maximum(sink, lens - window).astype(np.int32)
+        li = np.stack([last, win_off, np.full(len(lens), sink, np.int32)]).astype(np.int32)
+        att = np.where(npages > 0, lens - win_off + sink, 0)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    spec = W.spec("llama3_8b_bf16", True, B=len(lens), H_qo=H_qo, H_kv=H_kv, D=D, page_size=P,
+                  q_dtype=dt, kv_dtype=dt, out_dtype=dt, window=window, sink=sink, rotary_mode=rope)
+    return W.Workload(spec=spec, Q=wl.Q, pages=wl.pages, indptr=t(indptr),
+                      values=t(vals if len(vals) else np.zeros(1, np.int32)), length_info=t(li),
+                      k_rope_pos_offset=t(np.zeros(len(lens), np.int32)),
+                      q_rope_position=t(att.astype(np.int32)), seq_len=lens, attended=att,
+                      sm_scale=wl.sm_scale).to(DEV)
+
+
+def test_edge_empty_len1_fullpage():
+    wl = _custom([0, 1, 16, 32, 17, 0, 15])
+    out, lse = gpu_decode(wl)
+    assert pd.check_device_errors() == "PD_OK"
+    ro, rl, _ = oracle_decode(wl)
+    compare("bf16", out, lse, ro, rl)
+    assert torch.all(out[0] == 0) and torch.all(lse[0] == -5e4)
+    assert torch.all(out[5] == 0) and torch.all(lse[5] == -5e4)
+
+
+def test_edge_window_cases():
+    # window >= len, sink = 0, window start in the middle of a page, sink crossing a page
+    for lens, window, sink in [([10, 40, 100], 200, 0), ([40, 57, 123], 10, 0),
+                               ([40, 57, 123], 10, 4), ([90, 91], 30, 20)]:
+        wl = _custom(lens, window=window, sink=sink, dt="f16", rope=1)
+        _check(wl)
+        _check(wl, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+
+
+def test_edge_more_chunks_than_pages():
+    wl = _custom([33, 5, 70])
+    _check(wl, num_splits=64, max_kv_len_hint=70)
+
+
+def test_edge_all_empty_and_b0():
+    wl = _custom([0, 0, 0])
+    out, lse = gpu_decode(wl)
+    assert pd.check_device_errors() == "PD_OK"
+    assert torch.all(out == 0) and torch.all(lse == -5e4)
+    wl0 = _custom([5])
+    Q0 = wl0.Q[:0]
+    out0 = torch.empty((0, 8, 128), dtype=torch.bfloat16, device=DEV)
+    lse0 = torch.empty((0, 8), dtype=torch.float32, device=DEV)
+    pd.batch_decode_paged_kv(Q0, wl0.pages, wl0.indptr[:1], wl0.values, wl0.length_info[:0],
+                             None, None, out0, lse0)
+
+
+def test_caller_workspace():
+    wl = _wl("long_ctx_bf16", 3)
+    s = wl.spec
+    out = torch.empty((s.B, s.H_qo, s.D), dtype=torch.bfloat16, device=DEV)
+    desc = pd.make_desc(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info, out)
+    n = pd.workspace_size(desc)
+    assert n > 0
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    pd.workspace_init(ws)
+    for _ in range(2):  # counters must be left at zero for the next call
+        o, l = gpu_decode(wl, workspace=ws)
+        assert pd.check_device_errors() == "PD_OK"
+        ro, rl, _ = oracle_decode(wl)
+        compare("bf16", o, l, ro, rl)
+    small = torch.empty(n // 2, dtype=torch.uint8, device=DEV)
+    with pytest.raises(pd.PDError, match="WORKSPACE"):
+        gpu_decode(wl, workspace=small)
+
+
+def test_bad_page_id_is_reported_not_trapped():
+    wl = _custom([40, 20])
+    vals = wl.values.clone()
+    vals[1] = wl.max_pages + 5  # out of range: the row block is skipped, error recorded
+    bad = W.Workload(**{**wl.__dict__, "values": vals})
+    out, lse = gpu_decode(bad)
+    assert pd.check_device_errors() == "PD_ERR_BAD_PAGE"
+    assert pd.check_device_errors() == "PD_OK"  # the word was cleared
+    # both sides exclude the rows of the bad page and agree on the rest
+    ro, rl, st = oracle_decode(bad)
+    assert st == -1
+    compare("bf16", out, lse, ro, rl)
+
+
+def test_repeatable_and_stream():
+    wl = _wl("llama3_8b_bf16", 12)
+    o1, l1 = gpu_decode(wl)
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        o2, l2 = gpu_decode(wl, stream=st)
+    st.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
