@@ -40,7 +40,9 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned* err = nullptr;
-  void* ws = nullptr;
+  void* cnt = nullptr;  // split arrival counters (kept at zero between calls)
+  size_t cnt_bytes = 0;
+  void* ws = nullptr;   // partial (out, lse) of split sequences
   size_t ws_bytes = 0;
 };
 constexpr int kMaxDevices = 64;
@@ -314,33 +316,60 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   if (items == 0) return PD_OK;
 
   cudaStream_t s = (cudaStream_t)stream;
-  void* ws = d.workspace;
+  const int group = d.H_qo / d.H_kv;
+  const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
+  const size_t cnt_bytes = align_up((size_t)d.B * d.H_kv * n_z * sizeof(int), kWsAlign);
+  const size_t lse_bytes = align_up((size_t)items * d.H_qo * sizeof(float), kWsAlign);
+  int* counters = nullptr;
+  char* partials = nullptr;
   if (ws_need) {
-    if (ws) {
-      if (d.workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(ws) % kWsAlign) != 0)
+    if (d.workspace) {
+      // caller workspace: [counters][partial lse][partial out]; the counter prefix is
+      // cleared on the stream every call, since a previous call with another layout
+      // may have left partial results there.
+      if (d.workspace_bytes < ws_need || (reinterpret_cast<uintptr_t>(d.workspace) % kWsAlign) != 0)
         return fail(PD_ERR_WORKSPACE, "caller workspace smaller than pd_workspace_size() or not 256-byte aligned");
+      counters = (int*)d.workspace;
+      partials = (char*)d.workspace + cnt_bytes;
+      cudaError_t e = cudaMemsetAsync(counters, 0, cnt_bytes, s);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
     } else {
+      // library workspace: counters live in their own buffer, zeroed when it grows and
+      // left at zero by every completed call (the last block of a sequence resets its
+      // counter); partial results live in a second buffer.
       std::lock_guard<std::mutex> lk(g_mu);
-      if (ds->ws_bytes < ws_need) {
+      if (ds->cnt_bytes < cnt_bytes) {
+        if (ds->cnt) {
+          cudaError_t e = cudaFree(ds->cnt);
+          ds->cnt = nullptr;
+          ds->cnt_bytes = 0;
+          if (e != cudaSuccess) return cuda_fail(e, "cudaFree(counters)");
+        }
+        const size_t bytes = align_up(cnt_bytes * 2, 4096);
+        cudaError_t e = cudaMalloc(&ds->cnt, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(counters)");
+        e = cudaMemset(ds->cnt, 0, bytes);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(counters)");
+        ds->cnt_bytes = bytes;
+      }
+      const size_t part_bytes = ws_need - cnt_bytes;
+      if (ds->ws_bytes < part_bytes) {
         if (ds->ws) {
           cudaError_t e = cudaFree(ds->ws);
           ds->ws = nullptr;
           ds->ws_bytes = 0;
           if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
         }
-        const size_t bytes = align_up(ws_need + ws_need / 4, 1 << 20);
+        const size_t bytes = align_up(part_bytes + part_bytes / 4, 1 << 20);
         cudaError_t e = cudaMalloc(&ds->ws, bytes);
         if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-        e = cudaMemset(ds->ws, 0, bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
         ds->ws_bytes = bytes;
       }
-      ws = ds->ws;
+      counters = (int*)ds->cnt;
+      partials = (char*)ds->ws;
     }
   }
 
-  const int group = d.H_qo / d.H_kv;
-  const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
   DecodeParams p{};
   p.Q = Q;
   p.pages = pages;
@@ -352,12 +381,9 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.out = output;
   p.lse = lse;
   if (ws_need) {
-    char* w = (char*)ws;
-    p.counters = (int*)w;
-    w += align_up((size_t)d.B * d.H_kv * n_z * sizeof(int), kWsAlign);
-    p.part_lse = (float*)w;
-    w += align_up((size_t)items * d.H_qo * sizeof(float), kWsAlign);
-    p.part_o = (float*)w;
+    p.counters = counters;
+    p.part_lse = (float*)partials;
+    p.part_o = (float*)(partials + lse_bytes);
   }
   p.err = ds->err;
   p.max_pages = d.max_pages;
@@ -368,6 +394,7 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.P = d.page_size;
   p.group = group;
   p.n_z = n_z;
+  p.precise = d.kv_dtype == kF32 ? 1 : 0;
   p.window = d.sliding_window ? 1 : 0;
   p.rotary = rotary_mode;
   p.chunk_rows = chunk;

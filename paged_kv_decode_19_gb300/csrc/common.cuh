@@ -109,6 +109,22 @@ __device__ __forceinline__ void rope_cos_sin(int pos, unsigned long long F, floa
   __sincosf(ang, &s, &c);
 }
 
+// Same angle with fp32-level accuracy (for the fp32 path): the turn fraction is split
+// into a 24-bit head and an 8-bit tail, sin/cos(pi*x) of the head come from the
+// accurate sincospif, and the tail (< 2^-23 half-turns) is added to first order.
+__device__ __forceinline__ void rope_cos_sin_accurate(int pos, unsigned long long F, float& c,
+                                                      float& s) {
+  const unsigned long long t = (unsigned long long)(long long)pos * F;
+  const int hi = (int)(unsigned)(t >> 32);  // half-turns * 2^31, signed: x in [-1, 1)
+  const float xa = (float)(hi & ~0xff) * 4.656612873077393e-10f;  // exact (<= 24 bits) * 2^-31
+  const float xb = (float)(hi & 0xff) * 4.656612873077393e-10f;
+  float sa, ca;
+  sincospif(xa, &sa, &ca);
+  const float d = xb * 3.14159265358979f;
+  s = fmaf(ca, d, sa);
+  c = fmaf(-sa, d, ca);
+}
+
 // ----------------------------------------------------------------------------- error word
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);

@@ -33,6 +33,7 @@ struct DecodeParams {
   long long max_pages;
   int B, H_qo, H_kv, D, P, group, n_z;
   int window, rotary;
+  int precise;        // fp32 path: softmax weights via double-precision exp2
   int chunk_rows;     // attended rows per work item (INT_MAX: no split)
   int out_dtype;
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
@@ -83,8 +84,10 @@ __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
   return s;
 }
 
+// Work items of a sequence: ceil(L / chunk_rows), and one (empty) item for L = 0 so
+// that an empty sequence still gets its output written (out = 0, lse = -5e4).
 __device__ __forceinline__ int chunks_of(int L, int chunk_rows) {
-  return L > 0 ? 1 + (L - 1) / chunk_rows : 0;
+  return L > 0 ? 1 + (L - 1) / chunk_rows : 1;
 }
 
 struct Work {
@@ -127,7 +130,7 @@ __device__ bool locate_item(const DecodeParams& p, int item, Work& w) {
     }
     incl += warp_base;
     const int excl = incl - n;
-    if (b < p.B && n > 0 && item >= base + excl && item < base + incl) {
+    if (b < p.B && item >= base + excl && item < base + incl) {
       s_hit[0] = b;
       s_hit[1] = item - base - excl;
       s_hit[2] = n;
@@ -213,6 +216,11 @@ __device__ __forceinline__ int lookup_page(const DecodeParams& p, const SeqInfo&
 }
 
 // ---------------------------------------------------------------------------- finish
+// 2^x for the merge weights: fp32-accurate on the fp32 path, hardware ex2 otherwise.
+__device__ __forceinline__ float merge_exp2(const DecodeParams& p, float x) {
+  return p.precise ? (float)exp2((double)x) : fast_exp2(x);
+}
+
 __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, float v) {
   if (p.out_dtype == kF32) reinterpret_cast<float*>(p.out)[idx] = v;
   else if (p.out_dtype == kBF16) reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
@@ -240,7 +248,7 @@ __device__ void finish_block(const DecodeParams& p, const Work& w, int item, int
     float den = 0.f, num = 0.f;
 #pragma unroll
     for (int s = 0; s < NWS; ++s) {
-      const float a = fast_exp2(sm_m[s * 8 + j] - M);
+      const float a = merge_exp2(p, sm_m[s * 8 + j] - M);
       den += sm_d[s * 8 + j] * a;
       num += sm_o[(s * 8 + j) * D + d] * a;
     }
@@ -277,7 +285,7 @@ __device__ void finish_block(const DecodeParams& p, const Work& w, int item, int
     float den = 0.f, num = 0.f;
     for (int c = 0; c < w.nchunks; ++c) {
       const size_t it = (size_t)(w.first_item + c);
-      const float a = fast_exp2(__ldcg(p.part_lse + it * p.H_qo + hq) - M);
+      const float a = merge_exp2(p, __ldcg(p.part_lse + it * p.H_qo + hq) - M);
       den += a;
       num += a * __ldcg(p.part_o + (it * p.H_qo + hq) * D + d);
     }

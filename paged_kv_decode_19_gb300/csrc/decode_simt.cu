@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
       float x = a[e], y = bb[e];
       if (p.rotary) {
         float c, s;
-        rope_cos_sin(qpos, F[e], c, s);
+        rope_cos_sin_accurate(qpos, F[e], c, s);
         const float xr = x * c - y * s, yr = y * c + x * s;
         x = xr;
         y = yr;
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
         float x = ka[e], y = kb[e];
         if (p.rotary) {
           float c, s;
-          rope_cos_sin(kpos0 + r, F[e], c, s);
+          rope_cos_sin_accurate(kpos0 + r, F[e], c, s);
           const float xr = x * c - y * s, yr = y * c + x * s;
           x = xr;
           y = yr;
@@ -141,7 +141,14 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
         for (int e = 0; e < E; ++e) s = fmaf(q[j][e], k[e], s);
         s = warp_sum(s);
         const float mn = fmaxf(m[j], s);
-        const float a = fast_exp2(m[j] - mn), pj = fast_exp2(s - mn);
+        float a, pj;
+        if constexpr (std::is_same<KT, float>::value) {  // fp32 cache: fp32-accurate weights
+          a = (float)exp2((double)(m[j] - mn));
+          pj = (float)exp2((double)(s - mn));
+        } else {
+          a = fast_exp2(m[j] - mn);
+          pj = fast_exp2(s - mn);
+        }
         dsum[j] = dsum[j] * a + pj;
 #pragma unroll
         for (int e = 0; e < E; ++e) o[j][e] = fmaf(pj, v[e], o[j][e] * a);

@@ -62,7 +62,7 @@ def test_long_context_external_split_merge_tree():
     ipc, valc, lastc, koff, owner = W.split_chunks(wl.indptr.cpu().numpy(), wl.values.cpu().numpy(),
                                                    wl.seq_len, s.page_size, 32)
     nchunk = np.bincount(owner, minlength=s.B)
-    assert nchunk.max() == 32
+    assert 16 <= nchunk.max() <= 32
     Bc = len(owner)
     Qc = wl.Q[torch.from_numpy(owner).to(DEV)].contiguous()
     out = torch.empty((Bc, s.H_qo, s.D), dtype=torch.float32, device=DEV)
@@ -255,3 +255,28 @@ def test_repeatable_and_stream():
         o2, l2 = gpu_decode(wl, stream=st)
     st.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_split_counters_survive_layout_changes():
+    """A split call with few (sequence, head) counters followed by one with many: the
+    second call's counters must not see the first call's partial results."""
+    a = _wl("long_ctx_bf16", 13)
+    _check(a, "mma", num_splits=16, max_kv_len_hint=int(a.attended.max()))
+    b = _wl("window_sink_f16", 14, B=24)
+    _check(b, "mma", num_splits=3, max_kv_len_hint=int(b.attended.max()))
+    _check(a, "mma", num_splits=16, max_kv_len_hint=int(a.attended.max()))
+
+
+def test_caller_workspace_reused_across_layouts():
+    a = _wl("long_ctx_bf16", 15)
+    b = _wl("window_sink_f16", 16, B=24)
+    sizes = []
+    for wl in (a, b):
+        s = wl.spec
+        out = torch.empty((s.B, s.H_qo, s.D), dtype=wl.Q.dtype, device=DEV)
+        sizes.append(pd.workspace_size(pd.make_desc(wl.Q, wl.pages, wl.indptr, wl.values,
+                                                     wl.length_info, out)))
+    ws = torch.empty(max(sizes), dtype=torch.uint8, device=DEV)
+    pd.workspace_init(ws)
+    for wl in (a, b, a, b):
+        _check(wl, "mma", workspace=ws)

@@ -1,0 +1,57 @@
+"""Full-size workloads, in the launch configuration the benchmark times: sampled
+(sequence, head) outputs are recomputed one by one by the oracle; size-independent
+properties are checked on every output."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_decode_19_gb300 import workloads as W
+from tests._util import compare, gpu_decode, kind_of, oracle_decode
+
+pd = pytest.importorskip("paged_kv_decode_19_gb300")
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+SEED = 1000  # the benchmark's seed for rank 0
+
+
+def _sample_mask(wl, n_rand=6, seed=0):
+    s = wl.spec
+    rng = np.random.default_rng(seed)
+    mask = np.zeros((s.B, s.H_qo), bool)
+    longest = int(np.argmax(wl.attended))
+    shortest = int(np.argmin(wl.attended))
+    mask[longest, [0, s.H_qo - 1]] = True
+    mask[shortest, s.H_qo // 2] = True
+    for _ in range(n_rand):
+        mask[rng.integers(s.B), rng.integers(s.H_qo)] = True
+    return mask
+
+
+@pytest.mark.parametrize("name", list(W.SPECS))
+def test_fullsize_sampled(name):
+    wl = W.make(name, seed=SEED, device=DEV)
+    s = wl.spec
+    kw = dict(num_splits=1) if name == "tiny_fp32" else {}
+    ref_pages = None
+    if s.append:
+        ref_pages, bad = oracle.append_paged_kv(
+            W.bits(wl.pages), W.bits(wl.k_new), W.bits(wl.v_new), wl.slot_mapping.cpu().numpy(),
+            in_dtype=s.q_dtype, kv_dtype=s.kv_dtype, page_size=s.page_size, k_scale=wl.k_scale,
+            v_scale=wl.v_scale)
+        assert bad == 0
+        pd.append_paged_kv(wl.pages, wl.k_new, wl.v_new, wl.slot_mapping, wl.k_scale, wl.v_scale)
+        assert pd.check_device_errors() == "PD_OK"
+        assert np.array_equal(W.bits(wl.pages), ref_pages), "append not bit-exact at full size"
+    out, lse = gpu_decode(wl, **kw)
+    assert pd.check_device_errors() == "PD_OK"
+    # properties of every output: finite; each output element is a convex combination
+    # of V values, so |out| <= max |V| (times v_scale for e4m3)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    vmax = wl.pages[:, 1].float().abs().max().item() * (wl.v_scale if s.kv_dtype == "e4m3" else 1)
+    assert out.float().abs().max().item() <= vmax * (1 + 1e-2)
+    assert (lse > -5e4).all()
+    mask = _sample_mask(wl)
+    ro, rl, st = oracle_decode(wl, pages=ref_pages, mask=mask)
+    assert st == 0
+    compare(kind_of(wl), out, lse, ro, rl, mask=mask)

@@ -11,7 +11,9 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.mark.parametrize("dt,tol", [("f32", 2e-6), ("bf16", 1e-2), ("f16", 2e-3)])
+# f32: fp32-level; bf16/f16: the 16-bit bound of the decode contract (max abs 2e-2),
+# which covers rounding the merged values (|v| up to ~5) to the storage type.
+@pytest.mark.parametrize("dt,tol", [("f32", 2e-6), ("bf16", 2e-2), ("f16", 2e-2)])
 @pytest.mark.parametrize("shape", [(8, 32, 128), (3, 5, 64), (1, 1, 256), (7, 3, 96)])
 def test_merge_state(dt, tol, shape):
     g = torch.Generator().manual_seed(hash((dt, shape)) & 0xffff)
