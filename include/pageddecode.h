@@ -124,6 +124,41 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
                                    pd_stream_t stream);
 
 /*
+ * pd_batch_decode_paged_kv_noalloc — no counterpart in the source papers; an addition
+ * of this library for callers that cannot allocate device memory.  Some programs may
+ * not call cudaMalloc at all once they are running: a serving process that reserved
+ * all free HBM for its KV-cache pool at start-up (a later allocation would fail), a
+ * plug-in that lives inside a host framework that owns every device allocation, or a
+ * latency-critical loop that cannot afford the allocator's implicit synchronisation.
+ * This entry point computes exactly what pd_batch_decode_paged_kv computes, with the
+ * same arguments, but it never allocates: the split scratch (arrival counters and
+ * partial out/lse) is one static 16 MiB device array inside the library, present on
+ * every GPU that loads it until the process exits.
+ *   - desc->workspace must be NULL.
+ *   - If the batch would need more than 16 MiB of split scratch (about
+ *     4 * grid_items * H_qo * (D + 1) bytes, see pd_workspace_size), the call returns
+ *     PD_ERR_WORKSPACE without launching; bound it with desc->num_splits and
+ *     desc->max_kv_len_hint, or use pd_batch_decode_paged_kv.
+ *   - The first call on a device looks up the array's device address (a
+ *     cudaGetSymbolAddress, once per device, with that device current); make that
+ *     first call before any CUDA-graph stream capture.
+ *   - All calls share the one array: the counters are cleared on `stream` at the start
+ *     of every call, and the array keeps the last call's partials.  Two calls whose
+ *     work overlaps on the GPU (different streams, or different host threads without
+ *     ordering) race on it and give undefined results; serialise them.
+ * Returns the same statuses as pd_batch_decode_paged_kv.
+ */
+pd_status pd_batch_decode_paged_kv_noalloc(const void* Q, const void* pages,
+                                           const int32_t* page_table_indptr,
+                                           const int32_t* page_table_values,
+                                           const int32_t* length_info,
+                                           const int32_t* k_rope_pos_offset,
+                                           const int32_t* q_rope_position, void* output,
+                                           float* lse, int32_t rotary_mode, float rope_scale,
+                                           float rope_theta, float sm_scale,
+                                           const pd_decode_desc* desc, pd_stream_t stream);
+
+/*
  * merge_state_inplace — [TVM] `merge_state_inplace`.
  * For every (n, h):  m = max(S, S_o);  w = 2^(S - m);  w_o = 2^(S_o - m);
  *   V[n,h,:] <- V * w/(w+w_o) + V_other * w_o/(w+w_o);  S[n,h] <- log2(w + w_o) + m.

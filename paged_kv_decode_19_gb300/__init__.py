@@ -8,6 +8,7 @@ from ._lib import (  # noqa: F401
     PDError,
     append_paged_kv,
     batch_decode_paged_kv,
+    batch_decode_paged_kv_noalloc,
     check_device_errors,
     last_decode_variant,
     make_desc,

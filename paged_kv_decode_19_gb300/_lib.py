@@ -42,6 +42,7 @@ DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 # Every entry point declared in include/pageddecode.h.
 EXPORTS = (
     "pd_batch_decode_paged_kv",
+    "pd_batch_decode_paged_kv_noalloc",
     "pd_merge_state_inplace",
     "pd_append_paged_kv",
     "pd_workspace_size",
@@ -97,6 +98,8 @@ def lib():
             L.pd_batch_decode_paged_kv.argtypes = [P, P, P, P, P, P, P, P, P, i32, f32, f32, f32,
                                                    ctypes.POINTER(DecodeDesc), P]
             L.pd_batch_decode_paged_kv.restype = i32
+            L.pd_batch_decode_paged_kv_noalloc.argtypes = L.pd_batch_decode_paged_kv.argtypes
+            L.pd_batch_decode_paged_kv_noalloc.restype = i32
             L.pd_merge_state_inplace.argtypes = [P, P, P, P, i32, i32, i32, i32, P]
             L.pd_merge_state_inplace.restype = i32
             L.pd_append_paged_kv.argtypes = [P, P, P, P, i32, i32, i32, i32, i64, i32, i32, f32,
@@ -165,6 +168,26 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
                      v_scale=v_scale, workspace=workspace)
     _check(lib().pd_batch_decode_paged_kv(
+        _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
+        _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
+        _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta), float(sm_scale),
+        ctypes.byref(desc), _stream(stream)))
+    return output, lse
+
+
+def batch_decode_paged_kv_noalloc(Q, pages, page_table_indptr, page_table_values,
+                                  length_info, k_rope_pos_offset, q_rope_position, output, lse,
+                                  rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
+                                  *, k_scale=1.0, v_scale=1.0, num_splits=0, max_kv_len_hint=0,
+                                  stream=None):
+    """pd_batch_decode_paged_kv_noalloc: same result, split scratch in the library's
+    static device array (no device allocation)."""
+    if sm_scale is None:
+        sm_scale = Q.shape[-1] ** -0.5
+    desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
+                     num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
+                     v_scale=v_scale)
+    _check(lib().pd_batch_decode_paged_kv_noalloc(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
         _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta), float(sm_scale),

@@ -29,6 +29,9 @@ static pd_status fail(pd_status st, const std::string& msg) {
   t_last_error = msg;
   return st;
 }
+// Lets the library's other translation units set the message of a failure they return.
+void record_error(const char* msg) { t_last_error = msg; }
+
 static pd_status cuda_fail(cudaError_t e, const char* what) {
   return fail(PD_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }

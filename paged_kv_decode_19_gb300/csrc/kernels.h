@@ -28,6 +28,9 @@ cudaError_t launch_mma_f16(const DecodeParams& p, const CUtensorMap& map, int q_
 cudaError_t launch_mma_fp8(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
                            cudaStream_t st, MmaConfig* cfg);
 
+// Sets the thread's last-error message (api.cu).
+void record_error(const char* msg);
+
 // merge_state_inplace and append_paged_kv
 cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const float* S_other, int N,
                                int H, int D, int v_dtype, cudaStream_t st);
