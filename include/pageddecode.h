@@ -70,12 +70,14 @@ typedef struct {
   int32_t sliding_window;    /* 0: length_info is [B] = last_page_len.
                                 1: length_info is [3,B] = (last_page_len,
                                    window start offset, attention-sink length). */
-  int32_t num_splits;        /* KV chunks per sequence: 0 = automatic, 1 = never split,
-                                n > 1 = at most n chunks (needs max_kv_len_hint) */
+  int32_t num_splits;        /* block schedule: 0 = balanced (one resident wave of blocks,
+                                each taking an equal share of all pages of all sequences
+                                and heads); 1 = one block per (sequence, <=8-head slice),
+                                never split; n > 1 = balanced over about n blocks per
+                                (sequence, head slice) */
   int64_t max_pages;         /* pages buffer holds [max_pages,2,H_kv,P,D] */
   int64_t nnz_pages;         /* entries in page_table_values (= indptr[B]) */
-  int32_t max_kv_len_hint;   /* optional upper bound on attended rows per sequence (0 = none);
-                                tightens split planning, must not be exceeded */
+  int32_t max_kv_len_hint;   /* reserved (ignored); set to 0 */
   float k_scale;             /* E4M3 KV only: K = code * k_scale (else ignored) */
   float v_scale;             /* E4M3 KV only: V = code * v_scale (else ignored) */
   void* workspace;           /* optional caller workspace (device); NULL = library-managed */
@@ -105,8 +107,9 @@ typedef struct {
  *   k_rope_pos_offset, q_rope_position [B] int32; may be NULL when rotary_mode == 0.
  *   output      [B, H_qo, D] desc->out_dtype.   lse [B, H_qo] float32 (log2 units).
  * Scalars: rotary_mode (0 none, 1 RoPE), rope_scale, rope_theta, sm_scale.
- * Long sequences are split across thread blocks and the partial (out, lse) pairs
- * are merged on the device; the split plan uses only host-known sizes.
+ * Work is split across thread blocks by pages (see desc->num_splits); a sequence
+ * that several blocks share is merged on the device from their partial (out, lse)
+ * pairs by the last of them to finish.  The plan uses only host-known sizes.
  * Workspace: desc->workspace if non-NULL (at least pd_workspace_size(desc) bytes,
  * 256-byte aligned, zero-filled before its first use — see pd_workspace_init),
  * otherwise a per-device buffer the library allocates on first use and grows as
@@ -136,9 +139,9 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
  * every GPU that loads it until the process exits.
  *   - desc->workspace must be NULL.
  *   - If the batch would need more than 16 MiB of split scratch (about
- *     4 * grid_items * H_qo * (D + 1) bytes, see pd_workspace_size), the call returns
- *     PD_ERR_WORKSPACE without launching; bound it with desc->num_splits and
- *     desc->max_kv_len_hint, or use pd_batch_decode_paged_kv.
+ *     64 * grid_blocks * (D + 1) bytes plus 4 bytes per (sequence, head slice), see
+ *     pd_workspace_size), the call returns PD_ERR_WORKSPACE without launching; lower
+ *     desc->num_splits or use pd_batch_decode_paged_kv.
  *   - The first call on a device looks up the array's device address (a
  *     cudaGetSymbolAddress, once per device, with that device current); make that
  *     first call before any CUDA-graph stream capture.
@@ -197,13 +200,14 @@ pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream);
 
 /*
  * Host-only split planner (no CUDA calls): for `desc` on a GPU with `num_sms`
- * multiprocessors and `ctas_per_sm` resident decode blocks, returns the KV chunk
- * length in rows (*chunk_rows; INT32_MAX = no split), the number of work items the
- * grid provides (*grid_items) and the workspace bytes.  Used by the library and
- * exposed for tests.
+ * multiprocessors and `ctas_per_sm` resident decode blocks, returns the block schedule
+ * (*schedule: 0 = balanced shares of all pages, 1 = one block per (sequence, head
+ * slice)), the number of blocks (*grid_blocks) and the workspace bytes (per-segment
+ * arrival counters plus two partial (out, lse) slots per block; 0 when nothing is
+ * split).  Used by the library and exposed for tests.
  */
 pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_sm,
-                  int32_t* chunk_rows, int32_t* grid_items, size_t* workspace_bytes);
+                  int32_t* schedule, int32_t* grid_blocks, size_t* workspace_bytes);
 
 /* Synchronises `stream`, then reads and clears the current device's error word.
  * Returns PD_OK, PD_ERR_BAD_PAGE, PD_ERR_BAD_LENGTH, PD_ERR_BAD_SLOT or

@@ -233,7 +233,8 @@ def workspace_init(ws: torch.Tensor, stream=None):
 
 
 def plan(desc: DecodeDesc, num_sms: int, ctas_per_sm: int):
-    """Host-only split plan: (chunk_rows, grid_items, workspace_bytes)."""
+    """Host-only split plan: (schedule, grid_blocks, workspace_bytes); schedule 0 =
+    balanced shares of all pages, 1 = one block per (sequence, head slice)."""
     c, g, w = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_size_t()
     _check(lib().pd_plan(ctypes.byref(desc), num_sms, ctas_per_sm, ctypes.byref(c),
                          ctypes.byref(g), ctypes.byref(w)))

@@ -1,8 +1,6 @@
 // Host side of libpageddecode: argument validation, the split planner, workspace
-// and error-word management, TMA descriptor set-up and kernel dispatch.  Every
+// and error-word management and kernel dispatch.  Every
 // entry point of include/pageddecode.h is defined here.
-#include <cudaTypedefs.h>
-
 #include <algorithm>
 #include <climits>
 #include <cmath>
@@ -16,10 +14,10 @@
 
 namespace pd {
 
-// Split planner constants: aim for ~kWaves resident waves of equal-sized work items,
-// never cutting a sequence into chunks shorter than kMinChunkRows attended rows.
-constexpr int kWaves = 4;
-constexpr int kMinChunkRows = 128;
+// Split planner: the balanced schedule runs one resident wave of blocks (SMs x blocks
+// per SM); an explicit split count n > 1 asks for about n blocks per (sequence, head
+// slice) segment, capped at kMaxWaves resident waves.
+constexpr int kMaxWaves = 8;
 constexpr size_t kWsAlign = 256;
 
 static thread_local std::string t_last_error;
@@ -101,8 +99,6 @@ static pd_status validate_desc(const pd_decode_desc* d) {
   if ((long long)d->max_pages * 2 * d->H_kv > INT_MAX)
     return fail(PD_ERR_UNSUPPORTED, "max_pages * 2 * H_kv exceeds 2^31");
   if (d->num_splits < 0) return fail(PD_ERR_INVALID_ARG, "num_splits < 0");
-  if (d->num_splits > 1 && d->max_kv_len_hint <= 0)
-    return fail(PD_ERR_INVALID_ARG, "num_splits > 1 needs max_kv_len_hint");
   if (d->kv_dtype == kE4M3 && !(d->k_scale > 0.f && d->v_scale > 0.f && std::isfinite(d->k_scale) &&
                                 std::isfinite(d->v_scale)))
     return fail(PD_ERR_INVALID_ARG, "E4M3 KV needs finite positive k_scale and v_scale");
@@ -112,76 +108,35 @@ static pd_status validate_desc(const pd_decode_desc* d) {
 }
 
 // ---------------------------------------------------------------------------- planner
-static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int* chunk_rows,
-                      int* grid_items, size_t* ws_bytes) {
-  const int P = d->page_size;
+// Schedule, grid and workspace for `desc`.  *mode: kSchedBalanced or kSchedPerSegment;
+// *grid: blocks; workspace = per-segment counters + two partial slots per block.
+static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int* mode,
+                      int* grid, size_t* ws_bytes) {
   const int group = d->H_qo / d->H_kv;
   const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
-  long long est_rows = (long long)d->nnz_pages * P;
-  if (d->max_kv_len_hint > 0) est_rows = std::min(est_rows, (long long)d->B * d->max_kv_len_hint);
-  long long chunk;
+  const long long segments = (long long)d->B * d->H_kv * n_z;
+  const long long wave = (long long)std::max(num_sms, 1) * std::max(ctas_per_sm, 1);
+  long long g;
+  int m;
   if (d->num_splits == 1 || d->B == 0) {
-    chunk = INT_MAX;
+    m = kSchedPerSegment;
+    g = segments;
   } else {
-    const long long slots = (long long)std::max(num_sms, 1) * std::max(ctas_per_sm, 1) * kWaves;
-    const long long units = est_rows * d->H_kv * n_z;
-    chunk = std::max<long long>((units + slots - 1) / slots, kMinChunkRows);
-    if (d->num_splits > 1) chunk = std::max<long long>(chunk, (d->max_kv_len_hint + d->num_splits - 1) / d->num_splits);
-    chunk = (chunk + P - 1) / P * P;
-    if (chunk >= INT_MAX) chunk = INT_MAX;
+    m = kSchedBalanced;
+    // upper bound on work units (pages touched per segment, plus one per sequence)
+    const long long units = ((long long)d->nnz_pages + d->B) * d->H_kv * n_z;
+    g = d->num_splits > 1 ? std::min(segments * d->num_splits, wave * kMaxWaves) : wave;
+    g = std::max(1ll, std::min(g, units));
   }
-  long long items;
-  if (chunk == INT_MAX) {
-    items = d->B;
-  } else {
-    items = ((long long)d->nnz_pages * P + chunk - 1) / chunk + d->B;
-    if (d->max_kv_len_hint > 0)
-      items = std::min(items, (long long)d->B * ((d->max_kv_len_hint + chunk - 1) / chunk));
-  }
-  items = std::max<long long>(items, 0);
   size_t ws = 0;
-  if (chunk != INT_MAX) {
-    ws = align_up((size_t)d->B * d->H_kv * n_z * sizeof(int), kWsAlign) +
-         align_up((size_t)items * d->H_qo * sizeof(float), kWsAlign) +
-         align_up((size_t)items * d->H_qo * d->D * sizeof(float), kWsAlign);
+  if (m == kSchedBalanced) {
+    ws = align_up((size_t)segments * sizeof(int), kWsAlign) +
+         align_up((size_t)2 * g * kMaxGroupPerCta * sizeof(float), kWsAlign) +
+         align_up((size_t)2 * g * kMaxGroupPerCta * d->D * sizeof(float), kWsAlign);
   }
-  *chunk_rows = (int)chunk;
-  *grid_items = (int)std::min<long long>(items, INT_MAX);
+  *mode = m;
+  *grid = (int)std::min<long long>(g, INT_MAX);
   *ws_bytes = ws;
-}
-
-// ---------------------------------------------------------------------------- TMA map
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// pages viewed as a 3-D tensor [blocks = max_pages*2*H_kv][P][D]; box = 128 bytes of a
-// row x P rows x one block, 128B swizzle.
-static pd_status make_kv_map(const void* pages, const pd_decode_desc* d, CUtensorMap* map) {
-  auto fn = encode_fn();
-  if (!fn) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
-  const int eb = elem_bytes(d->kv_dtype);
-  const CUtensorMapDataType dt = eb == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
-  cuuint64_t dims[3] = {(cuuint64_t)d->D, (cuuint64_t)d->page_size,
-                        (cuuint64_t)d->max_pages * 2 * d->H_kv};
-  cuuint64_t strides[2] = {(cuuint64_t)d->D * eb, (cuuint64_t)d->D * eb * d->page_size};
-  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)d->page_size, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(map, dt, 3, const_cast<void*>(pages), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(PD_ERR_CUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
-  return PD_OK;
 }
 
 // Tensor-core variant eligibility (pages == nullptr: ignore the pointer's alignment).
@@ -193,11 +148,11 @@ static bool mma_path(const pd_decode_desc* d, const void* pages) {
   return false;
 }
 
-static cudaError_t mma_dispatch(const DecodeParams& p, const CUtensorMap& map, int q_dtype,
-                                int kv_dtype, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
-  if (kv_dtype == kBF16) return launch_mma_bf16(p, map, q_dtype, grid, st, cfg);
-  if (kv_dtype == kF16) return launch_mma_f16(p, map, q_dtype, grid, st, cfg);
-  return launch_mma_fp8(p, map, q_dtype, grid, st, cfg);
+static cudaError_t mma_dispatch(const DecodeParams& p, int q_dtype, int kv_dtype, dim3 grid,
+                                cudaStream_t st, MmaConfig* cfg) {
+  if (kv_dtype == kBF16) return launch_mma_bf16(p, q_dtype, grid, st, cfg);
+  if (kv_dtype == kF16) return launch_mma_f16(p, q_dtype, grid, st, cfg);
+  return launch_mma_fp8(p, q_dtype, grid, st, cfg);
 }
 
 // Fixed-point RoPE frequencies: F_i = 2^64 * frac(rope_scale / rope_theta^(2i/D) / (2 pi)).
@@ -225,11 +180,11 @@ const char* pd_get_last_error_string(void) { return t_last_error.c_str(); }
 const char* pd_last_decode_variant(void) { return t_last_variant; }
 
 pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_sm,
-                  int32_t* chunk_rows, int32_t* grid_items, size_t* workspace_bytes) {
+                  int32_t* schedule, int32_t* grid_blocks, size_t* workspace_bytes) {
   pd_status st = validate_desc(desc);
   if (st != PD_OK) return st;
-  if (!chunk_rows || !grid_items || !workspace_bytes) return fail(PD_ERR_INVALID_ARG, "NULL output");
-  plan_impl(desc, num_sms, ctas_per_sm, chunk_rows, grid_items, workspace_bytes);
+  if (!schedule || !grid_blocks || !workspace_bytes) return fail(PD_ERR_INVALID_ARG, "NULL output");
+  plan_impl(desc, num_sms, ctas_per_sm, schedule, grid_blocks, workspace_bytes);
   return PD_OK;
 }
 
@@ -242,8 +197,7 @@ static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary
   int n = 0;
   if (use_mma) {
     MmaConfig cfg{};
-    CUtensorMap dummy{};
-    e = mma_dispatch(p, dummy, d->q_dtype, d->kv_dtype, dim3(1), nullptr, &cfg);
+    e = mma_dispatch(p, d->q_dtype, d->kv_dtype, dim3(1), nullptr, &cfg);
     n = cfg.ctas_per_sm;
   } else {
     if (!simt_supports(d->q_dtype, d->kv_dtype, d->D)) return fail(PD_ERR_UNSUPPORTED, "dtype / head-dim combination");
@@ -265,9 +219,9 @@ size_t pd_workspace_size(const pd_decode_desc* desc) {
     for (int rot = 0; rot < 2; ++rot) {
       int ctas = 1;
       if (occupancy_for(desc, mma != 0, rot, &ctas) != PD_OK) continue;
-      int chunk, items;
+      int mode, grid;
       size_t ws;
-      plan_impl(desc, ds->num_sms, ctas, &chunk, &items, &ws);
+      plan_impl(desc, ds->num_sms, ctas, &mode, &grid, &ws);
       best = std::max(best, ws);
     }
   }
@@ -313,16 +267,16 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   int ctas = 1;
   st = occupancy_for(desc, use_mma, rotary_mode, &ctas);
   if (st != PD_OK) return st;
-  int chunk = 0, items = 0;
+  int mode = 0, grid_blocks = 0;
   size_t ws_need = 0;
-  plan_impl(desc, ds->num_sms, ctas, &chunk, &items, &ws_need);
-  if (items == 0) return PD_OK;
+  plan_impl(desc, ds->num_sms, ctas, &mode, &grid_blocks, &ws_need);
+  if (grid_blocks == 0) return PD_OK;
 
   cudaStream_t s = (cudaStream_t)stream;
   const int group = d.H_qo / d.H_kv;
   const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
   const size_t cnt_bytes = align_up((size_t)d.B * d.H_kv * n_z * sizeof(int), kWsAlign);
-  const size_t lse_bytes = align_up((size_t)items * d.H_qo * sizeof(float), kWsAlign);
+  const size_t lse_bytes = align_up((size_t)2 * grid_blocks * kMaxGroupPerCta * sizeof(float), kWsAlign);
   int* counters = nullptr;
   char* partials = nullptr;
   if (ws_need) {
@@ -400,7 +354,7 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.precise = d.kv_dtype == kF32 ? 1 : 0;
   p.window = d.sliding_window ? 1 : 0;
   p.rotary = rotary_mode;
-  p.chunk_rows = chunk;
+  p.mode = mode;
   p.out_dtype = d.out_dtype;
   const double log2e = 1.4426950408889634073599246810019;
   const double kdeq = d.kv_dtype == kE4M3 ? (double)d.k_scale : 1.0;
@@ -409,13 +363,10 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.out_scale = d.kv_dtype == kE4M3 ? d.v_scale : 1.f;
   if (rotary_mode) rope_table(rope_scale, rope_theta, d.D, p.rope_F);
 
-  const dim3 grid((unsigned)items, (unsigned)d.H_kv, (unsigned)n_z);
+  const dim3 grid((unsigned)grid_blocks);
   cudaError_t e;
   if (use_mma) {
-    CUtensorMap map;
-    st = make_kv_map(pages, desc, &map);
-    if (st != PD_OK) return st;
-    e = mma_dispatch(p, map, d.q_dtype, d.kv_dtype, grid, s, nullptr);
+    e = mma_dispatch(p, d.q_dtype, d.kv_dtype, grid, s, nullptr);
     t_last_variant = "mma";
   } else {
     if (!simt_supports(d.q_dtype, d.kv_dtype, d.D)) return fail(PD_ERR_UNSUPPORTED, "dtype / head-dim combination");

@@ -1,7 +1,8 @@
-// Pieces shared by the decode kernels: parameters, work-item location (length
-// decode + split plan), the row -> page mapping, and the per-block finish (merge
-// of the warps' softmax states, then either the final output or a partial state
-// plus an on-device merge of the sequence's partials by its last-finishing block).
+// Pieces shared by the decode kernels: parameters, length decode, the row -> page
+// mapping, the block schedule (which pages of which (sequence, KV head) a block
+// processes) and the finish of a block's share of a sequence (merge of the warps'
+// softmax states, then the final output, or a partial state that the last block of
+// the sequence to finish merges with the others).
 //
 // Source of the operation: Apache TVM `_decode_kernels.py`, `batch_decode_paged_kv`
 // (length_info, page-table addressing, base-2 online softmax, lse in log2 units)
@@ -13,8 +14,14 @@
 
 namespace pd {
 
-constexpr int kMaxGroupPerCta = 8;  // query heads one block serves (a grid z-slice)
+constexpr int kMaxGroupPerCta = 8;  // query heads one block serves at a time (a z-slice)
 constexpr int kMaxHalfDim = 128;    // D <= 256
+
+// Block schedules (DecodeParams::mode)
+enum : int {
+  kSchedBalanced = 0,   // all pages of all (sequence, head-slice) segments, cut into G equal shares
+  kSchedPerSegment = 1  // one block per (sequence, head-slice) segment: no split
+};
 
 struct DecodeParams {
   const void* Q;
@@ -26,15 +33,15 @@ struct DecodeParams {
   const int32_t* q_rope_position;
   void* out;
   float* lse;
-  float* part_o;    // [grid_items, H_qo, D] fp32 partial outputs (normalised)
-  float* part_lse;  // [grid_items, H_qo] fp32 partial lse (log2)
-  int* counters;    // [B, H_kv, n_z] arrivals per (sequence, KV head, head slice)
+  float* part_o;    // [2G][8][D] fp32 partial outputs (normalised): slot 2c + side
+  float* part_lse;  // [2G][8] fp32 partial lse (log2)
+  int* counters;    // [B * H_kv * n_z] pages merged so far per segment (reset by the last)
   unsigned* err;    // device error word
   long long max_pages;
   int B, H_qo, H_kv, D, P, group, n_z;
   int window, rotary;
-  int precise;        // fp32 path: softmax weights via double-precision exp2
-  int chunk_rows;     // attended rows per work item (INT_MAX: no split)
+  int precise;        // fp32 path: merge weights via double-precision exp2
+  int mode;           // kSchedBalanced / kSchedPerSegment
   int out_dtype;
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
   float q_prescale;   // split-operand MMA path: Q is pre-multiplied by this
@@ -84,74 +91,8 @@ __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
   return s;
 }
 
-// Work items of a sequence: ceil(L / chunk_rows), and one (empty) item for L = 0 so
-// that an empty sequence still gets its output written (out = 0, lse = -5e4).
-__device__ __forceinline__ int chunks_of(int L, int chunk_rows) {
-  return L > 0 ? 1 + (L - 1) / chunk_rows : 1;
-}
-
-struct Work {
-  int b, chunk, nchunks, first_item;
-  SeqInfo seq;
-};
-
-// Finds which (sequence, chunk) the work item `item` is: a block-wide exclusive scan
-// of the per-sequence chunk counts.  Returns false if `item` is past the last chunk.
-// Block 0 flags a plan overflow (more chunks than grid items).
-template <int NT>
-__device__ bool locate_item(const DecodeParams& p, int item, Work& w) {
-  __shared__ int s_warp[NT / 32];
-  __shared__ int s_hit[3];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) s_hit[0] = -1;
-  int base = 0;
-  for (int start = 0; start < p.B; start += NT) {
-    const int b = start + tid;
-    int n = 0, L = 0;
-    if (b < p.B) {
-      SeqInfo s = load_seq(p, b);
-      L = s.L;
-      n = chunks_of(L, p.chunk_rows);
-    }
-    int incl = n;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (lane == 31) s_warp[wid] = incl;
-    __syncthreads();
-    int warp_base = 0, total = 0;
-#pragma unroll
-    for (int i = 0; i < NT / 32; ++i) {
-      int v = s_warp[i];
-      if (i < wid) warp_base += v;
-      total += v;
-    }
-    incl += warp_base;
-    const int excl = incl - n;
-    if (b < p.B && item >= base + excl && item < base + incl) {
-      s_hit[0] = b;
-      s_hit[1] = item - base - excl;
-      s_hit[2] = n;
-    }
-    base += total;
-    __syncthreads();
-  }
-  __syncthreads();
-  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && tid == 0 && base > (int)gridDim.x)
-    set_error(p.err, kErrBadLength);
-  if (s_hit[0] < 0) return false;
-  w.b = s_hit[0];
-  w.chunk = s_hit[1];
-  w.nchunks = s_hit[2];
-  w.first_item = item - w.chunk;
-  w.seq = load_seq(p, w.b);
-  return true;
-}
-
 // ---------------------------------------------------------------------------- pieces
-// A chunk's attended rows [r0, r1) cover at most two contiguous runs of sequence
+// A sequence's attended rows [0, L) cover at most two contiguous runs of sequence
 // offsets (the sink run and the window run); each run is cut at page boundaries into
 // "pieces": one page, a slot range [s_lo, s_hi), first attended row r_lo.
 struct Pieces {
@@ -201,6 +142,12 @@ __device__ __forceinline__ Piece get_piece(const Pieces& c, int i, int P) {
   return q;
 }
 
+// Work units of a sequence: its pieces, or one (empty) unit when it has none, so that
+// an empty sequence still gets its output written (out = 0, lse = -5e4).
+__device__ __forceinline__ int units_of(const SeqInfo& s, int P) {
+  return s.L > 0 ? make_pieces(0, s.L, s, P).count() : 1;
+}
+
 // Physical page of piece page index `pidx` (or -1 when out of range -> error bit).
 __device__ __forceinline__ int lookup_page(const DecodeParams& p, const SeqInfo& s, int pidx) {
   if (pidx < 0 || pidx >= s.npages) {
@@ -215,6 +162,131 @@ __device__ __forceinline__ int lookup_page(const DecodeParams& p, const SeqInfo&
   return page;
 }
 
+// ---------------------------------------------------------------------------- schedule
+// Segments are (sequence b, head slice hz = hk * n_z + z) in the order b-major; segment
+// (b, hz) owns units [HZ * pre_b + hz * n_b, ... + n_b) of the global unit range [0, U),
+// with n_b = units_of(b), pre_b = sum of n_b' for b' < b, HZ = H_kv * n_z.
+// Balanced schedule: block c takes units [floor(c U / G), floor((c+1) U / G)).
+// Per-segment schedule: block c takes exactly segment c.
+struct Segment {
+  int b, hz, n;       // sequence, head slice, its units
+  long long off;      // first global unit of the segment
+  SeqInfo seq;
+};
+
+struct BlockRange {
+  long long x0, x1, U;
+  Segment seg;        // segment containing x0 (valid when x0 < x1)
+};
+
+// Block-wide: total units U, this block's range, and the segment holding its first unit.
+template <int NT>
+__device__ BlockRange block_range(const DecodeParams& p) {
+  __shared__ long long s_warp[NT / 32];
+  __shared__ long long s_hit[2];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int HZ = p.H_kv * p.n_z;
+  const long long G = gridDim.x;
+  BlockRange r;
+  // pass 1: U
+  long long total = 0;
+  for (int start = 0; start < p.B; start += NT) {
+    const int b = start + tid;
+    long long n = b < p.B ? units_of(load_seq(p, b), p.P) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    if (lane == 0) s_warp[wid] = n;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NT / 32; ++i) total += s_warp[i];
+    __syncthreads();
+  }
+  r.U = total * HZ;
+  const long long c = blockIdx.x;
+  long long target;
+  if (p.mode == kSchedBalanced) {
+    r.x0 = c * r.U / G;
+    r.x1 = (c + 1) * r.U / G;
+    target = r.x0;
+  } else {
+    r.x0 = r.x1 = -1;  // set below from the segment
+    target = c;        // segment index
+  }
+  // pass 2: the sequence holding `target` (a unit, or a segment index)
+  if (tid == 0) s_hit[0] = -1;
+  long long base = 0;
+  for (int start = 0; start < p.B; start += NT) {
+    const int b = start + tid;
+    const long long n = b < p.B ? (p.mode == kSchedBalanced ? (long long)units_of(load_seq(p, b), p.P) * HZ : HZ) : 0;
+    long long incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    long long wbase = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < NT / 32; ++i) {
+      const long long v = s_warp[i];
+      if (i < wid) wbase += v;
+      tot += v;
+    }
+    incl += wbase;
+    if (b < p.B && target >= base + incl - n && target < base + incl) {
+      s_hit[0] = b;
+      s_hit[1] = base + incl - n;  // balanced: first unit of b; per-segment: first segment of b
+    }
+    base += tot;
+    __syncthreads();
+  }
+  __syncthreads();
+  const int b = (int)s_hit[0];
+  if (b < 0) {
+    r.x0 = r.x1 = 0;
+    return r;
+  }
+  Segment& sg = r.seg;
+  sg.b = b;
+  sg.seq = load_seq(p, b);
+  sg.n = units_of(sg.seq, p.P);
+  if (p.mode == kSchedBalanced) {
+    const long long first = s_hit[1];  // = HZ * pre_b
+    sg.hz = (int)((target - first) / sg.n);
+    sg.off = first + (long long)sg.hz * sg.n;
+  } else {
+    // per-segment: units of earlier sequences are needed for the global offset, but
+    // only the segment's own range matters here; give it a private range
+    sg.hz = (int)(target - s_hit[1]);
+    sg.off = 0;
+    r.x0 = 0;
+    r.x1 = sg.n;
+  }
+  return r;
+}
+
+// Next segment after `s` (same sequence next head slice, or the next sequence).
+__device__ __forceinline__ bool next_segment(const DecodeParams& p, Segment& s) {
+  const int HZ = p.H_kv * p.n_z;
+  s.off += s.n;
+  if (s.hz + 1 < HZ) {
+    ++s.hz;
+    return true;
+  }
+  if (s.b + 1 >= p.B) return false;
+  ++s.b;
+  s.hz = 0;
+  s.seq = load_seq(p, s.b);
+  s.n = units_of(s.seq, p.P);
+  return true;
+}
+
+// Block whose balanced range holds global unit x: floor(((x+1) G - 1) / U).
+__device__ __forceinline__ long long block_of(long long x, long long U, long long G) {
+  return ((x + 1) * G - 1) / U;
+}
+
 // ---------------------------------------------------------------------------- finish
 // 2^x for the merge weights: fp32-accurate on the fp32 path, hardware ex2 otherwise.
 __device__ __forceinline__ float merge_exp2(const DecodeParams& p, float x) {
@@ -227,19 +299,24 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
   else reinterpret_cast<__half*>(p.out)[idx] = __float2half_rn(v);
 }
 
-// Merge the NWS warp states held in shared memory (sm_m/sm_d [NWS][8], sm_o
-// [NWS][8][D], unnormalised O, log2-unit m) and write the block's result for heads
-// [hq0, hq0+hcount).  A single-chunk sequence writes out/lse directly; otherwise the
-// block writes its partial (O/d, lse), and the last block of the sequence to finish
-// merges all partials of the sequence (S-way form of merge_state).
+// Finish this block's share [ua, ub) of segment `sg` (heads [hq0, hq0 + hcount)):
+// merge the NWS warp states in shared memory (sm_m/sm_d [NWS][8], sm_o [NWS][8][D],
+// unnormalised O, log2 m).  A whole segment writes out/lse; otherwise the block
+// writes its partial (O/d, lse) into slot 2c + side (side 0: the segment is this
+// block's first, 1: its last), adds its units to the segment's counter, and the block
+// that completes the count merges every partial of the segment (S-way merge_state).
+// Ends with a block barrier (shared memory is reusable afterwards).
 template <int NT, int NWS>
-__device__ void finish_block(const DecodeParams& p, const Work& w, int item, int hk, int z,
-                             int hq0, int hcount, const float* sm_m, const float* sm_d,
-                             const float* sm_o) {
+__device__ void finish_share(const DecodeParams& p, const BlockRange& br, const Segment& sg,
+                             int ua, int ub, int hq0, int hcount, const float* sm_m,
+                             const float* sm_d, const float* sm_o) {
   __shared__ int s_last;
   const int D = p.D;
   const int tid = threadIdx.x;
-  const bool split = w.nchunks > 1;
+  const bool whole = (ua == 0 && ub == sg.n);
+  const long long c = blockIdx.x;
+  const int side = (sg.off <= br.x0) ? 0 : 1;
+  const size_t slot = (size_t)(2 * c + side) * kMaxGroupPerCta;
   for (int idx = tid; idx < hcount * D; idx += NT) {
     const int j = idx / D, d = idx - j * D;
     float M = kEmptyM;
@@ -256,43 +333,57 @@ __device__ void finish_block(const DecodeParams& p, const Work& w, int item, int
     const float o = empty ? 0.f : num / den;
     const float l = empty ? kEmptyM : M + log2f(den);
     const int hq = hq0 + j;
-    if (!split) {
-      store_out(p, ((size_t)w.b * p.H_qo + hq) * D + d, o * p.out_scale);
-      if (d == 0) p.lse[(size_t)w.b * p.H_qo + hq] = l;
+    if (whole) {
+      store_out(p, ((size_t)sg.b * p.H_qo + hq) * D + d, o * p.out_scale);
+      if (d == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = l;
     } else {
-      p.part_o[((size_t)item * p.H_qo + hq) * D + d] = o;
-      if (d == 0) p.part_lse[(size_t)item * p.H_qo + hq] = l;
+      p.part_o[(slot + j) * D + d] = o;
+      if (d == 0) p.part_lse[slot + j] = l;
     }
   }
-  if (!split) return;
+  if (whole) {
+    __syncthreads();
+    return;
+  }
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    int* cnt = p.counters + ((size_t)w.b * p.H_kv + hk) * p.n_z + z;
-    const int prev = atomicAdd(cnt, 1);
-    s_last = (prev == w.nchunks - 1);
-    if (s_last) *cnt = 0;  // every other block of this sequence has arrived: reset for reuse
+    int* cnt = p.counters + (size_t)sg.b * p.H_kv * p.n_z + sg.hz;
+    const int mine = ub - ua;
+    const int prev = atomicAdd(cnt, mine);
+    s_last = (prev + mine == sg.n);
+    if (s_last) *cnt = 0;  // every other share of this segment has arrived: reset for reuse
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int idx = tid; idx < hcount * D; idx += NT) {
-    const int j = idx / D, d = idx - j * D;
-    const int hq = hq0 + j;
-    float M = kEmptyM;
-    for (int c = 0; c < w.nchunks; ++c)
-      M = fmaxf(M, __ldcg(p.part_lse + (size_t)(w.first_item + c) * p.H_qo + hq));
-    float den = 0.f, num = 0.f;
-    for (int c = 0; c < w.nchunks; ++c) {
-      const size_t it = (size_t)(w.first_item + c);
-      const float a = merge_exp2(p, __ldcg(p.part_lse + it * p.H_qo + hq) - M);
-      den += a;
-      num += a * __ldcg(p.part_o + (it * p.H_qo + hq) * D + d);
+  if (s_last) {
+    __threadfence();
+    const long long G = gridDim.x;
+    const long long c0 = block_of(sg.off, br.U, G), c1 = block_of(sg.off + sg.n - 1, br.U, G);
+    for (int idx = tid; idx < hcount * D; idx += NT) {
+      const int j = idx / D, d = idx - j * D;
+      const int hq = hq0 + j;
+      float M = kEmptyM;
+      for (long long cc = c0; cc <= c1; ++cc) {
+        const long long x0c = cc * br.U / G;
+        if ((cc + 1) * br.U / G <= x0c) continue;  // a block with no units wrote nothing
+        const size_t sl = (size_t)(2 * cc + (sg.off <= x0c ? 0 : 1)) * kMaxGroupPerCta;
+        M = fmaxf(M, __ldcg(p.part_lse + sl + j));
+      }
+      float den = 0.f, num = 0.f;
+      for (long long cc = c0; cc <= c1; ++cc) {
+        const long long x0c = cc * br.U / G;
+        if ((cc + 1) * br.U / G <= x0c) continue;
+        const size_t sl = (size_t)(2 * cc + (sg.off <= x0c ? 0 : 1)) * kMaxGroupPerCta;
+        const float a = merge_exp2(p, __ldcg(p.part_lse + sl + j) - M);
+        den += a;
+        num += a * __ldcg(p.part_o + (sl + j) * D + d);
+      }
+      const bool empty = !(M > kEmptyM);
+      store_out(p, ((size_t)sg.b * p.H_qo + hq) * D + d, empty ? 0.f : num / den * p.out_scale);
+      if (d == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = empty ? kEmptyM : M + log2f(den);
     }
-    const bool empty = !(M > kEmptyM);
-    store_out(p, ((size_t)w.b * p.H_qo + hq) * D + d, empty ? 0.f : num / den * p.out_scale);
-    if (d == 0) p.lse[(size_t)w.b * p.H_qo + hq] = empty ? kEmptyM : M + log2f(den);
   }
+  __syncthreads();
 }
 
 }  // namespace pd

@@ -64,8 +64,7 @@ extern "C" pd_status pd_batch_decode_paged_kv_noalloc(
   const size_t need = pd_workspace_size(desc);
   if (need > pd::kStaticScratchBytes) {
     pd::record_error("pd_batch_decode_paged_kv_noalloc: this batch needs more split scratch than the "
-                     "16 MiB static array holds; lower desc->num_splits (with max_kv_len_hint) or use "
-                     "pd_batch_decode_paged_kv");
+                     "16 MiB static array holds; lower desc->num_splits or use pd_batch_decode_paged_kv");
     return PD_ERR_WORKSPACE;
   }
   pd_decode_desc d = *desc;

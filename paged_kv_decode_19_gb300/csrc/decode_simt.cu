@@ -3,8 +3,8 @@
 // path would lose the 1e-5 accuracy the fp32 path keeps) and for shapes the MMA
 // kernel does not take.
 //
-// One block = one (work item, KV head, slice of <= 8 query heads).  Each warp walks
-// rows r0+w, r0+w+NW, ... of the item's chunk; a lane holds D/32 elements of a row:
+// A block walks its share of (sequence, KV head, slice of <= 8 query heads) segments
+// (see block_range); warps take groups of rows of a share; a lane holds D/32 elements of a row:
 // D/64 from each half, so a RoPE pair (d, d + D/2) sits in one lane.  Per row: the
 // q.k dot product is a warp sum, then the base-2 online softmax update of the TVM
 // `batch_decode_paged_kv` kernel (m, d, O) and the PV accumulate; the warps' states
@@ -49,14 +49,9 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
   __shared__ float sm_m[NW * 8], sm_d[NW * 8];
   __shared__ float sm_o[NW * 8 * D];
 
-  const int item = blockIdx.x, hk = blockIdx.y, z = blockIdx.z;
-  Work w;
-  if (!locate_item<NT>(p, item, w)) return;
+  const BlockRange br = block_range<NT>(p);
+  if (br.x0 >= br.x1) return;  // no units for this block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int hq0 = hk * p.group + z * kMaxGroupPerCta;
-  const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
-  const int r0 = w.chunk * p.chunk_rows;
-  const int r1 = (w.seq.L - r0 > p.chunk_rows) ? r0 + p.chunk_rows : w.seq.L;
   const int d0 = lane * H2, d1 = D / 2 + lane * H2;  // this lane's dims: [d0,d0+H2) and [d1,d1+H2)
 
   // rope frequencies of this lane
@@ -64,14 +59,35 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
 #pragma unroll
   for (int e = 0; e < H2; ++e) F[e] = p.rope_F[d0 + e];
 
+  // The block walks the segments (sequence, head slice) its unit range [x0, x1) touches;
+  // a share of pieces [ua, pend) is the contiguous attended-row range [r0, r1).
+  Segment sg = br.seg;
+  for (;;) {
+  const int ua = (int)max(br.x0 - sg.off, 0ll);
+  const int ub = (int)min(br.x1 - sg.off, (long long)sg.n);
+  const int hk = sg.hz / p.n_z, z = sg.hz - (sg.hz / p.n_z) * p.n_z;
+  const int hq0 = hk * p.group + z * kMaxGroupPerCta;
+  const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
+  int r0 = 0, r1 = 0;
+  if (sg.seq.L > 0) {
+    const Pieces pcs = make_pieces(0, sg.seq.L, sg.seq, p.P);
+    const int pend = min(ub, pcs.count());
+    if (pend > ua) {
+      const Piece first = get_piece(pcs, ua, p.P), last = get_piece(pcs, pend - 1, p.P);
+      r0 = first.r_lo;
+      r1 = last.r_lo + (last.s_hi - last.s_lo);
+    }
+  }
+  const SeqInfo& wseq = sg.seq;
+
   // Q rows of this block's heads, roped, in log2 units
   float q[kMaxGroupPerCta][E];
-  const int qpos = p.rotary ? p.q_rope_position[w.b] : 0;
+  const int qpos = p.rotary ? p.q_rope_position[sg.b] : 0;
 #pragma unroll
   for (int j = 0; j < kMaxGroupPerCta; ++j) {
     float a[H2], bb[H2];
     if (j < hcount) {
-      const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)w.b * p.H_qo + hq0 + j) * D;
+      const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + j) * D;
       RowHalf<QT, H2>::load(qrow + d0, a);
       RowHalf<QT, H2>::load(qrow + d1, bb);
     } else {
@@ -83,7 +99,8 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
       float x = a[e], y = bb[e];
       if (p.rotary) {
         float c, s;
-        rope_cos_sin_accurate(qpos, F[e], c, s);
+        if (std::is_same<KT, float>::value) rope_cos_sin_accurate(qpos, F[e], c, s);
+        else rope_cos_sin(qpos, F[e], c, s);
         const float xr = x * c - y * s, yr = y * c + x * s;
         x = xr;
         y = yr;
@@ -102,57 +119,92 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
     for (int e = 0; e < E; ++e) o[j][e] = 0.f;
   }
 
-  const int kpos0 = p.rotary ? p.k_rope_pos_offset[w.b] : 0;
+  const int kpos0 = p.rotary ? p.k_rope_pos_offset[sg.b] : 0;
   const KT* pages = reinterpret_cast<const KT*>(p.pages);
   const size_t kv_stride = (size_t)p.H_kv * p.P * D;  // K block -> V block of a page
-  for (int r = r0 + warp; r < r1; r += NW) {
-    const int so = r < w.seq.sink ? r : r - w.seq.sink + w.seq.win_off;
-    const int page = lookup_page(p, w.seq, so / p.P);
-    if (page < 0) continue;
-    const size_t kofs = (((size_t)page * 2 * p.H_kv + hk) * p.P + (so % p.P)) * D;
-    float k[E], v[E];
-    {
-      float ka[H2], kb[H2], va[H2], vb[H2];
-      RowHalf<KT, H2>::load(pages + kofs + d0, ka);
-      RowHalf<KT, H2>::load(pages + kofs + d1, kb);
-      RowHalf<KT, H2>::load(pages + kofs + kv_stride + d0, va);
-      RowHalf<KT, H2>::load(pages + kofs + kv_stride + d1, vb);
+  constexpr int R = 4;  // rows a warp loads before computing them (latency hiding)
+  for (int rbase = r0 + warp * R; rbase < r1; rbase += NW * R) {
+    float k[R][E], v[R][E];
+    bool ok[R];
 #pragma unroll
-      for (int e = 0; e < H2; ++e) {
-        float x = ka[e], y = kb[e];
-        if (p.rotary) {
-          float c, s;
-          rope_cos_sin_accurate(kpos0 + r, F[e], c, s);
-          const float xr = x * c - y * s, yr = y * c + x * s;
-          x = xr;
-          y = yr;
+    for (int u = 0; u < R; ++u) {
+      const int r = rbase + u;
+      ok[u] = false;
+#pragma unroll
+      for (int e = 0; e < E; ++e) k[u][e] = v[u][e] = 0.f;  // rows outside the share stay 0
+      if (r < r1) {
+        const int so = r < wseq.sink ? r : r - wseq.sink + wseq.win_off;
+        const int page = lookup_page(p, wseq, so / p.P);
+        if (page >= 0) {
+          ok[u] = true;
+          const size_t kofs = (((size_t)page * 2 * p.H_kv + hk) * p.P + (so % p.P)) * D;
+          float ka[H2], kb[H2], va[H2], vb[H2];
+          RowHalf<KT, H2>::load(pages + kofs + d0, ka);
+          RowHalf<KT, H2>::load(pages + kofs + d1, kb);
+          RowHalf<KT, H2>::load(pages + kofs + kv_stride + d0, va);
+          RowHalf<KT, H2>::load(pages + kofs + kv_stride + d1, vb);
+#pragma unroll
+          for (int e = 0; e < H2; ++e) {
+            k[u][e] = ka[e];
+            k[u][H2 + e] = kb[e];
+            v[u][e] = va[e];
+            v[u][H2 + e] = vb[e];
+          }
         }
-        k[e] = x;
-        k[H2 + e] = y;
-        v[e] = va[e];
-        v[H2 + e] = vb[e];
       }
     }
 #pragma unroll
+    for (int u = 0; u < R; ++u) {
+      if (ok[u] && p.rotary) {
+#pragma unroll
+        for (int e = 0; e < H2; ++e) {
+          float c, s;
+          if (std::is_same<KT, float>::value) rope_cos_sin_accurate(kpos0 + rbase + u, F[e], c, s);
+          else rope_cos_sin(kpos0 + rbase + u, F[e], c, s);
+          const float x = k[u][e], y = k[u][H2 + e];
+          k[u][e] = x * c - y * s;
+          k[u][H2 + e] = y * c + x * s;
+        }
+      }
+    }
+    // the group's scores, then one max / rescale for the group (the group's weights
+    // are independent of each other, so their exponentials overlap)
+#pragma unroll
     for (int j = 0; j < kMaxGroupPerCta; ++j) {
       if (j < hcount) {
-        float s = 0.f;
+        float sc[R];
+        float mg = m[j];
 #pragma unroll
-        for (int e = 0; e < E; ++e) s = fmaf(q[j][e], k[e], s);
-        s = warp_sum(s);
-        const float mn = fmaxf(m[j], s);
-        float a, pj;
-        if constexpr (std::is_same<KT, float>::value) {  // fp32 cache: fp32-accurate weights
-          a = (float)exp2((double)(m[j] - mn));
-          pj = (float)exp2((double)(s - mn));
-        } else {
-          a = fast_exp2(m[j] - mn);
-          pj = fast_exp2(s - mn);
+        for (int u = 0; u < R; ++u) {
+          float s = 0.f;
+#pragma unroll
+          for (int e = 0; e < E; ++e) s = fmaf(q[j][e], k[u][e], s);
+          s = warp_sum(s);
+          sc[u] = s;
+          if (ok[u]) mg = fmaxf(mg, s);
         }
-        dsum[j] = dsum[j] * a + pj;
+        float a, pw[R];
+        if constexpr (std::is_same<KT, float>::value) {  // fp32 cache: fp32-accurate weights
+          a = (float)exp2((double)(m[j] - mg));
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[j][e] = fmaf(pj, v[e], o[j][e] * a);
-        m[j] = mn;
+          for (int u = 0; u < R; ++u) pw[u] = ok[u] ? (float)exp2((double)(sc[u] - mg)) : 0.f;
+        } else {
+          a = fast_exp2(m[j] - mg);
+#pragma unroll
+          for (int u = 0; u < R; ++u) pw[u] = ok[u] ? fast_exp2(sc[u] - mg) : 0.f;
+        }
+        float dsum_g = 0.f;
+#pragma unroll
+        for (int u = 0; u < R; ++u) dsum_g += pw[u];
+        dsum[j] = dsum[j] * a + dsum_g;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+          float acc = o[j][e] * a;
+#pragma unroll
+          for (int u = 0; u < R; ++u) acc = fmaf(pw[u], v[u][e], acc);
+          o[j][e] = acc;
+        }
+        m[j] = mg;
       }
     }
   }
@@ -171,7 +223,9 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
     }
   }
   __syncthreads();
-  finish_block<NT, NW>(p, w, item, hk, z, hq0, hcount, sm_m, sm_d, sm_o);
+  finish_share<NT, NW>(p, br, sg, ua, ub, hq0, hcount, sm_m, sm_d, sm_o);
+  if (sg.off + sg.n >= br.x1 || !next_segment(p, sg)) break;
+  }  // segments
 }
 
 // ------------------------------------------------------------------------- dispatch

@@ -14,19 +14,19 @@ bool simt_supports(int q_dtype, int kv_dtype, int D);
 cudaError_t launch_decode_simt(const DecodeParams& p, int q_dtype, int kv_dtype, dim3 grid,
                                cudaStream_t st, int* ctas = nullptr);
 
-// Tensor-core decode (TMA page staging + mma.sync); see decode_mma.cuh for limits.
+// Tensor-core decode (register-direct page loads + mma.sync); see decode_mma.cuh.
 struct MmaConfig {
   int threads;       // block size
   int smem_bytes;    // dynamic shared memory
   int ctas_per_sm;   // occupancy (0 until queried)
 };
 // Launch (cfg == nullptr) or just query the launch configuration (cfg != nullptr).
-cudaError_t launch_mma_bf16(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
-                            cudaStream_t st, MmaConfig* cfg);
-cudaError_t launch_mma_f16(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
-                           cudaStream_t st, MmaConfig* cfg);
-cudaError_t launch_mma_fp8(const DecodeParams& p, const CUtensorMap& map, int q_dtype, dim3 grid,
-                           cudaStream_t st, MmaConfig* cfg);
+cudaError_t launch_mma_bf16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                           MmaConfig* cfg);
+cudaError_t launch_mma_f16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                           MmaConfig* cfg);
+cudaError_t launch_mma_fp8(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                           MmaConfig* cfg);
 
 // Sets the thread's last-error message (api.cu).
 void record_error(const char* msg);

@@ -9,8 +9,10 @@ import oracle
 from paged_kv_decode_19_gb300 import workloads as W
 
 # Tolerances (written here, used by every parity test):
-#   fp32       |gpu - ref| <= 1e-5 * (|ref| + 1e-2 * max|ref|)  (relative, with a floor
-#              for outputs near zero), lse |d| <= 1e-5 * max(1, |ref|)
+#   fp32       per (sequence, head) output vector: max_d |gpu - ref| <= 1e-5 * max_d |ref|
+#              (norm-wise relative error; elementwise relative error is ill-posed for
+#              components that are near-zero results of cancellation), lse |d| <= 1e-5 *
+#              max(1, |ref|)
 #   bf16/f16   max |out - ref| <= 2e-2, max |lse - ref| <= 2e-3 (log2 units)
 #   e4m3 KV    max |out - ref| <= 3e-2, max |lse - ref| <= 3e-2 vs the oracle on the
 #              dequantised cache
@@ -54,7 +56,8 @@ def compare(kind, out_gpu, lse_gpu, out_ref, lse_ref, mask=None):
     eo = np.abs(og - out_ref)
     el = np.abs(lg - lse_ref)
     if kind == "f32":
-        bound = 1e-5 * (np.abs(out_ref) + 1e-2 * np.abs(out_ref).max())
+        row_max = np.abs(out_ref).max(axis=-1, keepdims=True)
+        bound = 1e-5 * np.maximum(row_max, 1e-30)
         assert np.all(eo <= bound), f"fp32 out error {eo.max():.3e} (worst ratio {(eo / bound).max():.2f})"
         assert np.all(el <= 1e-5 * np.maximum(1.0, np.abs(lse_ref))), f"fp32 lse error {el.max():.3e}"
     else:

@@ -56,7 +56,7 @@ def _desc(**kw):
     (dict(H_qo=7), "PD_ERR_INVALID_ARG"), (dict(D=96), "PD_ERR_UNSUPPORTED"),
     (dict(page_size=0), "PD_ERR_INVALID_ARG"), (dict(q_dtype=3), "PD_ERR_INVALID_ARG"),
     (dict(out_dtype=3), "PD_ERR_INVALID_ARG"), (dict(kv_dtype=3, k_scale=0.0), "PD_ERR_INVALID_ARG"),
-    (dict(kv_dtype=1), "PD_ERR_UNSUPPORTED"), (dict(num_splits=4), "PD_ERR_INVALID_ARG"),
+    (dict(kv_dtype=1), "PD_ERR_UNSUPPORTED"), (dict(num_splits=-2), "PD_ERR_INVALID_ARG"),
     (dict(max_pages=0), "PD_ERR_INVALID_ARG"), (dict(B=-1), "PD_ERR_INVALID_ARG"),
 ])
 def test_decode_validation_without_gpu(L, bad, status):
@@ -89,22 +89,22 @@ def test_merge_and_append_validation_without_gpu(L):
 def test_planner_arithmetic(L):
     # llama3-8b-shaped decode: 32 sequences, 4608 pages of 16, 8 KV heads
     d = _desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, max_pages=16384)
-    chunk, items, ws = _lib.plan(d, 148, 3)
-    assert chunk % 16 == 0 and chunk >= 128
-    # every sequence fits: items >= sum over sequences of ceil(L/chunk) for any lengths
-    assert items >= (4608 * 16 + chunk - 1) // chunk
-    assert ws >= items * 32 * (128 + 1) * 4
-    # more resident blocks -> smaller chunks
-    assert _lib.plan(d, 148, 4)[0] <= chunk
-    # num_splits = 1: no split, no workspace
-    c1, i1, w1 = _lib.plan(_desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, num_splits=1), 148, 3)
-    assert c1 == 2**31 - 1 and i1 == 32 and w1 == 0
-    # explicit split count with a length hint
-    c2, i2, _ = _lib.plan(_desc(B=8, nnz_pages=40000, num_splits=32, max_kv_len_hint=131072), 148, 3)
-    assert c2 >= 131072 // 32 and i2 <= 8 * 32 + 8
-    # a length hint caps the grid
-    c3, i3, _ = _lib.plan(_desc(B=64, H_kv=4, H_qo=32, nnz_pages=64 * 640, max_kv_len_hint=4100), 148, 3)
-    assert i3 <= 64 * ((4100 + c3 - 1) // c3)
+    mode, grid, ws = _lib.plan(d, 148, 3)
+    assert mode == 0 and grid == 148 * 3  # balanced: one resident wave
+    # counters for 32 x 8 segments + two partial (lse, out[D]) slots per block
+    assert ws >= 32 * 8 * 4 + 2 * grid * 8 * (128 + 1) * 4
+    # num_splits = 1: one block per (sequence, head slice), no workspace
+    m1, g1, w1 = _lib.plan(_desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, num_splits=1), 148, 3)
+    assert m1 == 1 and g1 == 32 * 8 and w1 == 0
+    # group 16: two 8-head slices per KV head
+    m2, g2, _ = _lib.plan(_desc(B=4, H_qo=32, H_kv=2, nnz_pages=100, num_splits=1), 148, 3)
+    assert g2 == 4 * 2 * 2
+    # n > 1: about n blocks per segment, capped at 8 waves
+    _, g3, _ = _lib.plan(_desc(B=8, nnz_pages=40000, num_splits=32), 148, 3)
+    assert g3 == min(8 * 2 * 32, 8 * 148 * 3)
+    # tiny problems never get more blocks than work units
+    _, g4, _ = _lib.plan(_desc(B=2, H_qo=8, H_kv=2, nnz_pages=3), 148, 3)
+    assert g4 <= (3 + 2) * 2
 
 
 def test_python_binding_rejects_missing_library(tmp_path, monkeypatch):

@@ -61,14 +61,14 @@ def test_noalloc_matches_regular_entry_point_twice():
 
 def test_noalloc_rejects_scratch_beyond_its_maximum():
     L = _lib.lib()
-    # 1100 one-row sequences x 32 heads: at least one partial (out, lse) per sequence and
-    # head, ~20 MB of split scratch -- more than the 16 MiB array (the inputs are real,
-    # so even a wrongly accepted call would stay in bounds)
-    wl = W.make("llama3_8b_bf16", seed=22, reduced=True, B=1100, len_dist=("uniform", 1, 1),
-                pool=1200).to(DEV)
+    # 1100 sequences x 8 KV heads asked to split 64 ways: several thousand blocks, two
+    # partial (out, lse) slots each -- more than the 16 MiB array holds (the inputs are
+    # real, so even a wrongly accepted call would stay in bounds)
+    wl = W.make("llama3_8b_bf16", seed=22, reduced=True, B=1100, len_dist=("uniform", 1, 40),
+                pool=4000).to(DEV)
     out = torch.empty((wl.spec.B, wl.spec.H_qo, wl.spec.D), dtype=torch.bfloat16, device=DEV)
     lse = torch.empty((wl.spec.B, wl.spec.H_qo), dtype=torch.float32, device=DEV)
-    desc = _lib.make_desc(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info, out)
+    desc = _lib.make_desc(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info, out, num_splits=64)
     assert L.pd_workspace_size(ctypes.byref(desc)) > (16 << 20)
     st = _call(L.pd_batch_decode_paged_kv_noalloc, wl, out, lse, desc)
     assert _lib.STATUS[st] == "PD_ERR_WORKSPACE"
