@@ -40,7 +40,7 @@ struct DecodeParams {
   long long max_pages;
   int B, H_qo, H_kv, D, P, group, n_z;
   int window, rotary;
-  int precise;        // fp32 path: merge weights via double-precision exp2
+  int precise;        // fp32 path: merge weights via the accurate exp2f
   int mode;           // kSchedBalanced / kSchedPerSegment
   int out_dtype;
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
@@ -288,15 +288,157 @@ __device__ __forceinline__ long long block_of(long long x, long long U, long lon
 }
 
 // ---------------------------------------------------------------------------- finish
-// 2^x for the merge weights: fp32-accurate on the fp32 path, hardware ex2 otherwise.
+// 2^x for the merge weights: the accurate exp2f on the fp32 path, hardware ex2 otherwise.
 __device__ __forceinline__ float merge_exp2(const DecodeParams& p, float x) {
-  return p.precise ? (float)exp2((double)x) : fast_exp2(x);
+  return p.precise ? exp2f(x) : fast_exp2(x);
 }
 
 __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, float v) {
   if (p.out_dtype == kF32) reinterpret_cast<float*>(p.out)[idx] = v;
   else if (p.out_dtype == kBF16) reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
   else reinterpret_cast<__half*>(p.out)[idx] = __float2half_rn(v);
+}
+
+// Partial slot written by block cc for a segment whose first global unit is `off`,
+// or -1 when block cc's range is empty (it wrote nothing).
+__device__ __forceinline__ long long share_slot(long long cc, long long off, long long U,
+                                                long long G) {
+  const long long x0 = cc * U / G;
+  if ((cc + 1) * U / G <= x0) return -1;
+  return (2 * cc + (off <= x0 ? 0 : 1)) * kMaxGroupPerCta;
+}
+
+// Combine the partial states of every block holding units of segment `sg` into the
+// final out/lse (merge_state over S partials: lse = M + log2 sum_s 2^(lse_s - M),
+// out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M)).  Called by the block that
+// completed the segment's count.  All slots' lse are read in parallel (one slot per
+// thread), the weights go to shared memory, and each thread then sums its float4 of
+// (head, dims) over a chunk of slots with independent loads, so the merge costs a few
+// L2 round trips rather than one per slot.
+template <int NT>
+__device__ void merge_segment(const DecodeParams& p, const BlockRange& br, const Segment& sg,
+                              int hq0, int hcount) {
+  constexpr int G8 = kMaxGroupPerCta;
+  constexpr int kVec = G8 * 2 * kMaxHalfDim / 4 / NT;  // float4s per thread, at most
+  __shared__ float s_w[NT][G8];
+  __shared__ long long s_sl[NT];
+  __shared__ float s_red[NT / 32][G8];
+  __shared__ float s_M[G8], s_den[G8];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int D = p.D, D4 = D / 4;
+  const long long G = gridDim.x;
+  const long long c0 = block_of(sg.off, br.U, G);
+  const int ns = (int)(block_of(sg.off + sg.n - 1, br.U, G) - c0 + 1);
+  const long long sl0 = share_slot(c0, sg.off, br.U, G);  // block c0 always holds units
+  // pass 1: per-head maximum of the partial lse
+  float m[G8];
+#pragma unroll
+  for (int j = 0; j < G8; ++j) m[j] = kEmptyM;
+  for (int s = tid; s < ns; s += NT) {
+    const long long sl = share_slot(c0 + s, sg.off, br.U, G);
+    if (sl < 0) continue;
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
+    const float v[G8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < G8; ++j) m[j] = fmaxf(m[j], j < hcount ? v[j] : kEmptyM);
+  }
+#pragma unroll
+  for (int j = 0; j < G8; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m[j] = fmaxf(m[j], __shfl_xor_sync(0xffffffffu, m[j], o));
+    if (lane == 0) s_red[wid][j] = m[j];
+  }
+  __syncthreads();
+  if (tid < G8) {
+    float M = kEmptyM;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) M = fmaxf(M, s_red[w][tid]);
+    s_M[tid] = M;
+  }
+  __syncthreads();
+  float M[G8], den[G8];
+#pragma unroll
+  for (int j = 0; j < G8; ++j) {
+    M[j] = s_M[j];
+    den[j] = 0.f;
+  }
+  float4 acc[kVec > 0 ? kVec : 1];
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  // pass 2: weights of a chunk of NT slots, then the weighted sum of their outputs
+  for (int base = 0; base < ns; base += NT) {
+    const int s = base + tid;
+    if (s < ns) {
+      const long long sl = share_slot(c0 + s, sg.off, br.U, G);
+      float v[G8];
+      if (sl >= 0) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      }
+#pragma unroll
+      for (int j = 0; j < G8; ++j) {
+        const float w = (sl >= 0 && j < hcount) ? merge_exp2(p, v[j] - M[j]) : 0.f;
+        den[j] += w;
+        s_w[tid][j] = w;
+      }
+      s_sl[tid] = sl >= 0 ? sl : sl0;  // an empty block: weight 0 on a written slot
+    }
+    __syncthreads();
+    const int cnt = min(NT, ns - base);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) {
+      const int v = tid + e * NT;
+      if (v < hcount * D4) {
+        const int j = v / D4, d4 = v - j * D4;
+        float4 a = acc[e];
+#pragma unroll 8
+        for (int i = 0; i < cnt; ++i) {
+          const float w = s_w[i][j];
+          const float4 o = __ldcg(reinterpret_cast<const float4*>(p.part_o + (s_sl[i] + j) * D) + d4);
+          a.x += w * o.x;
+          a.y += w * o.y;
+          a.z += w * o.z;
+          a.w += w * o.w;
+        }
+        acc[e] = a;
+      }
+    }
+    __syncthreads();
+  }
+  // per-head sum of the weights
+#pragma unroll
+  for (int j = 0; j < G8; ++j) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den[j] += __shfl_xor_sync(0xffffffffu, den[j], o);
+    if (lane == 0) s_red[wid][j] = den[j];
+  }
+  __syncthreads();
+  if (tid < G8) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) t += s_red[w][tid];
+    s_den[tid] = t;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) {
+    const int v = tid + e * NT;
+    if (v < hcount * D4) {
+      const int j = v / D4, d4 = v - j * D4;
+      const int hq = hq0 + j;
+      const bool empty = !(s_M[j] > kEmptyM);
+      const float sc = empty ? 0.f : p.out_scale / s_den[j];
+      const size_t o = ((size_t)sg.b * p.H_qo + hq) * D + 4 * d4;
+      store_out(p, o + 0, acc[e].x * sc);
+      store_out(p, o + 1, acc[e].y * sc);
+      store_out(p, o + 2, acc[e].z * sc);
+      store_out(p, o + 3, acc[e].w * sc);
+      if (d4 == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = empty ? kEmptyM : s_M[j] + log2f(s_den[j]);
+    }
+  }
 }
 
 // Finish this block's share [ua, ub) of segment `sg` (heads [hq0, hq0 + hcount)):
@@ -357,31 +499,7 @@ __device__ void finish_share(const DecodeParams& p, const BlockRange& br, const 
   __syncthreads();
   if (s_last) {
     __threadfence();
-    const long long G = gridDim.x;
-    const long long c0 = block_of(sg.off, br.U, G), c1 = block_of(sg.off + sg.n - 1, br.U, G);
-    for (int idx = tid; idx < hcount * D; idx += NT) {
-      const int j = idx / D, d = idx - j * D;
-      const int hq = hq0 + j;
-      float M = kEmptyM;
-      for (long long cc = c0; cc <= c1; ++cc) {
-        const long long x0c = cc * br.U / G;
-        if ((cc + 1) * br.U / G <= x0c) continue;  // a block with no units wrote nothing
-        const size_t sl = (size_t)(2 * cc + (sg.off <= x0c ? 0 : 1)) * kMaxGroupPerCta;
-        M = fmaxf(M, __ldcg(p.part_lse + sl + j));
-      }
-      float den = 0.f, num = 0.f;
-      for (long long cc = c0; cc <= c1; ++cc) {
-        const long long x0c = cc * br.U / G;
-        if ((cc + 1) * br.U / G <= x0c) continue;
-        const size_t sl = (size_t)(2 * cc + (sg.off <= x0c ? 0 : 1)) * kMaxGroupPerCta;
-        const float a = merge_exp2(p, __ldcg(p.part_lse + sl + j) - M);
-        den += a;
-        num += a * __ldcg(p.part_o + (sl + j) * D + d);
-      }
-      const bool empty = !(M > kEmptyM);
-      store_out(p, ((size_t)sg.b * p.H_qo + hq) * D + d, empty ? 0.f : num / den * p.out_scale);
-      if (d == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = empty ? kEmptyM : M + log2f(den);
-    }
+    merge_segment<NT>(p, br, sg, hq0, hcount);
   }
   __syncthreads();
 }

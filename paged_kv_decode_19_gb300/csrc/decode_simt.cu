@@ -169,42 +169,56 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
     }
     // the group's scores, then one max / rescale for the group (the group's weights
     // are independent of each other, so their exponentials overlap)
+    float sc[kMaxGroupPerCta][R], mg[kMaxGroupPerCta];
 #pragma unroll
     for (int j = 0; j < kMaxGroupPerCta; ++j) {
-      if (j < hcount) {
-        float sc[R];
-        float mg = m[j];
+      mg[j] = m[j];
 #pragma unroll
-        for (int u = 0; u < R; ++u) {
-          float s = 0.f;
+      for (int u = 0; u < R; ++u) {
+        float s = 0.f;
+        if (j < hcount) {
 #pragma unroll
           for (int e = 0; e < E; ++e) s = fmaf(q[j][e], k[u][e], s);
           s = warp_sum(s);
-          sc[u] = s;
-          if (ok[u]) mg = fmaxf(mg, s);
         }
-        float a, pw[R];
-        if constexpr (std::is_same<KT, float>::value) {  // fp32 cache: fp32-accurate weights
-          a = (float)exp2((double)(m[j] - mg));
+        sc[j][u] = s;
+        if (ok[u]) mg[j] = fmaxf(mg[j], s);
+      }
+    }
+    // weights: w[j][u] = 2^(s - mg) for the rows, w[j][R] = 2^(m - mg) rescales the state
+    float w[kMaxGroupPerCta][R + 1];
+    if constexpr (std::is_same<KT, float>::value) {
+      // fp32 cache: the accurate exp2f (hardware ex2 is a few ulp short of fp32)
 #pragma unroll
-          for (int u = 0; u < R; ++u) pw[u] = ok[u] ? (float)exp2((double)(sc[u] - mg)) : 0.f;
-        } else {
-          a = fast_exp2(m[j] - mg);
+      for (int j = 0; j < kMaxGroupPerCta; ++j) {
 #pragma unroll
-          for (int u = 0; u < R; ++u) pw[u] = ok[u] ? fast_exp2(sc[u] - mg) : 0.f;
-        }
+        for (int u = 0; u < R; ++u) w[j][u] = ok[u] ? exp2f(sc[j][u] - mg[j]) : 0.f;
+        w[j][R] = exp2f(m[j] - mg[j]);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kMaxGroupPerCta; ++j) {
+#pragma unroll
+        for (int u = 0; u < R; ++u) w[j][u] = ok[u] ? fast_exp2(sc[j][u] - mg[j]) : 0.f;
+        w[j][R] = fast_exp2(m[j] - mg[j]);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxGroupPerCta; ++j) {
+      if (j < hcount) {
+        const float a = w[j][R];
         float dsum_g = 0.f;
 #pragma unroll
-        for (int u = 0; u < R; ++u) dsum_g += pw[u];
+        for (int u = 0; u < R; ++u) dsum_g += w[j][u];
         dsum[j] = dsum[j] * a + dsum_g;
 #pragma unroll
         for (int e = 0; e < E; ++e) {
           float acc = o[j][e] * a;
 #pragma unroll
-          for (int u = 0; u < R; ++u) acc = fmaf(pw[u], v[u][e], acc);
+          for (int u = 0; u < R; ++u) acc = fmaf(w[j][u], v[u][e], acc);
           o[j][e] = acc;
         }
-        m[j] = mg;
+        m[j] = mg[j];
       }
     }
   }
