@@ -108,31 +108,40 @@ static pd_status validate_desc(const pd_decode_desc* d) {
 }
 
 // ---------------------------------------------------------------------------- planner
-// Schedule, grid and workspace for `desc`.  *mode: kSchedBalanced or kSchedPerSegment;
-// *grid: blocks; workspace = per-segment counters + two partial slots per block.
-static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int* mode,
+// Schedule, grid and workspace for `desc` with `wpb` independent workers per block
+// (the tensor-core kernel's warps, or 1 for the SIMT kernel's blocks).  *mode:
+// kSchedBalanced or kSchedPerSegment; *grid: blocks; workspace = per-segment arrival
+// counters + two partial (lse, out) slots per worker.
+static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int wpb, int* mode,
                       int* grid, size_t* ws_bytes) {
   const int group = d->H_qo / d->H_kv;
   const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
   const long long segments = (long long)d->B * d->H_kv * n_z;
   const long long wave = (long long)std::max(num_sms, 1) * std::max(ctas_per_sm, 1);
+  wpb = std::max(wpb, 1);
   long long g;
   int m;
   if (d->num_splits == 1 || d->B == 0) {
     m = kSchedPerSegment;
-    g = segments;
+    g = (segments + wpb - 1) / wpb;
   } else {
     m = kSchedBalanced;
     // upper bound on work units (pages touched per segment, plus one per sequence)
     const long long units = ((long long)d->nnz_pages + d->B) * d->H_kv * n_z;
-    g = d->num_splits > 1 ? std::min(segments * d->num_splits, wave * kMaxWaves) : wave;
-    g = std::max(1ll, std::min(g, units));
+    if (d->num_splits > 1) {
+      const long long workers = std::min(segments * d->num_splits, wave * kMaxWaves * wpb);
+      g = (workers + wpb - 1) / wpb;
+    } else {
+      g = wave;
+    }
+    g = std::max(1ll, std::min(g, (units + wpb - 1) / wpb));
   }
   size_t ws = 0;
   if (m == kSchedBalanced) {
+    const size_t slots = (size_t)2 * g * wpb;
     ws = align_up((size_t)segments * sizeof(int), kWsAlign) +
-         align_up((size_t)2 * g * kMaxGroupPerCta * sizeof(float), kWsAlign) +
-         align_up((size_t)2 * g * kMaxGroupPerCta * d->D * sizeof(float), kWsAlign);
+         align_up(slots * kMaxGroupPerCta * sizeof(float), kWsAlign) +
+         align_up(slots * kMaxGroupPerCta * d->D * sizeof(float), kWsAlign);
   }
   *mode = m;
   *grid = (int)std::min<long long>(g, INT_MAX);
@@ -184,7 +193,8 @@ pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_
   pd_status st = validate_desc(desc);
   if (st != PD_OK) return st;
   if (!schedule || !grid_blocks || !workspace_bytes) return fail(PD_ERR_INVALID_ARG, "NULL output");
-  plan_impl(desc, num_sms, ctas_per_sm, schedule, grid_blocks, workspace_bytes);
+  plan_impl(desc, num_sms, ctas_per_sm, mma_path(desc, nullptr) ? kMmaWarps : 1, schedule,
+            grid_blocks, workspace_bytes);
   return PD_OK;
 }
 
@@ -221,7 +231,7 @@ size_t pd_workspace_size(const pd_decode_desc* desc) {
       if (occupancy_for(desc, mma != 0, rot, &ctas) != PD_OK) continue;
       int mode, grid;
       size_t ws;
-      plan_impl(desc, ds->num_sms, ctas, &mode, &grid, &ws);
+      plan_impl(desc, ds->num_sms, ctas, mma ? kMmaWarps : 1, &mode, &grid, &ws);
       best = std::max(best, ws);
     }
   }
@@ -269,14 +279,15 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   if (st != PD_OK) return st;
   int mode = 0, grid_blocks = 0;
   size_t ws_need = 0;
-  plan_impl(desc, ds->num_sms, ctas, &mode, &grid_blocks, &ws_need);
+  const int wpb = use_mma ? kMmaWarps : 1;
+  plan_impl(desc, ds->num_sms, ctas, wpb, &mode, &grid_blocks, &ws_need);
   if (grid_blocks == 0) return PD_OK;
 
   cudaStream_t s = (cudaStream_t)stream;
   const int group = d.H_qo / d.H_kv;
   const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
   const size_t cnt_bytes = align_up((size_t)d.B * d.H_kv * n_z * sizeof(int), kWsAlign);
-  const size_t lse_bytes = align_up((size_t)2 * grid_blocks * kMaxGroupPerCta * sizeof(float), kWsAlign);
+  const size_t lse_bytes = align_up((size_t)2 * grid_blocks * wpb * kMaxGroupPerCta * sizeof(float), kWsAlign);
   int* counters = nullptr;
   char* partials = nullptr;
   if (ws_need) {
@@ -356,6 +367,7 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.rotary = rotary_mode;
   p.mode = mode;
   p.out_dtype = d.out_dtype;
+  p.out_vec16 = (reinterpret_cast<uintptr_t>(output) % 16) == 0 ? 1 : 0;
   const double log2e = 1.4426950408889634073599246810019;
   const double kdeq = d.kv_dtype == kE4M3 ? (double)d.k_scale : 1.0;
   p.score_scale = (float)((double)sm_scale * log2e * kdeq);

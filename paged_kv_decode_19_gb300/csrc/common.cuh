@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <climits>
 #include <stdint.h>
 
 namespace pd {
@@ -126,6 +127,12 @@ __device__ __forceinline__ void rope_cos_sin_accurate(int pos, unsigned long lon
 }
 
 // ----------------------------------------------------------------------------- error word
+// Prefetch `bytes` (a multiple of 16) of global memory from a 16-byte aligned address
+// into L2 (bulk async prefetch; no completion to wait for).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }

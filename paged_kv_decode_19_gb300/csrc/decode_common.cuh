@@ -16,6 +16,7 @@ namespace pd {
 
 constexpr int kMaxGroupPerCta = 8;  // query heads one block serves at a time (a z-slice)
 constexpr int kMaxHalfDim = 128;    // D <= 256
+constexpr int kMmaWarps = 4;        // warps (independent workers) per tensor-core block
 
 // Block schedules (DecodeParams::mode)
 enum : int {
@@ -43,6 +44,7 @@ struct DecodeParams {
   int precise;        // fp32 path: merge weights via the accurate exp2f
   int mode;           // kSchedBalanced / kSchedPerSegment
   int out_dtype;
+  int out_vec16;      // out is 16-byte aligned (vector stores of whole runs)
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
   float q_prescale;   // split-operand MMA path: Q is pre-multiplied by this
   float out_scale;    // applied to the final output (v_scale for e4m3 KV)
@@ -282,9 +284,120 @@ __device__ __forceinline__ bool next_segment(const DecodeParams& p, Segment& s) 
   return true;
 }
 
-// Block whose balanced range holds global unit x: floor(((x+1) G - 1) / U).
-__device__ __forceinline__ long long block_of(long long x, long long U, long long G) {
+// Share (block or worker) whose balanced range holds global unit x, with G shares:
+// floor(((x+1) G - 1) / U).
+__device__ __forceinline__ long long share_of(long long x, long long U, long long G) {
   return ((x + 1) * G - 1) / U;
+}
+
+// ---------------------------------------------------------------------------- workers
+// Independent workers (warps of the tensor-core kernel): worker w = block * WPB + i.
+// Balanced schedule: worker w takes units [floor(w U / W), floor((w+1) U / W)) with
+// W = gridDim.x * WPB.  Per-segment schedule: worker w takes segment w whole.
+struct WorkerStart {
+  long long x0, x1, U;  // unit range (per-segment: [0, huge) of the segment), total units
+  long long off;        // first global unit of the segment holding x0
+  int b, hz;            // that segment; b < 0: this worker has no work
+};
+
+// Block-wide (ends with a block barrier): the start of each of the block's WPB workers.
+template <int NT, int WPB>
+__device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws) {
+  __shared__ long long s_warp[NT / 32];
+  __shared__ long long s_hit[WPB][2];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int HZ = p.H_kv * p.n_z;
+  const long long W = (long long)gridDim.x * WPB;
+  const long long w_first = (long long)blockIdx.x * WPB;
+  if (p.mode != kSchedBalanced) {
+    if (tid < WPB) {
+      const long long w = w_first + tid;
+      WorkerStart s;
+      s.U = (long long)p.B * HZ;
+      s.off = 0;
+      s.x0 = 0;
+      s.hz = 0;
+      s.b = -1;
+      s.x1 = 0;
+      if (w < s.U) {
+        s.b = (int)(w / HZ);
+        s.hz = (int)(w - (long long)s.b * HZ);
+        s.x1 = LLONG_MAX;
+      }
+      s_ws[tid] = s;
+    }
+    __syncthreads();
+    return;
+  }
+  // pass 1: total units
+  long long total = 0;
+  for (int start = 0; start < p.B; start += NT) {
+    const int b = start + tid;
+    long long n = b < p.B ? units_of(load_seq(p, b), p.P) : 0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    if (lane == 0) s_warp[wid] = n;
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < NT / 32; ++i) total += s_warp[i];
+    __syncthreads();
+  }
+  const long long U = total * HZ;
+  if (tid < WPB) s_hit[tid][0] = -1;
+  __syncthreads();
+  // pass 2: the sequence holding each worker's first unit
+  long long base = 0;
+  for (int start = 0; start < p.B; start += NT) {
+    const int b = start + tid;
+    const long long n = b < p.B ? (long long)units_of(load_seq(p, b), p.P) * HZ : 0;
+    long long incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s_warp[wid] = incl;
+    __syncthreads();
+    long long wbase = 0, tot = 0;
+#pragma unroll
+    for (int i = 0; i < NT / 32; ++i) {
+      const long long v = s_warp[i];
+      if (i < wid) wbase += v;
+      tot += v;
+    }
+    incl += wbase;
+    const long long lo = base + incl - n, hi = base + incl;
+#pragma unroll
+    for (int i = 0; i < WPB; ++i) {
+      const long long t = (w_first + i) * U / W;
+      if (b < p.B && t >= lo && t < hi) {
+        s_hit[i][0] = b;
+        s_hit[i][1] = lo;  // = HZ * (units of the sequences before b)
+      }
+    }
+    base += tot;
+    __syncthreads();
+  }
+  if (tid < WPB) {
+    const long long w = w_first + tid;
+    WorkerStart s;
+    s.U = U;
+    s.x0 = w * U / W;
+    s.x1 = (w + 1) * U / W;
+    s.b = (int)s_hit[tid][0];
+    s.hz = 0;
+    s.off = 0;
+    if (s.x0 >= s.x1 || s.b < 0) {
+      s.b = -1;
+      s.x1 = s.x0;
+    } else {
+      const int n = units_of(load_seq(p, s.b), p.P);
+      s.hz = (int)((s.x0 - s_hit[tid][1]) / n);
+      s.off = s_hit[tid][1] + (long long)s.hz * n;
+    }
+    s_ws[tid] = s;
+  }
+  __syncthreads();
 }
 
 // ---------------------------------------------------------------------------- finish
@@ -327,8 +440,8 @@ __device__ void merge_segment(const DecodeParams& p, const BlockRange& br, const
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int D = p.D, D4 = D / 4;
   const long long G = gridDim.x;
-  const long long c0 = block_of(sg.off, br.U, G);
-  const int ns = (int)(block_of(sg.off + sg.n - 1, br.U, G) - c0 + 1);
+  const long long c0 = share_of(sg.off, br.U, G);
+  const int ns = (int)(share_of(sg.off + sg.n - 1, br.U, G) - c0 + 1);
   const long long sl0 = share_slot(c0, sg.off, br.U, G);  // block c0 always holds units
   // pass 1: per-head maximum of the partial lse
   float m[G8];

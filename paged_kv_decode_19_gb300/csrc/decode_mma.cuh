@@ -1,13 +1,20 @@
 // Tensor-core decode kernel for 16-bit and FP8 KV caches (sm_103a).
 //
-// Block = one (work item, KV head, slice of <= 8 query heads): up to 8 query heads
-// that share one KV head, over one chunk of a sequence's attended rows; every K/V
-// byte of the chunk is read once per block.
+// Work split: the attended pages of every segment (sequence, KV head, slice of <= 8
+// query heads that share the KV head) form one list of U units (pages), cut into W
+// equal contiguous ranges, one per warp (W = blocks x 4).  Each warp is an independent
+// worker: it walks the segments its range touches, streams their pages in order and
+// finishes each segment on its own -- a segment it covers whole is written straight
+// to out/lse; otherwise it leaves a partial state (normalised O, lse) in one of its two
+// slots, and the worker that completes the segment's page count merges the slots
+// (merge_state over S partials).  Apart from the start-up scan that finds each
+// worker's first segment there is no block-wide barrier, so a worker switching
+// segments or merging never stalls the other warps of its block.
 //
-// Every warp streams its own 16-row tiles (one page = P/16 tiles; pages go to the
-// warps round-robin) straight from HBM into registers with 16-byte loads: on GB300
-// this gathers scattered 4 KB page blocks faster than TMA, bulk copies or cp.async
-// staging (see profiles/page_gather_probe.md).  The loads are laid out so that the
+// Every warp streams its 16-row tiles straight from HBM into registers with 16-byte
+// loads (on GB300 this gathers scattered 4 KB page blocks faster than TMA, bulk copies
+// or cp.async staging; see profiles/page_gather_probe.md), and prefetches the K and V
+// blocks of the pages a few pieces ahead into L2.  The loads are laid out so that the
 // registers already are mma.sync fragments:
 //   - S^T = K Q^T (m16n8k16, fp32 accumulate): A = the K tile (16 rows x 16 dims per
 //     k-tile), B = Q^T with the <= 8 query heads of the KV group as the n dimension.
@@ -16,13 +23,14 @@
 //   - online base-2 softmax on the accumulator fragments (TVM `batch_decode_paged_kv`:
 //     running max m, sum d, output O), P^T rebuilt as a B fragment with 4 shuffles;
 //   - O^T += V^T P^T: A = V^T built from 16-byte row loads with byte permutes (the
-//     output dims are permuted and written back in order at the end).
+//     output dims are permuted; each thread ends up with whole runs of 8 or 16
+//     consecutive output dims, stored with 16-byte stores).
 // The next tile's K loads are issued right after QK and its V loads right after PV,
-// so each warp keeps about one tile in flight while it computes.
+// so each warp keeps about one tile in registers in flight while it computes.
 // RoPE (rotate-half) is applied to K in registers before the MMA; rotated K and Q are
 // split into hi + lo 16-bit parts so the products keep ~16 mantissa bits.  FP8 codes
 // become f16 in registers (exact); k_scale folds into the score scale, v_scale into
-// the output.  The warps' states are merged at the end (finish_block).
+// the output.
 //
 // Limits: head dim 64/128 for 16-bit KV, 128 for FP8; page size a multiple of 16.
 #pragma once
@@ -32,7 +40,18 @@
 
 namespace pd {
 
-constexpr int kMmaWarps = 4;
+#ifndef PD_PREFETCH_PIECES
+#define PD_PREFETCH_PIECES 3
+#endif
+constexpr int kPrefetchPieces = PD_PREFETCH_PIECES;  // L2 prefetch distance, in pages
+#ifndef PD_MIN_BLOCKS_PLAIN
+#define PD_MIN_BLOCKS_PLAIN 1
+#endif
+// resident blocks per SM the register allocation targets (no-RoPE / RoPE kernels)
+template <bool ROPE>
+struct MinBlocks {
+  static constexpr int v = ROPE ? 1 : PD_MIN_BLOCKS_PLAIN;
+};
 
 template <typename KVT, typename QT, int D, bool ROPE>
 struct MmaTraits {
@@ -68,8 +87,142 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// Store a run of RL consecutive output dims of one (sequence, head) row.
+template <int RL>
+__device__ __forceinline__ void store_run(const DecodeParams& p, size_t idx, const float* v) {
+  if (p.out_vec16) {
+    if (p.out_dtype == kF32) {
+      float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + idx);
+#pragma unroll
+      for (int i = 0; i < RL / 4; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+      uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.out) + idx);
+#pragma unroll
+      for (int i = 0; i < RL / 8; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          w[k] = p.out_dtype == kBF16 ? pack2<__nv_bfloat16>(v[8 * i + 2 * k], v[8 * i + 2 * k + 1])
+                                      : pack2<__half>(v[8 * i + 2 * k], v[8 * i + 2 * k + 1]);
+        o[i] = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < RL; ++i) store_out(p, idx + i, v[i]);
+  }
+}
+
+// Merge of every worker's partial state of segment `sg` (worker count W, U units) into
+// out/lse by one warp: lse = M + log2 sum_s 2^(lse_s - M), out = sum_s 2^(lse_s - M) o_s
+// / sum_s 2^(lse_s - M).  Slot lse values are read one slot per lane; each lane then
+// sums its float4s of (head, dims) over the slots with independent loads.
+template <int D>
+__device__ void warp_merge(const DecodeParams& p, const Segment& sg, long long U, long long W,
+                           int hq0, int hcount, float (*s_w)[kMaxGroupPerCta], int* s_sl) {
+  constexpr int G8 = kMaxGroupPerCta;
+  constexpr int D4 = D / 4;
+  constexpr int kV = (G8 * D4 + 31) / 32;
+  const int lane = threadIdx.x & 31;
+  const long long w0 = share_of(sg.off, U, W);
+  const int ns = (int)(share_of(sg.off + sg.n - 1, U, W) - w0 + 1);
+  const long long sl0 = share_slot(w0, sg.off, U, W);  // worker w0 always holds units
+  float M[G8];
+#pragma unroll
+  for (int j = 0; j < G8; ++j) M[j] = kEmptyM;
+  for (int s = lane; s < ns; s += 32) {
+    const long long sl = share_slot(w0 + s, sg.off, U, W);
+    if (sl < 0) continue;
+    const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
+    const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
+    const float v[G8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < G8; ++j) M[j] = fmaxf(M[j], j < hcount ? v[j] : kEmptyM);
+  }
+#pragma unroll
+  for (int j = 0; j < G8; ++j)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(0xffffffffu, M[j], o));
+  float den[G8];
+#pragma unroll
+  for (int j = 0; j < G8; ++j) den[j] = 0.f;
+  float4 acc[kV];
+#pragma unroll
+  for (int e = 0; e < kV; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int base = 0; base < ns; base += 32) {
+    const int s = base + lane;
+    long long sl = -1;
+    float v[G8];
+#pragma unroll
+    for (int j = 0; j < G8; ++j) v[j] = kEmptyM;
+    if (s < ns) {
+      sl = share_slot(w0 + s, sg.off, U, W);
+      if (sl >= 0) {
+        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
+        const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < G8; ++j) {
+      const float w = (sl >= 0 && j < hcount) ? merge_exp2(p, v[j] - M[j]) : 0.f;
+      den[j] += w;
+      s_w[lane][j] = w;
+    }
+    s_sl[lane] = (int)(sl >= 0 ? sl : sl0);  // a worker with no units: weight 0, a written slot
+    __syncwarp();
+    const int cnt = min(32, ns - base);
+#pragma unroll 2
+    for (int i = 0; i < cnt; ++i) {
+      const float* po = p.part_o + (size_t)s_sl[i] * D;
+#pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        const int vi = lane + 32 * e;
+        if (vi < hcount * D4) {
+          const int j = vi / D4, d4 = vi - j * D4;
+          const float w = s_w[i][j];
+          const float4 o = __ldcg(reinterpret_cast<const float4*>(po + (size_t)j * D) + d4);
+          acc[e].x += w * o.x;
+          acc[e].y += w * o.y;
+          acc[e].z += w * o.z;
+          acc[e].w += w * o.w;
+        }
+      }
+    }
+    __syncwarp();
+  }
+#pragma unroll
+  for (int j = 0; j < G8; ++j)
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den[j] += __shfl_xor_sync(0xffffffffu, den[j], o);
+#pragma unroll
+  for (int e = 0; e < kV; ++e) {
+    const int vi = lane + 32 * e;
+    if (vi < hcount * D4) {
+      const int j = vi / D4, d4 = vi - j * D4;
+      float Mj = M[0], dj = den[0];
+#pragma unroll
+      for (int k = 1; k < G8; ++k)
+        if (k == j) {
+          Mj = M[k];
+          dj = den[k];
+        }
+      const bool empty = !(Mj > kEmptyM);
+      const float sc = empty ? 0.f : p.out_scale / dj;
+      const int hq = hq0 + j;
+      const size_t o = ((size_t)sg.b * p.H_qo + hq) * D + 4 * d4;
+      store_out(p, o + 0, acc[e].x * sc);
+      store_out(p, o + 1, acc[e].y * sc);
+      store_out(p, o + 2, acc[e].z * sc);
+      store_out(p, o + 3, acc[e].w * sc);
+      if (d4 == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = empty ? kEmptyM : Mj + log2f(dj);
+    }
+  }
+}
+
 template <typename KVT, typename QT, int D, bool ROPE, int NW>
-__global__ void __launch_bounds__(NW * 32)
+__global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = MmaTraits<KVT, QT, D, ROPE>;
   using MT = typename Tr::MT;
@@ -79,21 +232,15 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int KCH = Tr::kKCh;
   constexpr int VCH = Tr::kVCh;
   constexpr bool FP8 = Tr::kFp8;
-  __shared__ float sm_m[NW * 8], sm_d[NW * 8];
-  __shared__ float sm_o[NW * 8 * D];
-
-  const BlockRange br = block_range<NT>(p);
-  if (br.x0 >= br.x1) return;  // no units for this block
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int g_id = lane >> 2, q4 = lane & 3;
-  const int P = p.P;
-  const uint8_t* kv_base = reinterpret_cast<const uint8_t*>(p.pages);
-  const size_t block_bytes = (size_t)P * RB;                 // one (page, K|V, head) block
-  const size_t v_off = (size_t)p.H_kv * block_bytes;         // K block -> V block
-  __shared__ uint4 s_qf[KT][32];
+  constexpr int RL = FP8 ? 16 : 8;  // output run: consecutive dims a thread holds
+  constexpr int NR = 2 * KT / RL;   // runs per head and thread
+  __shared__ uint4 s_qf[NW][KT][32];                        // per-warp Q^T B fragments
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
   __shared__ float2 s_rot8[ROPE ? D / 2 : 1];               // e^(i * 8 * omega_f)
+  __shared__ WorkerStart s_start[NW];
+  __shared__ float s_mw[NW][32][kMaxGroupPerCta];           // per-warp merge weights
+  __shared__ int s_msl[NW][32];                             // per-warp merge slots
+
   if (ROPE) {
     for (int i = threadIdx.x; i < D / 2; i += NT) {
       const unsigned long long F = p.rope_F[i];
@@ -103,27 +250,133 @@ __global__ void __launch_bounds__(NW * 32)
       s_rot8[i] = make_float2(c8, s8);
     }
   }
+  worker_starts<NT, NW>(p, s_start);  // last block-wide barrier of the kernel
 
-  // The block walks the segments (sequence, head slice) its unit range [x0, x1) touches.
-  Segment sg = br.seg;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g_id = lane >> 2, q4 = lane & 3;
+  const WorkerStart ws = s_start[warp];
+  if (ws.b < 0) return;  // no units for this worker
+  const int P = p.P;
+  const uint8_t* kv_base = reinterpret_cast<const uint8_t*>(p.pages);
+  const size_t block_bytes = (size_t)P * RB;          // one (page, K|V, head) block
+  const size_t v_off = (size_t)p.H_kv * block_bytes;  // K block -> V block
+  const long long Wn = (long long)gridDim.x * NW;
+  const long long wid = (long long)blockIdx.x * NW + warp;
+
+  Segment sg;
+  sg.b = ws.b;
+  sg.hz = ws.hz;
+  sg.off = ws.off;
+  sg.seq = load_seq(p, sg.b);
+  sg.n = units_of(sg.seq, P);
+  const long long x1 = p.mode == kSchedBalanced ? ws.x1 : sg.off + sg.n;
+
+  // The worker walks the segments (sequence, head slice) its range [x0, x1) touches.
   for (;;) {
-  const int ua = (int)max(br.x0 - sg.off, 0ll);
-  const int ub = (int)min(br.x1 - sg.off, (long long)sg.n);
+  const int ua = (int)max(ws.x0 - sg.off, 0ll);
+  const int ub = (int)min(x1 - sg.off, (long long)sg.n);
   const int hk = sg.hz / p.n_z, z = sg.hz - (sg.hz / p.n_z) * p.n_z;
   const Pieces pcs = make_pieces(0, sg.seq.L, sg.seq, P);
   const int pend = min(ub, sg.seq.L > 0 ? pcs.count() : 0);  // pieces [ua, pend) here
   const int hq0 = hk * p.group + z * kMaxGroupPerCta;
   const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
 
+  // ---------------------------------------------------------------- tile stream
+  // Pieces [ua, pend) in order; their page ids are looked up 32 at a time (one per
+  // lane) and handed out with a shuffle.  A second cursor runs kPrefetchPieces pieces
+  // ahead and prefetches each page's K and V blocks into L2, so that the register loads
+  // of a tile mostly hit L2 and each warp keeps several pages in flight without
+  // spending registers on them.
+  struct Tile {
+    int piece, t, s_lo, s_hi, r_lo;
+    const uint8_t* kblk;  // K block of (page, hk); nullptr = no more tiles
+  };
+  struct PageBatch {
+    int base, page;  // pieces [base, base + 32): lane i holds the page of piece base + i
+  };
+  auto page_of = [&](PageBatch& pb, int j) -> int {  // j warp-uniform, ua <= j < pend
+    if (j >= pb.base + 32) {
+      pb.base = j;
+      const int jj = j + lane;
+      pb.page = jj < pend ? lookup_page(p, sg.seq, get_piece(pcs, jj, P).page_idx) : -1;
+    }
+    return __shfl_sync(0xffffffffu, pb.page, j - pb.base);
+  };
+  PageBatch pb_main{-64, -1}, pb_pf{-64, -1};
+  int pf_next = ua + 1;  // next piece to prefetch (the first is loaded straight away)
+  auto prefetch_to = [&](int jend) {  // prefetch pieces [pf_next, jend)
+    jend = min(jend, pend);
+    for (; pf_next < jend; ++pf_next) {
+      const int pg = page_of(pb_pf, pf_next);
+      if (pg >= 0 && lane == 0) {
+        const uint8_t* kb = kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes;
+        prefetch_l2_bulk(kb, (uint32_t)block_bytes);
+        prefetch_l2_bulk(kb + v_off, (uint32_t)block_bytes);
+      }
+    }
+  };
+  auto first_tile_from = [&](int j) -> Tile {  // first tile of piece j or later
+    Tile tl;
+    tl.kblk = nullptr;
+    for (; j < pend; ++j) {
+      const int pg = page_of(pb_main, j);
+      if (pg < 0) continue;  // bad page id: its rows are skipped (error already recorded)
+      const Piece pc = get_piece(pcs, j, P);
+      tl.piece = j;
+      tl.t = pc.s_lo >> 4;
+      tl.s_lo = pc.s_lo;
+      tl.s_hi = pc.s_hi;
+      tl.r_lo = pc.r_lo;
+      tl.kblk = kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes;
+      break;
+    }
+    prefetch_to(j + 1 + kPrefetchPieces);
+    return tl;
+  };
+  auto next_tile = [&](const Tile& c) -> Tile {
+    if ((c.t + 1) * 16 < c.s_hi) {
+      Tile n = c;
+      n.t = c.t + 1;
+      return n;
+    }
+    return first_tile_from(c.piece + 1);
+  };
+  uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
+  uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
+  auto load_k = [&](const Tile& c) {
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      const uint8_t* row = c.kblk + (size_t)(c.t * 16 + g_id + 8 * rr) * RB;
+#pragma unroll
+      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = ldg_stream(row + (4 * ch + q4) * 16);
+    }
+  };
+  auto load_v = [&](const Tile& c) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int slot = c.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
+      const uint8_t* row = c.kblk + v_off + (size_t)slot * RB;
+#pragma unroll
+      for (int j = 0; j < VCH; ++j) vr[i][j] = ldg_stream(row + (g_id + 8 * j) * 16);
+    }
+  };
+
+  // first tile's loads go out before the Q set-up, which then overlaps their latency
+  Tile cur = first_tile_from(ua);
+  if (cur.kblk) {
+    load_k(cur);
+    load_v(cur);
+  }
+
   // ---------------------------------------------------------------- Q^T B fragments
   // Per k-tile and lane: {hi b0, hi b1, lo b0, lo b1} with b0 = (k 2q..2q+1, head g_id),
-  // b1 = (k 2q+8..2q+9, head g_id) in the permuted dim order.  Built once per segment in
-  // shared memory (k-tile pairs kt / kt + KT/2 spread over the warps), read per k-tile.
+  // b1 = (k 2q+8..2q+9, head g_id) in the permuted dim order, in this warp's shared
+  // memory (k-tile pairs kt / kt + KT/2 together, for RoPE).
   {
     const bool have = g_id < hcount;
     const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have ? g_id : 0)) * D;
     const int qpos = ROPE ? p.q_rope_position[sg.b] : 0;
-    for (int kt = warp; kt < KT / 2; kt += NW) {
+    for (int kt = 0; kt < KT / 2; ++kt) {
       float qv[2][2][2];  // [pair member u: kt, kt + KT/2][half][e]
 #pragma unroll
       for (int u = 0; u < 2; ++u)
@@ -156,11 +409,11 @@ __global__ void __launch_bounds__(NW * 32)
             lo[h] = 0u;
           }
         }
-        s_qf[kt + u * (KT / 2)][lane] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+        s_qf[warp][kt + u * (KT / 2)][lane] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
       }
     }
   }
-  __syncthreads();
+  __syncwarp();
   const float post_scale = Tr::kQSplit ? 1.f : p.score_scale;
   const int kpos0 = ROPE ? p.k_rope_pos_offset[sg.b] : 0;
 
@@ -169,79 +422,13 @@ __global__ void __launch_bounds__(NW * 32)
 #pragma unroll
   for (int i = 0; i < KT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
-  // ---------------------------------------------------------------- tile stream
-  // This warp's pieces are warp, warp + NW, ...; their page ids are looked up 32 at
-  // a time (one per lane) and handed out with a shuffle.
-  struct Tile {
-    int piece, t, s_lo, s_hi, r_lo;
-    const uint8_t* kblk;  // K block of (page, hk); nullptr = no more tiles
-  };
-  const int my_pieces = pend - ua > warp ? (pend - ua - warp + NW - 1) / NW : 0;
-  int batch_base = -32, batch_page = -1;
-  auto page_for = [&](int j) -> int {  // j = index among this warp's pieces (warp-uniform)
-    if (j >= batch_base + 32) {
-      batch_base = j - (j % 32);
-      const int jj = batch_base + lane;
-      batch_page = jj < my_pieces ? lookup_page(p, sg.seq, get_piece(pcs, ua + warp + jj * NW, P).page_idx) : -1;
-    }
-    return __shfl_sync(0xffffffffu, batch_page, j - batch_base);
-  };
-  auto first_tile_from = [&](int j) -> Tile {  // first tile of this warp's piece j or later
-    Tile tl;
-    tl.kblk = nullptr;
-    for (; j < my_pieces; ++j) {
-      const int pg = page_for(j);
-      if (pg < 0) continue;  // bad page id: its rows are skipped (error already recorded)
-      const Piece pc = get_piece(pcs, ua + warp + j * NW, P);
-      tl.piece = j;
-      tl.t = pc.s_lo >> 4;
-      tl.s_lo = pc.s_lo;
-      tl.s_hi = pc.s_hi;
-      tl.r_lo = pc.r_lo;
-      tl.kblk = kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes;
-      break;
-    }
-    return tl;
-  };
-  auto next_tile = [&](const Tile& c) -> Tile {
-    if ((c.t + 1) * 16 < c.s_hi) {
-      Tile n = c;
-      n.t = c.t + 1;
-      return n;
-    }
-    return first_tile_from(c.piece + 1);
-  };
-  uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
-  uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
-  auto load_k = [&](const Tile& c) {
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      const uint8_t* row = c.kblk + (size_t)(c.t * 16 + g_id + 8 * rr) * RB;
-#pragma unroll
-      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = ldg_stream(row + (4 * ch + q4) * 16);
-    }
-  };
-  auto load_v = [&](const Tile& c) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int slot = c.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
-      const uint8_t* row = c.kblk + v_off + (size_t)slot * RB;
-#pragma unroll
-      for (int j = 0; j < VCH; ++j) vr[i][j] = ldg_stream(row + (g_id + 8 * j) * 16);
-    }
-  };
-
-  Tile cur = first_tile_from(0);
-  if (cur.kblk) {
-    load_k(cur);
-    load_v(cur);
-  }
   while (cur.kblk) {
     const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
     const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
     const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
     // ------------------------------------------------------------ S^T = K Q^T
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    // independent accumulators shorten the dependent MMA chain; summed after
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
     if constexpr (!ROPE) {
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
@@ -258,9 +445,9 @@ __global__ void __launch_bounds__(NW * 32)
           a[1] = comp(kr[1][kt >> 1], 2 * (kt & 1));
           a[3] = comp(kr[1][kt >> 1], 2 * (kt & 1) + 1);
         }
-        const uint4 qf = s_qf[kt][lane];
-        Mma<MT>::run(acc, a, qf.x, qf.y);
-        if (Tr::kQSplit) Mma<MT>::run(acc, a, qf.z, qf.w);
+        const uint4 qf = s_qf[warp][kt][lane];
+        Mma<MT>::run((kt & 1) ? acc1 : acc, a, qf.x, qf.y);
+        if (Tr::kQSplit) Mma<MT>::run(acc2, a, qf.z, qf.w);
       }
     } else {
       // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
@@ -309,13 +496,15 @@ __global__ void __launch_bounds__(NW * 32)
         }
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
-          const uint4 qf = s_qf[kt + u * (KT / 2)][lane];
+          const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
           Mma<MT>::run(acc, ahi[u], qf.x, qf.y);
-          Mma<MT>::run(acc, alo[u], qf.x, qf.y);
-          Mma<MT>::run(acc, ahi[u], qf.z, qf.w);
+          Mma<MT>::run(acc1, alo[u], qf.x, qf.y);
+          Mma<MT>::run(acc2, ahi[u], qf.z, qf.w);
         }
       }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] += acc1[i] + acc2[i];
     // K registers are free: start the next tile's K loads
     const Tile nxt = next_tile(cur);
     if (nxt.kblk) load_k(nxt);
@@ -401,24 +590,61 @@ __global__ void __launch_bounds__(NW * 32)
   st_d[0] = sum_over_groups(st_d[0]);
   st_d[1] = sum_over_groups(st_d[1]);
 
-  // ---------------------------------------------------------------- merge + finish
-  if (g_id == 0) {
-    sm_m[warp * 8 + 2 * q4] = st_m[0];
-    sm_m[warp * 8 + 2 * q4 + 1] = st_m[1];
-    sm_d[warp * 8 + 2 * q4] = st_d[0];
-    sm_d[warp * 8 + 2 * q4 + 1] = st_d[1];
-  }
+  // ---------------------------------------------------------------- finish the segment
+  // This thread holds heads 2q4 (c0, c2) and 2q4 + 1 (c1, c3); per head NR runs of RL
+  // consecutive dims: run r starts at dim 16 g_id (FP8) or 8 (g_id + 8 r).
+  const bool whole = (ua == 0 && ub == sg.n);
+  const size_t slot = (size_t)(2 * wid + (sg.off <= ws.x0 ? 0 : 1)) * kMaxGroupPerCta;
 #pragma unroll
-  for (int mt = 0; mt < KT; ++mt) {
-    const int dA = out_dim<FP8>(mt, g_id, 0), dB = out_dim<FP8>(mt, g_id, 1);
-    sm_o[(warp * 8 + 2 * q4) * D + dA] = oacc[mt][0];
-    sm_o[(warp * 8 + 2 * q4 + 1) * D + dA] = oacc[mt][1];
-    sm_o[(warp * 8 + 2 * q4) * D + dB] = oacc[mt][2];
-    sm_o[(warp * 8 + 2 * q4 + 1) * D + dB] = oacc[mt][3];
+  for (int hh = 0; hh < 2; ++hh) {
+    const int j = 2 * q4 + hh;
+    if (j < hcount) {
+      const bool empty = !(st_d[hh] > 0.f);
+      const float inv = empty ? 0.f : 1.f / st_d[hh];
+      const float l = empty ? kEmptyM : st_m[hh] + log2f(st_d[hh]);
+      const int hq = hq0 + j;
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const int d0 = FP8 ? 16 * g_id : 8 * (g_id + 8 * r);
+        float v[RL];
+#pragma unroll
+        for (int o = 0; o < RL; ++o) v[o] = oacc[r * (RL / 2) + (o >> 1)][hh + 2 * (o & 1)] * inv;
+        if (whole) {
+#pragma unroll
+          for (int o = 0; o < RL; ++o) v[o] *= p.out_scale;
+          store_run<RL>(p, ((size_t)sg.b * p.H_qo + hq) * D + d0, v);
+        } else {
+          float4* po = reinterpret_cast<float4*>(p.part_o + (slot + j) * D + d0);
+#pragma unroll
+          for (int i = 0; i < RL / 4; ++i) po[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
+      }
+      if (g_id == 0) {
+        if (whole) p.lse[(size_t)sg.b * p.H_qo + hq] = l;
+        else p.part_lse[slot + j] = l;
+      }
+    }
   }
-  __syncthreads();
-  finish_share<NT, NW>(p, br, sg, ua, ub, hq0, hcount, sm_m, sm_d, sm_o);
-  if (sg.off + sg.n >= br.x1 || !next_segment(p, sg)) break;
+  if (!whole) {
+    // publish the partial, count this worker's units; the worker completing the count
+    // merges every partial of the segment and resets the counter for the next call
+    __threadfence();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      int* cnt = p.counters + (size_t)sg.b * p.H_kv * p.n_z + sg.hz;
+      const int mine = ub - ua;
+      const int prev = atomicAdd(cnt, mine);
+      last = (prev + mine == sg.n);
+      if (last) *cnt = 0;
+    }
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __threadfence();
+      warp_merge<D>(p, sg, ws.U, Wn, hq0, hcount, s_mw[warp], s_msl[warp]);
+    }
+  }
+  if (sg.off + sg.n >= x1 || !next_segment(p, sg)) break;
   }  // segments
 }
 

@@ -87,24 +87,30 @@ def test_merge_and_append_validation_without_gpu(L):
 
 
 def test_planner_arithmetic(L):
-    # llama3-8b-shaped decode: 32 sequences, 4608 pages of 16, 8 KV heads
+    # llama3-8b-shaped bf16 decode: the tensor-core kernel, 4 independent workers (warps)
+    # per block
     d = _desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, max_pages=16384)
     mode, grid, ws = _lib.plan(d, 148, 3)
     assert mode == 0 and grid == 148 * 3  # balanced: one resident wave
-    # counters for 32 x 8 segments + two partial (lse, out[D]) slots per block
-    assert ws >= 32 * 8 * 4 + 2 * grid * 8 * (128 + 1) * 4
-    # num_splits = 1: one block per (sequence, head slice), no workspace
+    # counters for 32 x 8 segments + two partial (lse, out[D]) slots per worker
+    assert ws >= 32 * 8 * 4 + 2 * grid * 4 * 8 * (128 + 1) * 4
+    # num_splits = 1: one worker per (sequence, head slice), no workspace
     m1, g1, w1 = _lib.plan(_desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, num_splits=1), 148, 3)
-    assert m1 == 1 and g1 == 32 * 8 and w1 == 0
-    # group 16: two 8-head slices per KV head
+    assert m1 == 1 and g1 == 32 * 8 // 4 and w1 == 0
+    # group 16: two 8-head slices per KV head -> 16 segments -> 4 blocks of 4 workers
     m2, g2, _ = _lib.plan(_desc(B=4, H_qo=32, H_kv=2, nnz_pages=100, num_splits=1), 148, 3)
-    assert g2 == 4 * 2 * 2
-    # n > 1: about n blocks per segment, capped at 8 waves
+    assert g2 == (4 * 2 * 2) // 4
+    # n > 1: about n workers per segment (8 x 2 segments x 32), capped at 8 waves
     _, g3, _ = _lib.plan(_desc(B=8, nnz_pages=40000, num_splits=32), 148, 3)
-    assert g3 == min(8 * 2 * 32, 8 * 148 * 3)
-    # tiny problems never get more blocks than work units
+    assert g3 == min(8 * 2 * 32, 8 * 148 * 3 * 4) // 4
+    # an fp32 cache runs the SIMT kernel: one worker per block
+    _, g5, w5 = _lib.plan(_desc(B=8, nnz_pages=40000, num_splits=32, q_dtype=0, kv_dtype=0,
+                                out_dtype=0), 148, 3)
+    assert g5 == min(8 * 2 * 32, 8 * 148 * 3)
+    assert w5 >= 2 * g5 * 8 * (128 + 1) * 4
+    # tiny problems never get more workers than work units (rounded up to a block)
     _, g4, _ = _lib.plan(_desc(B=2, H_qo=8, H_kv=2, nnz_pages=3), 148, 3)
-    assert g4 <= (3 + 2) * 2
+    assert g4 <= -(-(3 + 2) * 2 // 4)
 
 
 def test_python_binding_rejects_missing_library(tmp_path, monkeypatch):
