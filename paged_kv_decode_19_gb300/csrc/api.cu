@@ -18,6 +18,12 @@ namespace pd {
 // per SM); an explicit split count n > 1 asks for about n blocks per (sequence, head
 // slice) segment, capped at kMaxWaves resident waves.
 constexpr int kMaxWaves = 8;
+#ifndef PD_SEG_COST_TILES
+#define PD_SEG_COST_TILES 4
+#endif
+// Cost of a segment's set-up and finish in the tensor-core schedule, in 16-row tiles
+// (measured: a warp crossing a segment boundary loses about 4-6 tiles' time).
+constexpr int kSegCostTiles = PD_SEG_COST_TILES;
 constexpr size_t kWsAlign = 256;
 
 static thread_local std::string t_last_error;
@@ -366,6 +372,9 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.window = d.sliding_window ? 1 : 0;
   p.rotary = rotary_mode;
   p.mode = mode;
+  // tensor-core schedule: a segment's set-up and finish cost about kSegCostTiles tiles
+  p.seg_cost = use_mma && mode == kSchedBalanced && kSegCostTiles > 0
+                   ? std::max(1, kSegCostTiles * 16 / d.page_size) : 0;
   p.out_dtype = d.out_dtype;
   p.out_vec16 = (reinterpret_cast<uintptr_t>(output) % 16) == 0 ? 1 : 0;
   const double log2e = 1.4426950408889634073599246810019;

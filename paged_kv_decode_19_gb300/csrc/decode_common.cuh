@@ -17,6 +17,7 @@ namespace pd {
 constexpr int kMaxGroupPerCta = 8;  // query heads one block serves at a time (a z-slice)
 constexpr int kMaxHalfDim = 128;    // D <= 256
 constexpr int kMmaWarps = 4;        // warps (independent workers) per tensor-core block
+constexpr int kStartCacheB = 1024;  // batch sizes whose start-up scan runs in shared memory
 
 // Block schedules (DecodeParams::mode)
 enum : int {
@@ -43,6 +44,8 @@ struct DecodeParams {
   int window, rotary;
   int precise;        // fp32 path: merge weights via the accurate exp2f
   int mode;           // kSchedBalanced / kSchedPerSegment
+  int seg_cost;       // worker schedule: extra cost units charged per segment (its set-up
+                      // and finish), so ranges that cross segment boundaries get fewer pages
   int out_dtype;
   int out_vec16;      // out is 16-byte aligned (vector stores of whole runs)
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
@@ -268,10 +271,11 @@ __device__ BlockRange block_range(const DecodeParams& p) {
   return r;
 }
 
-// Next segment after `s` (same sequence next head slice, or the next sequence).
-__device__ __forceinline__ bool next_segment(const DecodeParams& p, Segment& s) {
+// Next segment after `s` (same sequence next head slice, or the next sequence); each
+// segment spans its n units plus `extra` cost units on the schedule's line.
+__device__ __forceinline__ bool next_segment(const DecodeParams& p, Segment& s, int extra = 0) {
   const int HZ = p.H_kv * p.n_z;
-  s.off += s.n;
+  s.off += s.n + extra;
   if (s.hz + 1 < HZ) {
     ++s.hz;
     return true;
@@ -292,21 +296,26 @@ __device__ __forceinline__ long long share_of(long long x, long long U, long lon
 
 // ---------------------------------------------------------------------------- workers
 // Independent workers (warps of the tensor-core kernel): worker w = block * WPB + i.
-// Balanced schedule: worker w takes units [floor(w U / W), floor((w+1) U / W)) with
-// W = gridDim.x * WPB.  Per-segment schedule: worker w takes segment w whole.
+// Balanced schedule: every segment occupies n + C positions of a cost line (C =
+// p.seg_cost positions for its set-up and finish, then its n units); worker w takes
+// positions [floor(w U / W), floor((w+1) U / W)) of the line's U positions, with
+// W = gridDim.x * WPB, i.e. the units of each segment whose positions fall in its range.
+// Per-segment schedule: worker w takes segment w whole.
 struct WorkerStart {
-  long long x0, x1, U;  // unit range (per-segment: [0, huge) of the segment), total units
-  long long off;        // first global unit of the segment holding x0
+  long long x0, x1, U;  // cost-line range (per-segment: [0, huge)), line length
+  long long off;        // line position where the segment holding x0 starts
   int b, hz;            // that segment; b < 0: this worker has no work
 };
 
 // Block-wide (ends with a block barrier): the start of each of the block's WPB workers.
+// s_units: shared scratch of kStartCacheB ints.
 template <int NT, int WPB>
-__device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws) {
+__device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_units) {
   __shared__ long long s_warp[NT / 32];
   __shared__ long long s_hit[WPB][2];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const int HZ = p.H_kv * p.n_z;
+  const int C = p.seg_cost;
   const long long W = (long long)gridDim.x * WPB;
   const long long w_first = (long long)blockIdx.x * WPB;
   if (p.mode != kSchedBalanced) {
@@ -329,28 +338,18 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws) {
     __syncthreads();
     return;
   }
-  // pass 1: total units
-  long long total = 0;
-  for (int start = 0; start < p.B; start += NT) {
-    const int b = start + tid;
-    long long n = b < p.B ? units_of(load_seq(p, b), p.P) : 0;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
-    if (lane == 0) s_warp[wid] = n;
+  long long U;
+  if (p.B <= kStartCacheB) {
+    // one pass over the sequences: unit counts into shared memory, then a block-wide
+    // scan in which each thread owns `per` consecutive sequences
+    for (int b = tid; b < p.B; b += NT) s_units[b] = units_of(load_seq(p, b), p.P);
+    if (tid < WPB) s_hit[tid][0] = -1;
     __syncthreads();
-#pragma unroll
-    for (int i = 0; i < NT / 32; ++i) total += s_warp[i];
-    __syncthreads();
-  }
-  const long long U = total * HZ;
-  if (tid < WPB) s_hit[tid][0] = -1;
-  __syncthreads();
-  // pass 2: the sequence holding each worker's first unit
-  long long base = 0;
-  for (int start = 0; start < p.B; start += NT) {
-    const int b = start + tid;
-    const long long n = b < p.B ? (long long)units_of(load_seq(p, b), p.P) * HZ : 0;
-    long long incl = n;
+    const int per = (p.B + NT - 1) / NT;
+    const int b0 = min(tid * per, p.B), b1 = min(b0 + per, p.B);
+    long long mine = 0;
+    for (int b = b0; b < b1; ++b) mine += s_units[b] + C;
+    long long incl = mine;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const long long t = __shfl_up_sync(0xffffffffu, incl, o);
@@ -358,25 +357,78 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws) {
     }
     if (lane == 31) s_warp[wid] = incl;
     __syncthreads();
-    long long wbase = 0, tot = 0;
+    long long wbase = 0, total = 0;
 #pragma unroll
     for (int i = 0; i < NT / 32; ++i) {
       const long long v = s_warp[i];
       if (i < wid) wbase += v;
-      tot += v;
+      total += v;
     }
-    incl += wbase;
-    const long long lo = base + incl - n, hi = base + incl;
+    U = total * HZ;
+    long long lo = (wbase + incl - mine) * HZ;
+    for (int b = b0; b < b1; ++b) {
+      const long long hi = lo + (long long)(s_units[b] + C) * HZ;
 #pragma unroll
-    for (int i = 0; i < WPB; ++i) {
-      const long long t = (w_first + i) * U / W;
-      if (b < p.B && t >= lo && t < hi) {
-        s_hit[i][0] = b;
-        s_hit[i][1] = lo;  // = HZ * (units of the sequences before b)
+      for (int i = 0; i < WPB; ++i) {
+        const long long t = (w_first + i) * U / W;
+        if (t >= lo && t < hi) {
+          s_hit[i][0] = b;
+          s_hit[i][1] = lo;  // = HZ * (units of the sequences before b)
+        }
       }
+      lo = hi;
     }
-    base += tot;
     __syncthreads();
+  } else {
+    // pass 1: total units
+    long long total = 0;
+    for (int start = 0; start < p.B; start += NT) {
+      const int b = start + tid;
+      long long n = b < p.B ? units_of(load_seq(p, b), p.P) + C : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+      if (lane == 0) s_warp[wid] = n;
+      __syncthreads();
+#pragma unroll
+      for (int i = 0; i < NT / 32; ++i) total += s_warp[i];
+      __syncthreads();
+    }
+    U = total * HZ;
+    if (tid < WPB) s_hit[tid][0] = -1;
+    __syncthreads();
+    // pass 2: the sequence holding each worker's first unit
+    long long base = 0;
+    for (int start = 0; start < p.B; start += NT) {
+      const int b = start + tid;
+      const long long n = b < p.B ? (long long)(units_of(load_seq(p, b), p.P) + C) * HZ : 0;
+      long long incl = n;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (lane == 31) s_warp[wid] = incl;
+      __syncthreads();
+      long long wbase = 0, tot = 0;
+#pragma unroll
+      for (int i = 0; i < NT / 32; ++i) {
+        const long long v = s_warp[i];
+        if (i < wid) wbase += v;
+        tot += v;
+      }
+      incl += wbase;
+      const long long lo = base + incl - n, hi = base + incl;
+#pragma unroll
+      for (int i = 0; i < WPB; ++i) {
+        const long long t = (w_first + i) * U / W;
+        if (b < p.B && t >= lo && t < hi) {
+          s_hit[i][0] = b;
+          s_hit[i][1] = lo;
+        }
+      }
+      base += tot;
+      __syncthreads();
+    }
   }
   if (tid < WPB) {
     const long long w = w_first + tid;
@@ -391,7 +443,7 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws) {
       s.b = -1;
       s.x1 = s.x0;
     } else {
-      const int n = units_of(load_seq(p, s.b), p.P);
+      const int n = C + (s.b < kStartCacheB && p.B <= kStartCacheB ? s_units[s.b] : units_of(load_seq(p, s.b), p.P));
       s.hz = (int)((s.x0 - s_hit[tid][1]) / n);
       s.off = s_hit[tid][1] + (long long)s.hz * n;
     }

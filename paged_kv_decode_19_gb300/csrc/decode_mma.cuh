@@ -41,16 +41,22 @@
 namespace pd {
 
 #ifndef PD_PREFETCH_PIECES
-#define PD_PREFETCH_PIECES 3
+#define PD_PREFETCH_PIECES 1
 #endif
 constexpr int kPrefetchPieces = PD_PREFETCH_PIECES;  // L2 prefetch distance, in pages
 #ifndef PD_MIN_BLOCKS_PLAIN
 #define PD_MIN_BLOCKS_PLAIN 1
 #endif
-// resident blocks per SM the register allocation targets (no-RoPE / RoPE kernels)
-template <bool ROPE>
+#ifndef PD_MIN_BLOCKS_ROPE
+#define PD_MIN_BLOCKS_ROPE 1
+#endif
+// Resident blocks per SM the register allocation targets.  The FP8 kernel moves half
+// the bytes per tile of the 16-bit one, so it needs the extra warps of a third block
+// to keep enough loads in flight (measured: 3 blocks of <= 168 registers beat 2 of
+// 213 by ~15% on a 256-sequence FP8 cache).
+template <bool ROPE, bool FP8>
 struct MinBlocks {
-  static constexpr int v = ROPE ? 1 : PD_MIN_BLOCKS_PLAIN;
+  static constexpr int v = ROPE ? PD_MIN_BLOCKS_ROPE : FP8 ? 3 : PD_MIN_BLOCKS_PLAIN;
 };
 
 template <typename KVT, typename QT, int D, bool ROPE>
@@ -117,21 +123,23 @@ __device__ __forceinline__ void store_run(const DecodeParams& p, size_t idx, con
 // out/lse by one warp: lse = M + log2 sum_s 2^(lse_s - M), out = sum_s 2^(lse_s - M) o_s
 // / sum_s 2^(lse_s - M).  Slot lse values are read one slot per lane; each lane then
 // sums its float4s of (head, dims) over the slots with independent loads.
-template <int D>
-__device__ void warp_merge(const DecodeParams& p, const Segment& sg, long long U, long long W,
-                           int hq0, int hcount, float (*s_w)[kMaxGroupPerCta], int* s_sl) {
+template <int D, int kMergeBatch>
+__device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, int seg_c, int seg_n,
+                           long long U, long long W, int hq0, int hcount,
+                           float (*s_w)[kMaxGroupPerCta], int* s_sl) {
   constexpr int G8 = kMaxGroupPerCta;
   constexpr int D4 = D / 4;
   constexpr int kV = (G8 * D4 + 31) / 32;
   const int lane = threadIdx.x & 31;
-  const long long w0 = share_of(sg.off, U, W);
-  const int ns = (int)(share_of(sg.off + sg.n - 1, U, W) - w0 + 1);
-  const long long sl0 = share_slot(w0, sg.off, U, W);  // worker w0 always holds units
+  // workers whose ranges hold the segment's units (line positions seg_off + seg_c ...)
+  const long long w0 = share_of(seg_off + seg_c, U, W);
+  const int ns = (int)(share_of(seg_off + seg_c + seg_n - 1, U, W) - w0 + 1);
+  const long long sl0 = share_slot(w0, seg_off, U, W);  // worker w0 always holds units
   float M[G8];
 #pragma unroll
   for (int j = 0; j < G8; ++j) M[j] = kEmptyM;
   for (int s = lane; s < ns; s += 32) {
-    const long long sl = share_slot(w0 + s, sg.off, U, W);
+    const long long sl = share_slot(w0 + s, seg_off, U, W);
     if (sl < 0) continue;
     const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
     const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
@@ -156,7 +164,7 @@ __device__ void warp_merge(const DecodeParams& p, const Segment& sg, long long U
 #pragma unroll
     for (int j = 0; j < G8; ++j) v[j] = kEmptyM;
     if (s < ns) {
-      sl = share_slot(w0 + s, sg.off, U, W);
+      sl = share_slot(w0 + s, seg_off, U, W);
       if (sl >= 0) {
         const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
         const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
@@ -173,20 +181,36 @@ __device__ void warp_merge(const DecodeParams& p, const Segment& sg, long long U
     s_sl[lane] = (int)(sl >= 0 ? sl : sl0);  // a worker with no units: weight 0, a written slot
     __syncwarp();
     const int cnt = min(32, ns - base);
-#pragma unroll 2
-    for (int i = 0; i < cnt; ++i) {
-      const float* po = p.part_o + (size_t)s_sl[i] * D;
+    // kMergeBatch slots at a time: all their loads go out before any is used
+    for (int i0 = 0; i0 < cnt; i0 += kMergeBatch) {
+      float4 o[kMergeBatch][kV];
 #pragma unroll
-      for (int e = 0; e < kV; ++e) {
-        const int vi = lane + 32 * e;
-        if (vi < hcount * D4) {
-          const int j = vi / D4, d4 = vi - j * D4;
-          const float w = s_w[i][j];
-          const float4 o = __ldcg(reinterpret_cast<const float4*>(po + (size_t)j * D) + d4);
-          acc[e].x += w * o.x;
-          acc[e].y += w * o.y;
-          acc[e].z += w * o.z;
-          acc[e].w += w * o.w;
+      for (int u = 0; u < kMergeBatch; ++u) {
+        const float* po = p.part_o + (size_t)s_sl[min(i0 + u, cnt - 1)] * D;
+#pragma unroll
+        for (int e = 0; e < kV; ++e) {
+          const int vi = lane + 32 * e;
+          o[u][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (vi < hcount * D4) {
+            const int j = vi / D4, d4 = vi - j * D4;
+            o[u][e] = __ldcg(reinterpret_cast<const float4*>(po + (size_t)j * D) + d4);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kMergeBatch; ++u) {
+        if (i0 + u < cnt) {
+#pragma unroll
+          for (int e = 0; e < kV; ++e) {
+            const int vi = lane + 32 * e;
+            if (vi < hcount * D4) {
+              const float w = s_w[i0 + u][vi / D4];
+              acc[e].x += w * o[u][e].x;
+              acc[e].y += w * o[u][e].y;
+              acc[e].z += w * o[u][e].z;
+              acc[e].w += w * o[u][e].w;
+            }
+          }
         }
       }
     }
@@ -211,18 +235,18 @@ __device__ void warp_merge(const DecodeParams& p, const Segment& sg, long long U
       const bool empty = !(Mj > kEmptyM);
       const float sc = empty ? 0.f : p.out_scale / dj;
       const int hq = hq0 + j;
-      const size_t o = ((size_t)sg.b * p.H_qo + hq) * D + 4 * d4;
+      const size_t o = ((size_t)seg_b * p.H_qo + hq) * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
       store_out(p, o + 1, acc[e].y * sc);
       store_out(p, o + 2, acc[e].z * sc);
       store_out(p, o + 3, acc[e].w * sc);
-      if (d4 == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = empty ? kEmptyM : Mj + log2f(dj);
+      if (d4 == 0) p.lse[(size_t)seg_b * p.H_qo + hq] = empty ? kEmptyM : Mj + log2f(dj);
     }
   }
 }
 
 template <typename KVT, typename QT, int D, bool ROPE, int NW>
-__global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
+__global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::v)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = MmaTraits<KVT, QT, D, ROPE>;
   using MT = typename Tr::MT;
@@ -235,11 +259,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
   constexpr int RL = FP8 ? 16 : 8;  // output run: consecutive dims a thread holds
   constexpr int NR = 2 * KT / RL;   // runs per head and thread
   __shared__ uint4 s_qf[NW][KT][32];                        // per-warp Q^T B fragments
+  // dynamic shared memory: per-warp K tiles, two slots (also the start-up scan's and
+  // the merge's scratch, which never overlap a warp's K stream)
+  extern __shared__ uint4 pd_dyn_smem[];
+  auto s_kst = reinterpret_cast<uint4 (*)[2][2 * KCH][32]>(pd_dyn_smem);
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
   __shared__ float2 s_rot8[ROPE ? D / 2 : 1];               // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
-  __shared__ float s_mw[NW][32][kMaxGroupPerCta];           // per-warp merge weights
-  __shared__ int s_msl[NW][32];                             // per-warp merge slots
 
   if (ROPE) {
     for (int i = threadIdx.x; i < D / 2; i += NT) {
@@ -250,7 +276,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
       s_rot8[i] = make_float2(c8, s8);
     }
   }
-  worker_starts<NT, NW>(p, s_start);  // last block-wide barrier of the kernel
+  static_assert(sizeof(uint4) * NW * 2 * 2 * KCH * 32 >= sizeof(int) * kStartCacheB, "scan scratch");
+  worker_starts<NT, NW>(p, s_start, reinterpret_cast<int*>(pd_dyn_smem));  // last block-wide barrier
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g_id = lane >> 2, q4 = lane & 3;
@@ -269,17 +296,35 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
   sg.off = ws.off;
   sg.seq = load_seq(p, sg.b);
   sg.n = units_of(sg.seq, P);
-  const long long x1 = p.mode == kSchedBalanced ? ws.x1 : sg.off + sg.n;
+  // cost-line positions: a segment spans [off, off + C + n), its units from off + C
+  const int C = p.mode == kSchedBalanced ? p.seg_cost : 0;
+  const long long cx1 = p.mode == kSchedBalanced ? ws.x1 : sg.off + sg.n;
 
   // The worker walks the segments (sequence, head slice) its range [x0, x1) touches.
   for (;;) {
-  const int ua = (int)max(ws.x0 - sg.off, 0ll);
-  const int ub = (int)min(x1 - sg.off, (long long)sg.n);
+  const int ua = (int)min(max(ws.x0 - sg.off - C, 0ll), (long long)sg.n);
+  const int ub = (int)min(max(cx1 - sg.off - C, 0ll), (long long)sg.n);
+  if (ua < ub) {  // else only the segment's set-up positions fall in this range
   const int hk = sg.hz / p.n_z, z = sg.hz - (sg.hz / p.n_z) * p.n_z;
   const Pieces pcs = make_pieces(0, sg.seq.L, sg.seq, P);
   const int pend = min(ub, sg.seq.L > 0 ? pcs.count() : 0);  // pieces [ua, pend) here
   const int hq0 = hk * p.group + z * kMaxGroupPerCta;
   const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
+
+  // Raw Q of this lane's B-fragment elements (pairs of adjacent dims), loaded first:
+  // they are tiny and needed before anything else.
+  const bool have_q = g_id < hcount;
+  uint32_t qraw[KT][2];
+  {
+    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have_q ? g_id : 0)) * D;
+#pragma unroll
+    for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        qraw[kt][h] = have_q ? __ldg(reinterpret_cast<const uint32_t*>(qrow + frag_dim<FP8>(kt, h, 0, q4))) : 0u;
+  }
+  const int qpos = ROPE ? __ldg(p.q_rope_position + sg.b) : 0;
+  const int kpos0 = ROPE ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
 
   // ---------------------------------------------------------------- tile stream
   // Pieces [ua, pend) in order; their page ids are looked up 32 at a time (one per
@@ -330,7 +375,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
       tl.kblk = kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes;
       break;
     }
-    prefetch_to(j + 1 + kPrefetchPieces);
     return tl;
   };
   auto next_tile = [&](const Tile& c) -> Tile {
@@ -343,13 +387,18 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
   };
   uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
   uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
-  auto load_k = [&](const Tile& c) {
+  // K goes through this warp's two shared-memory slots (each lane copies and later
+  // reads back only its own chunks), so the next tile's K can be requested at the
+  // start of the current tile without holding registers; V is loaded straight into
+  // registers after PV, a full QK + softmax ahead of its use.
+  auto issue_k = [&](const Tile& c, int slot) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const uint8_t* row = c.kblk + (size_t)(c.t * 16 + g_id + 8 * rr) * RB;
 #pragma unroll
-      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = ldg_stream(row + (4 * ch + q4) * 16);
+      for (int ch = 0; ch < KCH; ++ch) cp_async16(&s_kst[warp][slot][rr * KCH + ch][lane], row + (4 * ch + q4) * 16);
     }
+    cp_async_commit();
   };
   auto load_v = [&](const Tile& c) {
 #pragma unroll
@@ -363,9 +412,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
 
   // first tile's loads go out before the Q set-up, which then overlaps their latency
   Tile cur = first_tile_from(ua);
+  int kslot = 0;
   if (cur.kblk) {
-    load_k(cur);
+    issue_k(cur, kslot);
     load_v(cur);
+    prefetch_to(cur.piece + 1 + kPrefetchPieces);  // after the tile's own loads
   }
 
   // ---------------------------------------------------------------- Q^T B fragments
@@ -373,25 +424,24 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
   // b1 = (k 2q+8..2q+9, head g_id) in the permuted dim order, in this warp's shared
   // memory (k-tile pairs kt / kt + KT/2 together, for RoPE).
   {
-    const bool have = g_id < hcount;
-    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have ? g_id : 0)) * D;
-    const int qpos = ROPE ? p.q_rope_position[sg.b] : 0;
+#pragma unroll
     for (int kt = 0; kt < KT / 2; ++kt) {
       float qv[2][2][2];  // [pair member u: kt, kt + KT/2][half][e]
 #pragma unroll
       for (int u = 0; u < 2; ++u)
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-#pragma unroll
-          for (int e = 0; e < 2; ++e)
-            qv[u][h][e] = have ? to_f32(qrow[frag_dim<FP8>(kt + u * (KT / 2), h, e, q4)]) : 0.f;
+        for (int h = 0; h < 2; ++h) {
+          const float2 f = unpack2<QT>(qraw[kt + u * (KT / 2)][h]);
+          qv[u][h][0] = f.x;
+          qv[u][h][1] = f.y;
+        }
       if (ROPE) {
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             float c, sn;
-            rope_cos_sin(qpos, p.rope_F[frag_dim<FP8>(kt, h, e, q4)], c, sn);
+            rope_cos_sin(qpos, s_ropeF[frag_dim<FP8>(kt, h, e, q4)], c, sn);
             const float x = qv[0][h][e], y = qv[1][h][e];
             qv[0][h][e] = x * c - y * sn;
             qv[1][h][e] = y * c + x * sn;
@@ -415,7 +465,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
   }
   __syncwarp();
   const float post_scale = Tr::kQSplit ? 1.f : p.score_scale;
-  const int kpos0 = ROPE ? p.k_rope_pos_offset[sg.b] : 0;
 
   float st_m[2] = {kEmptyM, kEmptyM}, st_d[2] = {0.f, 0.f};
   float oacc[KT][4];
@@ -423,6 +472,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
   for (int i = 0; i < KT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
   while (cur.kblk) {
+    // this tile's K has landed; request the next tile's K into the other slot
+    cp_async_wait_all();
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr)
+#pragma unroll
+      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = s_kst[warp][kslot][rr * KCH + ch][lane];
+    const Tile nxt = next_tile(cur);
+    if (nxt.kblk) {
+      issue_k(nxt, kslot ^ 1);
+      prefetch_to(nxt.piece + 1 + kPrefetchPieces);
+    }
     const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
     const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
     const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
@@ -505,9 +565,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc1[i] + acc2[i];
-    // K registers are free: start the next tile's K loads
-    const Tile nxt = next_tile(cur);
-    if (nxt.kblk) load_k(nxt);
     // ------------------------------------------------------------ online softmax (log2)
     float sc[4];
     sc[0] = v0 ? acc[0] * post_scale : -INFINITY;  // row g_id, heads 2q, 2q+1
@@ -586,6 +643,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
     }
     if (nxt.kblk) load_v(nxt);
     cur = nxt;
+    kslot ^= 1;
   }
   st_d[0] = sum_over_groups(st_d[0]);
   st_d[1] = sum_over_groups(st_d[1]);
@@ -641,27 +699,40 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE>::v)
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
       __threadfence();
-      warp_merge<D>(p, sg, ws.U, Wn, hq0, hcount, s_mw[warp], s_msl[warp]);
+      // slots whose loads are in flight together: fewer where registers are tight
+      constexpr int kBatch = MinBlocks<ROPE, FP8>::v >= 3 ? 1 : (KT > 4 ? 2 : 4);
+      static_assert(sizeof(uint4) * 2 * KCH * 32 >= sizeof(float) * 32 * kMaxGroupPerCta, "merge scratch");
+      warp_merge<D, kBatch>(p, sg.b, sg.off, C, sg.n, ws.U, Wn, hq0, hcount,
+                            reinterpret_cast<float (*)[kMaxGroupPerCta]>(&s_kst[warp][0][0][0]),
+                            reinterpret_cast<int*>(&s_kst[warp][1][0][0]));
     }
   }
-  if (sg.off + sg.n >= x1 || !next_segment(p, sg)) break;
+  }  // ua < ub
+  if (sg.off + C + sg.n >= cx1 || !next_segment(p, sg, C)) break;
   }  // segments
 }
 
 template <typename KVT, typename QT, int D, bool ROPE>
 static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
   constexpr int NW = kMmaWarps;
+  constexpr int dyn = (int)sizeof(uint4) * NW * 2 * 2 * MmaTraits<KVT, QT, D, ROPE>::kKCh * 32;
   auto kern = decode_mma_kernel<KVT, QT, D, ROPE, NW>;
+  static bool attr_set = false;  // set once per instantiation (idempotent if it races)
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   if (cfg) {
     cfg->threads = NW * 32;
-    cfg->smem_bytes = 0;
+    cfg->smem_bytes = dyn;
     int n = 0;
-    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NW * 32, 0);
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NW * 32, dyn);
     if (e != cudaSuccess) return e;
     cfg->ctas_per_sm = n;
     return cudaSuccess;
   }
-  kern<<<grid, NW * 32, 0, st>>>(p);
+  kern<<<grid, NW * 32, dyn, st>>>(p);
   return cudaGetLastError();
 }
 
