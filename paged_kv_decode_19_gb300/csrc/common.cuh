@@ -140,6 +140,10 @@ __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// wait until at most one committed group (the most recent) is still pending
+__device__ __forceinline__ void cp_async_wait_all_but_last() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
 
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);

@@ -119,121 +119,176 @@ __device__ __forceinline__ void store_run(const DecodeParams& p, size_t idx, con
   }
 }
 
-// Merge of every worker's partial state of segment `sg` (worker count W, U units) into
-// out/lse by one warp: lse = M + log2 sum_s 2^(lse_s - M), out = sum_s 2^(lse_s - M) o_s
-// / sum_s 2^(lse_s - M).  Slot lse values are read one slot per lane; each lane then
-// sums its float4s of (head, dims) over the slots with independent loads.
-template <int D, int kMergeBatch>
+// Merge of every worker's partial state of one segment into out/lse, by one warp:
+// lse = M + log2 sum_s 2^(lse_s - M), out = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),
+// over the workers s whose ranges hold the segment's units (cost-line positions
+// seg_off + seg_c ... seg_off + seg_c + seg_n - 1; W workers on a line of U positions).
+// HMAX bounds the heads of the slice (hcount), BATCH the slots whose partial rows are in
+// flight together.  With at most 32 slots, lane s reads slot s's lse and the weights come
+// from warp reductions; the first batch of partial rows is requested before that, so
+// the merge costs about one L2 round trip per batch.  s_w: this warp's shared scratch
+// of 34 x 8 floats, s_sl: 32 ints.
+template <int D, int HMAX, int BATCH>
 __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, int seg_c, int seg_n,
                            long long U, long long W, int hq0, int hcount,
                            float (*s_w)[kMaxGroupPerCta], int* s_sl) {
   constexpr int G8 = kMaxGroupPerCta;
   constexpr int D4 = D / 4;
-  constexpr int kV = (G8 * D4 + 31) / 32;
+  constexpr int kV = (HMAX * D4 + 31) / 32;  // float4 outputs per lane
+  static_assert(HMAX % 4 == 0 && HMAX <= G8, "HMAX");
   const int lane = threadIdx.x & 31;
-  // workers whose ranges hold the segment's units (line positions seg_off + seg_c ...)
   const long long w0 = share_of(seg_off + seg_c, U, W);
   const int ns = (int)(share_of(seg_off + seg_c + seg_n - 1, U, W) - w0 + 1);
   const long long sl0 = share_slot(w0, seg_off, U, W);  // worker w0 always holds units
-  float M[G8];
-#pragma unroll
-  for (int j = 0; j < G8; ++j) M[j] = kEmptyM;
-  for (int s = lane; s < ns; s += 32) {
-    const long long sl = share_slot(w0 + s, seg_off, U, W);
-    if (sl < 0) continue;
-    const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
-    const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
-    const float v[G8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int j = 0; j < G8; ++j) M[j] = fmaxf(M[j], j < hcount ? v[j] : kEmptyM);
-  }
-#pragma unroll
-  for (int j = 0; j < G8; ++j)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(0xffffffffu, M[j], o));
-  float den[G8];
-#pragma unroll
-  for (int j = 0; j < G8; ++j) den[j] = 0.f;
+  float* s_M = s_w[32];
+  float* s_den = s_w[33];
   float4 acc[kV];
 #pragma unroll
   for (int e = 0; e < kV; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int base = 0; base < ns; base += 32) {
-    const int s = base + lane;
-    long long sl = -1;
-    float v[G8];
+  auto load_rows = [&](float4 (&o)[BATCH][kV], int i0, int cnt) {
 #pragma unroll
-    for (int j = 0; j < G8; ++j) v[j] = kEmptyM;
-    if (s < ns) {
-      sl = share_slot(w0 + s, seg_off, U, W);
-      if (sl >= 0) {
-        const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl));
-        const float4 b = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + 1);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    for (int u = 0; u < BATCH; ++u) {
+      const float* po = p.part_o + (size_t)s_sl[min(i0 + u, cnt - 1)] * D;
+#pragma unroll
+      for (int e = 0; e < kV; ++e) {
+        const int vi = lane + 32 * e;
+        o[u][e] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (vi < hcount * D4) o[u][e] = __ldcg(reinterpret_cast<const float4*>(po + (size_t)(vi / D4) * D) + vi % D4);
       }
     }
+  };
+  auto add_rows = [&](const float4 (&o)[BATCH][kV], int i0, int cnt) {
 #pragma unroll
-    for (int j = 0; j < G8; ++j) {
-      const float w = (sl >= 0 && j < hcount) ? merge_exp2(p, v[j] - M[j]) : 0.f;
-      den[j] += w;
-      s_w[lane][j] = w;
-    }
-    s_sl[lane] = (int)(sl >= 0 ? sl : sl0);  // a worker with no units: weight 0, a written slot
-    __syncwarp();
-    const int cnt = min(32, ns - base);
-    // kMergeBatch slots at a time: all their loads go out before any is used
-    for (int i0 = 0; i0 < cnt; i0 += kMergeBatch) {
-      float4 o[kMergeBatch][kV];
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        const float* po = p.part_o + (size_t)s_sl[min(i0 + u, cnt - 1)] * D;
+    for (int u = 0; u < BATCH; ++u) {
+      if (i0 + u < cnt) {
 #pragma unroll
         for (int e = 0; e < kV; ++e) {
           const int vi = lane + 32 * e;
-          o[u][e] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (vi < hcount * D4) {
-            const int j = vi / D4, d4 = vi - j * D4;
-            o[u][e] = __ldcg(reinterpret_cast<const float4*>(po + (size_t)j * D) + d4);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kMergeBatch; ++u) {
-        if (i0 + u < cnt) {
-#pragma unroll
-          for (int e = 0; e < kV; ++e) {
-            const int vi = lane + 32 * e;
-            if (vi < hcount * D4) {
-              const float w = s_w[i0 + u][vi / D4];
-              acc[e].x += w * o[u][e].x;
-              acc[e].y += w * o[u][e].y;
-              acc[e].z += w * o[u][e].z;
-              acc[e].w += w * o[u][e].w;
-            }
+            const float w = s_w[i0 + u][vi / D4];
+            acc[e].x += w * o[u][e].x;
+            acc[e].y += w * o[u][e].y;
+            acc[e].z += w * o[u][e].z;
+            acc[e].w += w * o[u][e].w;
           }
         }
       }
     }
+  };
+  if (ns <= 32) {
+    long long sl = -1;
+    float v[HMAX];
+#pragma unroll
+    for (int j = 0; j < HMAX; ++j) v[j] = kEmptyM;
+    if (lane < ns) {
+      sl = share_slot(w0 + lane, seg_off, U, W);
+      if (sl >= 0) {
+#pragma unroll
+        for (int q = 0; q < HMAX / 4; ++q) {
+          const float4 a = __ldcg(reinterpret_cast<const float4*>(p.part_lse + sl) + q);
+          v[4 * q] = a.x;
+          v[4 * q + 1] = a.y;
+          v[4 * q + 2] = a.z;
+          v[4 * q + 3] = a.w;
+        }
+      }
+    }
+    s_sl[lane] = (int)(sl >= 0 ? sl : sl0);  // a worker with no units: weight 0, a written slot
     __syncwarp();
+    float4 o[BATCH][kV];
+    load_rows(o, 0, ns);  // independent of the weights: in flight during the reductions
+#pragma unroll
+    for (int j = 0; j < HMAX; ++j) {
+      const bool ok = sl >= 0 && j < hcount;
+      float M = ok ? v[j] : kEmptyM;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float w = ok ? merge_exp2(p, v[j] - M) : 0.f;
+      float den = w;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      s_w[lane][j] = den > 0.f ? w / den : 0.f;  // normalised weight of slot `lane`
+      if (lane == 0) {
+        s_M[j] = M;
+        s_den[j] = den;
+      }
+    }
+    __syncwarp();
+    add_rows(o, 0, ns);
+    for (int i0 = BATCH; i0 < ns; i0 += BATCH) {
+      load_rows(o, i0, ns);
+      add_rows(o, i0, ns);
+    }
+  } else {
+    // more than 32 slots: per-head maximum, then weights chunk by chunk (unnormalised)
+    float M[HMAX], den[HMAX];
+#pragma unroll
+    for (int j = 0; j < HMAX; ++j) {
+      M[j] = kEmptyM;
+      den[j] = 0.f;
+    }
+    for (int s = lane; s < ns; s += 32) {
+      const long long sl = share_slot(w0 + s, seg_off, U, W);
+      if (sl < 0) continue;
+#pragma unroll
+      for (int j = 0; j < HMAX; ++j) M[j] = fmaxf(M[j], j < hcount ? __ldcg(p.part_lse + sl + j) : kEmptyM);
+    }
+#pragma unroll
+    for (int j = 0; j < HMAX; ++j)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(0xffffffffu, M[j], off));
+    for (int base = 0; base < ns; base += 32) {
+      const int s = base + lane;
+      const long long sl = s < ns ? share_slot(w0 + s, seg_off, U, W) : -1;
+#pragma unroll
+      for (int j = 0; j < HMAX; ++j) {
+        const float w = (sl >= 0 && j < hcount) ? merge_exp2(p, __ldcg(p.part_lse + sl + j) - M[j]) : 0.f;
+        den[j] += w;
+        s_w[lane][j] = w;
+      }
+      s_sl[lane] = (int)(sl >= 0 ? sl : sl0);
+      __syncwarp();
+      const int cnt = min(32, ns - base);
+      float4 o[BATCH][kV];
+      for (int i0 = 0; i0 < cnt; i0 += BATCH) {
+        load_rows(o, i0, cnt);
+        add_rows(o, i0, cnt);
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int j = 0; j < HMAX; ++j)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den[j] += __shfl_xor_sync(0xffffffffu, den[j], off);
+    if (lane == 0) {
+#pragma unroll
+      for (int j = 0; j < HMAX; ++j) {
+        s_M[j] = M[j];
+        s_den[j] = den[j];
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < kV; ++e) {  // weights were not normalised on this path
+      const int vi = lane + 32 * e;
+      if (vi < hcount * D4) {
+        const float dj = s_den[vi / D4];
+        const float r = dj > 0.f ? 1.f / dj : 0.f;
+        acc[e].x *= r;
+        acc[e].y *= r;
+        acc[e].z *= r;
+        acc[e].w *= r;
+      }
+    }
   }
-#pragma unroll
-  for (int j = 0; j < G8; ++j)
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) den[j] += __shfl_xor_sync(0xffffffffu, den[j], o);
 #pragma unroll
   for (int e = 0; e < kV; ++e) {
     const int vi = lane + 32 * e;
     if (vi < hcount * D4) {
-      const int j = vi / D4, d4 = vi - j * D4;
-      float Mj = M[0], dj = den[0];
-#pragma unroll
-      for (int k = 1; k < G8; ++k)
-        if (k == j) {
-          Mj = M[k];
-          dj = den[k];
-        }
+      const int j = vi / D4, d4 = vi % D4;
+      const float Mj = s_M[j], dj = s_den[j];
       const bool empty = !(Mj > kEmptyM);
-      const float sc = empty ? 0.f : p.out_scale / dj;
+      const float sc = empty ? 0.f : p.out_scale;
       const int hq = hq0 + j;
       const size_t o = ((size_t)seg_b * p.H_qo + hq) * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
@@ -243,6 +298,7 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
       if (d4 == 0) p.lse[(size_t)seg_b * p.H_qo + hq] = empty ? kEmptyM : Mj + log2f(dj);
     }
   }
+  __syncwarp();
 }
 
 template <typename KVT, typename QT, int D, bool ROPE, int NW>
@@ -259,10 +315,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   constexpr int RL = FP8 ? 16 : 8;  // output run: consecutive dims a thread holds
   constexpr int NR = 2 * KT / RL;   // runs per head and thread
   __shared__ uint4 s_qf[NW][KT][32];                        // per-warp Q^T B fragments
-  // dynamic shared memory: per-warp K tiles, two slots (also the start-up scan's and
-  // the merge's scratch, which never overlap a warp's K stream)
-  extern __shared__ uint4 pd_dyn_smem[];
-  auto s_kst = reinterpret_cast<uint4 (*)[2][2 * KCH][32]>(pd_dyn_smem);
+  __shared__ int s_units[kStartCacheB];                     // start-up scan scratch
+  __shared__ float s_mw[NW][34][kMaxGroupPerCta];           // per-warp merge scratch
+  __shared__ int s_msl[NW][32];
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
   __shared__ float2 s_rot8[ROPE ? D / 2 : 1];               // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
@@ -276,13 +331,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       s_rot8[i] = make_float2(c8, s8);
     }
   }
-  static_assert(sizeof(uint4) * NW * 2 * 2 * KCH * 32 >= sizeof(int) * kStartCacheB, "scan scratch");
-  worker_starts<NT, NW>(p, s_start, reinterpret_cast<int*>(pd_dyn_smem));  // last block-wide barrier
+  worker_starts<NT, NW>(p, s_start, s_units);  // the last block-wide barrier of the kernel
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g_id = lane >> 2, q4 = lane & 3;
   const WorkerStart ws = s_start[warp];
   if (ws.b < 0) return;  // no units for this worker
+
   const int P = p.P;
   const uint8_t* kv_base = reinterpret_cast<const uint8_t*>(p.pages);
   const size_t block_bytes = (size_t)P * RB;          // one (page, K|V, head) block
@@ -387,24 +442,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   };
   uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
   uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
-  // K goes through this warp's two shared-memory slots (each lane copies and later
-  // reads back only its own chunks), so the next tile's K can be requested at the
-  // start of the current tile without holding registers; V is loaded straight into
-  // registers after PV, a full QK + softmax ahead of its use.
-  auto issue_k = [&](const Tile& c, int slot) {
+  auto load_k = [&](const Tile& c) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       const uint8_t* row = c.kblk + (size_t)(c.t * 16 + g_id + 8 * rr) * RB;
 #pragma unroll
-      for (int ch = 0; ch < KCH; ++ch) cp_async16(&s_kst[warp][slot][rr * KCH + ch][lane], row + (4 * ch + q4) * 16);
+      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = ldg_stream(row + (4 * ch + q4) * 16);
     }
-    cp_async_commit();
   };
   auto load_v = [&](const Tile& c) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int slot = c.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
-      const uint8_t* row = c.kblk + v_off + (size_t)slot * RB;
+      const int row_in_page = c.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
+      const uint8_t* row = c.kblk + v_off + (size_t)row_in_page * RB;
 #pragma unroll
       for (int j = 0; j < VCH; ++j) vr[i][j] = ldg_stream(row + (g_id + 8 * j) * 16);
     }
@@ -412,9 +462,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 
   // first tile's loads go out before the Q set-up, which then overlaps their latency
   Tile cur = first_tile_from(ua);
-  int kslot = 0;
   if (cur.kblk) {
-    issue_k(cur, kslot);
+    load_k(cur);
     load_v(cur);
     prefetch_to(cur.piece + 1 + kPrefetchPieces);  // after the tile's own loads
   }
@@ -472,17 +521,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   for (int i = 0; i < KT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
   while (cur.kblk) {
-    // this tile's K has landed; request the next tile's K into the other slot
-    cp_async_wait_all();
-#pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
-#pragma unroll
-      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = s_kst[warp][kslot][rr * KCH + ch][lane];
-    const Tile nxt = next_tile(cur);
-    if (nxt.kblk) {
-      issue_k(nxt, kslot ^ 1);
-      prefetch_to(nxt.piece + 1 + kPrefetchPieces);
-    }
     const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
     const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
     const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
@@ -565,6 +603,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc1[i] + acc2[i];
+    // K registers are free: start the next tile's K loads
+    const Tile nxt = next_tile(cur);
+    if (nxt.kblk) {
+      load_k(nxt);
+      prefetch_to(nxt.piece + 1 + kPrefetchPieces);
+    }
     // ------------------------------------------------------------ online softmax (log2)
     float sc[4];
     sc[0] = v0 ? acc[0] * post_scale : -INFINITY;  // row g_id, heads 2q, 2q+1
@@ -643,7 +687,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     }
     if (nxt.kblk) load_v(nxt);
     cur = nxt;
-    kslot ^= 1;
   }
   st_d[0] = sum_over_groups(st_d[0]);
   st_d[1] = sum_over_groups(st_d[1]);
@@ -699,12 +742,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
       __threadfence();
-      // slots whose loads are in flight together: fewer where registers are tight
-      constexpr int kBatch = MinBlocks<ROPE, FP8>::v >= 3 ? 1 : (KT > 4 ? 2 : 4);
-      static_assert(sizeof(uint4) * 2 * KCH * 32 >= sizeof(float) * 32 * kMaxGroupPerCta, "merge scratch");
-      warp_merge<D, kBatch>(p, sg.b, sg.off, C, sg.n, ws.U, Wn, hq0, hcount,
-                            reinterpret_cast<float (*)[kMaxGroupPerCta]>(&s_kst[warp][0][0][0]),
-                            reinterpret_cast<int*>(&s_kst[warp][1][0][0]));
+      // slot rows in flight together: about 16 float4 per lane (4 where registers are
+      // tight), for the slice's head count
+      constexpr int kBudget = MinBlocks<ROPE, FP8>::v >= 3 ? 4 : 16;
+      constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
+      float (*mw)[kMaxGroupPerCta] = s_mw[warp];
+      int* msl = s_msl[warp];
+      if (hcount <= 4)
+        warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1)>(p, sg.b, sg.off, C, sg.n, ws.U, Wn, hq0, hcount, mw, msl);
+      else
+        warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1)>(p, sg.b, sg.off, C, sg.n, ws.U, Wn, hq0, hcount, mw, msl);
     }
   }
   }  // ua < ub
@@ -715,14 +762,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 template <typename KVT, typename QT, int D, bool ROPE>
 static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
   constexpr int NW = kMmaWarps;
-  constexpr int dyn = (int)sizeof(uint4) * NW * 2 * 2 * MmaTraits<KVT, QT, D, ROPE>::kKCh * 32;
+  constexpr int dyn = 0;
   auto kern = decode_mma_kernel<KVT, QT, D, ROPE, NW>;
-  static bool attr_set = false;  // set once per instantiation (idempotent if it races)
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
   if (cfg) {
     cfg->threads = NW * 32;
     cfg->smem_bytes = dyn;
