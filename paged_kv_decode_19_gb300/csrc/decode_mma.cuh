@@ -318,6 +318,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   __shared__ int s_units[kStartCacheB];                     // start-up scan scratch
   __shared__ float s_mw[NW][34][kMaxGroupPerCta];           // per-warp merge scratch
   __shared__ int s_msl[NW][32];
+  __shared__ long long s_pend[NW][2][3];                    // per-warp deferred merges
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
   __shared__ float2 s_rot8[ROPE ? D / 2 : 1];               // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
@@ -354,6 +355,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   // cost-line positions: a segment spans [off, off + C + n), its units from off + C
   const int C = p.mode == kSchedBalanced ? p.seg_cost : 0;
   const long long cx1 = p.mode == kSchedBalanced ? ws.x1 : sg.off + sg.n;
+
+  int npend = 0;  // next free entry of s_pend[warp] (entries with b < 0 are unused)
+  if (lane < 2) s_pend[warp][lane][0] = -1;
+  __syncwarp();
 
   // The worker walks the segments (sequence, head slice) its range [x0, x1) touches.
   for (;;) {
@@ -741,22 +746,43 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     }
     last = __shfl_sync(0xffffffffu, last, 0);
     if (last) {
+      // the merge runs after this worker's last segment (only a worker's first and last
+      // segments can be partial, so there are at most two), keeping the tile loop's
+      // register budget free of it
       __threadfence();
-      // slot rows in flight together: about 16 float4 per lane (4 where registers are
-      // tight), for the slice's head count
-      constexpr int kBudget = MinBlocks<ROPE, FP8>::v >= 3 ? 4 : 16;
-      constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
-      float (*mw)[kMaxGroupPerCta] = s_mw[warp];
-      int* msl = s_msl[warp];
-      if (hcount <= 4)
-        warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1)>(p, sg.b, sg.off, C, sg.n, ws.U, Wn, hq0, hcount, mw, msl);
-      else
-        warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1)>(p, sg.b, sg.off, C, sg.n, ws.U, Wn, hq0, hcount, mw, msl);
+      if (lane == 0) {
+        s_pend[warp][npend][0] = sg.b;
+        s_pend[warp][npend][1] = sg.hz;
+        s_pend[warp][npend][2] = sg.off;
+      }
+      npend = 1;  // at most two entries: indices 0 and 1
     }
   }
   }  // ua < ub
   if (sg.off + C + sg.n >= cx1 || !next_segment(p, sg, C)) break;
   }  // segments
+
+  // ---------------------------------------------------------------- deferred merges
+  __syncwarp();
+  for (int i = 0; i < 2; ++i) {
+    const long long b = s_pend[warp][i][0];
+    if (b < 0) continue;
+    const int hz = (int)s_pend[warp][i][1];
+    const long long off = s_pend[warp][i][2];
+    const SeqInfo seq = load_seq(p, (int)b);
+    const int n = units_of(seq, P);
+    const int hk = hz / p.n_z, z = hz - hk * p.n_z;
+    const int hq0 = hk * p.group + z * kMaxGroupPerCta;
+    const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
+    // slot rows in flight together: about 16 float4 per lane (4 where registers are
+    // tight), for the slice's head count
+    constexpr int kBudget = MinBlocks<ROPE, FP8>::v >= 3 ? 4 : 16;
+    constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
+    if (hcount <= 4)
+      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hq0, hcount, s_mw[warp], s_msl[warp]);
+    else
+      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hq0, hcount, s_mw[warp], s_msl[warp]);
+  }
 }
 
 template <typename KVT, typename QT, int D, bool ROPE>
