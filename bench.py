@@ -2,9 +2,13 @@
 sequence) + batch_decode_paged_kv (gather, RoPE, GQA attention, on-device split
 merge), on the Llama-3-8B-shaped bf16 serving load by default.
 
-Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K timed steps; the L2
-is flushed (a 2x-L2 memset) before every timed step and each step is bracketed by
-CUDA events on the launching stream.  The decode kernel is timed by its own event
+Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K timed steps, each
+bracketed by CUDA events on the launching stream.  Inputs larger than L2: two replicas
+of the workload (same seed, separate device memory) alternate step by step, so a
+step's KV is never in L2 (the other replica streamed through it in between).  Inputs
+that fit in L2: the L2 is flushed before every timed step (a 2x-L2 buffer written,
+then another read, leaving it cold and clean).  The flushed decode time of the large
+workloads is reported as well (decode_us_l2_flushed).  The decode kernel is timed by its own event
 pair for the roofline.  `e2e` re-times the step through the public API from pinned
 host buffers (H2D of the step's inputs and D2H of out + lse inside the timed region).
 
@@ -166,80 +170,104 @@ def run_ours(args, ws, rank, local):
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = W.make(args.config, seed=1000 + rank, device=dev)
+    # Two replicas of the workload (same seed, separate device memory) alternate step by
+    # step: when one replica's attended KV exceeds L2, a step never finds its KV in L2
+    # (the other replica streamed through L2 in between), without a flush kernel.
+    # Smaller workloads flush L2 before every step instead (2x L2 written, then 2x L2
+    # read: cold and clean).
+    reps = []
+    for _ in range(2):
+        wl = W.make(args.config, seed=1000 + rank, device=dev)
+        reps.append((wl,) + _append_inputs(wl, dev))
+    wl = reps[0][0]
     s = wl.spec
-    k_new, v_new, slots = _append_inputs(wl, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    alternate = wl.kv_bytes_attended() > l2
     out = torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=dev)
     lse = torch.empty((s.B, s.H_qo), dtype=torch.float32, device=dev)
     split = dict(num_splits=1) if args.config == "tiny_fp32" else {}
     stream = torch.cuda.current_stream(dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    wbuf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    rbuf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
 
-    def step():
-        pd.append_paged_kv(wl.pages, k_new, v_new, slots, wl.k_scale, wl.v_scale)
-        pd.batch_decode_paged_kv(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info,
-                                 wl.k_rope_pos_offset, wl.q_rope_position, out, lse,
-                                 s.rotary_mode, s.rope_scale, s.rope_theta, wl.sm_scale,
-                                 k_scale=wl.k_scale, v_scale=wl.v_scale, **split)
+    def flush_l2():
+        # evict the workload from L2 by writing a buffer larger than L2, then read another
+        # one so the written lines are written back here rather than inside the timed step
+        wbuf.zero_()
+        rbuf.amax()
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
+    def append(r):
+        w, k_new, v_new, slots = r
+        pd.append_paged_kv(w.pages, k_new, v_new, slots, w.k_scale, w.v_scale)
+
+    def decode(r):
+        w = r[0]
+        pd.batch_decode_paged_kv(w.Q, w.pages, w.indptr, w.values, w.length_info,
+                                 w.k_rope_pos_offset, w.q_rope_position, out, lse,
+                                 s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
+                                 k_scale=w.k_scale, v_scale=w.v_scale, **split)
+
+    def timed_steps(n, flush):
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for i in range(n):
+            r = reps[i % 2]
+            if flush:
+                flush_l2()
+            e0, e1, e2 = ev[i]
+            e0.record(stream)
+            append(r)
+            e1.record(stream)
+            decode(r)
+            e2.record(stream)
+        torch.cuda.synchronize()
+        return ([e[0].elapsed_time(e[2]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev],
+                [e[0].elapsed_time(e[1]) for e in ev])
+
+    for i in range(max(args.warmup, 2)):
+        r = reps[i % 2]
+        append(r)
+        decode(r)
     torch.cuda.synchronize()
     assert pd.check_device_errors() == "PD_OK"
     variant = pd.last_decode_variant()
 
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            e0, e1, e2 = ev[i]
-            e0.record(stream)
-            pd.append_paged_kv(wl.pages, k_new, v_new, slots, wl.k_scale, wl.v_scale)
-            e1.record(stream)
-            pd.batch_decode_paged_kv(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info,
-                                     wl.k_rope_pos_offset, wl.q_rope_position, out, lse,
-                                     s.rotary_mode, s.rope_scale, s.rope_theta, wl.sm_scale,
-                                     k_scale=wl.k_scale, v_scale=wl.v_scale, **split)
-            e2.record(stream)
-        torch.cuda.synchronize()
+        step_ms, dec_ms, app_ms = timed_steps(args.steps, flush=not alternate)
     if ws > 1:
         torch.distributed.barrier()
-    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
-    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    app_ms = [e[0].elapsed_time(e[1]) for e in ev]
     assert pd.check_device_errors() == "PD_OK"
     launches = 2 * args.steps
+    # the same steps after a flush of L2 (for comparison; not the reported value)
+    _, dec_flushed_ms, _ = timed_steps(max(args.steps // 2, 3), flush=True)
 
     # end-to-end through the public API from pinned host buffers
-    host_in = {k: getattr(wl, k).cpu().pin_memory() for k in
-               ("Q", "indptr", "values", "length_info", "k_rope_pos_offset", "q_rope_position")}
-    host_in["k_new"], host_in["v_new"], host_in["slots"] = (k_new.cpu().pin_memory(),
-                                                            v_new.cpu().pin_memory(),
-                                                            slots.cpu().pin_memory())
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in host_in.items()}
+    names = ("Q", "indptr", "values", "length_info", "k_rope_pos_offset", "q_rope_position")
+    host_in = {k: getattr(wl, k).cpu().pin_memory() for k in names}
+    host_in["k_new"], host_in["v_new"], host_in["slots"] = (reps[0][1].cpu().pin_memory(),
+                                                            reps[0][2].cpu().pin_memory(),
+                                                            reps[0][3].cpu().pin_memory())
+    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        w, di = reps[i % 2][0], dev_in[i % 2]
+        if not alternate:
+            flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for k, v in host_in.items():
-            dev_in[k].copy_(v, non_blocking=True)
-        pd.append_paged_kv(wl.pages, dev_in["k_new"], dev_in["v_new"], dev_in["slots"],
-                           wl.k_scale, wl.v_scale)
-        pd.batch_decode_paged_kv(dev_in["Q"], wl.pages, dev_in["indptr"], dev_in["values"],
-                                 dev_in["length_info"], dev_in["k_rope_pos_offset"],
-                                 dev_in["q_rope_position"], out, lse, s.rotary_mode,
-                                 s.rope_scale, s.rope_theta, wl.sm_scale, k_scale=wl.k_scale,
-                                 v_scale=wl.v_scale, **split)
+            di[k].copy_(v, non_blocking=True)
+        pd.append_paged_kv(w.pages, di["k_new"], di["v_new"], di["slots"], w.k_scale, w.v_scale)
+        pd.batch_decode_paged_kv(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
+                                 di["k_rope_pos_offset"], di["q_rope_position"], out, lse,
+                                 s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
+                                 k_scale=w.k_scale, v_scale=w.v_scale, **split)
         out_h.copy_(out, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
         b.record(stream)
@@ -249,8 +277,9 @@ def run_ours(args, ws, rank, local):
 
     res = dict(step=statistics.mean(step_ms), dec=statistics.mean(dec_ms),
                dec_med=statistics.median(dec_ms), app=statistics.mean(app_ms),
+               dec_flushed=statistics.mean(dec_flushed_ms),
                e2e=statistics.mean(e2e_ms), launches=launches, variant=variant,
-               clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h)
+               clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h, alternate=alternate, l2=l2)
     return res
 
 
@@ -282,7 +311,7 @@ def main():
            "page_size": spec.page_size, "kv_dtype": spec.kv_dtype, "q_dtype": spec.q_dtype,
            "rotary_mode": spec.rotary_mode, "len_dist": list(spec.len_dist),
            "step": "append_paged_kv (1 token/seq) + batch_decode_paged_kv",
-           "l2": "flushed before every timed step (2x L2 memset)",
+           "l2": None,  # filled in below
            "parallelism": f"replicas x{ws} (each rank its own batch; no collective)"}
 
     if args.impl == "reference":
@@ -320,6 +349,10 @@ def main():
         torch.distributed.destroy_process_group() if ws > 1 else None
         return
     wl = res["wl"]
+    cfg["l2"] = (f"inputs larger than L2 ({wl.kv_bytes_attended() / 1e6:.0f} MB attended KV vs "
+                 f"{res['l2'] / 1e6:.0f} MB L2): two replicas alternate, no flush"
+                 if res["alternate"] else
+                 "flushed before every timed step: 2x L2 written, then 2x L2 read (cold, clean L2)")
     kv_bytes = wl.kv_bytes_attended()
     alg_bytes = kv_bytes + wl.io_bytes()
     peak, peak_kind = _peaks()
@@ -339,6 +372,7 @@ def main():
         "data": "synthetic",
         "config": cfg,
         "decode_us": round(dec_us, 2),
+        "decode_us_l2_flushed": round(res["dec_flushed"] * 1e3, 2),
         "append_us": round(res["app"] * 1e3, 2),
         "kv_read_gbs": round(kv_bytes / (dec_us * 1e-6) / 1e9, 1),
         "decode_variant": res["variant"],

@@ -361,6 +361,7 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   }
   p.err = ds->err;
   p.max_pages = d.max_pages;
+  p.nnz_pages = d.nnz_pages;
   p.B = d.B;
   p.H_qo = d.H_qo;
   p.H_kv = d.H_kv;

@@ -145,6 +145,20 @@ __device__ __forceinline__ void cp_async_wait_all_but_last() {
   asm volatile("cp.async.wait_group 1;" ::: "memory");
 }
 
+// Block `part` of `parts` prefetches its share of [base, base + bytes) into L2 (the
+// 16-byte aligned interior only: nothing outside the array is touched).
+__device__ __forceinline__ void prefetch_l2_share(const void* base, size_t bytes, unsigned part,
+                                                  unsigned parts) {
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(base);
+  const uintptr_t lo = (b0 + 15) & ~(uintptr_t)15, hi = (b0 + bytes) & ~(uintptr_t)15;
+  if (hi <= lo || parts == 0) return;
+  const uintptr_t chunk = (((hi - lo) + parts - 1) / parts + 15) & ~(uintptr_t)15;
+  const uintptr_t s = lo + chunk * part;
+  if (s >= hi) return;
+  const uintptr_t e = s + chunk < hi ? s + chunk : hi;
+  prefetch_l2_bulk(reinterpret_cast<const void*>(s), (uint32_t)(e - s));
+}
+
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }

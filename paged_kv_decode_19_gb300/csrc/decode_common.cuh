@@ -40,6 +40,7 @@ struct DecodeParams {
   int* counters;    // [B * H_kv * n_z] pages merged so far per segment (reset by the last)
   unsigned* err;    // device error word
   long long max_pages;
+  long long nnz_pages;  // entries of the page table (page_table_values)
   int B, H_qo, H_kv, D, P, group, n_z;
   int window, rotary;
   int precise;        // fp32 path: merge weights via the accurate exp2f
@@ -62,9 +63,17 @@ struct SeqInfo {
 };
 
 __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
+  // every load is issued up front (one round trip), then the fields are checked
+  const int i0 = __ldg(p.indptr + b), i1 = __ldg(p.indptr + b + 1);
+  const long long last = __ldg(p.length_info + b);
+  long long off = 0, sk = 0;
+  if (p.window) {
+    off = __ldg(p.length_info + p.B + b);
+    sk = __ldg(p.length_info + 2 * p.B + b);
+  }
   SeqInfo s;
-  s.page_begin = p.indptr[b];
-  s.npages = p.indptr[b + 1] - s.page_begin;
+  s.page_begin = i0;
+  s.npages = i1 - i0;
   s.L = 0;
   s.sink = 0;
   s.win_off = 0;
@@ -73,13 +82,11 @@ __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
     s.npages = 0;
     return s;
   }
-  long long last = p.length_info[b];
   long long L;
   if (!p.window) {
     L = (long long)(s.npages - 1) * p.P + last;
     s.sink = (int)min(max(L, 0ll), (long long)INT32_MAX);
   } else {
-    long long off = p.length_info[p.B + b], sk = p.length_info[2 * p.B + b];
     L = (long long)(s.npages - 1) * p.P + last - off + sk;
     if (sk < 0 || off < sk) {  // inconsistent window: sequence treated as empty
       set_error(p.err, kErrBadLength);

@@ -323,6 +323,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   __shared__ float2 s_rot8[ROPE ? D / 2 : 1];               // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
 
+  // Q and the page table are small and needed right after the start-up scan, when the
+  // first tiles of every worker flood HBM: each block prefetches its share into L2 now
+  if (threadIdx.x == 0) {
+    prefetch_l2_share(p.Q, (size_t)p.B * p.H_qo * D * sizeof(QT), blockIdx.x, gridDim.x);
+    if (p.values) prefetch_l2_share(p.values, (size_t)p.nnz_pages * sizeof(int32_t), blockIdx.x, gridDim.x);
+  }
   if (ROPE) {
     for (int i = threadIdx.x; i < D / 2; i += NT) {
       const unsigned long long F = p.rope_F[i];
