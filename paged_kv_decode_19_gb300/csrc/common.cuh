@@ -83,6 +83,33 @@ template <> __device__ __forceinline__ float2 unpack2<__half>(uint32_t v) {
   return __half22float2(h);
 }
 
+// Packed fp32x2 arithmetic (sm_100+): one instruction operates on a register pair.
+__device__ __forceinline__ unsigned long long f2_pack(float2 v) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 v;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+  return v;
+}
+__device__ __forceinline__ float2 mul_f2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 sub_f2(float2 a, float2 b) {
+  unsigned long long r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 fma_f2(float2 a, float2 b, float2 c) {  // a * b + c
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(r);
+}
+
 // Split x into hi + lo of the MMA input type (hi = RN(x), lo = RN(x - hi)); the pair
 // carries ~2x the mantissa bits, so products of split operands are near-fp32 exact.
 template <typename T>
@@ -90,6 +117,13 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   hi = pack2<T>(x0, x1);
   float2 h = unpack2<T>(hi);
   lo = pack2<T>(x0 - h.x, x1 - h.y);
+}
+// Same split of a pair, with the residual taken by one packed subtraction.
+template <typename T>
+__device__ __forceinline__ void split2(float2 x, uint32_t& hi, uint32_t& lo) {
+  hi = pack2<T>(x.x, x.y);
+  const float2 r = sub_f2(x, unpack2<T>(hi));
+  lo = pack2<T>(r.x, r.y);
 }
 
 __device__ __forceinline__ float fast_exp2(float x) {

@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   __shared__ int s_msl[NW][32];
   __shared__ long long s_pend[NW][2][3];                    // per-warp deferred merges
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
-  __shared__ float2 s_rot8[ROPE ? D / 2 : 1];               // e^(i * 8 * omega_f)
+  __shared__ __align__(16) float2 s_rot8[ROPE ? D / 2 : 2];  // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
 
   // Q and the page table are small and needed right after the start-up scan, when the
@@ -379,10 +379,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 
   // Raw Q of this lane's B-fragment elements (pairs of adjacent dims), loaded first:
   // they are tiny and needed before anything else.
-  const bool have_q = g_id < hcount;
+  // Split-operand slices of at most 4 heads pack Q's lo part into the unused MMA
+  // columns 4..7 (lane group g_id >= 4 builds head g_id - 4's lo fragment): K Q^T then
+  // takes 2 MMAs per k-tile instead of 3, and column h + 4 is folded into column h.
+  const bool pack4 = Tr::kQSplit && hcount <= 4;
+  const int qh = pack4 ? (g_id & 3) : g_id;  // the head this lane's B fragment holds
+  const bool have_q = qh < hcount;
   uint32_t qraw[KT][2];
   {
-    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have_q ? g_id : 0)) * D;
+    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have_q ? qh : 0)) * D;
 #pragma unroll
     for (int kt = 0; kt < KT; ++kt)
 #pragma unroll
@@ -519,7 +524,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
             lo[h] = 0u;
           }
         }
-        s_qf[warp][kt + u * (KT / 2)][lane] = make_uint4(hi[0], hi[1], lo[0], lo[1]);
+        s_qf[warp][kt + u * (KT / 2)][lane] =
+            !pack4 ? make_uint4(hi[0], hi[1], lo[0], lo[1])
+                   : (g_id < 4 ? make_uint4(hi[0], hi[1], 0u, 0u) : make_uint4(lo[0], lo[1], 0u, 0u));
       }
     }
   }
@@ -532,6 +539,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   for (int i = 0; i < KT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
   while (cur.kblk) {
+    const Tile nxt = next_tile(cur);
     const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
     const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
     const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
@@ -556,51 +564,33 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
         }
         const uint4 qf = s_qf[warp][kt][lane];
         Mma<MT>::run((kt & 1) ? acc1 : acc, a, qf.x, qf.y);
-        if (Tr::kQSplit) Mma<MT>::run(acc2, a, qf.z, qf.w);
+        if (Tr::kQSplit && !pack4) Mma<MT>::run(acc2, a, qf.z, qf.w);
       }
     } else {
       // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
       const int pos0 = kpos0 + cur.r_lo + (slot0 - cur.s_lo);  // row g_id; row g_id + 8 is pos0 + 8
-#pragma unroll
-      for (int kt = 0; kt < KT / 2; ++kt) {
-        uint32_t araw[2][4];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int ktu = kt + u * (KT / 2);
-          if constexpr (FP8) {
-            const uint32_t r0w = comp(kr[0][ktu >> 2], ktu & 3), r1w = comp(kr[1][ktu >> 2], ktu & 3);
-            araw[u][0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
-            araw[u][2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
-            araw[u][1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
-            araw[u][3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
-          } else {
-            araw[u][0] = comp(kr[0][ktu >> 1], 2 * (ktu & 1));
-            araw[u][2] = comp(kr[0][ktu >> 1], 2 * (ktu & 1) + 1);
-            araw[u][1] = comp(kr[1][ktu >> 1], 2 * (ktu & 1));
-            araw[u][3] = comp(kr[1][ktu >> 1], 2 * (ktu & 1) + 1);
-          }
-        }
+      // rotate, split and multiply the k-tile pair (kt, kt + KT/2) given its raw fragments
+      auto rope_pair = [&](int kt, const uint32_t (&araw)[2][4]) {
         uint32_t ahi[2][4], alo[2][4];
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-          // (cos, sin) of this half's two frequencies at rows g_id (direct) and g_id + 8
-          float cs[2][2][2];  // [row][e][cos|sin]
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int f = frag_dim<FP8>(kt, half, e, q4);
-            rope_cos_sin(pos0, s_ropeF[f], cs[0][e][0], cs[0][e][1]);
-            const float2 r8 = s_rot8[f];
-            cs[1][e][0] = cs[0][e][0] * r8.x - cs[0][e][1] * r8.y;
-            cs[1][e][1] = cs[0][e][1] * r8.x + cs[0][e][0] * r8.y;
-          }
+          // (cos, sin) of this half's two frequencies f, f + 1 (packed fp32 pairs) at
+          // rows g_id (direct) and g_id + 8 (rotated by 8 positions)
+          const int f = frag_dim<FP8>(kt, half, 0, q4);
+          float2 cs_c[2], cs_s[2];  // [row] (cos f, cos f+1), (sin f, sin f+1)
+          rope_cos_sin(pos0, s_ropeF[f], cs_c[0].x, cs_s[0].x);
+          rope_cos_sin(pos0, s_ropeF[f + 1], cs_c[0].y, cs_s[0].y);
+          const float4 r8 = *reinterpret_cast<const float4*>(&s_rot8[f]);  // (c8, s8) of f, f+1
+          const float2 r8c = make_float2(r8.x, r8.z), r8s = make_float2(r8.y, r8.w);
+          cs_c[1] = sub_f2(mul_f2(cs_c[0], r8c), mul_f2(cs_s[0], r8s));
+          cs_s[1] = fma_f2(cs_s[0], r8c, mul_f2(cs_c[0], r8s));
 #pragma unroll
           for (int row = 0; row < 2; ++row) {
             const int ai = 2 * half + row;
             const float2 x = unpack2<MT>(araw[0][ai]);
             const float2 y = unpack2<MT>(araw[1][ai]);
-            const float c0 = cs[row][0][0], s0 = cs[row][0][1], c1 = cs[row][1][0], s1 = cs[row][1][1];
-            split2<MT>(x.x * c0 - y.x * s0, x.y * c1 - y.y * s1, ahi[0][ai], alo[0][ai]);
-            split2<MT>(y.x * c0 + x.x * s0, y.y * c1 + x.y * s1, ahi[1][ai], alo[1][ai]);
+            split2<MT>(sub_f2(mul_f2(x, cs_c[row]), mul_f2(y, cs_s[row])), ahi[0][ai], alo[0][ai]);
+            split2<MT>(fma_f2(y, cs_c[row], mul_f2(x, cs_s[row])), ahi[1][ai], alo[1][ai]);
           }
         }
 #pragma unroll
@@ -608,14 +598,40 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
           const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
           Mma<MT>::run(acc, ahi[u], qf.x, qf.y);
           Mma<MT>::run(acc1, alo[u], qf.x, qf.y);
-          Mma<MT>::run(acc2, ahi[u], qf.z, qf.w);
+          if (!pack4) Mma<MT>::run(acc2, ahi[u], qf.z, qf.w);
+        }
+      };
+      {
+#pragma unroll
+        for (int kt = 0; kt < KT / 2; ++kt) {
+          uint32_t araw[2][4];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int ktu = kt + u * (KT / 2);
+            if constexpr (FP8) {
+              const uint32_t r0w = comp(kr[0][ktu >> 2], ktu & 3), r1w = comp(kr[1][ktu >> 2], ktu & 3);
+              araw[u][0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
+              araw[u][2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
+              araw[u][1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
+              araw[u][3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
+            } else {
+              araw[u][0] = comp(kr[0][ktu >> 1], 2 * (ktu & 1));
+              araw[u][2] = comp(kr[0][ktu >> 1], 2 * (ktu & 1) + 1);
+              araw[u][1] = comp(kr[1][ktu >> 1], 2 * (ktu & 1));
+              araw[u][3] = comp(kr[1][ktu >> 1], 2 * (ktu & 1) + 1);
+            }
+          }
+          rope_pair(kt, araw);
         }
       }
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[i] += acc1[i] + acc2[i];
+    if (pack4) {  // score(h) = column h + column h + 4 (held two lanes over)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+    }
     // K registers are free: start the next tile's K loads
-    const Tile nxt = next_tile(cur);
     if (nxt.kblk) {
       load_k(nxt);
       prefetch_to(nxt.piece + 1 + kPrefetchPieces);

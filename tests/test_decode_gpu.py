@@ -126,7 +126,7 @@ def test_fp8_f16_query_and_simt_variant():
 
 @pytest.mark.parametrize("kv", ["bf16", "f16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("group", [1, 2, 4, 8, 16])
+@pytest.mark.parametrize("group", [1, 2, 4, 8, 12, 16])
 def test_shape_sweep(kv, D, group):
     rope = group % 2 == 0
     wl = _wl("llama3_8b_bf16", 10 + group, q_dtype=kv, kv_dtype=kv, out_dtype=kv, D=D,
@@ -134,6 +134,18 @@ def test_shape_sweep(kv, D, group):
              rotary_mode=int(rope))
     _check(wl, "mma")
     _check(wl, "mma", num_splits=4, max_kv_len_hint=300)
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 12])
+@pytest.mark.parametrize("rope", [0, 1])
+def test_fp8_group_sweep(group, rope):
+    # small slices (<= 4 heads) pack Q's lo part into the spare MMA columns; group 12
+    # has an 8-head slice and a 4-head slice per KV head
+    wl = _wl("fp8_kv_highconc", 40 + group, H_kv=2, H_qo=2 * group, B=3,
+             len_dist=("lognormal", 200, 0.5, 1, 500), pool=64, rotary_mode=rope,
+             rope_theta=1e4)
+    _check(wl, "mma")
+    _check(wl, "mma", num_splits=3, max_kv_len_hint=500)
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])
