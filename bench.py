@@ -46,6 +46,30 @@ def _dist():
     return ws, rank, local
 
 
+def _sources_digest() -> str:
+    """sha256 over the CUDA/C++ sources of the library (identifies the kernel build)."""
+    import hashlib
+    d = os.path.join(ROOT, "paged_kv_decode_19_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()
+
+
+def _measured_traffic(config: str, batch: int):
+    """DRAM bytes (read + write) of one decode launch from the committed ncu record, if
+    it was taken on the current sources and the same workload; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(f"{config}:B={batch}")
+    if not rec or rec.get("sources_sha256") != _sources_digest():
+        return None
+    return int(rec["dram_bytes_per_launch"])
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -177,7 +201,7 @@ def run_ours(args, ws, rank, local):
     # read: cold and clean).
     reps = []
     for _ in range(2):
-        wl = W.make(args.config, seed=1000 + rank, device=dev)
+        wl = W.make(args.config, seed=1000 + rank, device=dev, **args.over)
         reps.append((wl,) + _append_inputs(wl, dev))
     wl = reps[0][0]
     s = wl.spec
@@ -301,10 +325,13 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--B", type=int, default=None,
+                    help="override the batch size (smaller cases for profiling)")
     args = ap.parse_args()
+    args.over = {} if args.B is None else {"B": args.B}
     args.warmup = max(args.warmup, 3)
     ws, rank, local = _dist()
-    spec = W.spec(args.config)
+    spec = W.spec(args.config, **args.over)
     cfg = {"workload": f"{args.config}: B={spec.B}, H_qo={spec.H_qo}, H_kv={spec.H_kv}, "
                        f"D={spec.D}, page_size={spec.page_size}, {spec.kv_dtype} KV",
            "B": spec.B, "H_qo": spec.H_qo, "H_kv": spec.H_kv, "D": spec.D,
@@ -317,7 +344,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        wl = W.make(args.config, seed=1000)
+        wl = W.make(args.config, seed=1000, **args.over)
         for _ in range(args.warmup):
             _oracle_sample(wl, 0.0)
         times = []
@@ -377,7 +404,8 @@ def main():
         "kv_read_gbs": round(kv_bytes / (dec_us * 1e-6) / 1e9, 1),
         "decode_variant": res["variant"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": _measured_traffic(args.config, spec.B),
                      "kernel": f"decode_{res['variant']}_kernel",
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(e2e_us / ws, 2), "unit": UNIT,

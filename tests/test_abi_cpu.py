@@ -77,6 +77,20 @@ def test_decode_null_pointers_rejected(L):
     assert b"RoPE" in L.pd_get_last_error_string()
 
 
+def test_decode_rejects_unaligned_q_or_pages(L):
+    # the kernels read Q and K/V rows with 16-byte vector loads: a pointer that is only
+    # element-aligned must be refused on the host, before any CUDA call (the pointers
+    # below are never dereferenced)
+    d = _desc()
+    p = ctypes.c_void_p
+    args = lambda q, pages: (p(q), p(pages), p(64), p(128), p(192), None, None, p(256), p(320), 0,
+                             1.0, 1e4, 0.1, ctypes.byref(d), None)
+    st = L.pd_batch_decode_paged_kv(*args(4096, 8194))
+    assert _lib.STATUS[st] == "PD_ERR_INVALID_ARG" and b"16-byte" in L.pd_get_last_error_string()
+    st = L.pd_batch_decode_paged_kv(*args(4098, 8192))
+    assert _lib.STATUS[st] == "PD_ERR_INVALID_ARG" and b"16-byte" in L.pd_get_last_error_string()
+
+
 def test_merge_and_append_validation_without_gpu(L):
     assert _lib.STATUS[L.pd_merge_state_inplace(None, None, None, None, 2, 2, 64, 3, None)] == "PD_ERR_INVALID_ARG"
     assert _lib.STATUS[L.pd_merge_state_inplace(None, None, None, None, 2, 2, 64, 0, None)] == "PD_ERR_INVALID_ARG"
