@@ -46,7 +46,7 @@ typedef enum {
   PD_ERR_BAD_PAGE = 4,      /* device: a page id or sequence offset was out of range */
   PD_ERR_BAD_LENGTH = 5,    /* device: length_info inconsistent, or more KV chunks than planned */
   PD_ERR_BAD_SLOT = 6,      /* device: an append slot lay beyond max_pages*page_size */
-  PD_ERR_TIMEOUT = 7,       /* device: an internal pipeline wait gave up (never expected) */
+  PD_ERR_TIMEOUT = 7,       /* device: reserved (the current kernels have no waits) */
   PD_ERR_WORKSPACE = 8      /* caller workspace too small or misaligned */
 } pd_status;
 

@@ -1,9 +1,9 @@
 // Device-side building blocks shared by the libpageddecode kernels (sm_103a).
 //
-// Everything here is inline PTX or CUDA intrinsics: mbarrier + TMA (bulk tensor
-// copies) for staging KV pages in shared memory, ldmatrix + mma.sync for the
-// small dense contractions, FP8/bf16/f16 conversions, the device error word and
-// bounded waits (no wait in this library can spin forever).
+// Everything here is inline PTX or CUDA intrinsics: mma.sync for the small dense
+// contractions, packed fp32x2 arithmetic, FP8/bf16/f16 conversions, the RoPE angle,
+// L2 prefetches and the device error word.  No kernel of this library waits on a
+// flag or barrier that another block sets.
 #pragma once
 
 #include <cuda.h>
@@ -19,10 +19,8 @@ namespace pd {
 enum : int { kF32 = 0, kF16 = 1, kBF16 = 2, kE4M3 = 3 };
 
 // device error word bits
+// (kErrTimeout is reserved: the current kernels have no wait that could time out)
 enum : unsigned { kErrBadPage = 1u, kErrBadLength = 2u, kErrBadSlot = 4u, kErrTimeout = 8u };
-
-// A wait that has not completed after this long is abandoned (error bit set).
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 // Initial running max of the online softmax (the TVM decode kernel's -5e4 sentinel);
 // together with d = 0 it is the empty state and the merge identity.
@@ -167,18 +165,6 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
-// 16-byte asynchronous global -> shared copy (L2 only), and its group commit / wait.
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const uint32_t d = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-// wait until at most one committed group (the most recent) is still pending
-__device__ __forceinline__ void cp_async_wait_all_but_last() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
-}
-
 // Block `part` of `parts` prefetches its share of [base, base + bytes) into L2 (the
 // 16-byte aligned interior only: nothing outside the array is touched).
 __device__ __forceinline__ void prefetch_l2_share(const void* base, size_t bytes, unsigned part,
@@ -197,88 +183,7 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }
 
-// ----------------------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return (uint32_t)__cvta_generic_to_shared(p);
-}
-
-__device__ __forceinline__ unsigned long long global_timer() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait for phase `parity` of an mbarrier; false after kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const unsigned long long t0 = global_timer();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer() - t0 > kWaitLimitNs) return false;
-  }
-  return true;
-}
-
-// 3-D tiled TMA load global -> shared, completion signalled on `bar` (tx bytes).
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z)
-      : "memory");
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                        uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
-                                          uint32_t& r3) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];"
-               : "=r"(r0), "=r"(r1)
-               : "r"(addr)
-               : "memory");
-}
-__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
-
-// D += A(16x16) * B(16x8), fp32 accumulate
+// ----------------------------------------------------------------------------- mma.sync
 template <typename T> struct Mma;
 template <> struct Mma<__nv_bfloat16> {
   static __device__ __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,

