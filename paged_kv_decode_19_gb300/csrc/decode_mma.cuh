@@ -44,6 +44,10 @@ namespace pd {
 #define PD_PREFETCH_PIECES 1
 #endif
 constexpr int kPrefetchPieces = PD_PREFETCH_PIECES;  // L2 prefetch distance, in pages
+#ifndef PD_QK_CHAINS
+#define PD_QK_CHAINS 2
+#endif
+constexpr int kQChains = PD_QK_CHAINS;  // independent accumulators of a tile's K Q^T
 #ifndef PD_MIN_BLOCKS_PLAIN
 #define PD_MIN_BLOCKS_PLAIN 1
 #endif
@@ -398,36 +402,36 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   const int kpos0 = ROPE ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
 
   // ---------------------------------------------------------------- tile stream
-  // Pieces [ua, pend) in order; their page ids are looked up 32 at a time (one per
-  // lane) and handed out with a shuffle.  A second cursor runs kPrefetchPieces pieces
-  // ahead and prefetches each page's K and V blocks into L2, so that the register loads
-  // of a tile mostly hit L2 and each warp keeps several pages in flight without
-  // spending registers on them.
+  // Pieces [ua, pend) in order.  Entering a piece, the warp prefetches the K and V
+  // blocks of the piece kPrefetchPieces ahead into L2, so that the register loads of a
+  // tile mostly hit L2 and each warp keeps more than one page in flight without
+  // spending registers on it.
   struct Tile {
     int piece, t, s_lo, s_hi, r_lo;
     const uint8_t* kblk;  // K block of (page, hk); nullptr = no more tiles
   };
-  struct PageBatch {
-    int base, page;  // pieces [base, base + 32): lane i holds the page of piece base + i
-  };
-  auto page_of = [&](PageBatch& pb, int j) -> int {  // j warp-uniform, ua <= j < pend
-    if (j >= pb.base + 32) {
-      pb.base = j;
-      const int jj = j + lane;
-      pb.page = jj < pend ? lookup_page(p, sg.seq, get_piece(pcs, jj, P).page_idx) : -1;
+  // This warp's pieces come 32 at a time: lane i holds piece base + i (its physical
+  // page or -1, its slot range, its first row), handed out with shuffles, so moving to
+  // the next piece costs a few shuffles and one (warp-uniform) branch.
+  int pb_base = -64, pb_page = -1, pb_slots = 0, pb_row = 0;
+  auto load_batch = [&](int j) {
+    pb_base = j;
+    const int jj = j + lane;
+    pb_page = -1;
+    if (jj < pend) {
+      const Piece pc = get_piece(pcs, jj, P);
+      pb_page = lookup_page(p, sg.seq, pc.page_idx);  // -1 (error recorded) if out of range
+      pb_slots = pc.s_lo | (pc.s_hi << 16);            // s_hi <= P <= 256
+      pb_row = pc.r_lo;
     }
-    return __shfl_sync(0xffffffffu, pb.page, j - pb.base);
   };
-  PageBatch pb_main{-64, -1}, pb_pf{-64, -1};
-  int pf_next = ua + 1;  // next piece to prefetch (the first is loaded straight away)
-  auto prefetch_to = [&](int jend) {  // prefetch pieces [pf_next, jend)
-    jend = min(jend, pend);
-    for (; pf_next < jend; ++pf_next) {
-      const int pg = page_of(pb_pf, pf_next);
+  auto kblock = [&](int pg) { return kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes; };
+  auto prefetch_piece = [&](int j) {  // K and V blocks of piece j into L2 (if in this batch)
+    if (j < pend && j < pb_base + 32) {
+      const int pg = __shfl_sync(0xffffffffu, pb_page, j - pb_base);
       if (pg >= 0 && lane == 0) {
-        const uint8_t* kb = kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes;
-        prefetch_l2_bulk(kb, (uint32_t)block_bytes);
-        prefetch_l2_bulk(kb + v_off, (uint32_t)block_bytes);
+        prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
+        prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
       }
     }
   };
@@ -435,15 +439,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     Tile tl;
     tl.kblk = nullptr;
     for (; j < pend; ++j) {
-      const int pg = page_of(pb_main, j);
+      if (j >= pb_base + 32) load_batch(j);
+      const int src = j - pb_base;
+      const int pg = __shfl_sync(0xffffffffu, pb_page, src);
       if (pg < 0) continue;  // bad page id: its rows are skipped (error already recorded)
-      const Piece pc = get_piece(pcs, j, P);
+      const int sl = __shfl_sync(0xffffffffu, pb_slots, src);
       tl.piece = j;
-      tl.t = pc.s_lo >> 4;
-      tl.s_lo = pc.s_lo;
-      tl.s_hi = pc.s_hi;
-      tl.r_lo = pc.r_lo;
-      tl.kblk = kv_base + (((size_t)pg * 2) * p.H_kv + hk) * block_bytes;
+      tl.s_lo = sl & 0xffff;
+      tl.s_hi = sl >> 16;
+      tl.t = tl.s_lo >> 4;
+      tl.r_lo = __shfl_sync(0xffffffffu, pb_row, src);
+      tl.kblk = kblock(pg);
       break;
     }
     return tl;
@@ -481,7 +487,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   if (cur.kblk) {
     load_k(cur);
     load_v(cur);
-    prefetch_to(cur.piece + 1 + kPrefetchPieces);  // after the tile's own loads
+    prefetch_piece(cur.piece + kPrefetchPieces);  // after the tile's own loads
   }
 
   // ---------------------------------------------------------------- Q^T B fragments
@@ -545,7 +551,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
     // ------------------------------------------------------------ S^T = K Q^T
     // independent accumulators shorten the dependent MMA chain; summed after
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+    // spread over kQChains independent accumulators: the products of one tile would
+    // otherwise form long chains of dependent MMAs (mma.sync latency, not throughput,
+    // bounds the tile loop)
+    float qacc[kQChains][4];
+#pragma unroll
+    for (int c = 0; c < kQChains; ++c) qacc[c][0] = qacc[c][1] = qacc[c][2] = qacc[c][3] = 0.f;
     if constexpr (!ROPE) {
 #pragma unroll
       for (int kt = 0; kt < KT; ++kt) {
@@ -563,8 +574,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
           a[3] = comp(kr[1][kt >> 1], 2 * (kt & 1) + 1);
         }
         const uint4 qf = s_qf[warp][kt][lane];
-        Mma<MT>::run((kt & 1) ? acc1 : acc, a, qf.x, qf.y);
-        if (Tr::kQSplit && !pack4) Mma<MT>::run(acc2, a, qf.z, qf.w);
+        Mma<MT>::run(qacc[(2 * kt) % kQChains], a, qf.x, qf.y);
+        if (Tr::kQSplit && !pack4) Mma<MT>::run(qacc[(2 * kt + 1) % kQChains], a, qf.z, qf.w);
       }
     } else {
       // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
@@ -596,9 +607,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
-          Mma<MT>::run(acc, ahi[u], qf.x, qf.y);
-          Mma<MT>::run(acc1, alo[u], qf.x, qf.y);
-          if (!pack4) Mma<MT>::run(acc2, ahi[u], qf.z, qf.w);
+          Mma<MT>::run(qacc[(3 * u + kt) % kQChains], ahi[u], qf.x, qf.y);
+          Mma<MT>::run(qacc[(3 * u + kt + 1) % kQChains], alo[u], qf.x, qf.y);
+          if (!pack4) Mma<MT>::run(qacc[(3 * u + kt + 2) % kQChains], ahi[u], qf.z, qf.w);
         }
       };
       {
@@ -625,8 +636,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
         }
       }
     }
+    float acc[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[i] += acc1[i] + acc2[i];
+    for (int i = 0; i < 4; ++i) {
+      acc[i] = qacc[0][i];
+#pragma unroll
+      for (int c = 1; c < kQChains; ++c) acc[i] += qacc[c][i];
+    }
     if (pack4) {  // score(h) = column h + column h + 4 (held two lanes over)
 #pragma unroll
       for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
@@ -634,7 +650,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     // K registers are free: start the next tile's K loads
     if (nxt.kblk) {
       load_k(nxt);
-      prefetch_to(nxt.piece + 1 + kPrefetchPieces);
+      if (nxt.piece != cur.piece) prefetch_piece(nxt.piece + kPrefetchPieces);
     }
     // ------------------------------------------------------------ online softmax (log2)
     float sc[4];
