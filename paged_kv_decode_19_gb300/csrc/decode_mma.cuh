@@ -437,7 +437,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   };
   auto first_tile_from = [&](int j) -> Tile {  // first tile of piece j or later
     Tile tl;
-    tl.kblk = nullptr;
+    tl.kblk = nullptr;  // no more tiles (the other fields stay defined)
+    tl.piece = pend;
+    tl.t = tl.s_lo = tl.s_hi = tl.r_lo = 0;
     for (; j < pend; ++j) {
       if (j >= pb_base + 32) load_batch(j);
       const int src = j - pb_base;
@@ -464,19 +466,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   };
   uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
   uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
-  auto load_k = [&](const Tile& c) {
+  auto load_k = [&](const uint8_t* kblk, int t) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const uint8_t* row = c.kblk + (size_t)(c.t * 16 + g_id + 8 * rr) * RB;
+      const uint8_t* row = kblk + (size_t)(t * 16 + g_id + 8 * rr) * RB;
 #pragma unroll
       for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = ldg_stream(row + (4 * ch + q4) * 16);
     }
   };
-  auto load_v = [&](const Tile& c) {
+  auto load_v = [&](const uint8_t* kblk, int t) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row_in_page = c.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
-      const uint8_t* row = c.kblk + v_off + (size_t)row_in_page * RB;
+      const int row_in_page = t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
+      const uint8_t* row = kblk + v_off + (size_t)row_in_page * RB;
 #pragma unroll
       for (int j = 0; j < VCH; ++j) vr[i][j] = ldg_stream(row + (g_id + 8 * j) * 16);
     }
@@ -485,8 +487,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   // first tile's loads go out before the Q set-up, which then overlaps their latency
   Tile cur = first_tile_from(ua);
   if (cur.kblk) {
-    load_k(cur);
-    load_v(cur);
+    load_k(cur.kblk, cur.t);
+    load_v(cur.kblk, cur.t);
     prefetch_piece(cur.piece + kPrefetchPieces);  // after the tile's own loads
   }
 
@@ -648,9 +650,19 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
     }
     // K registers are free: start the next tile's K loads
-    if (nxt.kblk) {
-      load_k(nxt);
-      if (nxt.piece != cur.piece) prefetch_piece(nxt.piece + kPrefetchPieces);
+    // next tile's K (after the last tile: this tile's block again, never used), then the
+    // L2 prefetch when a new piece starts
+    const uint8_t* nk = nxt.kblk ? nxt.kblk : cur.kblk;
+    const int nt = nxt.kblk ? nxt.t : cur.t;
+    load_k(nk, nt);
+    {
+      const int jpf = nxt.piece + kPrefetchPieces;
+      const bool pf = nxt.kblk && nxt.piece != cur.piece && jpf < pend && jpf < pb_base + 32;
+      const int pg = __shfl_sync(0xffffffffu, pb_page, min(max(jpf - pb_base, 0), 31));
+      if (pf && pg >= 0 && lane == 0) {
+        prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
+        prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
+      }
     }
     // ------------------------------------------------------------ online softmax (log2)
     float sc[4];
@@ -671,7 +683,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     st_d[1] = st_d[1] * al1 + pr[1] + pr[3];
     st_m[0] = mn0;
     st_m[1] = mn1;
-    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+    // 16-bit KV: unconditional (the vote and branch cost more than the multiplies);
+    // FP8 tiles carry half the bytes, there skipping the multiplies when no maximum
+    // moved measures faster
+    if (!FP8 || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         oacc[mt][0] *= al0;
@@ -696,14 +711,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     }
     // rows of this thread's V^T halves: 2q, 2q+1 (a0, a1) and 2q+8, 2q+9 (a2, a3);
     // rows outside the piece may hold anything (even NaN): zero them
-    uint32_t vm01 = 0xffffffffu, vm23 = 0xffffffffu;
-    if ((cur.t * 16 < cur.s_lo) || (cur.t * 16 + 16 > cur.s_hi)) {
-      const int rA = cur.t * 16 + 2 * q4, rB = rA + 8;
-      vm01 = ((rA >= cur.s_lo && rA < cur.s_hi) ? 0x0000ffffu : 0u) |
-             ((rA + 1 >= cur.s_lo && rA + 1 < cur.s_hi) ? 0xffff0000u : 0u);
-      vm23 = ((rB >= cur.s_lo && rB < cur.s_hi) ? 0x0000ffffu : 0u) |
-             ((rB + 1 >= cur.s_lo && rB + 1 < cur.s_hi) ? 0xffff0000u : 0u);
-    }
+    // (computed without a branch; all-ones for the rows of a full tile)
+    const int rA = cur.t * 16 + 2 * q4, rB = rA + 8;
+    const uint32_t vm01 = ((rA >= cur.s_lo && rA < cur.s_hi) ? 0x0000ffffu : 0u) |
+                          ((rA + 1 >= cur.s_lo && rA + 1 < cur.s_hi) ? 0xffff0000u : 0u);
+    const uint32_t vm23 = ((rB >= cur.s_lo && rB < cur.s_hi) ? 0x0000ffffu : 0u) |
+                          ((rB + 1 >= cur.s_lo && rB + 1 < cur.s_hi) ? 0xffff0000u : 0u);
     // ------------------------------------------------------------ O^T += V^T P^T
 #pragma unroll
     for (int mt = 0; mt < KT; ++mt) {
@@ -728,7 +741,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       }
       Mma<MT>::run(oacc[mt], a, pb0, pb1);
     }
-    if (nxt.kblk) load_v(nxt);
+    load_v(nk, nt);
     cur = nxt;
   }
   st_d[0] = sum_over_groups(st_d[0]);
