@@ -267,33 +267,50 @@ def run_ours(args, ws, rank, local):
     # the same steps after a flush of L2 (for comparison; not the reported value)
     _, dec_flushed_ms, _ = timed_steps(max(args.steps // 2, 3), flush=True)
 
-    # end-to-end through the public API from pinned host buffers
+    # end-to-end through the public API from pinned host memory: every step copies its
+    # inputs (one pinned staging buffer holding Q, the page table, length_info, the RoPE
+    # positions and the new tokens' K/V and slots) to the device, runs append + decode on
+    # views of that buffer, and reads out + lse back (one buffer); synchronous per step
     names = ("Q", "indptr", "values", "length_info", "k_rope_pos_offset", "q_rope_position")
-    host_in = {k: getattr(wl, k).cpu().pin_memory() for k in names}
-    host_in["k_new"], host_in["v_new"], host_in["slots"] = (reps[0][1].cpu().pin_memory(),
-                                                            reps[0][2].cpu().pin_memory(),
-                                                            reps[0][3].cpu().pin_memory())
-    dev_in = [{k: torch.empty_like(v, device=dev) for k, v in host_in.items()} for _ in range(2)]
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    srcs = {k: getattr(wl, k) for k in names}
+    srcs["k_new"], srcs["v_new"], srcs["slots"] = reps[0][1], reps[0][2], reps[0][3]
+    offs, total = {}, 0
+    for k, t in srcs.items():
+        total = (total + 255) // 256 * 256
+        offs[k] = total
+        total += t.numel() * t.element_size()
+    host_in = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for k, t in srcs.items():
+        nb = t.numel() * t.element_size()
+        host_in[offs[k]:offs[k] + nb].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    dev_in = [torch.empty(total, dtype=torch.uint8, device=dev) for _ in range(2)]
+
+    def views(buf):
+        return {k: buf[offs[k]:offs[k] + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                for k, t in srcs.items()}
+    dv = [views(b) for b in dev_in]
+    out_bytes = out.numel() * out.element_size()
+    lse_off = (out_bytes + 255) // 256 * 256
+    res_dev = torch.empty(lse_off + lse.numel() * 4, dtype=torch.uint8, device=dev)
+    out_e = res_dev[:out_bytes].view(out.dtype).view(out.shape)
+    lse_e = res_dev[lse_off:].view(torch.float32).view(lse.shape)
+    res_host = torch.empty(res_dev.numel(), dtype=torch.uint8).pin_memory()
+    h2d = total
+    d2h = res_dev.numel()
     e2e_ms = []
     for i in range(args.warmup + args.steps):
-        w, di = reps[i % 2][0], dev_in[i % 2]
+        w, di, buf = reps[i % 2][0], dv[i % 2], dev_in[i % 2]
         if not alternate:
             flush_l2()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for k, v in host_in.items():
-            di[k].copy_(v, non_blocking=True)
+        buf.copy_(host_in, non_blocking=True)
         pd.append_paged_kv(w.pages, di["k_new"], di["v_new"], di["slots"], w.k_scale, w.v_scale)
         pd.batch_decode_paged_kv(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
-                                 di["k_rope_pos_offset"], di["q_rope_position"], out, lse,
+                                 di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e,
                                  s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
                                  k_scale=w.k_scale, v_scale=w.v_scale, **split)
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        res_host.copy_(res_dev, non_blocking=True)
         b.record(stream)
         b.synchronize()
         if i >= args.warmup:

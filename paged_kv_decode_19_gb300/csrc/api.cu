@@ -51,6 +51,9 @@ struct DeviceState {
   size_t cnt_bytes = 0;
   void* ws = nullptr;   // partial (out, lse) of split sequences
   size_t ws_bytes = 0;
+  // resident blocks per SM of each kernel variant, queried once:
+  // [mma][q_dtype][kv_dtype][D 64/128/256][rotary]; 0 = not yet known
+  int occupancy[2][4][4][3][2] = {};
 };
 constexpr int kMaxDevices = 64;
 static DeviceState g_dev[kMaxDevices];
@@ -204,7 +207,15 @@ pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_
   return PD_OK;
 }
 
-static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary, int* ctas) {
+static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary, int* ctas,
+                               DeviceState* ds = nullptr) {
+  const int di = d->D == 64 ? 0 : d->D == 128 ? 1 : 2;
+  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rotary ? 1 : 0]
+                   : nullptr;
+  if (cached && *cached > 0) {
+    *ctas = *cached;
+    return PD_OK;
+  }
   DecodeParams p{};
   p.D = d->D;
   p.P = d->page_size;
@@ -221,6 +232,7 @@ static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary
   }
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   *ctas = std::max(n, 1);
+  if (cached) *cached = *ctas;
   return PD_OK;
 }
 
@@ -234,7 +246,7 @@ size_t pd_workspace_size(const pd_decode_desc* desc) {
     if (mma && !mma_path(desc, nullptr)) continue;
     for (int rot = 0; rot < 2; ++rot) {
       int ctas = 1;
-      if (occupancy_for(desc, mma != 0, rot, &ctas) != PD_OK) continue;
+      if (occupancy_for(desc, mma != 0, rot, &ctas, ds) != PD_OK) continue;
       int mode, grid;
       size_t ws;
       plan_impl(desc, ds->num_sms, ctas, mma ? kMmaWarps : 1, &mode, &grid, &ws);
@@ -281,7 +293,7 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   if (st != PD_OK) return st;
   const bool use_mma = mma_path(desc, pages);
   int ctas = 1;
-  st = occupancy_for(desc, use_mma, rotary_mode, &ctas);
+  st = occupancy_for(desc, use_mma, rotary_mode, &ctas, ds);
   if (st != PD_OK) return st;
   int mode = 0, grid_blocks = 0;
   size_t ws_need = 0;
