@@ -35,6 +35,8 @@
 // Limits: head dim 64/128 for 16-bit KV, 128 for FP8; page size a multiple of 16.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_common.cuh"
 #include "kernels.h"
 
@@ -546,203 +548,219 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 #pragma unroll
   for (int i = 0; i < KT; ++i) oacc[i][0] = oacc[i][1] = oacc[i][2] = oacc[i][3] = 0.f;
 
+  // The tile loop, instantiated with the Q packing decided at compile time (it is
+  // fixed for a segment; a runtime test inside the unrolled QK costs branches per tile).
+  auto tile_loop = [&](auto pack_tag) {
+    constexpr bool PK = decltype(pack_tag)::value;
   while (cur.kblk) {
-    const Tile nxt = next_tile(cur);
-    const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
-    const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
-    const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
-    // ------------------------------------------------------------ S^T = K Q^T
-    // independent accumulators shorten the dependent MMA chain; summed after
-    // spread over kQChains independent accumulators: the products of one tile would
-    // otherwise form long chains of dependent MMAs (mma.sync latency, not throughput,
-    // bounds the tile loop)
-    float qacc[kQChains][4];
-#pragma unroll
-    for (int c = 0; c < kQChains; ++c) qacc[c][0] = qacc[c][1] = qacc[c][2] = qacc[c][3] = 0.f;
-    if constexpr (!ROPE) {
-#pragma unroll
-      for (int kt = 0; kt < KT; ++kt) {
-        uint32_t a[4];
-        if constexpr (FP8) {
-          const uint32_t r0w = comp(kr[0][kt >> 2], kt & 3), r1w = comp(kr[1][kt >> 2], kt & 3);
-          a[0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
-          a[2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
-          a[1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
-          a[3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
-        } else {
-          a[0] = comp(kr[0][kt >> 1], 2 * (kt & 1));
-          a[2] = comp(kr[0][kt >> 1], 2 * (kt & 1) + 1);
-          a[1] = comp(kr[1][kt >> 1], 2 * (kt & 1));
-          a[3] = comp(kr[1][kt >> 1], 2 * (kt & 1) + 1);
-        }
-        const uint4 qf = s_qf[warp][kt][lane];
-        Mma<MT>::run(qacc[(2 * kt) % kQChains], a, qf.x, qf.y);
-        if (Tr::kQSplit && !pack4) Mma<MT>::run(qacc[(2 * kt + 1) % kQChains], a, qf.z, qf.w);
-      }
-    } else {
-      // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
-      const int pos0 = kpos0 + cur.r_lo + (slot0 - cur.s_lo);  // row g_id; row g_id + 8 is pos0 + 8
-      // rotate, split and multiply the k-tile pair (kt, kt + KT/2) given its raw fragments
-      auto rope_pair = [&](int kt, const uint32_t (&araw)[2][4]) {
-        uint32_t ahi[2][4], alo[2][4];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          // (cos, sin) of this half's two frequencies f, f + 1 (packed fp32 pairs) at
-          // rows g_id (direct) and g_id + 8 (rotated by 8 positions)
-          const int f = frag_dim<FP8>(kt, half, 0, q4);
-          float2 cs_c[2], cs_s[2];  // [row] (cos f, cos f+1), (sin f, sin f+1)
-          rope_cos_sin(pos0, s_ropeF[f], cs_c[0].x, cs_s[0].x);
-          rope_cos_sin(pos0, s_ropeF[f + 1], cs_c[0].y, cs_s[0].y);
-          const float4 r8 = *reinterpret_cast<const float4*>(&s_rot8[f]);  // (c8, s8) of f, f+1
-          const float2 r8c = make_float2(r8.x, r8.z), r8s = make_float2(r8.y, r8.w);
-          cs_c[1] = sub_f2(mul_f2(cs_c[0], r8c), mul_f2(cs_s[0], r8s));
-          cs_s[1] = fma_f2(cs_s[0], r8c, mul_f2(cs_c[0], r8s));
-#pragma unroll
-          for (int row = 0; row < 2; ++row) {
-            const int ai = 2 * half + row;
-            const float2 x = unpack2<MT>(araw[0][ai]);
-            const float2 y = unpack2<MT>(araw[1][ai]);
-            split2<MT>(sub_f2(mul_f2(x, cs_c[row]), mul_f2(y, cs_s[row])), ahi[0][ai], alo[0][ai]);
-            split2<MT>(fma_f2(y, cs_c[row], mul_f2(x, cs_s[row])), ahi[1][ai], alo[1][ai]);
+      const Tile nxt = next_tile(cur);
+      const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
+      const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
+      const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
+      // ------------------------------------------------------------ S^T = K Q^T
+      // independent accumulators shorten the dependent MMA chain; summed after
+      // spread over kQChains independent accumulators: the products of one tile would
+      // otherwise form long chains of dependent MMAs (mma.sync latency, not throughput,
+      // bounds the tile loop)
+      float qacc[kQChains][4];
+  #pragma unroll
+      for (int c = 0; c < kQChains; ++c) qacc[c][0] = qacc[c][1] = qacc[c][2] = qacc[c][3] = 0.f;
+      if constexpr (!ROPE) {
+  #pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+          uint32_t a[4];
+          if constexpr (FP8) {
+            const uint32_t r0w = comp(kr[0][kt >> 2], kt & 3), r1w = comp(kr[1][kt >> 2], kt & 3);
+            a[0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
+            a[2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
+            a[1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
+            a[3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
+          } else {
+            a[0] = comp(kr[0][kt >> 1], 2 * (kt & 1));
+            a[2] = comp(kr[0][kt >> 1], 2 * (kt & 1) + 1);
+            a[1] = comp(kr[1][kt >> 1], 2 * (kt & 1));
+            a[3] = comp(kr[1][kt >> 1], 2 * (kt & 1) + 1);
           }
+          const uint4 qf = s_qf[warp][kt][lane];
+          Mma<MT>::run(qacc[(2 * kt) % kQChains], a, qf.x, qf.y);
+          if (Tr::kQSplit && !PK) Mma<MT>::run(qacc[(2 * kt + 1) % kQChains], a, qf.z, qf.w);
         }
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
-          Mma<MT>::run(qacc[(3 * u + kt) % kQChains], ahi[u], qf.x, qf.y);
-          Mma<MT>::run(qacc[(3 * u + kt + 1) % kQChains], alo[u], qf.x, qf.y);
-          if (!pack4) Mma<MT>::run(qacc[(3 * u + kt + 2) % kQChains], ahi[u], qf.z, qf.w);
-        }
-      };
-      {
-#pragma unroll
-        for (int kt = 0; kt < KT / 2; ++kt) {
-          uint32_t araw[2][4];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int ktu = kt + u * (KT / 2);
-            if constexpr (FP8) {
-              const uint32_t r0w = comp(kr[0][ktu >> 2], ktu & 3), r1w = comp(kr[1][ktu >> 2], ktu & 3);
-              araw[u][0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
-              araw[u][2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
-              araw[u][1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
-              araw[u][3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
-            } else {
-              araw[u][0] = comp(kr[0][ktu >> 1], 2 * (ktu & 1));
-              araw[u][2] = comp(kr[0][ktu >> 1], 2 * (ktu & 1) + 1);
-              araw[u][1] = comp(kr[1][ktu >> 1], 2 * (ktu & 1));
-              araw[u][3] = comp(kr[1][ktu >> 1], 2 * (ktu & 1) + 1);
+      } else {
+        // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
+        const int pos0 = kpos0 + cur.r_lo + (slot0 - cur.s_lo);  // row g_id; row g_id + 8 is pos0 + 8
+        // rotate, split and multiply the k-tile pair (kt, kt + KT/2) given its raw fragments
+        auto rope_pair = [&](int kt, const uint32_t (&araw)[2][4]) {
+          uint32_t ahi[2][4], alo[2][4];
+  #pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            // (cos, sin) of this half's two frequencies f, f + 1 (packed fp32 pairs) at
+            // rows g_id (direct) and g_id + 8 (rotated by 8 positions)
+            const int f = frag_dim<FP8>(kt, half, 0, q4);
+            float2 cs_c[2], cs_s[2];  // [row] (cos f, cos f+1), (sin f, sin f+1)
+            rope_cos_sin(pos0, s_ropeF[f], cs_c[0].x, cs_s[0].x);
+            rope_cos_sin(pos0, s_ropeF[f + 1], cs_c[0].y, cs_s[0].y);
+            const float4 r8 = *reinterpret_cast<const float4*>(&s_rot8[f]);  // (c8, s8) of f, f+1
+            const float2 r8c = make_float2(r8.x, r8.z), r8s = make_float2(r8.y, r8.w);
+            cs_c[1] = sub_f2(mul_f2(cs_c[0], r8c), mul_f2(cs_s[0], r8s));
+            cs_s[1] = fma_f2(cs_s[0], r8c, mul_f2(cs_c[0], r8s));
+  #pragma unroll
+            for (int row = 0; row < 2; ++row) {
+              const int ai = 2 * half + row;
+              const float2 x = unpack2<MT>(araw[0][ai]);
+              const float2 y = unpack2<MT>(araw[1][ai]);
+              split2<MT>(sub_f2(mul_f2(x, cs_c[row]), mul_f2(y, cs_s[row])), ahi[0][ai], alo[0][ai]);
+              split2<MT>(fma_f2(y, cs_c[row], mul_f2(x, cs_s[row])), ahi[1][ai], alo[1][ai]);
             }
           }
-          rope_pair(kt, araw);
+  #pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
+            Mma<MT>::run(qacc[(3 * u + kt) % kQChains], ahi[u], qf.x, qf.y);
+            Mma<MT>::run(qacc[(3 * u + kt + 1) % kQChains], alo[u], qf.x, qf.y);
+            if (!PK) Mma<MT>::run(qacc[(3 * u + kt + 2) % kQChains], ahi[u], qf.z, qf.w);
+          }
+        };
+        {
+  #pragma unroll
+          for (int kt = 0; kt < KT / 2; ++kt) {
+            uint32_t araw[2][4];
+  #pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int ktu = kt + u * (KT / 2);
+              if constexpr (FP8) {
+                const uint32_t r0w = comp(kr[0][ktu >> 2], ktu & 3), r1w = comp(kr[1][ktu >> 2], ktu & 3);
+                araw[u][0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
+                araw[u][2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
+                araw[u][1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
+                araw[u][3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
+              } else {
+                araw[u][0] = comp(kr[0][ktu >> 1], 2 * (ktu & 1));
+                araw[u][2] = comp(kr[0][ktu >> 1], 2 * (ktu & 1) + 1);
+                araw[u][1] = comp(kr[1][ktu >> 1], 2 * (ktu & 1));
+                araw[u][3] = comp(kr[1][ktu >> 1], 2 * (ktu & 1) + 1);
+              }
+            }
+            rope_pair(kt, araw);
+          }
         }
       }
-    }
-    float acc[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[i] = qacc[0][i];
-#pragma unroll
-      for (int c = 1; c < kQChains; ++c) acc[i] += qacc[c][i];
-    }
-    if (pack4) {  // score(h) = column h + column h + 4 (held two lanes over)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
-    }
-    // K registers are free: start the next tile's K loads
-    // next tile's K (after the last tile: this tile's block again, never used), then the
-    // L2 prefetch when a new piece starts
-    const uint8_t* nk = nxt.kblk ? nxt.kblk : cur.kblk;
-    const int nt = nxt.kblk ? nxt.t : cur.t;
-    load_k(nk, nt);
-    {
-      const int jpf = nxt.piece + kPrefetchPieces;
-      const bool pf = nxt.kblk && nxt.piece != cur.piece && jpf < pend && jpf < pb_base + 32;
-      const int pg = __shfl_sync(0xffffffffu, pb_page, min(max(jpf - pb_base, 0), 31));
-      if (pf && pg >= 0 && lane == 0) {
-        prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
-        prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
+      float acc[4];
+  #pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        acc[i] = qacc[0][i];
+  #pragma unroll
+        for (int c = 1; c < kQChains; ++c) acc[i] += qacc[c][i];
       }
-    }
-    // ------------------------------------------------------------ online softmax (log2)
-    float sc[4];
-    sc[0] = v0 ? acc[0] * post_scale : -INFINITY;  // row g_id, heads 2q, 2q+1
-    sc[1] = v0 ? acc[1] * post_scale : -INFINITY;
-    sc[2] = v1 ? acc[2] * post_scale : -INFINITY;  // row g_id + 8
-    sc[3] = v1 ? acc[3] * post_scale : -INFINITY;
-    const float tm0 = max_over_groups(fmaxf(sc[0], sc[2]));
-    const float tm1 = max_over_groups(fmaxf(sc[1], sc[3]));
-    const float mn0 = fmaxf(st_m[0], tm0), mn1 = fmaxf(st_m[1], tm1);
-    const float al0 = fast_exp2(st_m[0] - mn0), al1 = fast_exp2(st_m[1] - mn1);
-    float pr[4];
-    pr[0] = fast_exp2(sc[0] - mn0);
-    pr[1] = fast_exp2(sc[1] - mn1);
-    pr[2] = fast_exp2(sc[2] - mn0);
-    pr[3] = fast_exp2(sc[3] - mn1);
-    st_d[0] = st_d[0] * al0 + pr[0] + pr[2];
-    st_d[1] = st_d[1] * al1 + pr[1] + pr[3];
-    st_m[0] = mn0;
-    st_m[1] = mn1;
-    // 16-bit KV: unconditional (the vote and branch cost more than the multiplies);
-    // FP8 tiles carry half the bytes, there skipping the multiplies when no maximum
-    // moved measures faster
-    if (!FP8 || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
+      if (PK) {  // score(h) = column h + column h + 4 (held two lanes over)
+  #pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
+      }
+      // K registers are free: start the next tile's K loads
+      // next tile's K (after the last tile: this tile's block again, never used), then the
+      // L2 prefetch when a new piece starts
+      const uint8_t* nk = nxt.kblk ? nxt.kblk : cur.kblk;
+      const int nt = nxt.kblk ? nxt.t : cur.t;
+      load_k(nk, nt);
+      {
+        const int jpf = nxt.piece + kPrefetchPieces;
+        const bool pf = nxt.kblk && nxt.piece != cur.piece && jpf < pend && jpf < pb_base + 32;
+        const int pg = __shfl_sync(0xffffffffu, pb_page, min(max(jpf - pb_base, 0), 31));
+        if (pf && pg >= 0 && lane == 0) {
+          prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
+          prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
+        }
+      }
+      // ------------------------------------------------------------ online softmax (log2)
+      float sc[4];
+      sc[0] = v0 ? acc[0] * post_scale : -INFINITY;  // row g_id, heads 2q, 2q+1
+      sc[1] = v0 ? acc[1] * post_scale : -INFINITY;
+      sc[2] = v1 ? acc[2] * post_scale : -INFINITY;  // row g_id + 8
+      sc[3] = v1 ? acc[3] * post_scale : -INFINITY;
+      const float tm0 = max_over_groups(fmaxf(sc[0], sc[2]));
+      const float tm1 = max_over_groups(fmaxf(sc[1], sc[3]));
+      const float mn0 = fmaxf(st_m[0], tm0), mn1 = fmaxf(st_m[1], tm1);
+      const float al0 = fast_exp2(st_m[0] - mn0), al1 = fast_exp2(st_m[1] - mn1);
+      float pr[4];
+      pr[0] = fast_exp2(sc[0] - mn0);
+      pr[1] = fast_exp2(sc[1] - mn1);
+      pr[2] = fast_exp2(sc[2] - mn0);
+      pr[3] = fast_exp2(sc[3] - mn1);
+      st_d[0] = st_d[0] * al0 + pr[0] + pr[2];
+      st_d[1] = st_d[1] * al1 + pr[1] + pr[3];
+      st_m[0] = mn0;
+      st_m[1] = mn1;
+      // 16-bit KV: unconditional (the vote and branch cost more than the multiplies);
+      // FP8 tiles carry half the bytes, there skipping the multiplies when no maximum
+      // moved measures faster
+      if (!FP8 || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+  #pragma unroll
+        for (int mt = 0; mt < KT; ++mt) {
+          oacc[mt][0] *= al0;
+          oacc[mt][1] *= al1;
+          oacc[mt][2] *= al0;
+          oacc[mt][3] *= al1;
+        }
+      }
+      // P^T as a B fragment: rows 2q,2q+1 | 2q+8,2q+9 of head g_id
+      uint32_t pb0, pb1;
+      {
+        const uint32_t x0 = pack2<MT>(pr[0], pr[2]);  // head 2q: rows g_id, g_id+8
+        const uint32_t x1 = pack2<MT>(pr[1], pr[3]);  // head 2q+1
+        const int srcA = 8 * q4 + (g_id >> 1), srcB = srcA + 4;
+        const uint32_t a0 = __shfl_sync(0xffffffffu, x0, srcA);
+        const uint32_t a1 = __shfl_sync(0xffffffffu, x1, srcA);
+        const uint32_t b0 = __shfl_sync(0xffffffffu, x0, srcB);
+        const uint32_t b1 = __shfl_sync(0xffffffffu, x1, srcB);
+        const uint32_t va = (g_id & 1) ? a1 : a0, vb = (g_id & 1) ? b1 : b0;
+        pb0 = __byte_perm(va, vb, 0x5410);
+        pb1 = __byte_perm(va, vb, 0x7632);
+      }
+      // rows outside the piece may hold anything (even NaN): in a partial tile (the first
+      // or last of a piece; warp-uniform test) this thread's V rows 2q, 2q+1, 2q+8, 2q+9
+      // that fall outside are zeroed in the registers, so full tiles need no masking
+      if (cur.t * 16 < cur.s_lo || cur.t * 16 + 16 > cur.s_hi) {
+  #pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = cur.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
+          if (r < cur.s_lo || r >= cur.s_hi) {
+  #pragma unroll
+            for (int j = 0; j < VCH; ++j) vr[i][j] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      }
+      // ------------------------------------------------------------ O^T += V^T P^T
+  #pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
-        oacc[mt][0] *= al0;
-        oacc[mt][1] *= al1;
-        oacc[mt][2] *= al0;
-        oacc[mt][3] *= al1;
+        uint32_t a[4];
+        if constexpr (FP8) {
+          const int ci = mt >> 1;
+          const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+          const uint32_t xy01 = __byte_perm(comp(vr[0][0], ci), comp(vr[1][0], ci), sel);
+          const uint32_t xy23 = __byte_perm(comp(vr[2][0], ci), comp(vr[3][0], ci), sel);
+          a[0] = e4m3x2_to_f16x2((uint16_t)(xy01 & 0xffff));
+          a[1] = e4m3x2_to_f16x2((uint16_t)(xy01 >> 16));
+          a[2] = e4m3x2_to_f16x2((uint16_t)(xy23 & 0xffff));
+          a[3] = e4m3x2_to_f16x2((uint16_t)(xy23 >> 16));
+        } else {
+          const int j = mt >> 2, ci = mt & 3;
+          const uint32_t x0 = comp(vr[0][j], ci), x1 = comp(vr[1][j], ci);
+          const uint32_t y0 = comp(vr[2][j], ci), y1 = comp(vr[3][j], ci);
+          a[0] = __byte_perm(x0, x1, 0x5410);
+          a[1] = __byte_perm(x0, x1, 0x7632);
+          a[2] = __byte_perm(y0, y1, 0x5410);
+          a[3] = __byte_perm(y0, y1, 0x7632);
+        }
+        Mma<MT>::run(oacc[mt], a, pb0, pb1);
       }
+      load_v(nk, nt);
+      cur = nxt;
     }
-    // P^T as a B fragment: rows 2q,2q+1 | 2q+8,2q+9 of head g_id
-    uint32_t pb0, pb1;
-    {
-      const uint32_t x0 = pack2<MT>(pr[0], pr[2]);  // head 2q: rows g_id, g_id+8
-      const uint32_t x1 = pack2<MT>(pr[1], pr[3]);  // head 2q+1
-      const int srcA = 8 * q4 + (g_id >> 1), srcB = srcA + 4;
-      const uint32_t a0 = __shfl_sync(0xffffffffu, x0, srcA);
-      const uint32_t a1 = __shfl_sync(0xffffffffu, x1, srcA);
-      const uint32_t b0 = __shfl_sync(0xffffffffu, x0, srcB);
-      const uint32_t b1 = __shfl_sync(0xffffffffu, x1, srcB);
-      const uint32_t va = (g_id & 1) ? a1 : a0, vb = (g_id & 1) ? b1 : b0;
-      pb0 = __byte_perm(va, vb, 0x5410);
-      pb1 = __byte_perm(va, vb, 0x7632);
-    }
-    // rows of this thread's V^T halves: 2q, 2q+1 (a0, a1) and 2q+8, 2q+9 (a2, a3);
-    // rows outside the piece may hold anything (even NaN): zero them
-    // (computed without a branch; all-ones for the rows of a full tile)
-    const int rA = cur.t * 16 + 2 * q4, rB = rA + 8;
-    const uint32_t vm01 = ((rA >= cur.s_lo && rA < cur.s_hi) ? 0x0000ffffu : 0u) |
-                          ((rA + 1 >= cur.s_lo && rA + 1 < cur.s_hi) ? 0xffff0000u : 0u);
-    const uint32_t vm23 = ((rB >= cur.s_lo && rB < cur.s_hi) ? 0x0000ffffu : 0u) |
-                          ((rB + 1 >= cur.s_lo && rB + 1 < cur.s_hi) ? 0xffff0000u : 0u);
-    // ------------------------------------------------------------ O^T += V^T P^T
-#pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      uint32_t a[4];
-      if constexpr (FP8) {
-        const int ci = mt >> 1;
-        const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-        const uint32_t xy01 = __byte_perm(comp(vr[0][0], ci), comp(vr[1][0], ci), sel);
-        const uint32_t xy23 = __byte_perm(comp(vr[2][0], ci), comp(vr[3][0], ci), sel);
-        a[0] = e4m3x2_to_f16x2((uint16_t)(xy01 & 0xffff)) & vm01;
-        a[1] = e4m3x2_to_f16x2((uint16_t)(xy01 >> 16)) & vm01;
-        a[2] = e4m3x2_to_f16x2((uint16_t)(xy23 & 0xffff)) & vm23;
-        a[3] = e4m3x2_to_f16x2((uint16_t)(xy23 >> 16)) & vm23;
-      } else {
-        const int j = mt >> 2, ci = mt & 3;
-        const uint32_t x0 = comp(vr[0][j], ci), x1 = comp(vr[1][j], ci);
-        const uint32_t y0 = comp(vr[2][j], ci), y1 = comp(vr[3][j], ci);
-        a[0] = __byte_perm(x0, x1, 0x5410) & vm01;
-        a[1] = __byte_perm(x0, x1, 0x7632) & vm01;
-        a[2] = __byte_perm(y0, y1, 0x5410) & vm23;
-        a[3] = __byte_perm(y0, y1, 0x7632) & vm23;
-      }
-      Mma<MT>::run(oacc[mt], a, pb0, pb1);
-    }
-    load_v(nk, nt);
-    cur = nxt;
+  };
+  if constexpr (Tr::kQSplit) {
+    if (pack4) tile_loop(std::true_type{});
+    else tile_loop(std::false_type{});
+  } else {
+    tile_loop(std::false_type{});
   }
   st_d[0] = sum_over_groups(st_d[0]);
   st_d[1] = sum_over_groups(st_d[1]);
