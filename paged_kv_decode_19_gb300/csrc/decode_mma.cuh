@@ -458,13 +458,26 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     }
     return tl;
   };
+  // Common cases without a branch: the next tile of the same piece, or the first tile of
+  // the next piece when it is in the current batch and has a valid page; anything else
+  // (a batch reload, a bad page id, the end) takes the slow path.
   auto next_tile = [&](const Tile& c) -> Tile {
-    if ((c.t + 1) * 16 < c.s_hi) {
-      Tile n = c;
-      n.t = c.t + 1;
-      return n;
-    }
-    return first_tile_from(c.piece + 1);
+    const bool same = (c.t + 1) * 16 < c.s_hi;
+    const int j = c.piece + 1;
+    const int src = min(max(j - pb_base, 0), 31);
+    const int pg = __shfl_sync(0xffffffffu, pb_page, src);
+    const int sl = __shfl_sync(0xffffffffu, pb_slots, src);
+    const int rl = __shfl_sync(0xffffffffu, pb_row, src);
+    const bool fast = same || (j < pend && j - pb_base < 32 && pg >= 0);
+    if (!fast) return first_tile_from(j);
+    Tile n;
+    n.piece = same ? c.piece : j;
+    n.s_lo = same ? c.s_lo : (sl & 0xffff);
+    n.s_hi = same ? c.s_hi : (sl >> 16);
+    n.t = same ? c.t + 1 : ((sl & 0xffff) >> 4);
+    n.r_lo = same ? c.r_lo : rl;
+    n.kblk = same ? c.kblk : kblock(pg);
+    return n;
   };
   uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
   uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
