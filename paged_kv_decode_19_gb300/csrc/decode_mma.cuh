@@ -576,10 +576,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       // otherwise form long chains of dependent MMAs (mma.sync latency, not throughput,
       // bounds the tile loop)
       float qacc[kQChains][4];
-  #pragma unroll
+#pragma unroll
       for (int c = 0; c < kQChains; ++c) qacc[c][0] = qacc[c][1] = qacc[c][2] = qacc[c][3] = 0.f;
       if constexpr (!ROPE) {
-  #pragma unroll
+#pragma unroll
         for (int kt = 0; kt < KT; ++kt) {
           uint32_t a[4];
           if constexpr (FP8) {
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
         // rotate, split and multiply the k-tile pair (kt, kt + KT/2) given its raw fragments
         auto rope_pair = [&](int kt, const uint32_t (&araw)[2][4]) {
           uint32_t ahi[2][4], alo[2][4];
-  #pragma unroll
+#pragma unroll
           for (int half = 0; half < 2; ++half) {
             // (cos, sin) of this half's two frequencies f, f + 1 (packed fp32 pairs) at
             // rows g_id (direct) and g_id + 8 (rotated by 8 positions)
@@ -616,7 +616,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
             const float2 r8c = make_float2(r8.x, r8.z), r8s = make_float2(r8.y, r8.w);
             cs_c[1] = sub_f2(mul_f2(cs_c[0], r8c), mul_f2(cs_s[0], r8s));
             cs_s[1] = fma_f2(cs_s[0], r8c, mul_f2(cs_c[0], r8s));
-  #pragma unroll
+#pragma unroll
             for (int row = 0; row < 2; ++row) {
               const int ai = 2 * half + row;
               const float2 x = unpack2<MT>(araw[0][ai]);
@@ -625,7 +625,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
               split2<MT>(fma_f2(y, cs_c[row], mul_f2(x, cs_s[row])), ahi[1][ai], alo[1][ai]);
             }
           }
-  #pragma unroll
+#pragma unroll
           for (int u = 0; u < 2; ++u) {
             const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
             Mma<MT>::run(qacc[(3 * u + kt) % kQChains], ahi[u], qf.x, qf.y);
@@ -634,10 +634,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
           }
         };
         {
-  #pragma unroll
+#pragma unroll
           for (int kt = 0; kt < KT / 2; ++kt) {
             uint32_t araw[2][4];
-  #pragma unroll
+#pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int ktu = kt + u * (KT / 2);
               if constexpr (FP8) {
@@ -658,14 +658,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
         }
       }
       float acc[4];
-  #pragma unroll
+#pragma unroll
       for (int i = 0; i < 4; ++i) {
         acc[i] = qacc[0][i];
-  #pragma unroll
+#pragma unroll
         for (int c = 1; c < kQChains; ++c) acc[i] += qacc[c][i];
       }
       if (PK) {  // score(h) = column h + column h + 4 (held two lanes over)
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
       }
       // K registers are free: start the next tile's K loads
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       // FP8 tiles carry half the bytes, there skipping the multiplies when no maximum
       // moved measures faster
       if (!FP8 || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-  #pragma unroll
+#pragma unroll
         for (int mt = 0; mt < KT; ++mt) {
           oacc[mt][0] *= al0;
           oacc[mt][1] *= al1;
@@ -732,17 +732,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       // or last of a piece; warp-uniform test) this thread's V rows 2q, 2q+1, 2q+8, 2q+9
       // that fall outside are zeroed in the registers, so full tiles need no masking
       if (cur.t * 16 < cur.s_lo || cur.t * 16 + 16 > cur.s_hi) {
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = cur.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
           if (r < cur.s_lo || r >= cur.s_hi) {
-  #pragma unroll
+#pragma unroll
             for (int j = 0; j < VCH; ++j) vr[i][j] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
       }
       // ------------------------------------------------------------ O^T += V^T P^T
-  #pragma unroll
+#pragma unroll
       for (int mt = 0; mt < KT; ++mt) {
         uint32_t a[4];
         if constexpr (FP8) {
