@@ -325,9 +325,11 @@ def run_ours(args, ws, rank, local):
 
 
 def _max_over_ranks(x: float, ws: int) -> float:
+    """Max of x over the ranks of the default process group (the replicas' times)."""
     if ws == 1:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if torch.distributed.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
 

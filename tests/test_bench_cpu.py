@@ -1,0 +1,63 @@
+"""Host-side pieces of bench.py that need no GPU: the replicas' max-over-ranks
+reduction (two gloo ranks on CPU) and the source-matched DRAM traffic record."""
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, ws, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(ws))
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        # each replica reports its own time; every rank learns the slowest
+        q.put((rank, bench._max_over_ranks(10.0 + 5.0 * rank, ws), bench._dist()))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[1] for g in got] == [15.0, 15.0]
+    assert [g[2][:2] for g in got] == [(2, 0), (2, 1)]  # (world size, rank) from the env
+
+
+def test_single_rank_is_identity():
+    assert bench._max_over_ranks(3.5, 1) == 3.5
+
+
+def test_traffic_record_only_for_matching_sources(tmp_path, monkeypatch):
+    digest = bench._sources_digest()
+    assert digest == bench._sources_digest() and len(digest) == 64
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"cfgA:B=4": {"sources_sha256": digest, "dram_bytes_per_launch": 1234},
+           "cfgB:B=4": {"sources_sha256": "0" * 64, "dram_bytes_per_launch": 99}}
+    (prof / "dram_traffic.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "_sources_digest", lambda: digest)
+    assert bench._measured_traffic("cfgA", 4) == 1234
+    assert bench._measured_traffic("cfgB", 4) is None   # taken on other sources
+    assert bench._measured_traffic("cfgA", 8) is None   # another batch size
