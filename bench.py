@@ -363,6 +363,7 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
+        cfg["l2"] = "not applicable (the fp64 oracle on the host cores)"
         wl = W.make(args.config, seed=1000, **args.over)
         for _ in range(args.warmup):
             _oracle_sample(wl, 0.0)
