@@ -70,17 +70,19 @@ typedef struct {
   int32_t sliding_window;    /* 0: length_info is [B] = last_page_len.
                                 1: length_info is [3,B] = (last_page_len,
                                    window start offset, attention-sink length). */
-  int32_t num_splits;        /* block schedule: 0 = balanced (one resident wave of blocks,
-                                each taking an equal share of all pages of all sequences
-                                and heads); 1 = one block per (sequence, <=8-head slice),
-                                never split; n > 1 = balanced over about n blocks per
-                                (sequence, head slice) */
+  int32_t num_splits;        /* work split: 0 = balanced (one resident wave of blocks;
+                                each worker -- a warp of the tensor-core kernel, a block
+                                of the SIMT kernel -- takes an equal share of all pages
+                                of all sequences and heads); 1 = one worker per
+                                (sequence, <=8-head slice), never split; n > 1 =
+                                balanced over about n workers per (sequence, head slice) */
   int64_t max_pages;         /* pages buffer holds [max_pages,2,H_kv,P,D] */
   int64_t nnz_pages;         /* entries in page_table_values (= indptr[B]) */
   int32_t max_kv_len_hint;   /* reserved (ignored); set to 0 */
   float k_scale;             /* E4M3 KV only: K = code * k_scale (else ignored) */
   float v_scale;             /* E4M3 KV only: V = code * v_scale (else ignored) */
-  void* workspace;           /* optional caller workspace (device); NULL = library-managed */
+  void* workspace;           /* optional caller workspace (device, 256-byte aligned);
+                                NULL = library-managed */
   size_t workspace_bytes;    /* size of `workspace` */
 } pd_decode_desc;
 
@@ -99,7 +101,7 @@ typedef struct {
  *   s_r = sm_scale * log2(e) * q.k_r;  out = sum_r 2^(s_r) v_r / sum_r 2^(s_r);
  *   lse = log2(sum_r 2^(s_r)).  An empty sequence gives out = 0, lse = -5e4.
  * Arguments (all device pointers):
- *   Q           [B, H_qo, D] desc->q_dtype, contiguous.
+ *   Q           [B, H_qo, D] desc->q_dtype, contiguous, 16-byte aligned.
  *   pages       [max_pages, 2, H_kv, P, D] desc->kv_dtype, contiguous, 16-byte aligned.
  *   page_table_indptr [B+1] int32, non-decreasing, indptr[0] = 0.
  *   page_table_values [nnz_pages] int32 physical page ids.
@@ -107,9 +109,12 @@ typedef struct {
  *   k_rope_pos_offset, q_rope_position [B] int32; may be NULL when rotary_mode == 0.
  *   output      [B, H_qo, D] desc->out_dtype.   lse [B, H_qo] float32 (log2 units).
  * Scalars: rotary_mode (0 none, 1 RoPE), rope_scale, rope_theta, sm_scale.
- * Work is split across thread blocks by pages (see desc->num_splits); a sequence
- * that several blocks share is merged on the device from their partial (out, lse)
- * pairs by the last of them to finish.  The plan uses only host-known sizes.
+ * Work is split by pages (see desc->num_splits); a (sequence, head slice) that
+ * several workers share is merged on the device from their partial (out, lse) pairs
+ * by the worker that completes its page count.  The grid uses only host-known sizes;
+ * each block finds its workers' shares with a scan of indptr/length_info.
+ * Q or pages not 16-byte aligned: PD_ERR_INVALID_ARG (both kernels read rows with
+ * 16-byte vector loads).
  * Workspace: desc->workspace if non-NULL (at least pd_workspace_size(desc) bytes,
  * 256-byte aligned, zero-filled before its first use — see pd_workspace_init),
  * otherwise a per-device buffer the library allocates on first use and grows as
@@ -200,11 +205,13 @@ pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream);
 
 /*
  * Host-only split planner (no CUDA calls): for `desc` on a GPU with `num_sms`
- * multiprocessors and `ctas_per_sm` resident decode blocks, returns the block schedule
- * (*schedule: 0 = balanced shares of all pages, 1 = one block per (sequence, head
+ * multiprocessors and `ctas_per_sm` resident decode blocks, returns the schedule
+ * (*schedule: 0 = balanced shares of all pages, 1 = one worker per (sequence, head
  * slice)), the number of blocks (*grid_blocks) and the workspace bytes (per-segment
- * arrival counters plus two partial (out, lse) slots per block; 0 when nothing is
- * split).  Used by the library and exposed for tests.
+ * arrival counters plus two partial (out, lse) slots per worker; 0 when nothing is
+ * split).  Workers per block: 4 (warps) when desc selects the tensor-core kernel
+ * (16-bit or E4M3 KV, page_size % 16 == 0, D = 64/128, D = 128 for E4M3), else 1.
+ * Used by the library and exposed for tests.
  */
 pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_sm,
                   int32_t* schedule, int32_t* grid_blocks, size_t* workspace_bytes);
