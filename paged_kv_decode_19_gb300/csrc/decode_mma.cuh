@@ -1,8 +1,9 @@
 // Tensor-core decode kernel for 16-bit and FP8 KV caches (sm_103a).
 //
 // Work split: the attended pages of every segment (sequence, KV head, slice of <= 8
-// query heads that share the KV head) form one list of U units (pages), cut into W
-// equal contiguous ranges, one per warp (W = blocks x 4).  Each warp is an independent
+// query heads that share the KV head) lie on one cost line (each segment: a fixed
+// set-up cost, then one unit per page), cut into W equal contiguous ranges, one per
+// warp (W = blocks x 4).  Each warp is an independent
 // worker: it walks the segments its range touches, streams their pages in order and
 // finishes each segment on its own -- a segment it covers whole is written straight
 // to out/lse; otherwise it leaves a partial state (normalised O, lse) in one of its two
@@ -22,11 +23,15 @@
 //     k order is permuted to match, and Q's B fragments use the same permutation.
 //   - online base-2 softmax on the accumulator fragments (TVM `batch_decode_paged_kv`:
 //     running max m, sum d, output O), P^T rebuilt as a B fragment with 4 shuffles;
-//   - O^T += V^T P^T: A = V^T built from 16-byte row loads with byte permutes (the
-//     output dims are permuted; each thread ends up with whole runs of 8 or 16
-//     consecutive output dims, stored with 16-byte stores).
+//   - O^T += V^T P^T: A = V^T built from 16-byte row loads with byte permutes.  The
+//     output dims are permuted: m-tile mt row g_id (+8) holds dim 16 g_id + 2 mt (+1)
+//     for FP8, 8 (g_id + 8 (mt >> 2)) + 2 (mt & 3) (+1) otherwise, so each thread ends
+//     up with whole runs of 16 or 8 consecutive output dims (16-byte stores).
 // The next tile's K loads are issued right after QK and its V loads right after PV,
-// so each warp keeps about one tile in registers in flight while it computes.
+// so each warp keeps about one tile in registers in flight while it computes.  The
+// tile loop is kept nearly branch-free (its instruction fetch and branch stalls
+// measurably limit it): the next piece comes from a per-lane cache by shuffles, the
+// Q-packing mode is a compile-time parameter, and only partial tiles take a branch.
 // RoPE (rotate-half) is applied to K in registers before the MMA; rotated K and Q are
 // split into hi + lo 16-bit parts so the products keep ~16 mantissa bits.  FP8 codes
 // become f16 in registers (exact); k_scale folds into the score scale, v_scale into
@@ -84,12 +89,6 @@ template <bool FP8>
 __device__ __forceinline__ int frag_dim(int kt, int half, int e, int q4) {
   return FP8 ? 16 * (4 * (kt >> 2) + q4) + 4 * (kt & 3) + 2 * half + e
              : 8 * (4 * (kt >> 1) + q4) + 4 * (kt & 1) + 2 * half + e;
-}
-
-// Output dim of O^T fragment row (m-tile mt, row g_id or g_id + 8 when `hi`).
-template <bool FP8>
-__device__ __forceinline__ int out_dim(int mt, int g_id, int hi) {
-  return FP8 ? 16 * g_id + 2 * mt + hi : 8 * (g_id + 8 * (mt >> 2)) + 2 * (mt & 3) + hi;
 }
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
