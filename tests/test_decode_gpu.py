@@ -148,6 +148,14 @@ def test_fp8_group_sweep(group, rope):
     _check(wl, "mma", num_splits=3, max_kv_len_hint=500)
 
 
+@pytest.mark.parametrize("splits", [0, 1])
+def test_batch_above_start_scan_cache(splits):
+    # more than 1024 sequences: the tensor-core kernel's start-up scan takes its
+    # two-pass path (per-sequence unit counts no longer kept in shared memory)
+    wl = _wl("llama3_8b_bf16", 77, B=1100, len_dist=("uniform", 1, 40), pool=4000)
+    _check(wl, "mma", num_splits=splits)
+
+
 @pytest.mark.parametrize("D", [64, 128, 256])
 def test_fp32_dims(D):
     wl = W.make("tiny_fp32", seed=D, D=D, rotary_mode=1, rope_theta=1e4).to(DEV)
