@@ -55,6 +55,7 @@ constexpr int kPrefetchPieces = PD_PREFETCH_PIECES;  // L2 prefetch distance, in
 #define PD_QK_CHAINS 2
 #endif
 constexpr int kQChains = PD_QK_CHAINS;  // independent accumulators of a tile's K Q^T
+constexpr float kLazyMax = 8.f;  // slack of the lazy running max (log2 units)
 #ifndef PD_MIN_BLOCKS_PLAIN
 #define PD_MIN_BLOCKS_PLAIN 1
 #endif
@@ -688,31 +689,37 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       sc[1] = v0 ? acc[1] * post_scale : -INFINITY;
       sc[2] = v1 ? acc[2] * post_scale : -INFINITY;  // row g_id + 8
       sc[3] = v1 ? acc[3] * post_scale : -INFINITY;
-      const float tm0 = max_over_groups(fmaxf(sc[0], sc[2]));
-      const float tm1 = max_over_groups(fmaxf(sc[1], sc[3]));
-      const float mn0 = fmaxf(st_m[0], tm0), mn1 = fmaxf(st_m[1], tm1);
-      const float al0 = fast_exp2(st_m[0] - mn0), al1 = fast_exp2(st_m[1] - mn1);
-      float pr[4];
-      pr[0] = fast_exp2(sc[0] - mn0);
-      pr[1] = fast_exp2(sc[1] - mn1);
-      pr[2] = fast_exp2(sc[2] - mn0);
-      pr[3] = fast_exp2(sc[3] - mn1);
-      st_d[0] = st_d[0] * al0 + pr[0] + pr[2];
-      st_d[1] = st_d[1] * al1 + pr[1] + pr[3];
-      st_m[0] = mn0;
-      st_m[1] = mn1;
-      // 16-bit KV: unconditional (the vote and branch cost more than the multiplies);
-      // FP8 tiles carry half the bytes, there skipping the multiplies when no maximum
-      // moved measures faster
-      if (!FP8 || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+      // Lazy running max: the reference max m moves only when some score exceeds it by
+      // more than kLazyMax (log2 units; a warp vote), so the tile max reduction and the
+      // rescale of O and d run on the first tile and then rarely.  Probabilities stay
+      // <= 2^kLazyMax, and out = O/d, lse = m + log2 d are exact for any reference m.
+      {
+        const float over = fmaxf(fmaxf(sc[0], sc[2]) - st_m[0], fmaxf(sc[1], sc[3]) - st_m[1]);
+        if (__any_sync(0xffffffffu, over > kLazyMax)) {
+          const float tm0 = max_over_groups(fmaxf(sc[0], sc[2]));
+          const float tm1 = max_over_groups(fmaxf(sc[1], sc[3]));
+          const float mn0 = fmaxf(st_m[0], tm0), mn1 = fmaxf(st_m[1], tm1);
+          const float al0 = fast_exp2(st_m[0] - mn0), al1 = fast_exp2(st_m[1] - mn1);
+          st_d[0] *= al0;
+          st_d[1] *= al1;
+          st_m[0] = mn0;
+          st_m[1] = mn1;
 #pragma unroll
-        for (int mt = 0; mt < KT; ++mt) {
-          oacc[mt][0] *= al0;
-          oacc[mt][1] *= al1;
-          oacc[mt][2] *= al0;
-          oacc[mt][3] *= al1;
+          for (int mt = 0; mt < KT; ++mt) {
+            oacc[mt][0] *= al0;
+            oacc[mt][1] *= al1;
+            oacc[mt][2] *= al0;
+            oacc[mt][3] *= al1;
+          }
         }
       }
+      float pr[4];
+      pr[0] = fast_exp2(sc[0] - st_m[0]);
+      pr[1] = fast_exp2(sc[1] - st_m[1]);
+      pr[2] = fast_exp2(sc[2] - st_m[0]);
+      pr[3] = fast_exp2(sc[3] - st_m[1]);
+      st_d[0] += pr[0] + pr[2];
+      st_d[1] += pr[1] + pr[3];
       // P^T as a B fragment: rows 2q,2q+1 | 2q+8,2q+9 of head g_id
       uint32_t pb0, pb1;
       {
