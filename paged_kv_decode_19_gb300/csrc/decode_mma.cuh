@@ -391,15 +391,24 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   const bool pack4 = Tr::kQSplit && hcount <= 4;
   const int qh = pack4 ? (g_id & 3) : g_id;  // the head this lane's B fragment holds
   const bool have_q = qh < hcount;
-  uint32_t qraw[KT][2];
+  // The lane's Q elements (dims frag_dim(kt, h, e, q4)) form KT/2 contiguous 16-byte
+  // chunks, loaded with one vector load each: chunk c starts at element 8 (4c + q4)
+  // (16-bit KV) or 16 (4 (c >> 1) + q4) + 8 (c & 1) (FP8 KV).
+  constexpr int QCH = KT / 2;
+  uint4 qchunk[QCH];
   {
     const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have_q ? qh : 0)) * D;
 #pragma unroll
-    for (int kt = 0; kt < KT; ++kt)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        qraw[kt][h] = have_q ? __ldg(reinterpret_cast<const uint32_t*>(qrow + frag_dim<FP8>(kt, h, 0, q4))) : 0u;
+    for (int c = 0; c < QCH; ++c) {
+      const int e0 = FP8 ? 16 * (4 * (c >> 1) + q4) + 8 * (c & 1) : 8 * (4 * c + q4);
+      qchunk[c] = have_q ? __ldg(reinterpret_cast<const uint4*>(qrow + e0)) : make_uint4(0u, 0u, 0u, 0u);
+    }
   }
+  // the pair of Q elements (kt, h, e = 0..1) of this lane's B fragment
+  auto qraw = [&](int kt, int h) -> uint32_t {
+    return FP8 ? comp(qchunk[2 * (kt >> 2) + ((kt & 3) >> 1)], 2 * (kt & 1) + h)
+               : comp(qchunk[kt >> 1], 2 * (kt & 1) + h);
+  };
   const int qpos = ROPE ? __ldg(p.q_rope_position + sg.b) : 0;
   const int kpos0 = ROPE ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
 
@@ -519,7 +528,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       for (int u = 0; u < 2; ++u)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          const float2 f = unpack2<QT>(qraw[kt + u * (KT / 2)][h]);
+          const float2 f = unpack2<QT>(qraw(kt + u * (KT / 2), h));
           qv[u][h][0] = f.x;
           qv[u][h][1] = f.y;
         }
