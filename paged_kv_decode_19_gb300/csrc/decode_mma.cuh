@@ -32,8 +32,11 @@
 // tile loop is kept nearly branch-free (its instruction fetch and branch stalls
 // measurably limit it): the next piece comes from a per-lane cache by shuffles, the
 // Q-packing mode is a compile-time parameter, and only partial tiles take a branch.
-// RoPE (rotate-half) is applied to K in registers before the MMA; rotated K and Q are
-// split into hi + lo 16-bit parts so the products keep ~16 mantissa bits.  FP8 codes
+// RoPE (rotate-half) is applied to K in registers before the MMA; rotated K is rounded
+// once to f16 (11 significant bits; a score error of about 2^-12 of |q| |k| sqrt(D)
+// scale) and multiplied with Q split into f16 hi + lo parts, one MMA per k-tile when
+// the hi and lo parts share the n dimension (<= 4 heads).  The rotated K of a bf16
+// cache must stay inside the f16 range (|k| < 46000).  FP8 codes
 // become f16 in registers (exact); k_scale folds into the score scale, v_scale into
 // the output.
 //
@@ -81,6 +84,9 @@ struct MmaTraits {
   static constexpr int kKCh = kRowBytes / 64;    // 16-byte K chunks per row per thread
   static constexpr int kVCh = kRowBytes / 128;   // 16-byte V chunks per row per thread
   static constexpr bool kQSplit = ROPE || kFp8 || !std::is_same<QT, MT>::value;
+  // QK tensor-core type: rotated K is rounded once to f16 (11-bit significand, against
+  // bf16's 8), Q is split into f16 hi + lo, so a score keeps about 11 bits of K'
+  using QKT = typename std::conditional<ROPE, __half, MT>::type;
   static_assert(kRowBytes == 128 || kRowBytes == 256, "row must be 128 or 256 bytes");
 };
 
@@ -312,6 +318,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = MmaTraits<KVT, QT, D, ROPE>;
   using MT = typename Tr::MT;
+  using QKT = typename Tr::QKT;
   constexpr int NT = NW * 32;
   constexpr int KT = Tr::kKT;
   constexpr int RB = Tr::kRowBytes;
@@ -550,9 +557,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           if (Tr::kQSplit) {
-            split2<MT>(qv[u][h][0] * p.q_prescale, qv[u][h][1] * p.q_prescale, hi[h], lo[h]);
+            split2<QKT>(qv[u][h][0] * p.q_prescale, qv[u][h][1] * p.q_prescale, hi[h], lo[h]);
           } else {
-            hi[h] = pack2<MT>(qv[u][h][0], qv[u][h][1]);
+            hi[h] = pack2<QKT>(qv[u][h][0], qv[u][h][1]);
             lo[h] = 0u;
           }
         }
@@ -610,9 +617,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       } else {
         // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
         const int pos0 = kpos0 + cur.r_lo + (slot0 - cur.s_lo);  // row g_id; row g_id + 8 is pos0 + 8
-        // rotate, split and multiply the k-tile pair (kt, kt + KT/2) given its raw fragments
+        // rotate, round and multiply the k-tile pair (kt, kt + KT/2) given its raw fragments
         auto rope_pair = [&](int kt, const uint32_t (&araw)[2][4]) {
-          uint32_t ahi[2][4], alo[2][4];
+          uint32_t ar[2][4];  // rotated K of k-tiles kt, kt + KT/2 (f16)
 #pragma unroll
           for (int half = 0; half < 2; ++half) {
             // (cos, sin) of this half's two frequencies f, f + 1 (packed fp32 pairs) at
@@ -630,16 +637,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
               const int ai = 2 * half + row;
               const float2 x = unpack2<MT>(araw[0][ai]);
               const float2 y = unpack2<MT>(araw[1][ai]);
-              split2<MT>(sub_f2(mul_f2(x, cs_c[row]), mul_f2(y, cs_s[row])), ahi[0][ai], alo[0][ai]);
-              split2<MT>(fma_f2(y, cs_c[row], mul_f2(x, cs_s[row])), ahi[1][ai], alo[1][ai]);
+              const float2 xr = sub_f2(mul_f2(x, cs_c[row]), mul_f2(y, cs_s[row]));
+              const float2 yr = fma_f2(y, cs_c[row], mul_f2(x, cs_s[row]));
+              ar[0][ai] = pack2<QKT>(xr.x, xr.y);
+              ar[1][ai] = pack2<QKT>(yr.x, yr.y);
             }
           }
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const uint4 qf = s_qf[warp][kt + u * (KT / 2)][lane];
-            Mma<MT>::run(qacc[(3 * u + kt) % kQChains], ahi[u], qf.x, qf.y);
-            Mma<MT>::run(qacc[(3 * u + kt + 1) % kQChains], alo[u], qf.x, qf.y);
-            if (!PK) Mma<MT>::run(qacc[(3 * u + kt + 2) % kQChains], ahi[u], qf.z, qf.w);
+            Mma<QKT>::run(qacc[(2 * u + kt) % kQChains], ar[u], qf.x, qf.y);
+            if (!PK) Mma<QKT>::run(qacc[(2 * u + kt + 1) % kQChains], ar[u], qf.z, qf.w);
           }
         };
         {

@@ -216,6 +216,24 @@ def test_edge_window_cases():
         _check(wl, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_edge_rope_short_rows_large_positions(dt):
+    # one to four rows per sequence: each lse rests on a few scores, so the rounding of
+    # the rotated K to f16 is not averaged away; positions near 2^17 give large angles
+    wl = _custom([1 + i % 4 for i in range(64)], H_qo=32, H_kv=8, dt=dt, rope=1, seed=5)
+    wl.k_rope_pos_offset += 131000
+    wl.q_rope_position += 131000
+    ro, rl, _ = oracle_decode(wl)
+    for kw in ({}, {"num_splits": 1}):
+        out, lse = gpu_decode(wl, **kw)
+        assert pd.check_device_errors() == "PD_OK"
+        compare(dt, out, lse, ro, rl)
+        # one f16 rounding of the rotated K (N(0,1) data, D = 128) gives an lse error of
+        # about 3e-4 rms on a one-row sequence; a bf16 rounding would give 8x that
+        rms = float(np.sqrt(np.mean((lse.double().cpu().numpy() - rl) ** 2)))
+        assert rms <= 6e-4, rms
+
+
 def test_edge_more_chunks_than_pages():
     wl = _custom([33, 5, 70])
     _check(wl, num_splits=64, max_kv_len_hint=70)
