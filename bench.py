@@ -5,11 +5,15 @@ merge), on the Llama-3-8B-shaped bf16 serving load by default.
 Prints ONE JSON line (rank 0).  Timing: W warm-up steps, then K timed steps, each
 bracketed by CUDA events on the launching stream.  Inputs larger than L2: two replicas
 of the workload (same seed, separate device memory) alternate step by step, so a
-step's KV is never in L2 (the other replica streamed through it in between).  Inputs
+step's KV is never in L2 (the other replica streamed through it in between), and the
+K steps run back to back between one pair of events (value = elapsed / K): the decode
+follows the append directly and starts under it (programmatic dependent launch with
+PD_DECODE_EARLY_INPUTS), and the next step's append under the decode's tail.  Inputs
 that fit in L2: the L2 is flushed before every timed step (a 2x-L2 buffer written,
-then another read, leaving it cold and clean).  The flushed decode time of the large
-workloads is reported as well (decode_us_l2_flushed).  The decode kernel is timed by its own event
-pair for the roofline.  `e2e` re-times the step through the public API from pinned
+then another read, leaving it cold and clean) and each step has its own events.  A
+second pass of the same steps puts events between the kernels, which times each
+kernel alone (decode_us, append_us and the roofline).  The flushed decode time of the
+large workloads is reported as well (decode_us_l2_flushed).  `e2e` re-times the step through the public API from pinned
 host buffers (H2D of the step's inputs and D2H of out + lse inside the timed region).
 
 --impl reference times the fp64 oracle (the CPU baseline) on a bounded sample.
@@ -225,13 +229,18 @@ def run_ours(args, ws, rank, local):
         pd.append_paged_kv(w.pages, k_new, v_new, slots, w.k_scale, w.v_scale)
 
     def decode(r):
+        # the decode follows the append on the stream: its start-up (work split scan,
+        # page table, Q) may run under the append (PD_DECODE_EARLY_INPUTS)
         w = r[0]
         pd.batch_decode_paged_kv(w.Q, w.pages, w.indptr, w.values, w.length_info,
                                  w.k_rope_pos_offset, w.q_rope_position, out, lse,
                                  s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
-                                 k_scale=w.k_scale, v_scale=w.v_scale, **split)
+                                 k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
+                                 **split)
 
-    def timed_steps(n, flush):
+    def timed_steps(n, flush, breakdown):
+        # breakdown=True records an event between append and decode, which times each
+        # kernel alone (the decode then no longer starts under the append)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
         for i in range(n):
             r = reps[i % 2]
@@ -240,10 +249,13 @@ def run_ours(args, ws, rank, local):
             e0, e1, e2 = ev[i]
             e0.record(stream)
             append(r)
-            e1.record(stream)
+            if breakdown:
+                e1.record(stream)
             decode(r)
             e2.record(stream)
         torch.cuda.synchronize()
+        if not breakdown:
+            return [e[0].elapsed_time(e[2]) for e in ev], None, None
         return ([e[0].elapsed_time(e[2]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev],
                 [e[0].elapsed_time(e[1]) for e in ev])
 
@@ -258,14 +270,35 @@ def run_ours(args, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    def timed_run(n):
+        # n steps back to back, one event pair around them all: a step's decode may
+        # overlap the next step's append and start-up, as in a serving loop
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            r = reps[i % 2]
+            append(r)
+            decode(r)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) / n]
+
     with ClockSampler(local) as clk:
-        step_ms, dec_ms, app_ms = timed_steps(args.steps, flush=not alternate)
+        if alternate:
+            step_ms = timed_run(args.steps)
+        else:  # the flush must stay outside the timed region: one event pair per step
+            step_ms, _, _ = timed_steps(args.steps, flush=True, breakdown=False)
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        # the same steps again, each kernel timed alone (decode_us, append_us, roofline)
+        _, dec_ms, app_ms = timed_steps(args.steps, flush=not alternate, breakdown=True)
     if ws > 1:
         torch.distributed.barrier()
     assert pd.check_device_errors() == "PD_OK"
     launches = 2 * args.steps
     # the same steps after a flush of L2 (for comparison; not the reported value)
-    _, dec_flushed_ms, _ = timed_steps(max(args.steps // 2, 3), flush=True)
+    _, dec_flushed_ms, _ = timed_steps(max(args.steps // 2, 3), flush=True, breakdown=True)
 
     # end-to-end through the public API from pinned host memory: every step copies its
     # inputs (one pinned staging buffer holding Q, the page table, length_info, the RoPE
@@ -309,7 +342,8 @@ def run_ours(args, ws, rank, local):
         pd.batch_decode_paged_kv(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
                                  di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e,
                                  s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
-                                 k_scale=w.k_scale, v_scale=w.v_scale, **split)
+                                 k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
+                                 **split)
         res_host.copy_(res_dev, non_blocking=True)
         b.record(stream)
         b.synchronize()
@@ -397,7 +431,8 @@ def main():
         return
     wl = res["wl"]
     cfg["l2"] = (f"inputs larger than L2 ({wl.kv_bytes_attended() / 1e6:.0f} MB attended KV vs "
-                 f"{res['l2'] / 1e6:.0f} MB L2): two replicas alternate, no flush"
+                 f"{res['l2'] / 1e6:.0f} MB L2): two replicas alternate, no flush; the "
+                 "steps run back to back between one pair of events"
                  if res["alternate"] else
                  "flushed before every timed step: 2x L2 written, then 2x L2 read (cold, clean L2)")
     kv_bytes = wl.kv_bytes_attended()

@@ -81,10 +81,28 @@ typedef struct {
   int32_t max_kv_len_hint;   /* reserved (ignored); set to 0 */
   float k_scale;             /* E4M3 KV only: K = code * k_scale (else ignored) */
   float v_scale;             /* E4M3 KV only: V = code * v_scale (else ignored) */
+  int32_t flags;             /* 0 or PD_DECODE_EARLY_INPUTS (see below) */
   void* workspace;           /* optional caller workspace (device, 256-byte aligned);
                                 NULL = library-managed */
   size_t workspace_bytes;    /* size of `workspace` */
 } pd_decode_desc;
+
+/*
+ * Launch order.  Every kernel of this library is launched with programmatic stream
+ * serialisation (CUDA programmatic dependent launch): it may be scheduled while the
+ * kernel before it on the stream is finishing, and it waits for that kernel to complete
+ * before it reads any caller memory or writes anything.  Results are the same as with
+ * plain stream order.
+ * PD_DECODE_EARLY_INPUTS in desc->flags lets the decode read Q, page_table_indptr,
+ * page_table_values, length_info and the RoPE positions while the previous kernel on
+ * the stream still runs; only its page reads and its writes wait for that kernel.
+ * The caller asserts that the kernel enqueued just before the decode writes none of
+ * those inputs, and that everything enqueued before that kernel is complete once it
+ * starts: both hold when it is pd_append_paged_kv (which writes only the pages and,
+ * itself, waits for its predecessor before it lets the decode start).  The decode then
+ * runs its start-up (work split scan, page-table and Q loads) under the append.
+ */
+#define PD_DECODE_EARLY_INPUTS 1
 
 /*
  * batch_decode_paged_kv — [TVM] `batch_decode_paged_kv`.

@@ -79,6 +79,7 @@ class DecodeDesc(ctypes.Structure):
         ("max_kv_len_hint", ctypes.c_int32),
         ("k_scale", ctypes.c_float),
         ("v_scale", ctypes.c_float),
+        ("flags", ctypes.c_int32),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
     ]
@@ -140,8 +141,11 @@ def _stream(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
+DECODE_EARLY_INPUTS = 1
+
+
 def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_kv_len_hint=0,
-              k_scale=1.0, v_scale=1.0, workspace=None) -> DecodeDesc:
+              k_scale=1.0, v_scale=1.0, workspace=None, early_inputs=False) -> DecodeDesc:
     B, H_qo, D = Q.shape
     max_pages, two, H_kv, P, D2 = pages.shape
     if two != 2 or D2 != D:
@@ -152,6 +156,7 @@ def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_k
         sliding_window=int(length_info.dim() == 2), num_splits=int(num_splits),
         max_pages=max_pages, nnz_pages=int(values.numel()) if values is not None else 0,
         max_kv_len_hint=int(max_kv_len_hint), k_scale=float(k_scale), v_scale=float(v_scale),
+        flags=DECODE_EARLY_INPUTS if early_inputs else 0,
         workspace=None if workspace is None else workspace.data_ptr(),
         workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
 
@@ -160,13 +165,15 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
                           k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                           rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                           v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                          stream=None):
-    """pd_batch_decode_paged_kv on device tensors; writes `output` and `lse`."""
+                          early_inputs=False, stream=None):
+    """pd_batch_decode_paged_kv on device tensors; writes `output` and `lse`.
+    early_inputs=True sets PD_DECODE_EARLY_INPUTS: only right after append_paged_kv (or
+    another kernel that writes none of Q, the page table, lengths and positions)."""
     if sm_scale is None:
         sm_scale = Q.shape[-1] ** -0.5
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
-                     v_scale=v_scale, workspace=workspace)
+                     v_scale=v_scale, workspace=workspace, early_inputs=early_inputs)
     _check(lib().pd_batch_decode_paged_kv(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -179,14 +186,14 @@ def batch_decode_paged_kv_noalloc(Q, pages, page_table_indptr, page_table_values
                                   length_info, k_rope_pos_offset, q_rope_position, output, lse,
                                   rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
                                   *, k_scale=1.0, v_scale=1.0, num_splits=0, max_kv_len_hint=0,
-                                  stream=None):
+                                  early_inputs=False, stream=None):
     """pd_batch_decode_paged_kv_noalloc: same result, split scratch in the library's
     static device array (no device allocation)."""
     if sm_scale is None:
         sm_scale = Q.shape[-1] ** -0.5
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
-                     v_scale=v_scale)
+                     v_scale=v_scale, early_inputs=early_inputs)
     _check(lib().pd_batch_decode_paged_kv_noalloc(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),

@@ -108,6 +108,7 @@ static pd_status validate_desc(const pd_decode_desc* d) {
   if ((long long)d->max_pages * 2 * d->H_kv > INT_MAX)
     return fail(PD_ERR_UNSUPPORTED, "max_pages * 2 * H_kv exceeds 2^31");
   if (d->num_splits < 0) return fail(PD_ERR_INVALID_ARG, "num_splits < 0");
+  if (d->flags & ~PD_DECODE_EARLY_INPUTS) return fail(PD_ERR_INVALID_ARG, "unknown bits in flags");
   if (d->kv_dtype == kE4M3 && !(d->k_scale > 0.f && d->v_scale > 0.f && std::isfinite(d->k_scale) &&
                                 std::isfinite(d->v_scale)))
     return fail(PD_ERR_INVALID_ARG, "E4M3 KV needs finite positive k_scale and v_scale");
@@ -390,6 +391,7 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
                    ? std::max(1, kSegCostTiles * 16 / d.page_size) : 0;
   p.out_dtype = d.out_dtype;
   p.out_vec16 = (reinterpret_cast<uintptr_t>(output) % 16) == 0 ? 1 : 0;
+  p.early_inputs = (d.flags & PD_DECODE_EARLY_INPUTS) ? 1 : 0;
   const double log2e = 1.4426950408889634073599246810019;
   const double kdeq = d.kv_dtype == kE4M3 ? (double)d.k_scale : 1.0;
   p.score_scale = (float)((double)sm_scale * log2e * kdeq);

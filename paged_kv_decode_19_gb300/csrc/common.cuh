@@ -13,6 +13,8 @@
 #include <climits>
 #include <stdint.h>
 
+#include <utility>
+
 namespace pd {
 
 // dtype codes (mirror pd_dtype in include/pageddecode.h)
@@ -156,6 +158,35 @@ __device__ __forceinline__ void rope_cos_sin_accurate(int pos, unsigned long lon
   const float d = xb * 3.14159265358979f;
   s = fmaf(ca, d, sa);
   c = fmaf(-sa, d, ca);
+}
+
+// ----------------------------------------------------------------------------- launch order
+// Programmatic dependent launch: every kernel of the library is launched with
+// programmatic stream serialisation, so it may start while the kernel before it on the
+// stream is still finishing.  pdl_wait() returns once every grid it depends on has
+// completed with its writes visible (at once when launched without the attribute);
+// a kernel reads nothing that its predecessor may write, and writes nothing, before it.
+// pdl_release() lets the next such kernel start; it is called only after pdl_wait(),
+// so a kernel that starts early knows that everything before its predecessor is done.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 // ----------------------------------------------------------------------------- error word

@@ -49,6 +49,7 @@ struct DecodeParams {
                       // and finish), so ranges that cross segment boundaries get fewer pages
   int out_dtype;
   int out_vec16;      // out is 16-byte aligned (vector stores of whole runs)
+  int early_inputs;   // Q, page table, lengths and positions may be read before pdl_wait()
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
   float q_prescale;   // split-operand MMA path: Q is pre-multiplied by this
   float out_scale;    // applied to the final output (v_scale for e4m3 KV)

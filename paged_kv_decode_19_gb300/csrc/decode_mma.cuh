@@ -351,6 +351,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       s_rot8[i] = make_float2(c8, s8);
     }
   }
+  // By default nothing of the caller's is read before the kernel launched before this
+  // one on the stream has completed; with early_inputs the scan, the page table and Q
+  // are read while it finishes, and only the first page read (or write) waits.
+  if (!p.early_inputs) {
+    pdl_wait();
+    pdl_release();
+  }
   worker_starts<NT, NW>(p, s_start, s_units);  // the last block-wide barrier of the kernel
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -517,6 +524,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 
   // first tile's loads go out before the Q set-up, which then overlaps their latency
   Tile cur = first_tile_from(ua);
+  if (p.early_inputs) {  // pages may still be written by the previous kernel until here
+    pdl_wait();
+    pdl_release();
+  }
   if (cur.kblk) {
     load_k(cur.kblk, cur.t);
     load_v(cur.kblk, cur.t);
@@ -904,8 +915,7 @@ static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t s
     cfg->ctas_per_sm = n;
     return cudaSuccess;
   }
-  kern<<<grid, NW * 32, dyn, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NW * 32), dyn, st, p);
 }
 
 template <typename KVT, typename QT, int D>

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
   __shared__ float sm_m[NW * 8], sm_d[NW * 8];
   __shared__ float sm_o[NW * 8 * D];
 
+  pdl_wait();  // nothing of the caller's is read before the previous kernel completes
+  pdl_release();
   const BlockRange br = block_range<NT>(p);
   if (br.x0 >= br.x1) return;  // no units for this block
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -249,8 +251,7 @@ static cudaError_t launch_simt_d(const DecodeParams& p, dim3 grid, cudaStream_t 
   constexpr int NW = 4;
   auto kern = decode_simt_kernel<KT, QT, D, NW>;
   if (ctas) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, NW * 32, 0);
-  kern<<<grid, NW * 32, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kern, grid, dim3(NW * 32), 0, st, p);
 }
 
 template <typename KT, typename QT>

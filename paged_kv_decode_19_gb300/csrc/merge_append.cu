@@ -16,6 +16,8 @@ template <typename VT>
 __global__ void merge_state_kernel(VT* __restrict__ V, float* __restrict__ S,
                                    const VT* __restrict__ Vo, const float* __restrict__ So,
                                    int rows, int D) {
+  pdl_wait();
+  pdl_release();
   const int warps = blockDim.x >> 5;
   const int row = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
@@ -38,15 +40,15 @@ cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const flo
   const int threads = 256, per = threads / 32;
   const dim3 grid((rows + per - 1) / per);
   if (v_dtype == kF32)
-    merge_state_kernel<float><<<grid, threads, 0, st>>>((float*)V, S, (const float*)V_other, S_other, rows, D);
-  else if (v_dtype == kBF16)
-    merge_state_kernel<__nv_bfloat16><<<grid, threads, 0, st>>>(
-        (__nv_bfloat16*)V, S, (const __nv_bfloat16*)V_other, S_other, rows, D);
-  else if (v_dtype == kF16)
-    merge_state_kernel<__half><<<grid, threads, 0, st>>>((__half*)V, S, (const __half*)V_other, S_other, rows, D);
-  else
-    return cudaErrorInvalidValue;
-  return cudaGetLastError();
+    return launch_pdl(merge_state_kernel<float>, grid, dim3(threads), 0, st, (float*)V, S,
+                      (const float*)V_other, S_other, rows, D);
+  if (v_dtype == kBF16)
+    return launch_pdl(merge_state_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st,
+                      (__nv_bfloat16*)V, S, (const __nv_bfloat16*)V_other, S_other, rows, D);
+  if (v_dtype == kF16)
+    return launch_pdl(merge_state_kernel<__half>, grid, dim3(threads), 0, st, (__half*)V, S,
+                      (const __half*)V_other, S_other, rows, D);
+  return cudaErrorInvalidValue;
 }
 
 template <typename IT, typename OT>
@@ -68,6 +70,8 @@ __global__ void append_kernel(OT* __restrict__ pages, const IT* __restrict__ k_n
                               const IT* __restrict__ v_new, const int64_t* __restrict__ slots,
                               int T, int H_kv, int D, int P, long long max_pages, float k_scale,
                               float v_scale, unsigned* err) {
+  pdl_wait();  // inputs and pages are the previous kernel's to write until it completes
+  pdl_release();
   const int th = blockIdx.x;
   const int t = th / H_kv, h = th - t * H_kv;
   const int kv = blockIdx.y;
@@ -92,14 +96,14 @@ static cudaError_t append_in(void* pages, const void* k, const void* v, const in
   const int threads = D < 128 ? D : 128;
   const IT* kk = (const IT*)k;
   const IT* vv = (const IT*)v;
+  const dim3 block(threads);
   switch (kv_dtype) {
-    case kF32: append_kernel<IT, float><<<grid, threads, 0, st>>>((float*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
-    case kF16: append_kernel<IT, __half><<<grid, threads, 0, st>>>((__half*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
-    case kBF16: append_kernel<IT, __nv_bfloat16><<<grid, threads, 0, st>>>((__nv_bfloat16*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
-    case kE4M3: append_kernel<IT, F8><<<grid, threads, 0, st>>>((F8*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err); break;
+    case kF32: return launch_pdl(append_kernel<IT, float>, grid, block, 0, st, (float*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
+    case kF16: return launch_pdl(append_kernel<IT, __half>, grid, block, 0, st, (__half*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
+    case kBF16: return launch_pdl(append_kernel<IT, __nv_bfloat16>, grid, block, 0, st, (__nv_bfloat16*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
+    case kE4M3: return launch_pdl(append_kernel<IT, F8>, grid, block, 0, st, (F8*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 cudaError_t launch_append(void* pages, const void* k_new, const void* v_new,

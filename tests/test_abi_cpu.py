@@ -38,10 +38,13 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_desc_layout_matches_header():
-    # int32 x10, int64 x2, int32, float x2, void*, size_t
+    # int32 x10, int64 x2, int32, float x2, int32, void*, size_t
     assert ctypes.sizeof(_lib.DecodeDesc) == 88
     assert _lib.DecodeDesc.max_pages.offset == 40
+    assert _lib.DecodeDesc.flags.offset == 68
     assert _lib.DecodeDesc.workspace.offset == 72
+    text = open(HEADER).read()
+    assert re.search(r"#define PD_DECODE_EARLY_INPUTS (\d+)", text).group(1) == str(_lib.DECODE_EARLY_INPUTS)
 
 
 def _desc(**kw):
@@ -58,6 +61,7 @@ def _desc(**kw):
     (dict(out_dtype=3), "PD_ERR_INVALID_ARG"), (dict(kv_dtype=3, k_scale=0.0), "PD_ERR_INVALID_ARG"),
     (dict(kv_dtype=1), "PD_ERR_UNSUPPORTED"), (dict(num_splits=-2), "PD_ERR_INVALID_ARG"),
     (dict(max_pages=0), "PD_ERR_INVALID_ARG"), (dict(B=-1), "PD_ERR_INVALID_ARG"),
+    (dict(flags=2), "PD_ERR_INVALID_ARG"),
 ])
 def test_decode_validation_without_gpu(L, bad, status):
     d = _desc(**bad)

@@ -117,6 +117,34 @@ def test_fp8_append_then_decode(seed):
     compare("e4m3", out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("name", ["fp8_kv_highconc", "llama3_8b_bf16", "window_sink_f16"])
+def test_early_inputs_decode_starts_under_append(name):
+    # With PD_DECODE_EARLY_INPUTS the decode reads Q and the page table while the append
+    # before it still runs (programmatic dependent launch): the rows the append writes
+    # must reach it, and of two such steps on the same out/lse the second must stand.
+    wl = _wl(name, 21, append=True)
+    other = _wl(name, 22, append=True)
+    s = wl.spec
+    ref_pages, bad = oracle.append_paged_kv(
+        W.bits(wl.pages), W.bits(wl.k_new), W.bits(wl.v_new), wl.slot_mapping.cpu().numpy(),
+        in_dtype=s.q_dtype, kv_dtype=s.kv_dtype, page_size=s.page_size, k_scale=wl.k_scale,
+        v_scale=wl.v_scale)
+    assert bad == 0
+    out = torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=DEV)
+    lse = torch.empty((s.B, s.H_qo), dtype=torch.float32, device=DEV)
+    for w in (other, wl):
+        pd.append_paged_kv(w.pages, w.k_new, w.v_new, w.slot_mapping, w.k_scale, w.v_scale)
+        pd.batch_decode_paged_kv(w.Q, w.pages, w.indptr, w.values, w.length_info,
+                                 w.k_rope_pos_offset, w.q_rope_position, out, lse,
+                                 s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
+                                 k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True)
+    torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    assert np.array_equal(W.bits(wl.pages), ref_pages)
+    ro, rl, _ = oracle_decode(wl, pages=ref_pages)
+    compare(kind_of(wl), out, lse, ro, rl)
+
+
 def test_fp8_f16_query_and_simt_variant():
     wl = _wl("fp8_kv_highconc", 8, q_dtype="f16", out_dtype="f16")
     _check(wl, "mma")
