@@ -133,6 +133,11 @@ typedef struct {
  * each block finds its workers' shares with a scan of indptr/length_info.
  * Q or pages not 16-byte aligned: PD_ERR_INVALID_ARG (both kernels read rows with
  * 16-byte vector loads).
+ * Arithmetic: f16, bf16 and E4M3 caches run on tensor cores (fp32 accumulation, Q
+ * split into hi + lo 16-bit parts where it is not already of the cache's type, P
+ * rounded to the cache's 16-bit type for P.V); with RoPE the rotated K is rounded
+ * once to f16, so a bf16 cache must keep |k| below 46000.  f32 caches run an fp32
+ * kernel without tensor cores.
  * Workspace: desc->workspace if non-NULL (at least pd_workspace_size(desc) bytes,
  * 256-byte aligned, zero-filled before its first use — see pd_workspace_init),
  * otherwise a per-device buffer the library allocates on first use and grows as
