@@ -160,6 +160,11 @@ __device__ __forceinline__ void rope_cos_sin_accurate(int pos, unsigned long lon
   c = fmaf(-sa, d, ca);
 }
 
+// Acquire-release fence at GPU scope: with a relaxed atomic after it (release) or
+// before it (acquire) it orders a worker's partial results against the arrival
+// counter, without the sequentially consistent fence of __threadfence().
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ----------------------------------------------------------------------------- launch order
 // Programmatic dependent launch: every kernel of the library is launched with
 // programmatic stream serialisation, so it may start while the kernel before it on the

@@ -660,7 +660,7 @@ __device__ void finish_share(const DecodeParams& p, const BlockRange& br, const 
     __syncthreads();
     return;
   }
-  __threadfence();
+  fence_acq_rel_gpu();
   __syncthreads();
   if (tid == 0) {
     int* cnt = p.counters + (size_t)sg.b * p.H_kv * p.n_z + sg.hz;
@@ -671,7 +671,7 @@ __device__ void finish_share(const DecodeParams& p, const BlockRange& br, const 
   }
   __syncthreads();
   if (s_last) {
-    __threadfence();
+    fence_acq_rel_gpu();
     merge_segment<NT>(p, br, sg, hq0, hcount);
   }
   __syncthreads();

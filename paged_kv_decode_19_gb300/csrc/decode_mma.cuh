@@ -331,7 +331,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   __shared__ int s_units[kStartCacheB];                     // start-up scan scratch
   __shared__ float s_mw[NW][34][kMaxGroupPerCta];           // per-warp merge scratch
   __shared__ int s_msl[NW][32];
-  __shared__ long long s_pend[NW][2][3];                    // per-warp deferred merges
+  __shared__ long long s_pend[NW][2][4];                    // per-warp deferred merges
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
   __shared__ __align__(16) float2 s_rot8[ROPE ? D / 2 : 2];  // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
@@ -525,6 +525,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   // first tile's loads go out before the Q set-up, which then overlaps their latency
   Tile cur = first_tile_from(ua);
   if (p.early_inputs) {  // pages may still be written by the previous kernel until here
+    // the first tile's blocks can come into L2 meanwhile: L2 is where the previous
+    // kernel's writes land, so a line fetched now still sees them
+    if (cur.kblk && lane == 0) {
+      prefetch_l2_bulk(cur.kblk, (uint32_t)block_bytes);
+      prefetch_l2_bulk(cur.kblk + v_off, (uint32_t)block_bytes);
+    }
     pdl_wait();
     pdl_release();
   }
@@ -850,7 +856,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   if (!whole) {
     // publish the partial, count this worker's units; the worker completing the count
     // merges every partial of the segment and resets the counter for the next call
-    __threadfence();
+    fence_acq_rel_gpu();
     __syncwarp();
     int last = 0;
     if (lane == 0) {
@@ -865,11 +871,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       // the merge runs after this worker's last segment (only a worker's first and last
       // segments can be partial, so there are at most two), keeping the tile loop's
       // register budget free of it
-      __threadfence();
+      fence_acq_rel_gpu();
       if (lane == 0) {
         s_pend[warp][npend][0] = sg.b;
         s_pend[warp][npend][1] = sg.hz;
         s_pend[warp][npend][2] = sg.off;
+        s_pend[warp][npend][3] = sg.n;
       }
       npend = 1;  // at most two entries: indices 0 and 1
     }
@@ -885,8 +892,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     if (b < 0) continue;
     const int hz = (int)s_pend[warp][i][1];
     const long long off = s_pend[warp][i][2];
-    const SeqInfo seq = load_seq(p, (int)b);
-    const int n = units_of(seq, P);
+    const int n = (int)s_pend[warp][i][3];
     const int hk = hz / p.n_z, z = hz - hk * p.n_z;
     const int hq0 = hk * p.group + z * kMaxGroupPerCta;
     const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
