@@ -9,6 +9,9 @@ method's arithmetic.
 What each function restates (page title / section):
   * ``batch_decode_paged_kv`` — Apache TVM ``_decode_kernels.py``,
     ``_attention_decode_cpu``, written as two-pass softmax attention in fp64.
+  * ``batch_decode_paged_kv_mq`` — the same with q_len query tokens per sequence,
+    causal among the new tokens (vllm-cpu ``nki_flash_attn.py``,
+    ``flash_paged_attention``: context open, active tokens causal).
   * ``merge_state`` — same page, ``_merge_state_inplace_cpu``.
   * ``append_paged_kv`` — vllm-cpu ``nki_flash_attn.py``, ``reshape_and_cache``,
     on the TVM page layout, with the FP8 encode of the NKI Attention Block TKG
@@ -57,6 +60,9 @@ def lib():
             i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
             L.oracle_batch_decode_paged_kv.argtypes = [
                 P, i32, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i64, i32, i32,
+                f64, f64, f64, f64, f64, P]
+            L.oracle_batch_decode_paged_kv_mq.argtypes = [
+                P, i32, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, i32,
                 f64, f64, f64, f64, f64, P]
             L.oracle_batch_decode_paged_kv.restype = i32
             L.oracle_merge_state.argtypes = [P, P, P, P, i32, i32, i32]
@@ -167,6 +173,45 @@ def batch_decode_paged_kv(Q, pages, indptr, values, length_info, k_rope_pos_offs
     if st == -2:
         raise ValueError("oracle: bad arguments")
     return out, lse, st
+
+
+def batch_decode_paged_kv_mq(Q, pages, indptr, values, length_info, k_rope_pos_offset,
+                             q_rope_position, *, q_len, q_dtype, kv_dtype, H_kv, page_size,
+                             rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
+                             k_scale=1.0, v_scale=1.0, mask=None):
+    """Multi-query decode: returns (out [B,q_len,H_qo,D] f64, lse [B,q_len,H_qo] f64 log2
+    units, status).  Q: [B,q_len,H_qo,D] typed bits (or [B*q_len,H_qo,D]); length_info
+    [B] (no sliding window).  Token t of sequence b sees the attended rows
+    r < L_b - q_len + 1 + t; its RoPE position is q_rope_position[b] + t.
+    """
+    if int(q_len) < 1:
+        raise ValueError("oracle: q_len must be >= 1")
+    Qb = _bits(Q, q_dtype)
+    Pb = _bits(pages, kv_dtype)
+    H_qo, D = Qb.shape[-2:]
+    indptr = _c(indptr, np.int32)
+    B = indptr.size - 1
+    assert Qb.size == B * q_len * H_qo * D, (Qb.shape, B, q_len)
+    Qb = Qb.reshape(B * q_len, H_qo, D)
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    max_pages = Pb.shape[0]
+    assert Pb.shape[1:] == (2, H_kv, page_size, D), Pb.shape
+    values = _c(values, np.int32) if values is not None and np.size(values) else np.zeros(1, np.int32)
+    li = _c(length_info, np.int32)
+    kro = _c(k_rope_pos_offset if k_rope_pos_offset is not None else np.zeros(B), np.int32)
+    qrp = _c(q_rope_position if q_rope_position is not None else np.zeros(B), np.int32)
+    out = np.full((B * q_len, H_qo, D), np.nan)
+    lse = np.full((B * q_len, H_qo), np.nan)
+    m = None if mask is None else _c(mask, np.uint8)
+    st = lib().oracle_batch_decode_paged_kv_mq(
+        _ptr(Qb), DTYPES[q_dtype], _ptr(Pb), DTYPES[kv_dtype], _ptr(indptr), _ptr(values),
+        _ptr(li), _ptr(kro), _ptr(qrp), _ptr(out), _ptr(lse), B, int(q_len), H_qo, H_kv, D,
+        page_size, max_pages, int(rotary_mode), float(rope_scale), float(rope_theta),
+        float(sm_scale), float(k_scale), float(v_scale), _ptr(m))
+    if st == -2:
+        raise ValueError("oracle: bad arguments")
+    return out.reshape(B, q_len, H_qo, D), lse.reshape(B, q_len, H_qo), st
 
 
 def merge_state(V, S, V_other, S_other):

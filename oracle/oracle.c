@@ -274,15 +274,22 @@ void oracle_rope(double* x, int D, double pos, double rope_scale, double rope_th
 /* excluded), -2 on bad arguments.                                            */
 /* ------------------------------------------------------------------------- */
 
-int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, int kv_dtype,
-                                 const int32_t* indptr, const int32_t* values,
-                                 const int32_t* length_info, const int32_t* k_rope_pos_offset,
-                                 const int32_t* q_rope_position, double* out, double* lse, int B,
-                                 int H_qo, int H_kv, int D, int P, int64_t max_pages, int window,
-                                 int rotary_mode, double rope_scale, double rope_theta,
-                                 double sm_scale, double k_scale, double v_scale,
-                                 const uint8_t* mask) {
+/* Multi-query form (q_len >= 1 query tokens per sequence): the last q_len attended  */
+/* rows of sequence b are the new tokens' own K/V, already in the cache, and token t  */
+/* (0-based) sees rows r < L - q_len + 1 + t: the cached context in full and the new  */
+/* tokens causally ([vllm-cpu] nki_flash_attn.py, flash_paged_attention: the context  */
+/* part of the mask is open, the active part causal).  Token t's RoPE position is     */
+/* q_rope_position[b] + t.  Q, out: rows (b*q_len + t)*H_qo + h; lse likewise; mask   */
+/* [B*q_len*H_qo].  q_len = 1 is batch_decode_paged_kv.  No sliding window (-2).      */
+static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dtype,
+                       const int32_t* indptr, const int32_t* values, const int32_t* length_info,
+                       const int32_t* k_rope_pos_offset, const int32_t* q_rope_position,
+                       double* out, double* lse, int B, int q_len, int H_qo, int H_kv, int D,
+                       int P, int64_t max_pages, int window, int rotary_mode, double rope_scale,
+                       double rope_theta, double sm_scale, double k_scale, double v_scale,
+                       const uint8_t* mask) {
   if (B < 0 || H_kv <= 0 || H_qo % H_kv != 0 || D <= 0 || D % 2 || P <= 0) return -2;
+  if (q_len < 1 || (q_len > 1 && window)) return -2;
   int group = H_qo / H_kv;
   int status = 0;
   double* q = (double*)malloc(sizeof(double) * D);
@@ -306,16 +313,23 @@ int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, 
       slot_of[r] = so % P;
       valid[r] = 1;
     }
+    for (int t = 0; t < q_len; ++t)
     for (int h = 0; h < H_qo; ++h) {
-      if (mask && !mask[(size_t)b * H_qo + h]) continue;
+      const size_t row = ((size_t)b * q_len + t) * H_qo + h; /* (sequence, token, head) */
+      if (mask && !mask[row]) continue;
       int hk = h / group;
-      double* o = out + ((size_t)b * H_qo + h) * D;
-      for (int d = 0; d < D; ++d) q[d] = load_elem(Q, q_dtype, ((size_t)b * H_qo + h) * D + d);
-      if (rotary_mode == 1) oracle_rope(q, D, (double)q_rope_position[b], rope_scale, rope_theta);
+      /* rows this token sees: all L for a single token, else causal among the new ones */
+      int64_t Lt = L - q_len + 1 + t;
+      if (Lt > L) Lt = L;
+      if (Lt < 0) Lt = 0;
+      double* o = out + row * D;
+      for (int d = 0; d < D; ++d) q[d] = load_elem(Q, q_dtype, row * D + d);
+      if (rotary_mode == 1)
+        oracle_rope(q, D, (double)q_rope_position[b] + (double)t, rope_scale, rope_theta);
       /* pass 1: scores t_r and their maximum */
       double M = -INFINITY;
       int64_t n_valid = 0;
-      for (int64_t r = 0; r < L; ++r) {
+      for (int64_t r = 0; r < Lt; ++r) {
         if (!valid[r]) continue;
         size_t kbase = ((((size_t)page_of[r] * 2 + 0) * H_kv + hk) * P + slot_of[r]) * D;
         for (int d = 0; d < D; ++d) {
@@ -332,13 +346,13 @@ int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, 
       }
       if (n_valid == 0) { /* R4: empty sequence */
         for (int d = 0; d < D; ++d) o[d] = 0.0;
-        lse[(size_t)b * H_qo + h] = -5e4;
+        lse[row] = -5e4;
         continue;
       }
       /* pass 2: softmax weights, their sum, and the weighted sum of V rows */
       double den = 0.0;
       for (int d = 0; d < D; ++d) o[d] = 0.0;
-      for (int64_t r = 0; r < L; ++r) {
+      for (int64_t r = 0; r < Lt; ++r) {
         if (!valid[r]) continue;
         double w = exp(score[r] - M);
         den += w;
@@ -350,7 +364,7 @@ int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, 
         }
       }
       for (int d = 0; d < D; ++d) o[d] /= den;
-      lse[(size_t)b * H_qo + h] = (M + log(den)) / log(2.0); /* natural -> log2 units */
+      lse[row] = (M + log(den)) / log(2.0); /* natural -> log2 units */
     }
     free(page_of);
     free(slot_of);
@@ -360,6 +374,32 @@ int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, 
   free(q);
   free(k);
   return status;
+}
+
+int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, int kv_dtype,
+                                 const int32_t* indptr, const int32_t* values,
+                                 const int32_t* length_info, const int32_t* k_rope_pos_offset,
+                                 const int32_t* q_rope_position, double* out, double* lse, int B,
+                                 int H_qo, int H_kv, int D, int P, int64_t max_pages, int window,
+                                 int rotary_mode, double rope_scale, double rope_theta,
+                                 double sm_scale, double k_scale, double v_scale,
+                                 const uint8_t* mask) {
+  return decode_impl(Q, q_dtype, pages, kv_dtype, indptr, values, length_info, k_rope_pos_offset,
+                     q_rope_position, out, lse, B, 1, H_qo, H_kv, D, P, max_pages, window,
+                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, mask);
+}
+
+int oracle_batch_decode_paged_kv_mq(const void* Q, int q_dtype, const void* pages, int kv_dtype,
+                                    const int32_t* indptr, const int32_t* values,
+                                    const int32_t* length_info, const int32_t* k_rope_pos_offset,
+                                    const int32_t* q_rope_position, double* out, double* lse,
+                                    int B, int q_len, int H_qo, int H_kv, int D, int P,
+                                    int64_t max_pages, int rotary_mode, double rope_scale,
+                                    double rope_theta, double sm_scale, double k_scale,
+                                    double v_scale, const uint8_t* mask) {
+  return decode_impl(Q, q_dtype, pages, kv_dtype, indptr, values, length_info, k_rope_pos_offset,
+                     q_rope_position, out, lse, B, q_len, H_qo, H_kv, D, P, max_pages, 0,
+                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, mask);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -411,3 +411,82 @@ def test_append_out_of_range_slot_counted():
     got, bad = oracle.append_paged_kv(pages, k, k, np.array([8, 3], np.int64), in_dtype="f32",
                                       kv_dtype="f32", page_size=4)
     assert bad == 1 and got.view(np.float32)[0, 0, 0, 3].tolist() == [1.0] * 4
+
+
+# --------------------------------------------------------------------------- multi-query decode
+
+def _run_mq(Q, pages, indptr, values, li, H_kv, P, q_len, **kw):
+    return oracle.batch_decode_paged_kv_mq(Q, pages, indptr, values, li, kw.pop("kro", None),
+                                           kw.pop("qrp", None), q_len=q_len, q_dtype="f32",
+                                           kv_dtype="f32", H_kv=H_kv, page_size=P, **kw)
+
+
+def test_mq_dense_causal_bruteforce():
+    """q_len query tokens per sequence vs scipy softmax on the dense K/V with the causal
+    limit written out: token t sees rows 0 .. L - q_len + t (none when that is < 0)."""
+    rng = np.random.default_rng(11)
+    for (H_qo, H_kv, D, P, lens, q_len) in [(4, 2, 4, 2, [5, 3, 7], 3), (2, 1, 4, 4, [2, 6], 3),
+                                            (3, 3, 8, 3, [4], 4)]:
+        B = len(lens)
+        _, pages, indptr, values, last, dense = _paged_case(rng, B, H_qo, H_kv, D, P, lens)
+        Q = _f32(rng.standard_normal((B, q_len, H_qo, D)))
+        sm = 0.41
+        out, lse, st = _run_mq(Q, pages, indptr, values, last, H_kv, P, q_len, sm_scale=sm)
+        assert st == 0 and out.shape == (B, q_len, H_qo, D)
+        g = H_qo // H_kv
+        for b in range(B):
+            Kb, Vb = dense[b]
+            for t in range(q_len):
+                n = lens[b] - q_len + 1 + t  # rows 0 .. n-1
+                for h in range(H_qo):
+                    if n <= 0:
+                        assert np.all(out[b, t, h] == 0) and lse[b, t, h] == -5e4
+                        continue
+                    s = sm * (Kb[:n, h // g, :] @ Q[b, t, h].astype(np.float64))
+                    np.testing.assert_allclose(out[b, t, h], softmax(s) @ Vb[:n, h // g, :],
+                                               rtol=0, atol=1e-12)
+                    assert abs(lse[b, t, h] - logsumexp(s) * LOG2E) < 1e-12
+
+
+def test_mq_single_token_is_decode():
+    rng = np.random.default_rng(12)
+    Q, pages, indptr, values, last, _ = _paged_case(rng, 3, 4, 2, 8, 4, [9, 1, 6])
+    o1, l1, _ = _run(Q, pages, indptr, values, last, 2, 4, sm_scale=0.3)
+    o2, l2, _ = _run_mq(Q, pages, indptr, values, last, 2, 4, 1, sm_scale=0.3)
+    assert np.array_equal(o1, o2[:, 0]) and np.array_equal(l1, l2[:, 0])
+
+
+def test_mq_token_equals_truncated_decode_with_rope():
+    """Token t = a single-token decode of the sequence cut to its first L - q_len + 1 + t
+    rows (last_page_len adjusted) with the query at q_rope_position + t."""
+    rng = np.random.default_rng(13)
+    P, q_len, H_qo, H_kv, D = 4, 3, 4, 2, 8
+    lens = [10, 5]
+    B = len(lens)
+    _, pages, indptr, values, last, _ = _paged_case(rng, B, H_qo, H_kv, D, P, lens)
+    Q = _f32(rng.standard_normal((B, q_len, H_qo, D)))
+    kro = np.array([3, 0], np.int32)
+    qrp = np.array([20, 7], np.int32)
+    kw = dict(rotary_mode=1, rope_theta=100.0, sm_scale=0.35)
+    out, lse, st = _run_mq(Q, pages, indptr, values, last, H_kv, P, q_len, kro=kro, qrp=qrp, **kw)
+    assert st == 0
+    for b in range(B):
+        for t in range(q_len):
+            n = lens[b] - q_len + 1 + t
+            npg = (n + P - 1) // P
+            ip = np.array([0, npg], np.int32)
+            vals = values[indptr[b]:indptr[b] + npg]
+            li = np.array([n - (npg - 1) * P], np.int32)
+            o1, l1, _ = oracle.batch_decode_paged_kv(
+                Q[b:b + 1, t], pages, ip, vals, li, kro[b:b + 1], qrp[b:b + 1] + t, q_dtype="f32",
+                kv_dtype="f32", H_kv=H_kv, page_size=P, **kw)
+            np.testing.assert_allclose(out[b, t], o1[0], rtol=0, atol=1e-12)
+            np.testing.assert_allclose(lse[b, t], l1[0], rtol=0, atol=1e-12)
+
+
+def test_mq_rejects_bad_q_len():
+    rng = np.random.default_rng(14)
+    Q, pages, indptr, values, last, _ = _paged_case(rng, 1, 2, 1, 4, 4, [5])
+    with pytest.raises(ValueError):
+        oracle.batch_decode_paged_kv_mq(Q, pages, indptr, values, last, None, None, q_len=0,
+                                        q_dtype="f32", kv_dtype="f32", H_kv=1, page_size=4)
