@@ -190,6 +190,36 @@ pd_status pd_batch_decode_paged_kv_noalloc(const void* Q, const void* pages,
                                            const pd_decode_desc* desc, pd_stream_t stream);
 
 /*
+ * pd_batch_decode_paged_kv_mq — multi-query decode: q_len query tokens per sequence
+ * (speculative decoding, small chunks of prefill), causal among the new tokens.  The
+ * new tokens' K/V are already in the cache (pd_append_paged_kv): they are the last
+ * q_len attended rows of each sequence.  Token t (0-based) of sequence b sees the
+ * attended rows r < L_b - q_len + 1 + t: the cached context in full and the new tokens
+ * up to itself, as the active part of the mask of [VLLM] `flash_paged_attention`
+ * (context open, active tokens causal); a token with no row gives out = 0,
+ * lse = -5e4.  Its RoPE position is q_rope_position[b] + t.  q_len = 1 computes
+ * exactly pd_batch_decode_paged_kv.
+ * Arguments as pd_batch_decode_paged_kv, except:
+ *   Q      [B, q_len, H_qo, D] desc->q_dtype;  output [B, q_len, H_qo, D];
+ *   lse    [B, q_len, H_qo] float32 (log2 units);  q_len >= 1.
+ * The work unit is (sequence, KV head, slice of <= 8 query columns), a column being
+ * one (token, head) of the KV head's group, so each KV page is read once for all
+ * tokens and heads of a slice.  Runs on the tensor-core kernel only: f16/bf16 KV
+ * (D 64 or 128) or E4M3 KV (D 128), page size a multiple of 16; otherwise
+ * PD_ERR_UNSUPPORTED, as is desc->sliding_window != 0.  A caller workspace must hold
+ * pd_workspace_size_mq(desc, q_len) bytes.
+ */
+pd_status pd_batch_decode_paged_kv_mq(const void* Q, const void* pages,
+                                      const int32_t* page_table_indptr,
+                                      const int32_t* page_table_values,
+                                      const int32_t* length_info,
+                                      const int32_t* k_rope_pos_offset,
+                                      const int32_t* q_rope_position, void* output, float* lse,
+                                      int32_t q_len, int32_t rotary_mode, float rope_scale,
+                                      float rope_theta, float sm_scale,
+                                      const pd_decode_desc* desc, pd_stream_t stream);
+
+/*
  * merge_state_inplace — [TVM] `merge_state_inplace`.
  * For every (n, h):  m = max(S, S_o);  w = 2^(S - m);  w_o = 2^(S_o - m);
  *   V[n,h,:] <- V * w/(w+w_o) + V_other * w_o/(w+w_o);  S[n,h] <- log2(w + w_o) + m.
@@ -222,6 +252,9 @@ pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
 /* Bytes of workspace pd_batch_decode_paged_kv needs for `desc` on the current device
  * (0 on invalid desc).  Host-only apart from reading the device's SM count. */
 size_t pd_workspace_size(const pd_decode_desc* desc);
+
+/* The same for pd_batch_decode_paged_kv_mq with q_len query tokens per sequence. */
+size_t pd_workspace_size_mq(const pd_decode_desc* desc, int32_t q_len);
 
 /* Zero-fill a caller-provided workspace before its first use (enqueued on stream). */
 pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream);

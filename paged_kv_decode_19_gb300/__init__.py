@@ -9,6 +9,7 @@ from ._lib import (  # noqa: F401
     append_paged_kv,
     batch_decode_paged_kv,
     batch_decode_paged_kv_noalloc,
+    batch_decode_paged_kv_mq,
     check_device_errors,
     last_decode_variant,
     make_desc,

@@ -43,6 +43,8 @@ DTYPE_NAMES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
 EXPORTS = (
     "pd_batch_decode_paged_kv",
     "pd_batch_decode_paged_kv_noalloc",
+    "pd_batch_decode_paged_kv_mq",
+    "pd_workspace_size_mq",
     "pd_merge_state_inplace",
     "pd_append_paged_kv",
     "pd_workspace_size",
@@ -101,6 +103,11 @@ def lib():
             L.pd_batch_decode_paged_kv.restype = i32
             L.pd_batch_decode_paged_kv_noalloc.argtypes = L.pd_batch_decode_paged_kv.argtypes
             L.pd_batch_decode_paged_kv_noalloc.restype = i32
+            a = list(L.pd_batch_decode_paged_kv.argtypes)
+            L.pd_batch_decode_paged_kv_mq.argtypes = a[:9] + [i32] + a[9:]
+            L.pd_batch_decode_paged_kv_mq.restype = i32
+            L.pd_workspace_size_mq.argtypes = [ctypes.POINTER(DecodeDesc), i32]
+            L.pd_workspace_size_mq.restype = ctypes.c_size_t
             L.pd_merge_state_inplace.argtypes = [P, P, P, P, i32, i32, i32, i32, P]
             L.pd_merge_state_inplace.restype = i32
             L.pd_append_paged_kv.argtypes = [P, P, P, P, i32, i32, i32, i32, i64, i32, i32, f32,
@@ -199,6 +206,30 @@ def batch_decode_paged_kv_noalloc(Q, pages, page_table_indptr, page_table_values
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
         _ptr(lse), int(rotary_mode), float(rope_scale), float(rope_theta), float(sm_scale),
         ctypes.byref(desc), _stream(stream)))
+    return output, lse
+
+
+def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, length_info,
+                             k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
+                             rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
+                             v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
+                             early_inputs=False, stream=None):
+    """pd_batch_decode_paged_kv_mq: Q [B, q_len, H_qo, D], output [B, q_len, H_qo, D],
+    lse [B, q_len, H_qo]; token t of a sequence sees its rows up to itself."""
+    if Q.dim() != 4:
+        raise ValueError("Q must be [B, q_len, H_qo, D]")
+    B, q_len, H_qo, D = Q.shape
+    if sm_scale is None:
+        sm_scale = D ** -0.5
+    desc = make_desc(Q[:, 0], pages, page_table_indptr,
+                     page_table_values, length_info, output, num_splits=num_splits,
+                     max_kv_len_hint=max_kv_len_hint, k_scale=k_scale, v_scale=v_scale,
+                     workspace=workspace, early_inputs=early_inputs)
+    _check(lib().pd_batch_decode_paged_kv_mq(
+        _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
+        _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
+        _ptr(lse), int(q_len), int(rotary_mode), float(rope_scale), float(rope_theta),
+        float(sm_scale), ctypes.byref(desc), _stream(stream)))
     return output, lse
 
 

@@ -52,8 +52,8 @@ struct DeviceState {
   void* ws = nullptr;   // partial (out, lse) of split sequences
   size_t ws_bytes = 0;
   // resident blocks per SM of each kernel variant, queried once:
-  // [mma][q_dtype][kv_dtype][D 64/128/256][rotary]; 0 = not yet known
-  int occupancy[2][4][4][3][2] = {};
+  // [mma][q_dtype][kv_dtype][D 64/128/256][rotary][multi-query]; 0 = not yet known
+  int occupancy[2][4][4][3][2][2] = {};
 };
 constexpr int kMaxDevices = 64;
 static DeviceState g_dev[kMaxDevices];
@@ -122,10 +122,12 @@ static pd_status validate_desc(const pd_decode_desc* d) {
 // (the tensor-core kernel's warps, or 1 for the SIMT kernel's blocks).  *mode:
 // kSchedBalanced or kSchedPerSegment; *grid: blocks; workspace = per-segment arrival
 // counters + two partial (lse, out) slots per worker.
+// q_len: query tokens per sequence (multi-query decode); a segment's query columns
+// (q_len x group per KV head) come in slices of at most kMaxGroupPerCta.
 static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int wpb, int* mode,
-                      int* grid, size_t* ws_bytes) {
-  const int group = d->H_qo / d->H_kv;
-  const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
+                      int* grid, size_t* ws_bytes, int q_len = 1) {
+  const int ncol = (d->H_qo / d->H_kv) * q_len;
+  const int n_z = (ncol + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
   const long long segments = (long long)d->B * d->H_kv * n_z;
   const long long wave = (long long)std::max(num_sms, 1) * std::max(ctas_per_sm, 1);
   wpb = std::max(wpb, 1);
@@ -169,6 +171,11 @@ static bool mma_path(const pd_decode_desc* d, const void* pages) {
 
 static cudaError_t mma_dispatch(const DecodeParams& p, int q_dtype, int kv_dtype, dim3 grid,
                                 cudaStream_t st, MmaConfig* cfg) {
+  if (p.q_len > 1) {
+    if (kv_dtype == kBF16) return launch_mma_mq_bf16(p, q_dtype, grid, st, cfg);
+    if (kv_dtype == kF16) return launch_mma_mq_f16(p, q_dtype, grid, st, cfg);
+    return launch_mma_mq_fp8(p, q_dtype, grid, st, cfg);
+  }
   if (kv_dtype == kBF16) return launch_mma_bf16(p, q_dtype, grid, st, cfg);
   if (kv_dtype == kF16) return launch_mma_f16(p, q_dtype, grid, st, cfg);
   return launch_mma_fp8(p, q_dtype, grid, st, cfg);
@@ -209,9 +216,10 @@ pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_
 }
 
 static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary, int* ctas,
-                               DeviceState* ds = nullptr) {
+                               DeviceState* ds = nullptr, int q_len = 1) {
   const int di = d->D == 64 ? 0 : d->D == 128 ? 1 : 2;
-  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rotary ? 1 : 0]
+  const int mq = q_len > 1 ? 1 : 0;
+  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rotary ? 1 : 0][mq]
                    : nullptr;
   if (cached && *cached > 0) {
     *ctas = *cached;
@@ -221,6 +229,7 @@ static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary
   p.D = d->D;
   p.P = d->page_size;
   p.rotary = rotary;
+  p.q_len = q_len;
   cudaError_t e;
   int n = 0;
   if (use_mma) {
@@ -237,24 +246,31 @@ static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary
   return PD_OK;
 }
 
-size_t pd_workspace_size(const pd_decode_desc* desc) {
-  if (validate_desc(desc) != PD_OK) return 0;
+static size_t workspace_size_q(const pd_decode_desc* desc, int q_len) {
+  if (validate_desc(desc) != PD_OK || q_len < 1) return 0;
   DeviceState* ds = nullptr;
   if (device_state(&ds) != PD_OK) return 0;
   // the largest plan over the variants a call with this desc may take
   size_t best = 0;
   for (int mma = 0; mma < 2; ++mma) {
     if (mma && !mma_path(desc, nullptr)) continue;
+    if (!mma && q_len > 1) continue;  // the multi-query form runs on the tensor-core kernel only
     for (int rot = 0; rot < 2; ++rot) {
       int ctas = 1;
-      if (occupancy_for(desc, mma != 0, rot, &ctas, ds) != PD_OK) continue;
+      if (occupancy_for(desc, mma != 0, rot, &ctas, ds, q_len) != PD_OK) continue;
       int mode, grid;
       size_t ws;
-      plan_impl(desc, ds->num_sms, ctas, mma ? kMmaWarps : 1, &mode, &grid, &ws);
+      plan_impl(desc, ds->num_sms, ctas, mma ? kMmaWarps : 1, &mode, &grid, &ws, q_len);
       best = std::max(best, ws);
     }
   }
   return best;
+}
+
+size_t pd_workspace_size(const pd_decode_desc* desc) { return workspace_size_q(desc, 1); }
+
+size_t pd_workspace_size_mq(const pd_decode_desc* desc, int32_t q_len) {
+  return workspace_size_q(desc, q_len);
 }
 
 pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream) {
@@ -264,14 +280,15 @@ pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream) {
   return PD_OK;
 }
 
-pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
-                                   const int32_t* page_table_indptr,
-                                   const int32_t* page_table_values, const int32_t* length_info,
-                                   const int32_t* k_rope_pos_offset,
-                                   const int32_t* q_rope_position, void* output, float* lse,
-                                   int32_t rotary_mode, float rope_scale, float rope_theta,
-                                   float sm_scale, const pd_decode_desc* desc,
-                                   pd_stream_t stream) {
+}  // extern "C"
+
+// Both decode entry points: q_len query tokens per sequence (1: batch_decode_paged_kv).
+static pd_status decode_call(const void* Q, const void* pages, const int32_t* page_table_indptr,
+                             const int32_t* page_table_values, const int32_t* length_info,
+                             const int32_t* k_rope_pos_offset, const int32_t* q_rope_position,
+                             void* output, float* lse, int q_len, int32_t rotary_mode,
+                             float rope_scale, float rope_theta, float sm_scale,
+                             const pd_decode_desc* desc, pd_stream_t stream) {
   pd_status st = validate_desc(desc);
   if (st != PD_OK) return st;
   const pd_decode_desc& d = *desc;
@@ -293,18 +310,22 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   st = device_state(&ds);
   if (st != PD_OK) return st;
   const bool use_mma = mma_path(desc, pages);
+  if (q_len > 1 && !use_mma)
+    return fail(PD_ERR_UNSUPPORTED, "multi-query decode runs on the tensor-core kernel only: "
+                                    "f16/bf16 (D 64 or 128) or E4M3 (D 128) KV, page size a multiple of 16");
   int ctas = 1;
-  st = occupancy_for(desc, use_mma, rotary_mode, &ctas, ds);
+  st = occupancy_for(desc, use_mma, rotary_mode, &ctas, ds, q_len);
   if (st != PD_OK) return st;
   int mode = 0, grid_blocks = 0;
   size_t ws_need = 0;
   const int wpb = use_mma ? kMmaWarps : 1;
-  plan_impl(desc, ds->num_sms, ctas, wpb, &mode, &grid_blocks, &ws_need);
+  plan_impl(desc, ds->num_sms, ctas, wpb, &mode, &grid_blocks, &ws_need, q_len);
   if (grid_blocks == 0) return PD_OK;
 
   cudaStream_t s = (cudaStream_t)stream;
   const int group = d.H_qo / d.H_kv;
-  const int n_z = (group + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
+  const int ncol = group * q_len;
+  const int n_z = (ncol + kMaxGroupPerCta - 1) / kMaxGroupPerCta;
   const size_t cnt_bytes = align_up((size_t)d.B * d.H_kv * n_z * sizeof(int), kWsAlign);
   const size_t lse_bytes = align_up((size_t)2 * grid_blocks * wpb * kMaxGroupPerCta * sizeof(float), kWsAlign);
   int* counters = nullptr;
@@ -382,6 +403,8 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   p.P = d.page_size;
   p.group = group;
   p.n_z = n_z;
+  p.q_len = q_len;
+  p.ncol = ncol;
   p.precise = d.kv_dtype == kF32 ? 1 : 0;
   p.window = d.sliding_window ? 1 : 0;
   p.rotary = rotary_mode;
@@ -411,6 +434,39 @@ pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
   }
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return PD_OK;
+}
+
+extern "C" {
+
+pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
+                                   const int32_t* page_table_indptr,
+                                   const int32_t* page_table_values, const int32_t* length_info,
+                                   const int32_t* k_rope_pos_offset,
+                                   const int32_t* q_rope_position, void* output, float* lse,
+                                   int32_t rotary_mode, float rope_scale, float rope_theta,
+                                   float sm_scale, const pd_decode_desc* desc,
+                                   pd_stream_t stream) {
+  return decode_call(Q, pages, page_table_indptr, page_table_values, length_info,
+                     k_rope_pos_offset, q_rope_position, output, lse, 1, rotary_mode, rope_scale,
+                     rope_theta, sm_scale, desc, stream);
+}
+
+pd_status pd_batch_decode_paged_kv_mq(const void* Q, const void* pages,
+                                      const int32_t* page_table_indptr,
+                                      const int32_t* page_table_values,
+                                      const int32_t* length_info,
+                                      const int32_t* k_rope_pos_offset,
+                                      const int32_t* q_rope_position, void* output, float* lse,
+                                      int32_t q_len, int32_t rotary_mode, float rope_scale,
+                                      float rope_theta, float sm_scale,
+                                      const pd_decode_desc* desc, pd_stream_t stream) {
+  if (q_len < 1) return fail(PD_ERR_INVALID_ARG, "q_len must be >= 1");
+  if (desc && desc->sliding_window)
+    return fail(PD_ERR_UNSUPPORTED, "multi-query decode has no sliding-window form");
+  if (desc && (long long)desc->B * q_len > INT_MAX) return fail(PD_ERR_UNSUPPORTED, "B * q_len exceeds 2^31");
+  return decode_call(Q, pages, page_table_indptr, page_table_values, length_info,
+                     k_rope_pos_offset, q_rope_position, output, lse, q_len, rotary_mode,
+                     rope_scale, rope_theta, sm_scale, desc, stream);
 }
 
 pd_status pd_merge_state_inplace(void* V, float* S, const void* V_other, const float* S_other,

@@ -42,6 +42,8 @@ struct DecodeParams {
   long long max_pages;
   long long nnz_pages;  // entries of the page table (page_table_values)
   int B, H_qo, H_kv, D, P, group, n_z;
+  int q_len;          // query tokens per sequence (multi-query decode; 1 = plain decode)
+  int ncol;           // query columns per KV head: q_len * group, in slices of <= 8
   int window, rotary;
   int precise;        // fp32 path: merge weights via the accurate exp2f
   int mode;           // kSchedBalanced / kSchedPerSegment
@@ -62,6 +64,14 @@ struct DecodeParams {
 struct SeqInfo {
   int L, sink, win_off, page_begin, npages;
 };
+
+// Row of (sequence b, query column c of KV head hk) in Q, out and lse: column c is query
+// token c / group and head hk * group + c % group (with one token per sequence, c is
+// the head's index within the group).
+__device__ __forceinline__ size_t col_row(const DecodeParams& p, int b, int hk, int c) {
+  const int t = c / p.group;
+  return ((size_t)b * p.q_len + t) * p.H_qo + hk * p.group + (c - t * p.group);
+}
 
 __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
   // every load is issued up front (one round trip), then the fields are checked

@@ -142,7 +142,7 @@ __device__ __forceinline__ void store_run(const DecodeParams& p, size_t idx, con
 // of 34 x 8 floats, s_sl: 32 ints.
 template <int D, int HMAX, int BATCH>
 __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, int seg_c, int seg_n,
-                           long long U, long long W, int hq0, int hcount,
+                           long long U, long long W, int hk, int c0, int hcount,
                            float (*s_w)[kMaxGroupPerCta], int* s_sl) {
   constexpr int G8 = kMaxGroupPerCta;
   constexpr int D4 = D / 4;
@@ -301,19 +301,19 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
       const float Mj = s_M[j], dj = s_den[j];
       const bool empty = !(Mj > kEmptyM);
       const float sc = empty ? 0.f : p.out_scale;
-      const int hq = hq0 + j;
-      const size_t o = ((size_t)seg_b * p.H_qo + hq) * D + 4 * d4;
+      const size_t row = col_row(p, seg_b, hk, c0 + j);
+      const size_t o = row * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
       store_out(p, o + 1, acc[e].y * sc);
       store_out(p, o + 2, acc[e].z * sc);
       store_out(p, o + 3, acc[e].w * sc);
-      if (d4 == 0) p.lse[(size_t)seg_b * p.H_qo + hq] = empty ? kEmptyM : Mj + log2f(dj);
+      if (d4 == 0) p.lse[row] = empty ? kEmptyM : Mj + log2f(dj);
     }
   }
   __syncwarp();
 }
 
-template <typename KVT, typename QT, int D, bool ROPE, int NW>
+template <typename KVT, typename QT, int D, bool ROPE, int NW, bool MQ>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::v)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using Tr = MmaTraits<KVT, QT, D, ROPE>;
@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   // Q and the page table are small and needed right after the start-up scan, when the
   // first tiles of every worker flood HBM: each block prefetches its share into L2 now
   if (threadIdx.x == 0) {
-    prefetch_l2_share(p.Q, (size_t)p.B * p.H_qo * D * sizeof(QT), blockIdx.x, gridDim.x);
+    prefetch_l2_share(p.Q, (size_t)p.B * p.q_len * p.H_qo * D * sizeof(QT), blockIdx.x, gridDim.x);
     if (p.values) prefetch_l2_share(p.values, (size_t)p.nnz_pages * sizeof(int32_t), blockIdx.x, gridDim.x);
   }
   if (ROPE) {
@@ -394,8 +394,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   const int hk = sg.hz / p.n_z, z = sg.hz - (sg.hz / p.n_z) * p.n_z;
   const Pieces pcs = make_pieces(0, sg.seq.L, sg.seq, P);
   const int pend = min(ub, sg.seq.L > 0 ? pcs.count() : 0);  // pieces [ua, pend) here
-  const int hq0 = hk * p.group + z * kMaxGroupPerCta;
-  const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
+  const int c0 = z * kMaxGroupPerCta;                      // first query column of the slice
+  const int hcount = min(kMaxGroupPerCta, p.ncol - c0);  // its columns (heads x tokens)
 
   // Raw Q of this lane's B-fragment elements (pairs of adjacent dims), loaded first:
   // they are tiny and needed before anything else.
@@ -411,7 +411,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   constexpr int QCH = KT / 2;
   uint4 qchunk[QCH];
   {
-    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + (have_q ? qh : 0)) * D;
+    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + col_row(p, sg.b, hk, c0 + (have_q ? qh : 0)) * D;
 #pragma unroll
     for (int c = 0; c < QCH; ++c) {
       const int e0 = FP8 ? 16 * (4 * (c >> 1) + q4) + 8 * (c & 1) : 8 * (4 * c + q4);
@@ -423,7 +423,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     return FP8 ? comp(qchunk[2 * (kt >> 2) + ((kt & 3) >> 1)], 2 * (kt & 1) + h)
                : comp(qchunk[kt >> 1], 2 * (kt & 1) + h);
   };
-  const int qpos = ROPE ? __ldg(p.q_rope_position + sg.b) : 0;
+  // query position: q_rope_position[b], plus the token index of this lane's column
+  const int qpos = ROPE ? __ldg(p.q_rope_position + sg.b) + (MQ ? (c0 + qh) / p.group : 0) : 0;
+  // multi-query: attended-row limits of this lane's two score columns (token t sees rows
+  // r < L - q_len + 1 + t; packed slices keep columns 0..3, folded into lanes q4 and q4^2)
+  int lim0 = 0, lim1 = 0;
+  if constexpr (MQ) {
+    const int cc = c0 + (pack4 ? 2 * (q4 & 1) : 2 * q4);
+    lim0 = sg.seq.L - p.q_len + 1 + cc / p.group;
+    lim1 = sg.seq.L - p.q_len + 1 + (cc + 1) / p.group;
+  }
   const int kpos0 = ROPE ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
 
   // ---------------------------------------------------------------- tile stream
@@ -723,6 +732,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       sc[1] = v0 ? acc[1] * post_scale : -INFINITY;
       sc[2] = v1 ? acc[2] * post_scale : -INFINITY;  // row g_id + 8
       sc[3] = v1 ? acc[3] * post_scale : -INFINITY;
+      if constexpr (MQ) {  // causal among the new tokens
+        const int r0 = cur.r_lo + (slot0 - cur.s_lo);  // attended index of row g_id
+        if (r0 >= lim0) sc[0] = -INFINITY;
+        if (r0 >= lim1) sc[1] = -INFINITY;
+        if (r0 + 8 >= lim0) sc[2] = -INFINITY;
+        if (r0 + 8 >= lim1) sc[3] = -INFINITY;
+      }
       // Lazy running max: the reference max m moves only when some score exceeds it by
       // more than kLazyMax (log2 units; a warp vote), so the tile max reduction and the
       // rescale of O and d run on the first tile and then rarely.  Probabilities stay
@@ -830,7 +846,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
       const bool empty = !(st_d[hh] > 0.f);
       const float inv = empty ? 0.f : 1.f / st_d[hh];
       const float l = empty ? kEmptyM : st_m[hh] + log2f(st_d[hh]);
-      const int hq = hq0 + j;
+      const size_t row = col_row(p, sg.b, hk, c0 + j);
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         const int d0 = FP8 ? 16 * g_id : 8 * (g_id + 8 * r);
@@ -840,7 +856,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
         if (whole) {
 #pragma unroll
           for (int o = 0; o < RL; ++o) v[o] *= p.out_scale;
-          store_run<RL>(p, ((size_t)sg.b * p.H_qo + hq) * D + d0, v);
+          store_run<RL>(p, row * D + d0, v);
         } else {
           float4* po = reinterpret_cast<float4*>(p.part_o + (slot + j) * D + d0);
 #pragma unroll
@@ -848,7 +864,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
         }
       }
       if (g_id == 0) {
-        if (whole) p.lse[(size_t)sg.b * p.H_qo + hq] = l;
+        if (whole) p.lse[row] = l;
         else p.part_lse[slot + j] = l;
       }
     }
@@ -894,24 +910,24 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
     const long long off = s_pend[warp][i][2];
     const int n = (int)s_pend[warp][i][3];
     const int hk = hz / p.n_z, z = hz - hk * p.n_z;
-    const int hq0 = hk * p.group + z * kMaxGroupPerCta;
-    const int hcount = min(kMaxGroupPerCta, p.group - z * kMaxGroupPerCta);
+    const int c0 = z * kMaxGroupPerCta;
+    const int hcount = min(kMaxGroupPerCta, p.ncol - c0);
     // slot rows in flight together: about 16 float4 per lane (4 where registers are
     // tight), for the slice's head count
     constexpr int kBudget = MinBlocks<ROPE, FP8>::v >= 3 ? 4 : 16;
     constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
     if (hcount <= 4)
-      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hq0, hcount, s_mw[warp], s_msl[warp]);
+      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
     else
-      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hq0, hcount, s_mw[warp], s_msl[warp]);
+      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
   }
 }
 
-template <typename KVT, typename QT, int D, bool ROPE>
+template <typename KVT, typename QT, int D, bool ROPE, bool MQ>
 static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
   constexpr int NW = kMmaWarps;
   constexpr int dyn = 0;
-  auto kern = decode_mma_kernel<KVT, QT, D, ROPE, NW>;
+  auto kern = decode_mma_kernel<KVT, QT, D, ROPE, NW, MQ>;
   if (cfg) {
     cfg->threads = NW * 32;
     cfg->smem_bytes = dyn;
@@ -924,10 +940,12 @@ static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t s
   return launch_pdl(kern, grid, dim3(NW * 32), dyn, st, p);
 }
 
-template <typename KVT, typename QT, int D>
+// MQ: the multi-query form (query columns = tokens x heads, causal among the tokens);
+// a separate instantiation, so the single-token kernel carries none of it.
+template <typename KVT, typename QT, int D, bool MQ>
 static cudaError_t launch_mma_r(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
-  if (p.rotary) return launch_mma_t<KVT, QT, D, true>(p, grid, st, cfg);
-  return launch_mma_t<KVT, QT, D, false>(p, grid, st, cfg);
+  if (p.rotary) return launch_mma_t<KVT, QT, D, true, MQ>(p, grid, st, cfg);
+  return launch_mma_t<KVT, QT, D, false, MQ>(p, grid, st, cfg);
 }
 
 }  // namespace pd

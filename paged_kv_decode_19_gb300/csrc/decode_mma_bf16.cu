@@ -6,8 +6,8 @@ namespace pd {
 cudaError_t launch_mma_bf16(const DecodeParams& p, int q_dtype, dim3 grid,
                            cudaStream_t st, MmaConfig* cfg) {
   (void)q_dtype;
-  if (p.D == 64) return launch_mma_r<__nv_bfloat16, __nv_bfloat16, 64>(p, grid, st, cfg);
-  if (p.D == 128) return launch_mma_r<__nv_bfloat16, __nv_bfloat16, 128>(p, grid, st, cfg);
+  if (p.D == 64) return launch_mma_r<__nv_bfloat16, __nv_bfloat16, 64, false>(p, grid, st, cfg);
+  if (p.D == 128) return launch_mma_r<__nv_bfloat16, __nv_bfloat16, 128, false>(p, grid, st, cfg);
   return cudaErrorInvalidValue;
 }
 

@@ -6,8 +6,8 @@ namespace pd {
 cudaError_t launch_mma_f16(const DecodeParams& p, int q_dtype, dim3 grid,
                            cudaStream_t st, MmaConfig* cfg) {
   (void)q_dtype;
-  if (p.D == 64) return launch_mma_r<__half, __half, 64>(p, grid, st, cfg);
-  if (p.D == 128) return launch_mma_r<__half, __half, 128>(p, grid, st, cfg);
+  if (p.D == 64) return launch_mma_r<__half, __half, 64, false>(p, grid, st, cfg);
+  if (p.D == 128) return launch_mma_r<__half, __half, 128, false>(p, grid, st, cfg);
   return cudaErrorInvalidValue;
 }
 

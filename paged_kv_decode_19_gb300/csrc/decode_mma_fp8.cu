@@ -7,8 +7,8 @@ cudaError_t launch_mma_fp8(const DecodeParams& p, int q_dtype, dim3 grid,
                            cudaStream_t st, MmaConfig* cfg) {
   (void)q_dtype;
   if (p.D != 128) return cudaErrorInvalidValue;
-  if (q_dtype == kBF16) return launch_mma_r<F8, __nv_bfloat16, 128>(p, grid, st, cfg);
-  if (q_dtype == kF16) return launch_mma_r<F8, __half, 128>(p, grid, st, cfg);
+  if (q_dtype == kBF16) return launch_mma_r<F8, __nv_bfloat16, 128, false>(p, grid, st, cfg);
+  if (q_dtype == kF16) return launch_mma_r<F8, __half, 128, false>(p, grid, st, cfg);
   return cudaErrorInvalidValue;
 }
 

@@ -27,6 +27,13 @@ cudaError_t launch_mma_f16(const DecodeParams& p, int q_dtype, dim3 grid, cudaSt
                            MmaConfig* cfg);
 cudaError_t launch_mma_fp8(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
                            MmaConfig* cfg);
+// The same for the multi-query form (p.q_len > 1).
+cudaError_t launch_mma_mq_bf16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                               MmaConfig* cfg);
+cudaError_t launch_mma_mq_f16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                              MmaConfig* cfg);
+cudaError_t launch_mma_mq_fp8(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                              MmaConfig* cfg);
 
 // Sets the thread's last-error message (api.cu).
 void record_error(const char* msg);

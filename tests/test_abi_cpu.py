@@ -136,3 +136,15 @@ def test_python_binding_rejects_missing_library(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _lib.lib()
+
+
+def test_multi_query_validation_without_gpu(L):
+    d = _desc()
+    args = lambda q_len, dd: (None, None, None, None, None, None, None, None, None, q_len, 0, 1.0,
+                              1e4, 0.1, ctypes.byref(dd), None)
+    assert _lib.STATUS[L.pd_batch_decode_paged_kv_mq(*args(0, d))] == "PD_ERR_INVALID_ARG"
+    dw = _desc(sliding_window=1)
+    assert _lib.STATUS[L.pd_batch_decode_paged_kv_mq(*args(2, dw))] == "PD_ERR_UNSUPPORTED"
+    # the desc is validated as for the single-token entry point
+    assert _lib.STATUS[L.pd_batch_decode_paged_kv_mq(*args(2, _desc(D=96)))] == "PD_ERR_UNSUPPORTED"
+    assert L.pd_batch_decode_paged_kv_mq(*args(2, _desc(B=0))) == 0
