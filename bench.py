@@ -99,14 +99,23 @@ def _oracle_sample(wl: W.Workload, budget_s: float):
     t0 = time.perf_counter()
     nseq = rows = 0
     for b in range(s.B):
-        mask = np.zeros((s.B, s.H_qo), bool)
-        mask[b] = True
-        oracle.batch_decode_paged_kv(
-            Q, pages, ip, vals, li, kro, qrp, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
-            H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode,
-            rope_scale=s.rope_scale, rope_theta=s.rope_theta, sm_scale=wl.sm_scale,
-            sliding_window=s.window is not None, k_scale=wl.k_scale, v_scale=wl.v_scale,
-            mask=mask)
+        if s.q_len > 1:
+            mask = np.zeros((s.B, s.q_len, s.H_qo), bool)
+            mask[b] = True
+            oracle.batch_decode_paged_kv_mq(
+                Q, pages, ip, vals, li, kro, qrp, q_len=s.q_len, q_dtype=s.q_dtype,
+                kv_dtype=s.kv_dtype, H_kv=s.H_kv, page_size=s.page_size,
+                rotary_mode=s.rotary_mode, rope_scale=s.rope_scale, rope_theta=s.rope_theta,
+                sm_scale=wl.sm_scale, k_scale=wl.k_scale, v_scale=wl.v_scale, mask=mask)
+        else:
+            mask = np.zeros((s.B, s.H_qo), bool)
+            mask[b] = True
+            oracle.batch_decode_paged_kv(
+                Q, pages, ip, vals, li, kro, qrp, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
+                H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode,
+                rope_scale=s.rope_scale, rope_theta=s.rope_theta, sm_scale=wl.sm_scale,
+                sliding_window=s.window is not None, k_scale=wl.k_scale, v_scale=wl.v_scale,
+                mask=mask)
         nseq += 1
         rows += int(wl.attended[b])
         if time.perf_counter() - t0 >= budget_s:
@@ -177,21 +186,25 @@ class ClockSampler:
 
 
 def _append_inputs(wl: W.Workload, device):
-    """New-token K/V (one per sequence, at row len-1) for the step's append."""
+    """New-token K/V for the step's append: q_len tokens per sequence, at rows
+    len-q_len .. len-1 (one token, at row len-1, for the single-token decode)."""
     s = wl.spec
     if wl.k_new is not None:
         return wl.k_new, wl.v_new, wl.slot_mapping
     g = torch.Generator(device=device)
     g.manual_seed(12345)
     dt = W.TORCH_DTYPES[s.q_dtype]
-    k = torch.randn((s.B, s.H_kv, s.D), generator=g, device=device).to(dt)
-    v = torch.randn((s.B, s.H_kv, s.D), generator=g, device=device).to(dt)
+    T = s.B * s.q_len
+    k = torch.randn((T, s.H_kv, s.D), generator=g, device=device).to(dt)
+    v = torch.randn((T, s.H_kv, s.D), generator=g, device=device).to(dt)
     ip = wl.indptr.cpu().numpy()
     vals = wl.values.cpu().numpy()
-    row = np.maximum(wl.seq_len - 1, 0)
-    slots = np.where(wl.seq_len > 0,
-                     vals[ip[:-1] + row // s.page_size].astype(np.int64) * s.page_size
-                     + row % s.page_size, -1)
+    row = (wl.seq_len[:, None] - s.q_len + np.arange(s.q_len)[None, :]).reshape(-1)
+    seq = np.repeat(np.arange(s.B), s.q_len)
+    ok = row >= 0
+    rr = np.maximum(row, 0)
+    slots = np.where(ok, vals[np.minimum(ip[seq] + rr // s.page_size, max(len(vals) - 1, 0))]
+                     .astype(np.int64) * s.page_size + rr % s.page_size, -1)
     return k, v, torch.from_numpy(slots.astype(np.int64)).to(device)
 
 
@@ -213,8 +226,11 @@ def run_ours(args, ws, rank, local):
     s = wl.spec
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     alternate = wl.kv_bytes_attended() > l2
-    out = torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=dev)
-    lse = torch.empty((s.B, s.H_qo), dtype=torch.float32, device=dev)
+    qdims = (s.B,) if s.q_len == 1 else (s.B, s.q_len)
+    out = torch.empty(qdims + (s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=dev)
+    lse = torch.empty(qdims + (s.H_qo,), dtype=torch.float32, device=dev)
+    # q_len query tokens per sequence: the multi-query entry point
+    decode_api = pd.batch_decode_paged_kv if s.q_len == 1 else pd.batch_decode_paged_kv_mq
     split = dict(num_splits=1) if args.config == "tiny_fp32" else {}
     stream = torch.cuda.current_stream(dev)
     wbuf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
@@ -234,11 +250,9 @@ def run_ours(args, ws, rank, local):
         # the decode follows the append on the stream: its start-up (work split scan,
         # page table, Q) may run under the append (PD_DECODE_EARLY_INPUTS)
         w = r[0]
-        pd.batch_decode_paged_kv(w.Q, w.pages, w.indptr, w.values, w.length_info,
-                                 w.k_rope_pos_offset, w.q_rope_position, out, lse,
-                                 s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
-                                 k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
-                                 **split)
+        decode_api(w.Q, w.pages, w.indptr, w.values, w.length_info, w.k_rope_pos_offset,
+                   w.q_rope_position, out, lse, s.rotary_mode, s.rope_scale, s.rope_theta,
+                   w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True, **split)
 
     def prefill(n):
         # a spin kernel of about 60 us per step keeps the device busy (at load clocks)
@@ -350,11 +364,10 @@ def run_ours(args, ws, rank, local):
         a.record(stream)
         buf.copy_(host_in, non_blocking=True)
         pd.append_paged_kv(w.pages, di["k_new"], di["v_new"], di["slots"], w.k_scale, w.v_scale)
-        pd.batch_decode_paged_kv(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
-                                 di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e,
-                                 s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
-                                 k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
-                                 **split)
+        decode_api(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
+                   di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e, s.rotary_mode,
+                   s.rope_scale, s.rope_theta, w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale,
+                   early_inputs=True, **split)
         res_host.copy_(res_dev, non_blocking=True)
         b.record(stream)
         b.synchronize()
@@ -400,8 +413,10 @@ def main():
                        f"D={spec.D}, page_size={spec.page_size}, {spec.kv_dtype} KV",
            "B": spec.B, "H_qo": spec.H_qo, "H_kv": spec.H_kv, "D": spec.D,
            "page_size": spec.page_size, "kv_dtype": spec.kv_dtype, "q_dtype": spec.q_dtype,
-           "rotary_mode": spec.rotary_mode, "len_dist": list(spec.len_dist),
-           "step": "append_paged_kv (1 token/seq) + batch_decode_paged_kv",
+           "rotary_mode": spec.rotary_mode, "len_dist": list(spec.len_dist), "q_len": spec.q_len,
+           "step": ("append_paged_kv (1 token/seq) + batch_decode_paged_kv" if spec.q_len == 1 else
+                    f"append_paged_kv ({spec.q_len} tokens/seq) + batch_decode_paged_kv_mq "
+                    f"(q_len={spec.q_len}, causal among the new tokens)"),
            "l2": None,  # filled in below
            "parallelism": f"replicas x{ws} (each rank its own batch; no collective)"}
 

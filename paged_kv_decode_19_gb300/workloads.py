@@ -15,6 +15,9 @@ CSR page table, ``length_info`` ``[B]`` or ``[3,B]``):
   long_ctx_bf16      B=8,   H 32/8, D=128, P=16, bf16, len U[32768,131072]
   window_sink_f16    B=64,  H 32/4, D=128, P=16, f16, len U[4096,16384], window 4096, sink 4, RoPE 1e4
   fp8_kv_highconc    B=256, H 64/8, D=128, P=32, e4m3 KV (+ bf16 Q), lognormal len, + append
+  spec_decode_bf16   llama3_8b_bf16 with 2 query tokens per sequence (multi-query decode,
+                     causal among them: speculative decoding's verification step; the
+                     2 x 4 (token, head) columns of a KV head fill one 8-column MMA tile)
 
 Each has a ``reduced`` variant (same structure, fewer/shorter sequences) that the
 oracle finishes in seconds.
@@ -57,6 +60,7 @@ class Spec:
     sink: int = 0
     append: bool = False       # one new token per sequence, written before attention
     max_splits: int = 0        # external split count (long-context chunking)
+    q_len: int = 1             # query tokens per sequence (multi-query decode, causal)
 
 
 SPECS = {
@@ -72,6 +76,9 @@ SPECS = {
                             window=4096, sink=4),
     "fp8_kv_highconc": Spec("fp8_kv_highconc", 256, 64, 8, 128, 32, "bf16", "e4m3", "bf16",
                             ("lognormal", 2048, 0.6, 64, 8192), append=True),
+    "spec_decode_bf16": Spec("spec_decode_bf16", 32, 32, 8, 128, 16, "bf16", "bf16", "bf16",
+                             ("uniform", 512, 4096), pool=16384, rotary_mode=1,
+                             rope_theta=500000.0, q_len=2),
 }
 
 # Reduced variants: same heads/dtypes/page size/features, sizes the oracle handles in
@@ -82,6 +89,7 @@ REDUCED = {
     "long_ctx_bf16": dict(B=2, len_dist=("uniform", 1500, 3000)),
     "window_sink_f16": dict(B=5, len_dist=("uniform", 200, 900), window=300),
     "fp8_kv_highconc": dict(B=6, len_dist=("lognormal", 300, 0.6, 20, 700)),
+    "spec_decode_bf16": dict(B=5, len_dist=("uniform", 17, 700), pool=512),
 }
 
 
@@ -97,7 +105,7 @@ def spec(name: str, reduced: bool = False, **overrides) -> Spec:
 @dataclasses.dataclass
 class Workload:
     spec: Spec
-    Q: torch.Tensor                 # [B,H_qo,D] q_dtype
+    Q: torch.Tensor                 # [B,H_qo,D] q_dtype ([B,q_len,H_qo,D] multi-query)
     pages: torch.Tensor             # [max_pages,2,H_kv,P,D] kv_dtype
     indptr: torch.Tensor            # [B+1] int32
     values: torch.Tensor            # [nnz] int32
@@ -127,7 +135,7 @@ class Workload:
         s = self.spec
         qes = torch.empty(0, dtype=self.Q.dtype).element_size()
         oes = torch.empty(0, dtype=TORCH_DTYPES[s.out_dtype]).element_size()
-        return s.B * s.H_qo * s.D * (qes + oes) + s.B * s.H_qo * 4
+        return s.q_len * (s.B * s.H_qo * s.D * (qes + oes) + s.B * s.H_qo * 4)
 
     def to(self, device) -> "Workload":
         def mv(x):
@@ -198,6 +206,8 @@ def make(name: str, seed: int = 0, reduced: bool = False, device="cpu", **overri
         attended[npages == 0] = 0
     k_off = np.zeros(s.B, np.int32)
     q_pos = attended.astype(np.int32)  # query sits right after the attended (compacted) rows
+    if s.q_len > 1:  # the new tokens are the last q_len cached rows: token t at its own row
+        q_pos = np.maximum(attended - s.q_len, 0).astype(np.int32)
 
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
@@ -212,7 +222,8 @@ def make(name: str, seed: int = 0, reduced: bool = False, device="cpu", **overri
     else:
         pages = x.to(TORCH_DTYPES[s.kv_dtype])
     del x
-    Q = _randn((s.B, s.H_qo, s.D), gen, device).to(TORCH_DTYPES[s.q_dtype])
+    qshape = (s.B, s.H_qo, s.D) if s.q_len == 1 else (s.B, s.q_len, s.H_qo, s.D)
+    Q = _randn(qshape, gen, device).to(TORCH_DTYPES[s.q_dtype])
     k_new = v_new = slot_mapping = None
     if s.append:
         in_dt = TORCH_DTYPES[s.q_dtype]

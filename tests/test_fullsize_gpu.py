@@ -43,6 +43,9 @@ def test_fullsize_sampled(name):
         pd.append_paged_kv(wl.pages, wl.k_new, wl.v_new, wl.slot_mapping, wl.k_scale, wl.v_scale)
         assert pd.check_device_errors() == "PD_OK"
         assert np.array_equal(W.bits(wl.pages), ref_pages), "append not bit-exact at full size"
+    if s.q_len > 1:
+        _fullsize_multi_query(wl)
+        return
     out, lse = gpu_decode(wl, **kw)
     assert pd.check_device_errors() == "PD_OK"
     # properties of every output: finite; each output element is a convex combination
@@ -53,5 +56,33 @@ def test_fullsize_sampled(name):
     assert (lse > -5e4).all()
     mask = _sample_mask(wl)
     ro, rl, st = oracle_decode(wl, pages=ref_pages, mask=mask)
+    assert st == 0
+    compare(kind_of(wl), out, lse, ro, rl, mask=mask)
+
+
+def _fullsize_multi_query(wl):
+    """Multi-query workload: the same properties, and sampled (sequence, token, head)
+    outputs against the oracle's multi-query form."""
+    s = wl.spec
+    out = torch.empty((s.B, s.q_len, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=DEV)
+    lse = torch.empty((s.B, s.q_len, s.H_qo), dtype=torch.float32, device=DEV)
+    pd.batch_decode_paged_kv_mq(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info,
+                                wl.k_rope_pos_offset, wl.q_rope_position, out, lse, s.rotary_mode,
+                                s.rope_scale, s.rope_theta, wl.sm_scale)
+    assert pd.check_device_errors() == "PD_OK"
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+    vmax = wl.pages[:, 1].float().abs().max().item()
+    assert out.float().abs().max().item() <= vmax * (1 + 1e-2)
+    assert (lse > -5e4).all()
+    m2 = _sample_mask(wl)
+    mask = np.zeros((s.B, s.q_len, s.H_qo), bool)
+    for t in range(s.q_len):
+        mask[:, t] = np.roll(m2, t, axis=1)
+    ro, rl, st = oracle.batch_decode_paged_kv_mq(
+        W.bits(wl.Q), W.bits(wl.pages), wl.indptr.cpu().numpy(), wl.values.cpu().numpy(),
+        wl.length_info.cpu().numpy(), wl.k_rope_pos_offset.cpu().numpy(),
+        wl.q_rope_position.cpu().numpy(), q_len=s.q_len, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
+        H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode, rope_scale=s.rope_scale,
+        rope_theta=s.rope_theta, sm_scale=wl.sm_scale, mask=mask)
     assert st == 0
     compare(kind_of(wl), out, lse, ro, rl, mask=mask)
