@@ -1,7 +1,7 @@
 // Tensor-core decode kernel for 16-bit and FP8 KV caches (sm_103a).
 //
 // Work split: the attended pages of every segment (sequence, KV head, slice of <= 8
-// query heads that share the KV head) lie on one cost line (each segment: a fixed
+// query columns that share the KV head) lie on one cost line (each segment: a fixed
 // set-up cost, then one unit per page), cut into W equal contiguous ranges, one per
 // warp (W = blocks x 4).  Each warp is an independent
 // worker: it walks the segments its range touches, streams their pages in order and
@@ -18,7 +18,9 @@
 // prefetches the K and V blocks of the next page into L2.  The loads are laid out so
 // that the registers already are mma.sync fragments:
 //   - S^T = K Q^T (m16n8k16, fp32 accumulate): A = the K tile (16 rows x 16 dims per
-//     k-tile), B = Q^T with the <= 8 query heads of the KV group as the n dimension.
+//     k-tile), B = Q^T with the <= 8 query columns of the slice as the n dimension:
+//     the query heads of the KV group, or in the multi-query form (MQ) its (token,
+//     head) pairs, each token t masked beyond its causal limit L - q_len + 1 + t.
 //     A thread loads 16 contiguous bytes of its rows per chunk; the dot product's
 //     k order is permuted to match, and Q's B fragments use the same permutation.
 //   - online base-2 softmax on the accumulator fragments (TVM `batch_decode_paged_kv`:
@@ -399,11 +401,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
 
   // Raw Q of this lane's B-fragment elements (pairs of adjacent dims), loaded first:
   // they are tiny and needed before anything else.
-  // Split-operand slices of at most 4 heads pack Q's lo part into the unused MMA
-  // columns 4..7 (lane group g_id >= 4 builds head g_id - 4's lo fragment): K Q^T then
-  // takes 2 MMAs per k-tile instead of 3, and column h + 4 is folded into column h.
+  // Split-operand slices of at most 4 columns pack Q's lo part into the unused MMA
+  // columns 4..7 (lane group g_id >= 4 builds column g_id - 4's lo fragment): K Q^T then
+  // takes one MMA per k-tile instead of two, and column h + 4 is folded into column h.
   const bool pack4 = Tr::kQSplit && hcount <= 4;
-  const int qh = pack4 ? (g_id & 3) : g_id;  // the head this lane's B fragment holds
+  const int qh = pack4 ? (g_id & 3) : g_id;  // the column this lane's B fragment holds
   const bool have_q = qh < hcount;
   // The lane's Q elements (dims frag_dim(kt, h, e, q4)) form KT/2 contiguous 16-byte
   // chunks, loaded with one vector load each: chunk c starts at element 8 (4c + q4)
