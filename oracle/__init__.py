@@ -73,6 +73,7 @@ def lib():
             L.oracle_decode.argtypes = [P, i32, P, i64]
             L.oracle_encode.argtypes = [P, i32, P, i64]
             L.oracle_rope.argtypes = [P, i32, f64, f64, f64]
+            L.oracle_rope_interleaved.argtypes = [P, i32, f64, f64, f64]
             L.oracle_attended_offsets.argtypes = [P, P, i32, i32, i32, i32, P, i64]
             L.oracle_attended_offsets.restype = i64
             L.oracle_e4m3_encode.argtypes = [f64]
@@ -122,10 +123,12 @@ def encode(values, dt):
     return out
 
 
-def rope(x, pos, rope_scale, rope_theta):
-    """Rotate-half RoPE of one head vector in fp64 (reading R2)."""
+def rope(x, pos, rope_scale, rope_theta, interleaved=False):
+    """RoPE of one head vector in fp64: rotate-half (reading R2), or the interleaved
+    pair layout (rotary_mode 2)."""
     v = _c(x, np.float64).copy()
-    lib().oracle_rope(_ptr(v), v.shape[-1], float(pos), float(rope_scale), float(rope_theta))
+    f = lib().oracle_rope_interleaved if interleaved else lib().oracle_rope
+    f(_ptr(v), v.shape[-1], float(pos), float(rope_scale), float(rope_theta))
     return v
 
 

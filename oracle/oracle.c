@@ -260,6 +260,27 @@ void oracle_rope(double* x, int D, double pos, double rope_scale, double rope_th
   }
 }
 
+/* The interleaved layout ([NKI] `rope_contiguous_layout` = False): frequency i      */
+/* rotates the adjacent pair (2i, 2i+1) instead of (i, i + D/2); same angles.        */
+void oracle_rope_interleaved(double* x, int D, double pos, double rope_scale,
+                             double rope_theta) {
+  for (int i = 0; i < D / 2; ++i) {
+    double inv_freq = 1.0 / pow(rope_theta, (2.0 * i) / (double)D);
+    double ang = pos * rope_scale * inv_freq;
+    double c = cos(ang), s = sin(ang);
+    double a = x[2 * i], b = x[2 * i + 1];
+    x[2 * i] = a * c - b * s;
+    x[2 * i + 1] = b * c + a * s;
+  }
+}
+
+/* rotary_mode: 0 none, 1 rotate-half, 2 interleaved pairs */
+static void apply_rope(int rotary_mode, double* x, int D, double pos, double rope_scale,
+                       double rope_theta) {
+  if (rotary_mode == 1) oracle_rope(x, D, pos, rope_scale, rope_theta);
+  if (rotary_mode == 2) oracle_rope_interleaved(x, D, pos, rope_scale, rope_theta);
+}
+
 /* ------------------------------------------------------------------------- */
 /* batch_decode_paged_kv: [TVM] `_attention_decode_cpu`, restated from the    */
 /* plain definition of softmax attention (two passes, fp64):                  */
@@ -289,7 +310,7 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
                        double rope_theta, double sm_scale, double k_scale, double v_scale,
                        const uint8_t* mask) {
   if (B < 0 || H_kv <= 0 || H_qo % H_kv != 0 || D <= 0 || D % 2 || P <= 0) return -2;
-  if (q_len < 1 || (q_len > 1 && window)) return -2;
+  if (q_len < 1 || (q_len > 1 && window) || rotary_mode < 0 || rotary_mode > 2) return -2;
   int group = H_qo / H_kv;
   int status = 0;
   double* q = (double*)malloc(sizeof(double) * D);
@@ -324,8 +345,8 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
       if (Lt < 0) Lt = 0;
       double* o = out + row * D;
       for (int d = 0; d < D; ++d) q[d] = load_elem(Q, q_dtype, row * D + d);
-      if (rotary_mode == 1)
-        oracle_rope(q, D, (double)q_rope_position[b] + (double)t, rope_scale, rope_theta);
+      apply_rope(rotary_mode, q, D, (double)q_rope_position[b] + (double)t, rope_scale,
+                 rope_theta);
       /* pass 1: scores t_r and their maximum */
       double M = -INFINITY;
       int64_t n_valid = 0;
@@ -336,8 +357,8 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
           k[d] = load_elem(pages, kv_dtype, kbase + d);
           if (kv_dtype == OR_E4M3) k[d] *= k_scale;
         }
-        if (rotary_mode == 1)
-          oracle_rope(k, D, (double)k_rope_pos_offset[b] + (double)r, rope_scale, rope_theta);
+        apply_rope(rotary_mode, k, D, (double)k_rope_pos_offset[b] + (double)r, rope_scale,
+                   rope_theta);
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += q[d] * k[d];
         score[r] = sm_scale * dot;

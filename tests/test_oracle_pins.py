@@ -261,6 +261,42 @@ def test_rope_matches_complex_rotation():
         np.testing.assert_allclose(y, np.concatenate([z.real, z.imag]), rtol=0, atol=1e-12)
 
 
+def test_rope_interleaved_matches_complex_rotation():
+    """Interleaved layout: z_i = x_{2i} + i x_{2i+1} times the same exp(i angle_i)."""
+    rng = np.random.default_rng(22)
+    D = 16
+    x = rng.standard_normal(D)
+    for pos, sc, th in [(0, 1.0, 1e4), (1, 1.0, 100.0), (37, 0.5, 5e5), (4096, 1.0, 5e5)]:
+        y = oracle.rope(x, pos, sc, th, interleaved=True)
+        i = np.arange(D // 2)
+        z = (x[0::2] + 1j * x[1::2]) * np.exp(1j * pos * sc * th ** (-2.0 * i / D))
+        want = np.empty(D)
+        want[0::2], want[1::2] = z.real, z.imag
+        np.testing.assert_allclose(y, want, rtol=0, atol=1e-12)
+
+
+def test_rope_interleaved_is_rotate_half_on_permuted_dims():
+    """Moving dim 2i to i and 2i+1 to i + D/2 turns the interleaved layout into the
+    rotate-half one; decode with either layout on correspondingly permuted Q/K gives
+    the same output once V is permuted back."""
+    rng = np.random.default_rng(23)
+    D = 8
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])  # half layout <- dims
+    x = rng.standard_normal(D)
+    y = oracle.rope(x, 77, 1.0, 1e3, interleaved=True)
+    np.testing.assert_allclose(y[perm], oracle.rope(x[perm], 77, 1.0, 1e3), rtol=0, atol=1e-12)
+    Q, pages, indptr, values, last, _ = _paged_case(rng, 2, 4, 2, D, 4, [9, 3])
+    kro, qrp = np.array([2, 5], np.int32), np.array([11, 8], np.int32)
+    kw = dict(q_dtype="f32", kv_dtype="f32", H_kv=2, page_size=4, rope_theta=1e3)
+    o_il, l_il, _ = oracle.batch_decode_paged_kv(Q, pages, indptr, values, last, kro, qrp,
+                                                 rotary_mode=2, **kw)
+    o_hf, l_hf, _ = oracle.batch_decode_paged_kv(np.ascontiguousarray(Q[..., perm]),
+                                                 np.ascontiguousarray(pages[..., perm]), indptr,
+                                                 values, last, kro, qrp, rotary_mode=1, **kw)
+    np.testing.assert_allclose(o_il[..., perm], o_hf, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_il, l_hf, rtol=0, atol=1e-12)
+
+
 def test_rope_identity_at_zero_and_norm():
     rng = np.random.default_rng(13)
     x = rng.standard_normal(8)
