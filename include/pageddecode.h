@@ -113,9 +113,12 @@ typedef struct {
  *                    offset r (r < sink) or r - sink + win_off.
  *   page  page_table_values[indptr[b] + off / P], slot off % P;
  *         K row = pages[page, 0, hk, slot, :], V row = pages[page, 1, hk, slot, :].
- *   RoPE  (rotary_mode == 1) rotate-half over the full head dim with angle
- *         pos * rope_scale / rope_theta^(2i/D); Q at q_rope_position[b],
- *         K row r at k_rope_pos_offset[b] + r.
+ *   RoPE  (rotary_mode == 1) rotate-half over the full head dim: frequency i
+ *         rotates the pair (i, i + D/2) by the angle pos * rope_scale /
+ *         rope_theta^(2i/D); Q at q_rope_position[b], K row r at
+ *         k_rope_pos_offset[b] + r.  rotary_mode == 2: the interleaved layout of
+ *         [NKI] (`rope_contiguous_layout` = False), frequency i rotating the pair
+ *         (2i, 2i + 1) by the same angle.
  *   s_r = sm_scale * log2(e) * q.k_r;  out = sum_r 2^(s_r) v_r / sum_r 2^(s_r);
  *   lse = log2(sum_r 2^(s_r)).  An empty sequence gives out = 0, lse = -5e4.
  * Arguments (all device pointers):
@@ -126,7 +129,8 @@ typedef struct {
  *   length_info [B] or [3,B] int32 (see desc->sliding_window).
  *   k_rope_pos_offset, q_rope_position [B] int32; may be NULL when rotary_mode == 0.
  *   output      [B, H_qo, D] desc->out_dtype.   lse [B, H_qo] float32 (log2 units).
- * Scalars: rotary_mode (0 none, 1 RoPE), rope_scale, rope_theta, sm_scale.
+ * Scalars: rotary_mode (0 none, 1 RoPE rotate-half, 2 RoPE interleaved), rope_scale,
+ * rope_theta, sm_scale.
  * Work is split by pages (see desc->num_splits); a (sequence, head slice) that
  * several workers share is merged on the device from their partial (out, lse) pairs
  * by the worker that completes its page count.  The grid uses only host-known sizes;

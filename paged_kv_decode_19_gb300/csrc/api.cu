@@ -52,8 +52,8 @@ struct DeviceState {
   void* ws = nullptr;   // partial (out, lse) of split sequences
   size_t ws_bytes = 0;
   // resident blocks per SM of each kernel variant, queried once:
-  // [mma][q_dtype][kv_dtype][D 64/128/256][rotary][multi-query]; 0 = not yet known
-  int occupancy[2][4][4][3][2][2] = {};
+  // [mma][q_dtype][kv_dtype][D 64/128/256][rotary 0/1/2][multi-query]; 0 = not yet known
+  int occupancy[2][4][4][3][3][2] = {};
 };
 constexpr int kMaxDevices = 64;
 static DeviceState g_dev[kMaxDevices];
@@ -219,7 +219,7 @@ static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary
                                DeviceState* ds = nullptr, int q_len = 1) {
   const int di = d->D == 64 ? 0 : d->D == 128 ? 1 : 2;
   const int mq = q_len > 1 ? 1 : 0;
-  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rotary ? 1 : 0][mq]
+  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rotary == 2 ? 2 : rotary ? 1 : 0][mq]
                    : nullptr;
   if (cached && *cached > 0) {
     *ctas = *cached;
@@ -255,7 +255,7 @@ static size_t workspace_size_q(const pd_decode_desc* desc, int q_len) {
   for (int mma = 0; mma < 2; ++mma) {
     if (mma && !mma_path(desc, nullptr)) continue;
     if (!mma && q_len > 1) continue;  // the multi-query form runs on the tensor-core kernel only
-    for (int rot = 0; rot < 2; ++rot) {
+    for (int rot = 0; rot < 3; ++rot) {
       int ctas = 1;
       if (occupancy_for(desc, mma != 0, rot, &ctas, ds, q_len) != PD_OK) continue;
       int mode, grid;
@@ -292,10 +292,10 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   pd_status st = validate_desc(desc);
   if (st != PD_OK) return st;
   const pd_decode_desc& d = *desc;
-  if (rotary_mode != 0 && rotary_mode != 1) return fail(PD_ERR_INVALID_ARG, "rotary_mode must be 0 or 1");
-  if (rotary_mode == 1 && (!k_rope_pos_offset || !q_rope_position))
+  if (rotary_mode < 0 || rotary_mode > 2) return fail(PD_ERR_INVALID_ARG, "rotary_mode must be 0, 1 or 2");
+  if (rotary_mode != 0 && (!k_rope_pos_offset || !q_rope_position))
     return fail(PD_ERR_INVALID_ARG, "RoPE needs k_rope_pos_offset and q_rope_position");
-  if (rotary_mode == 1 && !(rope_theta > 0.f && std::isfinite(rope_theta) && std::isfinite(rope_scale)))
+  if (rotary_mode != 0 && !(rope_theta > 0.f && std::isfinite(rope_theta) && std::isfinite(rope_scale)))
     return fail(PD_ERR_INVALID_ARG, "rope_theta must be finite and positive");
   if (!std::isfinite(sm_scale)) return fail(PD_ERR_INVALID_ARG, "sm_scale must be finite");
   if (d.B == 0) return PD_OK;

@@ -315,9 +315,11 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
   __syncwarp();
 }
 
-template <typename KVT, typename QT, int D, bool ROPE, int NW, bool MQ>
-__global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::v)
+template <typename KVT, typename QT, int D, int RM, int NW, bool MQ>
+__global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 1)>::v)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
+  constexpr bool ROPE = RM != 0;  // RM: 0 no RoPE, 1 rotate-half, 2 interleaved pairs
+  constexpr bool IL = RM == 2;
   using Tr = MmaTraits<KVT, QT, D, ROPE>;
   using MT = typename Tr::MT;
   using QKT = typename Tr::QKT;
@@ -567,7 +569,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
           qv[u][h][0] = f.x;
           qv[u][h][1] = f.y;
         }
-      if (ROPE) {
+      if (ROPE && !IL) {  // rotate-half: dims d (k-tile kt) and d + D/2 (kt + KT/2)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -577,6 +579,18 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
             const float x = qv[0][h][e], y = qv[1][h][e];
             qv[0][h][e] = x * c - y * sn;
             qv[1][h][e] = y * c + x * sn;
+          }
+      }
+      if (IL) {  // interleaved: the element pair (2i, 2i + 1) of a fragment, frequency i
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            float c, sn;
+            rope_cos_sin(qpos, s_ropeF[frag_dim<FP8>(kt + u * (KT / 2), h, 0, q4) >> 1], c, sn);
+            const float x = qv[u][h][0], y = qv[u][h][1];
+            qv[u][h][0] = x * c - y * sn;
+            qv[u][h][1] = y * c + x * sn;
           }
       }
 #pragma unroll
@@ -641,6 +655,47 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
           const uint4 qf = s_qf[warp][kt][lane];
           Mma<MT>::run(qacc[(2 * kt) % kQChains], a, qf.x, qf.y);
           if (Tr::kQSplit && !PK) Mma<MT>::run(qacc[(2 * kt + 1) % kQChains], a, qf.z, qf.w);
+        }
+      } else if constexpr (IL) {
+        // interleaved RoPE on K in registers: each A-fragment register holds the pair
+        // (2i, 2i + 1) of one row, rotated by frequency i; rows g_id and g_id + 8 (8
+        // positions further) go through the rotation together as an fp32x2 pair
+        const int pos0 = kpos0 + cur.r_lo + (slot0 - cur.s_lo);
+#pragma unroll
+        for (int kt = 0; kt < KT; ++kt) {
+          uint32_t araw[4];
+          if constexpr (FP8) {
+            const uint32_t r0w = comp(kr[0][kt >> 2], kt & 3), r1w = comp(kr[1][kt >> 2], kt & 3);
+            araw[0] = e4m3x2_to_f16x2((uint16_t)(r0w & 0xffff));
+            araw[2] = e4m3x2_to_f16x2((uint16_t)(r0w >> 16));
+            araw[1] = e4m3x2_to_f16x2((uint16_t)(r1w & 0xffff));
+            araw[3] = e4m3x2_to_f16x2((uint16_t)(r1w >> 16));
+          } else {
+            araw[0] = comp(kr[0][kt >> 1], 2 * (kt & 1));
+            araw[2] = comp(kr[0][kt >> 1], 2 * (kt & 1) + 1);
+            araw[1] = comp(kr[1][kt >> 1], 2 * (kt & 1));
+            araw[3] = comp(kr[1][kt >> 1], 2 * (kt & 1) + 1);
+          }
+          uint32_t ar[4];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const int f = frag_dim<FP8>(kt, half, 0, q4) >> 1;
+            float c0, s0;
+            rope_cos_sin(pos0, s_ropeF[f], c0, s0);
+            const float2 r8 = s_rot8[f];  // (cos, sin) of 8 positions
+            const float2 cc = make_float2(c0, c0 * r8.x - s0 * r8.y);
+            const float2 ss = make_float2(s0, s0 * r8.x + c0 * r8.y);
+            const float2 a0 = unpack2<MT>(araw[2 * half]);      // row g_id: (2i, 2i + 1)
+            const float2 a1 = unpack2<MT>(araw[2 * half + 1]);  // row g_id + 8
+            const float2 x = make_float2(a0.x, a1.x), y = make_float2(a0.y, a1.y);
+            const float2 xr = sub_f2(mul_f2(x, cc), mul_f2(y, ss));
+            const float2 yr = fma_f2(y, cc, mul_f2(x, ss));
+            ar[2 * half] = pack2<QKT>(xr.x, yr.x);
+            ar[2 * half + 1] = pack2<QKT>(xr.y, yr.y);
+          }
+          const uint4 qf = s_qf[warp][kt][lane];
+          Mma<QKT>::run(qacc[kt % kQChains], ar, qf.x, qf.y);
+          if (!PK) Mma<QKT>::run(qacc[(kt + 1) % kQChains], ar, qf.z, qf.w);
         }
       } else {
         // RoPE on K in registers: k-tiles kt and kt + KT/2 hold dims d and d + D/2
@@ -925,11 +980,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<ROPE, (sizeof(KVT) == 1)>::
   }
 }
 
-template <typename KVT, typename QT, int D, bool ROPE, bool MQ>
+template <typename KVT, typename QT, int D, int RM, bool MQ>
 static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
   constexpr int NW = kMmaWarps;
   constexpr int dyn = 0;
-  auto kern = decode_mma_kernel<KVT, QT, D, ROPE, NW, MQ>;
+  auto kern = decode_mma_kernel<KVT, QT, D, RM, NW, MQ>;
   if (cfg) {
     cfg->threads = NW * 32;
     cfg->smem_bytes = dyn;
@@ -946,8 +1001,9 @@ static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t s
 // a separate instantiation, so the single-token kernel carries none of it.
 template <typename KVT, typename QT, int D, bool MQ>
 static cudaError_t launch_mma_r(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
-  if (p.rotary) return launch_mma_t<KVT, QT, D, true, MQ>(p, grid, st, cfg);
-  return launch_mma_t<KVT, QT, D, false, MQ>(p, grid, st, cfg);
+  if (p.rotary == 1) return launch_mma_t<KVT, QT, D, 1, MQ>(p, grid, st, cfg);
+  if (p.rotary == 2) return launch_mma_t<KVT, QT, D, 2, MQ>(p, grid, st, cfg);
+  return launch_mma_t<KVT, QT, D, 0, MQ>(p, grid, st, cfg);
 }
 
 }  // namespace pd

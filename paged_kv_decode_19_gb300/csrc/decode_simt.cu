@@ -41,6 +41,31 @@ struct RowHalf {  // N consecutive elements of a row, loaded with one vector acc
   }
 };
 
+// A lane's Q or K values of one row: halves [d0, d0 + H2) and [d1, d1 + H2) (rotate-half
+// pairs (d, d + D/2) share a lane slot e), or, for the interleaved RoPE layout, the
+// element pairs (2i, 2i + 1) for i in [d0, d0 + H2), even elements in `a` and odd in
+// `b`: the RoPE pair again shares slot e with frequency d0 + e.  Q and K take the same
+// order, so q.k is unchanged; V and the output keep the halves.
+template <typename T, int H2>
+__device__ __forceinline__ void load_qk_row(const T* row, int d0, int d1, bool interleaved,
+                                            float (&a)[H2], float (&b)[H2]) {
+  if (!interleaved) {
+    RowHalf<T, H2>::load(row + d0, a);
+    RowHalf<T, H2>::load(row + d1, b);
+    return;
+  }
+  float lo[H2], hi[H2];  // elements 2 d0 .. 2 d0 + 2 H2 - 1
+  RowHalf<T, H2>::load(row + 2 * d0, lo);
+  RowHalf<T, H2>::load(row + 2 * d0 + H2, hi);
+#pragma unroll
+  for (int e = 0; e < H2; ++e) {
+    const float x = 2 * e < H2 ? lo[2 * e] : hi[2 * e - H2];
+    const float y = 2 * e + 1 < H2 ? lo[2 * e + 1] : hi[2 * e + 1 - H2];
+    a[e] = x;
+    b[e] = y;
+  }
+}
+
 template <typename KT, typename QT, int D, int NW>
 __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NT = NW * 32;
@@ -90,8 +115,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
     float a[H2], bb[H2];
     if (j < hcount) {
       const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + j) * D;
-      RowHalf<QT, H2>::load(qrow + d0, a);
-      RowHalf<QT, H2>::load(qrow + d1, bb);
+      load_qk_row<QT, H2>(qrow, d0, d1, p.rotary == 2, a, bb);
     } else {
 #pragma unroll
       for (int e = 0; e < H2; ++e) a[e] = bb[e] = 0.f;
@@ -141,8 +165,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
           ok[u] = true;
           const size_t kofs = (((size_t)page * 2 * p.H_kv + hk) * p.P + (so % p.P)) * D;
           float ka[H2], kb[H2], va[H2], vb[H2];
-          RowHalf<KT, H2>::load(pages + kofs + d0, ka);
-          RowHalf<KT, H2>::load(pages + kofs + d1, kb);
+          load_qk_row<KT, H2>(pages + kofs, d0, d1, p.rotary == 2, ka, kb);
           RowHalf<KT, H2>::load(pages + kofs + kv_stride + d0, va);
           RowHalf<KT, H2>::load(pages + kofs + kv_stride + d1, vb);
 #pragma unroll

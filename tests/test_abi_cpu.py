@@ -70,6 +70,13 @@ def test_decode_validation_without_gpu(L, bad, status):
     assert _lib.STATUS[st] == status, L.pd_get_last_error_string()
 
 
+def test_decode_rotary_mode_range(L):
+    d = _desc()
+    st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 3,
+                                    1.0, 1e4, 0.1, ctypes.byref(d), None)
+    assert _lib.STATUS[st] == "PD_ERR_INVALID_ARG" and b"0, 1 or 2" in L.pd_get_last_error_string()
+
+
 def test_decode_null_pointers_rejected(L):
     d = _desc()
     st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 0,

@@ -346,3 +346,28 @@ def test_caller_workspace_reused_across_layouts():
     pd.workspace_init(ws)
     for wl in (a, b, a, b):
         _check(wl, "mma", workspace=ws)
+
+
+# ----------------------------------------------------------------------------- interleaved RoPE
+
+@pytest.mark.parametrize("kv", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("group", [2, 4, 8])
+def test_rope_interleaved_mma(kv, D, group):
+    # rotary_mode 2: the pair (2i, 2i + 1) shares frequency i (one A-fragment register)
+    wl = _wl("llama3_8b_bf16", 80 + group, q_dtype=kv, kv_dtype=kv, out_dtype=kv, D=D,
+             H_kv=2, H_qo=2 * group, B=3, len_dist=("uniform", 1, 300), pool=200, rotary_mode=2)
+    _check(wl, "mma")
+    _check(wl, "mma", num_splits=3, max_kv_len_hint=300)
+
+
+def test_rope_interleaved_fp8_and_window():
+    _check(_wl("fp8_kv_highconc", 90, rotary_mode=2, rope_theta=1e4), "mma")
+    _check(_wl("window_sink_f16", 91, rotary_mode=2), "mma")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_rope_interleaved_simt(D):
+    wl = W.make("tiny_fp32", seed=92 + D, D=D, rotary_mode=2, rope_theta=1e4).to(DEV)
+    _check(wl, "simt")
+    _check(_wl("llama3_8b_bf16", 93, page_size=8, pool=1200, rotary_mode=2), "simt")

@@ -158,3 +158,9 @@ def test_mq_after_append_with_early_inputs():
     assert pd.check_device_errors() == "PD_OK"
     ro, rl, _ = _oracle(wl, Q, q_len, pages=ref_pages)
     compare("bf16", out, lse, ro, rl)
+
+
+def test_mq_interleaved_rope():
+    wl, Q = _mq("llama3_8b_bf16", 66, 2, rotary_mode=2)
+    _check(wl, Q)
+    _check(wl, Q, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
