@@ -60,10 +60,10 @@ def lib():
             i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
             L.oracle_batch_decode_paged_kv.argtypes = [
                 P, i32, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i64, i32, i32,
-                f64, f64, f64, f64, f64, P]
+                f64, f64, f64, f64, f64, P, P]
             L.oracle_batch_decode_paged_kv_mq.argtypes = [
                 P, i32, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, i32,
-                f64, f64, f64, f64, f64, P]
+                f64, f64, f64, f64, f64, P, P]
             L.oracle_batch_decode_paged_kv.restype = i32
             L.oracle_merge_state.argtypes = [P, P, P, P, i32, i32, i32]
             L.oracle_merge_state.restype = None
@@ -147,11 +147,13 @@ def attended_offsets(indptr, length_info, b, page_size, window):
 def batch_decode_paged_kv(Q, pages, indptr, values, length_info, k_rope_pos_offset,
                           q_rope_position, *, q_dtype, kv_dtype, H_kv, page_size,
                           rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
-                          sliding_window=False, k_scale=1.0, v_scale=1.0, mask=None):
+                          sliding_window=False, k_scale=1.0, v_scale=1.0, mask=None, sink=None):
     """Returns (out [B,H_qo,D] f64, lse [B,H_qo] f64 log2 units, status).
 
     Q: [B,H_qo,D] typed bits; pages: [max_pages,2,H_kv,P,D] typed bits.
     ``mask`` (bool [B,H_qo]) restricts which rows are computed (others are NaN).
+    ``sink`` ([H_qo], natural units): a learned logit per query head, one more softmax
+    term with a zero value row.
     """
     Qb = _bits(Q, q_dtype)
     Pb = _bits(pages, kv_dtype)
@@ -172,16 +174,25 @@ def batch_decode_paged_kv(Q, pages, indptr, values, length_info, k_rope_pos_offs
         _ptr(Qb), DTYPES[q_dtype], _ptr(Pb), DTYPES[kv_dtype], _ptr(indptr), _ptr(values),
         _ptr(li), _ptr(kro), _ptr(qrp), _ptr(out), _ptr(lse), B, H_qo, H_kv, D, page_size,
         max_pages, int(bool(sliding_window)), int(rotary_mode), float(rope_scale),
-        float(rope_theta), float(sm_scale), float(k_scale), float(v_scale), _ptr(m))
+        float(rope_theta), float(sm_scale), float(k_scale), float(v_scale), _ptr(_sink(sink, H_qo)),
+        _ptr(m))
     if st == -2:
         raise ValueError("oracle: bad arguments")
     return out, lse, st
 
 
+def _sink(sink, H_qo):
+    if sink is None:
+        return None
+    a = _c(sink, np.float64)
+    assert a.shape == (H_qo,), a.shape
+    return a
+
+
 def batch_decode_paged_kv_mq(Q, pages, indptr, values, length_info, k_rope_pos_offset,
                              q_rope_position, *, q_len, q_dtype, kv_dtype, H_kv, page_size,
                              rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
-                             k_scale=1.0, v_scale=1.0, mask=None):
+                             k_scale=1.0, v_scale=1.0, mask=None, sink=None):
     """Multi-query decode: returns (out [B,q_len,H_qo,D] f64, lse [B,q_len,H_qo] f64 log2
     units, status).  Q: [B,q_len,H_qo,D] typed bits (or [B*q_len,H_qo,D]); length_info
     [B] (no sliding window).  Token t of sequence b sees the attended rows
@@ -211,7 +222,7 @@ def batch_decode_paged_kv_mq(Q, pages, indptr, values, length_info, k_rope_pos_o
         _ptr(Qb), DTYPES[q_dtype], _ptr(Pb), DTYPES[kv_dtype], _ptr(indptr), _ptr(values),
         _ptr(li), _ptr(kro), _ptr(qrp), _ptr(out), _ptr(lse), B, int(q_len), H_qo, H_kv, D,
         page_size, max_pages, int(rotary_mode), float(rope_scale), float(rope_theta),
-        float(sm_scale), float(k_scale), float(v_scale), _ptr(m))
+        float(sm_scale), float(k_scale), float(v_scale), _ptr(_sink(sink, H_qo)), _ptr(m))
     if st == -2:
         raise ValueError("oracle: bad arguments")
     return out.reshape(B, q_len, H_qo, D), lse.reshape(B, q_len, H_qo), st

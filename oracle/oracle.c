@@ -291,6 +291,8 @@ static void apply_rope(int rotary_mode, double* x, int D, double pos, double rop
 /* indptr [B+1]; values [nnz]; length_info [B] or [3,B]; out [B,H_qo,D] and   */
 /* lse [B,H_qo] as doubles.  KV head of Q head h is h / (H_qo/H_kv).           */
 /* `mask` (nullable, [B*H_qo]) selects which (b,h) to compute; others untouched.*/
+/* `sink` (nullable, [H_qo]): a learned logit per query head, one more softmax  */
+/* term exp(sink[h]) with a zero value row (so lse includes it).               */
 /* Returns 0, or -1 if a page id or offset is out of range (the row is then   */
 /* excluded), -2 on bad arguments.                                            */
 /* ------------------------------------------------------------------------- */
@@ -308,7 +310,7 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
                        double* out, double* lse, int B, int q_len, int H_qo, int H_kv, int D,
                        int P, int64_t max_pages, int window, int rotary_mode, double rope_scale,
                        double rope_theta, double sm_scale, double k_scale, double v_scale,
-                       const uint8_t* mask) {
+                       const double* sink, const uint8_t* mask) {
   if (B < 0 || H_kv <= 0 || H_qo % H_kv != 0 || D <= 0 || D % 2 || P <= 0) return -2;
   if (q_len < 1 || (q_len > 1 && window) || rotary_mode < 0 || rotary_mode > 2) return -2;
   int group = H_qo / H_kv;
@@ -365,13 +367,16 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
         if (score[r] > M) M = score[r];
         ++n_valid;
       }
-      if (n_valid == 0) { /* R4: empty sequence */
+      /* a learned sink (NKI TKG `sink`, one logit per query head) is one more score, */
+      /* sink[h] in natural units, whose value row is zero                             */
+      if (sink && sink[h] > M) M = sink[h];
+      if (n_valid == 0 && !sink) { /* R4: empty sequence */
         for (int d = 0; d < D; ++d) o[d] = 0.0;
         lse[row] = -5e4;
         continue;
       }
       /* pass 2: softmax weights, their sum, and the weighted sum of V rows */
-      double den = 0.0;
+      double den = sink ? exp(sink[h] - M) : 0.0;
       for (int d = 0; d < D; ++d) o[d] = 0.0;
       for (int64_t r = 0; r < Lt; ++r) {
         if (!valid[r]) continue;
@@ -404,10 +409,11 @@ int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, 
                                  int H_qo, int H_kv, int D, int P, int64_t max_pages, int window,
                                  int rotary_mode, double rope_scale, double rope_theta,
                                  double sm_scale, double k_scale, double v_scale,
-                                 const uint8_t* mask) {
+                                 const double* sink, const uint8_t* mask) {
   return decode_impl(Q, q_dtype, pages, kv_dtype, indptr, values, length_info, k_rope_pos_offset,
                      q_rope_position, out, lse, B, 1, H_qo, H_kv, D, P, max_pages, window,
-                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, mask);
+                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, sink,
+                     mask);
 }
 
 int oracle_batch_decode_paged_kv_mq(const void* Q, int q_dtype, const void* pages, int kv_dtype,
@@ -417,10 +423,10 @@ int oracle_batch_decode_paged_kv_mq(const void* Q, int q_dtype, const void* page
                                     int B, int q_len, int H_qo, int H_kv, int D, int P,
                                     int64_t max_pages, int rotary_mode, double rope_scale,
                                     double rope_theta, double sm_scale, double k_scale,
-                                    double v_scale, const uint8_t* mask) {
+                                    double v_scale, const double* sink, const uint8_t* mask) {
   return decode_impl(Q, q_dtype, pages, kv_dtype, indptr, values, length_info, k_rope_pos_offset,
                      q_rope_position, out, lse, B, q_len, H_qo, H_kv, D, P, max_pages, 0,
-                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, mask);
+                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, sink, mask);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -526,3 +526,53 @@ def test_mq_rejects_bad_q_len():
     with pytest.raises(ValueError):
         oracle.batch_decode_paged_kv_mq(Q, pages, indptr, values, last, None, None, q_len=0,
                                         q_dtype="f32", kv_dtype="f32", H_kv=1, page_size=4)
+
+
+# --------------------------------------------------------------------------- learned sinks
+
+def test_sink_bruteforce_and_virtual_row():
+    """A per-head sink logit joins the softmax with a zero value row: brute force with
+    scipy on the dense K/V plus one extra score, for decode and multi-query decode."""
+    rng = np.random.default_rng(31)
+    H_qo, H_kv, D, P, lens = 4, 2, 8, 4, [7, 0, 2]
+    B = len(lens)
+    Q, pages, indptr, values, last, dense = _paged_case(rng, B, H_qo, H_kv, D, P, lens)
+    sink = rng.standard_normal(H_qo) * 2
+    sm = 0.3
+    out, lse, st = _run(Q, pages, indptr, values, last, H_kv, P, sm_scale=sm, sink=sink)
+    assert st == 0
+    g = H_qo // H_kv
+    for b in range(B):
+        Kb, Vb = dense[b]
+        for h in range(H_qo):
+            s = np.concatenate([sm * (Kb[:, h // g, :] @ Q[b, h].astype(np.float64)), [sink[h]]])
+            Vx = np.concatenate([Vb[:, h // g, :], np.zeros((1, D))])
+            np.testing.assert_allclose(out[b, h], softmax(s) @ Vx, rtol=0, atol=1e-12)
+            assert abs(lse[b, h] - logsumexp(s) * LOG2E) < 1e-12
+    # an empty sequence keeps only the sink: out 0, lse = sink in log2 units
+    assert np.all(out[1] == 0) and np.allclose(lse[1], sink * LOG2E, rtol=0, atol=1e-12)
+    Qm = _f32(rng.standard_normal((B, 2, H_qo, D)))
+    o2, l2, _ = _run_mq(Qm, pages, indptr, values, last, H_kv, P, 2, sm_scale=sm, sink=sink)
+    for b in range(B):
+        Kb, Vb = dense[b]
+        for t in range(2):
+            n = max(lens[b] - 2 + 1 + t, 0)
+            for h in range(H_qo):
+                s = np.concatenate([sm * (Kb[:n, h // g, :] @ Qm[b, t, h].astype(np.float64)),
+                                    [sink[h]]])
+                Vx = np.concatenate([Vb[:n, h // g, :], np.zeros((1, D))])
+                np.testing.assert_allclose(o2[b, t, h], softmax(s) @ Vx, rtol=0, atol=1e-12)
+                assert abs(l2[b, t, h] - logsumexp(s) * LOG2E) < 1e-12
+
+
+def test_sink_is_one_merge_with_a_zero_state():
+    """Adding the sink equals merge_state of the sink-free result with the state
+    (V = 0, S = sink log2 e): the sink enters once, wherever the split falls."""
+    rng = np.random.default_rng(32)
+    Q, pages, indptr, values, last, _ = _paged_case(rng, 2, 4, 2, 8, 4, [9, 5])
+    sink = rng.standard_normal(4)
+    o0, l0, _ = _run(Q, pages, indptr, values, last, 2, 4)
+    o1, l1, _ = _run(Q, pages, indptr, values, last, 2, 4, sink=sink)
+    Vm, Sm = oracle.merge_state(o0, l0, np.zeros_like(o0), np.broadcast_to(sink * LOG2E, l0.shape))
+    np.testing.assert_allclose(o1, Vm, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, Sm, rtol=0, atol=1e-12)
