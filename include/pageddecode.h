@@ -85,6 +85,12 @@ typedef struct {
   void* workspace;           /* optional caller workspace (device, 256-byte aligned);
                                 NULL = library-managed */
   size_t workspace_bytes;    /* size of `workspace` */
+  const float* sink;         /* optional device array [H_qo] float32, or NULL: a learned
+                                logit per query head ([NKI] `sink`), in natural units,
+                                that joins the softmax as one more score with a zero value
+                                row -- out = sum_r e^(t_r) v_r / (e^sink + sum_r e^(t_r)),
+                                t_r = sm_scale q.k_r, and lse includes it (an empty
+                                sequence gives out = 0, lse = sink * log2(e)) */
 } pd_decode_desc;
 
 /*

@@ -84,6 +84,7 @@ class DecodeDesc(ctypes.Structure):
         ("flags", ctypes.c_int32),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("sink", ctypes.c_void_p),
     ]
 
 
@@ -152,7 +153,8 @@ DECODE_EARLY_INPUTS = 1
 
 
 def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_kv_len_hint=0,
-              k_scale=1.0, v_scale=1.0, workspace=None, early_inputs=False) -> DecodeDesc:
+              k_scale=1.0, v_scale=1.0, workspace=None, early_inputs=False,
+              sink=None) -> DecodeDesc:
     B, H_qo, D = Q.shape
     max_pages, two, H_kv, P, D2 = pages.shape
     if two != 2 or D2 != D:
@@ -165,14 +167,23 @@ def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_k
         max_kv_len_hint=int(max_kv_len_hint), k_scale=float(k_scale), v_scale=float(v_scale),
         flags=DECODE_EARLY_INPUTS if early_inputs else 0,
         workspace=None if workspace is None else workspace.data_ptr(),
-        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+        workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+        sink=_sink_ptr(sink, H_qo))
+
+
+def _sink_ptr(sink, H_qo):
+    if sink is None:
+        return None
+    if sink.dtype != torch.float32 or sink.numel() != H_qo or not sink.is_contiguous():
+        raise ValueError("sink must be a contiguous float32 tensor of H_qo values")
+    return sink.data_ptr()
 
 
 def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length_info,
                           k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                           rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                           v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                          early_inputs=False, stream=None):
+                          early_inputs=False, sink=None, stream=None):
     """pd_batch_decode_paged_kv on device tensors; writes `output` and `lse`.
     early_inputs=True sets PD_DECODE_EARLY_INPUTS: only right after append_paged_kv (or
     another kernel that writes none of Q, the page table, lengths and positions)."""
@@ -180,7 +191,8 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
         sm_scale = Q.shape[-1] ** -0.5
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
-                     v_scale=v_scale, workspace=workspace, early_inputs=early_inputs)
+                     v_scale=v_scale, workspace=workspace, early_inputs=early_inputs,
+                     sink=sink)
     _check(lib().pd_batch_decode_paged_kv(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -193,14 +205,14 @@ def batch_decode_paged_kv_noalloc(Q, pages, page_table_indptr, page_table_values
                                   length_info, k_rope_pos_offset, q_rope_position, output, lse,
                                   rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
                                   *, k_scale=1.0, v_scale=1.0, num_splits=0, max_kv_len_hint=0,
-                                  early_inputs=False, stream=None):
+                                  early_inputs=False, sink=None, stream=None):
     """pd_batch_decode_paged_kv_noalloc: same result, split scratch in the library's
     static device array (no device allocation)."""
     if sm_scale is None:
         sm_scale = Q.shape[-1] ** -0.5
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
-                     v_scale=v_scale, early_inputs=early_inputs)
+                     v_scale=v_scale, early_inputs=early_inputs, sink=sink)
     _check(lib().pd_batch_decode_paged_kv_noalloc(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -213,7 +225,7 @@ def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, len
                              k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                              rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                              v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                             early_inputs=False, stream=None):
+                             early_inputs=False, sink=None, stream=None):
     """pd_batch_decode_paged_kv_mq: Q [B, q_len, H_qo, D], output [B, q_len, H_qo, D],
     lse [B, q_len, H_qo]; token t of a sequence sees its rows up to itself."""
     if Q.dim() != 4:
@@ -224,7 +236,7 @@ def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, len
     desc = make_desc(Q[:, 0], pages, page_table_indptr,
                      page_table_values, length_info, output, num_splits=num_splits,
                      max_kv_len_hint=max_kv_len_hint, k_scale=k_scale, v_scale=v_scale,
-                     workspace=workspace, early_inputs=early_inputs)
+                     workspace=workspace, early_inputs=early_inputs, sink=sink)
     _check(lib().pd_batch_decode_paged_kv_mq(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),

@@ -415,6 +415,7 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   p.out_dtype = d.out_dtype;
   p.out_vec16 = (reinterpret_cast<uintptr_t>(output) % 16) == 0 ? 1 : 0;
   p.early_inputs = (d.flags & PD_DECODE_EARLY_INPUTS) ? 1 : 0;
+  p.sink = d.sink;
   const double log2e = 1.4426950408889634073599246810019;
   const double kdeq = d.kv_dtype == kE4M3 ? (double)d.k_scale : 1.0;
   p.score_scale = (float)((double)sm_scale * log2e * kdeq);

@@ -52,6 +52,7 @@ struct DecodeParams {
   int out_dtype;
   int out_vec16;      // out is 16-byte aligned (vector stores of whole runs)
   int early_inputs;   // Q, page table, lengths and positions may be read before pdl_wait()
+  const float* sink;  // [H_qo] learned logit per query head (natural units), or nullptr
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
   float q_prescale;   // split-operand MMA path: Q is pre-multiplied by this
   float out_scale;    // applied to the final output (v_scale for e4m3 KV)
@@ -71,6 +72,26 @@ struct SeqInfo {
 __device__ __forceinline__ size_t col_row(const DecodeParams& p, int b, int hk, int c) {
   const int t = c / p.group;
   return ((size_t)b * p.q_len + t) * p.H_qo + hk * p.group + (c - t * p.group);
+}
+
+// Query head of column c of KV head hk.
+__device__ __forceinline__ int col_head(const DecodeParams& p, int hk, int c) {
+  return hk * p.group + c % p.group;
+}
+
+// A learned sink logit of query head h joins the softmax as one more score with a zero
+// value row.  Given a final, sink-free output (o, lse = l; l = kEmptyM when no row was
+// attended), the result is o * scale with lse: the merge of (o, l) with (0, sink log2 e).
+struct SinkAdj {
+  float scale, lse;
+};
+__device__ __forceinline__ SinkAdj apply_sink(const DecodeParams& p, int h, float l) {
+  if (!p.sink) return {1.f, l};
+  const float ls = __ldg(p.sink + h) * 1.4426950408889634f;
+  const float m = fmaxf(l, ls);
+  const float a = l > kEmptyM ? exp2f(l - m) : 0.f;  // weight of the attended rows
+  const float den = a + exp2f(ls - m);
+  return {a / den, m + log2f(den)};
 }
 
 __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
@@ -613,13 +634,14 @@ __device__ void merge_segment(const DecodeParams& p, const BlockRange& br, const
       const int j = v / D4, d4 = v - j * D4;
       const int hq = hq0 + j;
       const bool empty = !(s_M[j] > kEmptyM);
-      const float sc = empty ? 0.f : p.out_scale / s_den[j];
+      const SinkAdj sa = apply_sink(p, hq, empty ? kEmptyM : s_M[j] + log2f(s_den[j]));
+      const float sc = empty ? 0.f : p.out_scale / s_den[j] * sa.scale;
       const size_t o = ((size_t)sg.b * p.H_qo + hq) * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
       store_out(p, o + 1, acc[e].y * sc);
       store_out(p, o + 2, acc[e].z * sc);
       store_out(p, o + 3, acc[e].w * sc);
-      if (d4 == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = empty ? kEmptyM : s_M[j] + log2f(s_den[j]);
+      if (d4 == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = sa.lse;
     }
   }
 }
@@ -659,8 +681,9 @@ __device__ void finish_share(const DecodeParams& p, const BlockRange& br, const 
     const float l = empty ? kEmptyM : M + log2f(den);
     const int hq = hq0 + j;
     if (whole) {
-      store_out(p, ((size_t)sg.b * p.H_qo + hq) * D + d, o * p.out_scale);
-      if (d == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = l;
+      const SinkAdj sa = apply_sink(p, hq, l);
+      store_out(p, ((size_t)sg.b * p.H_qo + hq) * D + d, o * p.out_scale * sa.scale);
+      if (d == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = sa.lse;
     } else {
       p.part_o[(slot + j) * D + d] = o;
       if (d == 0) p.part_lse[slot + j] = l;

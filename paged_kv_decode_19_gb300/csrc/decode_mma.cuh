@@ -302,14 +302,15 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
       const int j = vi / D4, d4 = vi % D4;
       const float Mj = s_M[j], dj = s_den[j];
       const bool empty = !(Mj > kEmptyM);
-      const float sc = empty ? 0.f : p.out_scale;
+      const SinkAdj sa = apply_sink(p, col_head(p, hk, c0 + j), empty ? kEmptyM : Mj + log2f(dj));
+      const float sc = empty ? 0.f : p.out_scale * sa.scale;
       const size_t row = col_row(p, seg_b, hk, c0 + j);
       const size_t o = row * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
       store_out(p, o + 1, acc[e].y * sc);
       store_out(p, o + 2, acc[e].z * sc);
       store_out(p, o + 3, acc[e].w * sc);
-      if (d4 == 0) p.lse[row] = empty ? kEmptyM : Mj + log2f(dj);
+      if (d4 == 0) p.lse[row] = sa.lse;
     }
   }
   __syncwarp();
@@ -901,9 +902,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
     const int j = 2 * q4 + hh;
     if (j < hcount) {
       const bool empty = !(st_d[hh] > 0.f);
-      const float inv = empty ? 0.f : 1.f / st_d[hh];
-      const float l = empty ? kEmptyM : st_m[hh] + log2f(st_d[hh]);
+      float inv = empty ? 0.f : 1.f / st_d[hh];
+      float l = empty ? kEmptyM : st_m[hh] + log2f(st_d[hh]);
       const size_t row = col_row(p, sg.b, hk, c0 + j);
+      if (whole) {  // a final output: the head's sink joins here (a partial leaves it to the merge)
+        const SinkAdj sa = apply_sink(p, col_head(p, hk, c0 + j), l);
+        inv *= sa.scale;
+        l = sa.lse;
+      }
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
         const int d0 = FP8 ? 16 * g_id : 8 * (g_id + 8 * r);

@@ -38,8 +38,9 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_desc_layout_matches_header():
-    # int32 x10, int64 x2, int32, float x2, int32, void*, size_t
-    assert ctypes.sizeof(_lib.DecodeDesc) == 88
+    # int32 x10, int64 x2, int32, float x2, int32, void*, size_t, const float*
+    assert ctypes.sizeof(_lib.DecodeDesc) == 96
+    assert _lib.DecodeDesc.sink.offset == 88
     assert _lib.DecodeDesc.max_pages.offset == 40
     assert _lib.DecodeDesc.flags.offset == 68
     assert _lib.DecodeDesc.workspace.offset == 72
@@ -50,7 +51,7 @@ def test_desc_layout_matches_header():
 def _desc(**kw):
     d = dict(B=4, H_qo=8, H_kv=2, D=128, page_size=16, q_dtype=2, kv_dtype=2, out_dtype=2,
              sliding_window=0, num_splits=0, max_pages=100, nnz_pages=40, max_kv_len_hint=0,
-             k_scale=1.0, v_scale=1.0, workspace=None, workspace_bytes=0)
+             k_scale=1.0, v_scale=1.0, workspace=None, workspace_bytes=0, sink=None)
     d.update(kw)
     return _lib.DecodeDesc(**d)
 

@@ -371,3 +371,47 @@ def test_rope_interleaved_simt(D):
     wl = W.make("tiny_fp32", seed=92 + D, D=D, rotary_mode=2, rope_theta=1e4).to(DEV)
     _check(wl, "simt")
     _check(_wl("llama3_8b_bf16", 93, page_size=8, pool=1200, rotary_mode=2), "simt")
+
+
+# ----------------------------------------------------------------------------- learned sinks
+
+def _sink(wl, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    return (torch.randn(wl.spec.H_qo, generator=g, device=DEV) * 3).float()
+
+
+@pytest.mark.parametrize("name,over", [("llama3_8b_bf16", {}), ("fp8_kv_highconc", {}),
+                                       ("window_sink_f16", {}), ("tiny_fp32", {})])
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_sink_logits(name, over, splits):
+    # a per-head logit joins the softmax with a zero value row, once per (sequence, head)
+    # whether the segment is split or not
+    wl = _wl(name, 94, **over)
+    sk = _sink(wl, 95)
+    kw = dict(num_splits=splits)
+    if splits == 3:
+        kw["max_kv_len_hint"] = int(wl.attended.max())
+    out, lse = gpu_decode(wl, sink=sk, **kw)
+    assert pd.check_device_errors() == "PD_OK"
+    ro, rl, st = oracle_decode(wl, sink=sk.cpu().numpy())
+    assert st == 0
+    compare(kind_of(wl), out, lse, ro, rl)
+
+
+def test_sink_empty_sequence_and_noalloc():
+    wl = _custom([0, 5, 40], seed=9)
+    sk = _sink(wl, 96)
+    out, lse = gpu_decode(wl, sink=sk)
+    ro, rl, _ = oracle_decode(wl, sink=sk.cpu().numpy())
+    compare("bf16", out, lse, ro, rl)
+    assert torch.all(out[0] == 0)
+    torch.testing.assert_close(lse[0], sk * 1.4426950408889634, rtol=0, atol=1e-5)
+    s = wl.spec
+    out2 = torch.empty_like(out)
+    lse2 = torch.empty_like(lse)
+    pd.batch_decode_paged_kv_noalloc(wl.Q, wl.pages, wl.indptr, wl.values, wl.length_info,
+                                     wl.k_rope_pos_offset, wl.q_rope_position, out2, lse2,
+                                     s.rotary_mode, s.rope_scale, s.rope_theta, wl.sm_scale,
+                                     sink=sk)
+    assert torch.equal(out2, out) and torch.equal(lse2, lse)

@@ -164,3 +164,22 @@ def test_mq_interleaved_rope():
     wl, Q = _mq("llama3_8b_bf16", 66, 2, rotary_mode=2)
     _check(wl, Q)
     _check(wl, Q, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_mq_sink_logits(splits):
+    q_len = 2
+    wl, Q = _mq("llama3_8b_bf16", 67, q_len)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(68)
+    sk = (torch.randn(wl.spec.H_qo, generator=g, device=DEV) * 3).float()
+    kw = dict(num_splits=splits, max_kv_len_hint=int(wl.attended.max())) if splits else {}
+    out, lse = _gpu(wl, Q, sink=sk, **kw)
+    s = wl.spec
+    ro, rl, _ = oracle.batch_decode_paged_kv_mq(
+        W.bits(Q), W.bits(wl.pages), wl.indptr.cpu().numpy(), wl.values.cpu().numpy(),
+        wl.length_info.cpu().numpy(), wl.k_rope_pos_offset.cpu().numpy(),
+        wl.q_rope_position.cpu().numpy(), q_len=q_len, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
+        H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode, rope_scale=s.rope_scale,
+        rope_theta=s.rope_theta, sm_scale=wl.sm_scale, sink=sk.cpu().numpy())
+    compare("bf16", out, lse, ro, rl)
