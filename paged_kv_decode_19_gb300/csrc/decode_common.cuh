@@ -69,14 +69,18 @@ struct SeqInfo {
 // Row of (sequence b, query column c of KV head hk) in Q, out and lse: column c is query
 // token c / group and head hk * group + c % group (with one token per sequence, c is
 // the head's index within the group).
+// MQ = false: one token per sequence (no division).
+template <bool MQ>
 __device__ __forceinline__ size_t col_row(const DecodeParams& p, int b, int hk, int c) {
+  if (!MQ) return (size_t)b * p.H_qo + hk * p.group + c;
   const int t = c / p.group;
   return ((size_t)b * p.q_len + t) * p.H_qo + hk * p.group + (c - t * p.group);
 }
 
 // Query head of column c of KV head hk.
+template <bool MQ>
 __device__ __forceinline__ int col_head(const DecodeParams& p, int hk, int c) {
-  return hk * p.group + c % p.group;
+  return hk * p.group + (MQ ? c % p.group : c);
 }
 
 // A learned sink logit of query head h joins the softmax as one more score with a zero
@@ -634,7 +638,8 @@ __device__ void merge_segment(const DecodeParams& p, const BlockRange& br, const
       const int j = v / D4, d4 = v - j * D4;
       const int hq = hq0 + j;
       const bool empty = !(s_M[j] > kEmptyM);
-      const SinkAdj sa = apply_sink(p, hq, empty ? kEmptyM : s_M[j] + log2f(s_den[j]));
+      const SinkAdj sa = p.sink ? apply_sink(p, hq, empty ? kEmptyM : s_M[j] + log2f(s_den[j]))
+                                : SinkAdj{1.f, empty ? kEmptyM : s_M[j] + log2f(s_den[j])};
       const float sc = empty ? 0.f : p.out_scale / s_den[j] * sa.scale;
       const size_t o = ((size_t)sg.b * p.H_qo + hq) * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
@@ -681,7 +686,7 @@ __device__ void finish_share(const DecodeParams& p, const BlockRange& br, const 
     const float l = empty ? kEmptyM : M + log2f(den);
     const int hq = hq0 + j;
     if (whole) {
-      const SinkAdj sa = apply_sink(p, hq, l);
+      const SinkAdj sa = p.sink ? apply_sink(p, hq, l) : SinkAdj{1.f, l};
       store_out(p, ((size_t)sg.b * p.H_qo + hq) * D + d, o * p.out_scale * sa.scale);
       if (d == 0) p.lse[(size_t)sg.b * p.H_qo + hq] = sa.lse;
     } else {

@@ -142,7 +142,7 @@ __device__ __forceinline__ void store_run(const DecodeParams& p, size_t idx, con
 // from warp reductions; the first batch of partial rows is requested before that, so
 // the merge costs about one L2 round trip per batch.  s_w: this warp's shared scratch
 // of 34 x 8 floats, s_sl: 32 ints.
-template <int D, int HMAX, int BATCH>
+template <int D, int HMAX, int BATCH, bool MQ>
 __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, int seg_c, int seg_n,
                            long long U, long long W, int hk, int c0, int hcount,
                            float (*s_w)[kMaxGroupPerCta], int* s_sl) {
@@ -295,22 +295,35 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
       }
     }
   }
+  // per column: output scale and final lse (with the head's sink, if any), by lane j
+  __syncwarp();
+  if (lane < hcount) {
+    const float Mj = s_M[lane], dj = s_den[lane];
+    const bool empty = !(Mj > kEmptyM);
+    float sc = empty ? 0.f : p.out_scale;
+    float l = empty ? kEmptyM : Mj + log2f(dj);
+    if (p.sink) {
+      const SinkAdj sa = apply_sink(p, col_head<MQ>(p, hk, c0 + lane), l);
+      sc *= sa.scale;
+      l = sa.lse;
+    }
+    s_w[0][lane] = sc;  // the weight rows are free again
+    s_w[1][lane] = l;
+  }
+  __syncwarp();
 #pragma unroll
   for (int e = 0; e < kV; ++e) {
     const int vi = lane + 32 * e;
     if (vi < hcount * D4) {
       const int j = vi / D4, d4 = vi % D4;
-      const float Mj = s_M[j], dj = s_den[j];
-      const bool empty = !(Mj > kEmptyM);
-      const SinkAdj sa = apply_sink(p, col_head(p, hk, c0 + j), empty ? kEmptyM : Mj + log2f(dj));
-      const float sc = empty ? 0.f : p.out_scale * sa.scale;
-      const size_t row = col_row(p, seg_b, hk, c0 + j);
+      const float sc = s_w[0][j];
+      const size_t row = col_row<MQ>(p, seg_b, hk, c0 + j);
       const size_t o = row * D + 4 * d4;
       store_out(p, o + 0, acc[e].x * sc);
       store_out(p, o + 1, acc[e].y * sc);
       store_out(p, o + 2, acc[e].z * sc);
       store_out(p, o + 3, acc[e].w * sc);
-      if (d4 == 0) p.lse[row] = sa.lse;
+      if (d4 == 0) p.lse[row] = s_w[1][j];
     }
   }
   __syncwarp();
@@ -416,7 +429,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
   constexpr int QCH = KT / 2;
   uint4 qchunk[QCH];
   {
-    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + col_row(p, sg.b, hk, c0 + (have_q ? qh : 0)) * D;
+    const QT* qrow = reinterpret_cast<const QT*>(p.Q) + col_row<MQ>(p, sg.b, hk, c0 + (have_q ? qh : 0)) * D;
 #pragma unroll
     for (int c = 0; c < QCH; ++c) {
       const int e0 = FP8 ? 16 * (4 * (c >> 1) + q4) + 8 * (c & 1) : 8 * (4 * c + q4);
@@ -904,9 +917,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
       const bool empty = !(st_d[hh] > 0.f);
       float inv = empty ? 0.f : 1.f / st_d[hh];
       float l = empty ? kEmptyM : st_m[hh] + log2f(st_d[hh]);
-      const size_t row = col_row(p, sg.b, hk, c0 + j);
-      if (whole) {  // a final output: the head's sink joins here (a partial leaves it to the merge)
-        const SinkAdj sa = apply_sink(p, col_head(p, hk, c0 + j), l);
+      const size_t row = col_row<MQ>(p, sg.b, hk, c0 + j);
+      if (whole && p.sink) {  // a final output: the head's sink joins here (a partial leaves it to the merge)
+        const SinkAdj sa = apply_sink(p, col_head<MQ>(p, hk, c0 + j), l);
         inv *= sa.scale;
         l = sa.lse;
       }
@@ -980,9 +993,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
     constexpr int kBudget = MinBlocks<ROPE, FP8>::v >= 3 ? 4 : 16;
     constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
     if (hcount <= 4)
-      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
+      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
     else
-      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1)>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
+      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
   }
 }
 
