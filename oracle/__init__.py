@@ -13,6 +13,8 @@ What each function restates (page title / section):
     causal among the new tokens (vllm-cpu ``nki_flash_attn.py``,
     ``flash_paged_attention``: context open, active tokens causal).
   * ``merge_state`` — same page, ``_merge_state_inplace_cpu``.
+  * ``append_paged_kv_rope`` / ``k_rotated`` — the NKI TKG order (RoPE, then the
+    cache update): K stored rotated, the decode rotating only Q.
   * ``append_paged_kv`` — vllm-cpu ``nki_flash_attn.py``, ``reshape_and_cache``,
     on the TVM page layout, with the FP8 encode of the NKI Attention Block TKG
     reference (``k_scale``/``v_scale``, OCP e4m3fn).
@@ -60,10 +62,10 @@ def lib():
             i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
             L.oracle_batch_decode_paged_kv.argtypes = [
                 P, i32, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i64, i32, i32,
-                f64, f64, f64, f64, f64, P, P]
+                f64, f64, f64, f64, f64, i32, P, P]
             L.oracle_batch_decode_paged_kv_mq.argtypes = [
                 P, i32, P, i32, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i64, i32,
-                f64, f64, f64, f64, f64, P, P]
+                f64, f64, f64, f64, f64, i32, P, P]
             L.oracle_batch_decode_paged_kv.restype = i32
             L.oracle_merge_state.argtypes = [P, P, P, P, i32, i32, i32]
             L.oracle_merge_state.restype = None
@@ -73,6 +75,9 @@ def lib():
             L.oracle_decode.argtypes = [P, i32, P, i64]
             L.oracle_encode.argtypes = [P, i32, P, i64]
             L.oracle_rope.argtypes = [P, i32, f64, f64, f64]
+            L.oracle_append_paged_kv_rope.argtypes = [P, i32, P, P, i32, P, i32, i32, i32, i32,
+                                                      i64, ctypes.c_float, ctypes.c_float, P,
+                                                      i32, f64, f64]
             L.oracle_rope_interleaved.argtypes = [P, i32, f64, f64, f64]
             L.oracle_attended_offsets.argtypes = [P, P, i32, i32, i32, i32, P, i64]
             L.oracle_attended_offsets.restype = i64
@@ -147,13 +152,15 @@ def attended_offsets(indptr, length_info, b, page_size, window):
 def batch_decode_paged_kv(Q, pages, indptr, values, length_info, k_rope_pos_offset,
                           q_rope_position, *, q_dtype, kv_dtype, H_kv, page_size,
                           rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
-                          sliding_window=False, k_scale=1.0, v_scale=1.0, mask=None, sink=None):
+                          sliding_window=False, k_scale=1.0, v_scale=1.0, mask=None, sink=None,
+                          k_rotated=False):
     """Returns (out [B,H_qo,D] f64, lse [B,H_qo] f64 log2 units, status).
 
     Q: [B,H_qo,D] typed bits; pages: [max_pages,2,H_kv,P,D] typed bits.
     ``mask`` (bool [B,H_qo]) restricts which rows are computed (others are NaN).
     ``sink`` ([H_qo], natural units): a learned logit per query head, one more softmax
-    term with a zero value row.
+    term with a zero value row.  ``k_rotated``: the cache holds K already rotated
+    (``append_paged_kv_rope``); only Q is rotated.
     """
     Qb = _bits(Q, q_dtype)
     Pb = _bits(pages, kv_dtype)
@@ -174,8 +181,8 @@ def batch_decode_paged_kv(Q, pages, indptr, values, length_info, k_rope_pos_offs
         _ptr(Qb), DTYPES[q_dtype], _ptr(Pb), DTYPES[kv_dtype], _ptr(indptr), _ptr(values),
         _ptr(li), _ptr(kro), _ptr(qrp), _ptr(out), _ptr(lse), B, H_qo, H_kv, D, page_size,
         max_pages, int(bool(sliding_window)), int(rotary_mode), float(rope_scale),
-        float(rope_theta), float(sm_scale), float(k_scale), float(v_scale), _ptr(_sink(sink, H_qo)),
-        _ptr(m))
+        float(rope_theta), float(sm_scale), float(k_scale), float(v_scale), int(bool(k_rotated)),
+        _ptr(_sink(sink, H_qo)), _ptr(m))
     if st == -2:
         raise ValueError("oracle: bad arguments")
     return out, lse, st
@@ -192,7 +199,7 @@ def _sink(sink, H_qo):
 def batch_decode_paged_kv_mq(Q, pages, indptr, values, length_info, k_rope_pos_offset,
                              q_rope_position, *, q_len, q_dtype, kv_dtype, H_kv, page_size,
                              rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
-                             k_scale=1.0, v_scale=1.0, mask=None, sink=None):
+                             k_scale=1.0, v_scale=1.0, mask=None, sink=None, k_rotated=False):
     """Multi-query decode: returns (out [B,q_len,H_qo,D] f64, lse [B,q_len,H_qo] f64 log2
     units, status).  Q: [B,q_len,H_qo,D] typed bits (or [B*q_len,H_qo,D]); length_info
     [B] (no sliding window).  Token t of sequence b sees the attended rows
@@ -222,7 +229,8 @@ def batch_decode_paged_kv_mq(Q, pages, indptr, values, length_info, k_rope_pos_o
         _ptr(Qb), DTYPES[q_dtype], _ptr(Pb), DTYPES[kv_dtype], _ptr(indptr), _ptr(values),
         _ptr(li), _ptr(kro), _ptr(qrp), _ptr(out), _ptr(lse), B, int(q_len), H_qo, H_kv, D,
         page_size, max_pages, int(rotary_mode), float(rope_scale), float(rope_theta),
-        float(sm_scale), float(k_scale), float(v_scale), _ptr(_sink(sink, H_qo)), _ptr(m))
+        float(sm_scale), float(k_scale), float(v_scale), int(bool(k_rotated)),
+        _ptr(_sink(sink, H_qo)), _ptr(m))
     if st == -2:
         raise ValueError("oracle: bad arguments")
     return out.reshape(B, q_len, H_qo, D), lse.reshape(B, q_len, H_qo), st
@@ -237,6 +245,26 @@ def merge_state(V, S, V_other, S_other):
     N, H, D = V.shape
     lib().oracle_merge_state(_ptr(V), _ptr(S), _ptr(Vo), _ptr(So), N, H, D)
     return V, S
+
+
+def append_paged_kv_rope(pages, k_new, v_new, slot_mapping, positions, *, in_dtype, kv_dtype,
+                         page_size, rotary_mode, rope_scale=1.0, rope_theta=1e4, k_scale=1.0,
+                         v_scale=1.0):
+    """append_paged_kv with each new K row rotated (fp64) at positions[t] first; returns
+    (new pages bits, number of out-of-range slots skipped)."""
+    Pb = _bits(pages, kv_dtype).copy()
+    kb = _bits(k_new, in_dtype)
+    vb = _bits(v_new, in_dtype)
+    T, H_kv, D = kb.shape
+    sm = _c(slot_mapping, np.int64)
+    pos = _c(positions, np.int32)
+    bad = lib().oracle_append_paged_kv_rope(
+        _ptr(Pb), DTYPES[kv_dtype], _ptr(kb), _ptr(vb), DTYPES[in_dtype], _ptr(sm), T, H_kv, D,
+        page_size, Pb.shape[0], np.float32(k_scale), np.float32(v_scale), _ptr(pos),
+        int(rotary_mode), float(rope_scale), float(rope_theta))
+    if bad == -2:
+        raise ValueError("oracle: bad arguments")
+    return Pb, bad
 
 
 def append_paged_kv(pages, k_new, v_new, slot_mapping, *, in_dtype, kv_dtype, page_size,

@@ -291,6 +291,8 @@ static void apply_rope(int rotary_mode, double* x, int D, double pos, double rop
 /* indptr [B+1]; values [nnz]; length_info [B] or [3,B]; out [B,H_qo,D] and   */
 /* lse [B,H_qo] as doubles.  KV head of Q head h is h / (H_qo/H_kv).           */
 /* `mask` (nullable, [B*H_qo]) selects which (b,h) to compute; others untouched.*/
+/* `k_rotated`: the cache holds K already rotated (append with RoPE); only Q is */
+/* rotated here.                                                                */
 /* `sink` (nullable, [H_qo]): a learned logit per query head, one more softmax  */
 /* term exp(sink[h]) with a zero value row (so lse includes it).               */
 /* Returns 0, or -1 if a page id or offset is out of range (the row is then   */
@@ -310,7 +312,7 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
                        double* out, double* lse, int B, int q_len, int H_qo, int H_kv, int D,
                        int P, int64_t max_pages, int window, int rotary_mode, double rope_scale,
                        double rope_theta, double sm_scale, double k_scale, double v_scale,
-                       const double* sink, const uint8_t* mask) {
+                       int k_rotated, const double* sink, const uint8_t* mask) {
   if (B < 0 || H_kv <= 0 || H_qo % H_kv != 0 || D <= 0 || D % 2 || P <= 0) return -2;
   if (q_len < 1 || (q_len > 1 && window) || rotary_mode < 0 || rotary_mode > 2) return -2;
   int group = H_qo / H_kv;
@@ -359,8 +361,9 @@ static int decode_impl(const void* Q, int q_dtype, const void* pages, int kv_dty
           k[d] = load_elem(pages, kv_dtype, kbase + d);
           if (kv_dtype == OR_E4M3) k[d] *= k_scale;
         }
-        apply_rope(rotary_mode, k, D, (double)k_rope_pos_offset[b] + (double)r, rope_scale,
-                   rope_theta);
+        if (!k_rotated) /* else the cache holds K rotated at append time */
+          apply_rope(rotary_mode, k, D, (double)k_rope_pos_offset[b] + (double)r, rope_scale,
+                     rope_theta);
         double dot = 0.0;
         for (int d = 0; d < D; ++d) dot += q[d] * k[d];
         score[r] = sm_scale * dot;
@@ -409,11 +412,11 @@ int oracle_batch_decode_paged_kv(const void* Q, int q_dtype, const void* pages, 
                                  int H_qo, int H_kv, int D, int P, int64_t max_pages, int window,
                                  int rotary_mode, double rope_scale, double rope_theta,
                                  double sm_scale, double k_scale, double v_scale,
-                                 const double* sink, const uint8_t* mask) {
+                                 int k_rotated, const double* sink, const uint8_t* mask) {
   return decode_impl(Q, q_dtype, pages, kv_dtype, indptr, values, length_info, k_rope_pos_offset,
                      q_rope_position, out, lse, B, 1, H_qo, H_kv, D, P, max_pages, window,
-                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, sink,
-                     mask);
+                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, k_rotated,
+                     sink, mask);
 }
 
 int oracle_batch_decode_paged_kv_mq(const void* Q, int q_dtype, const void* pages, int kv_dtype,
@@ -423,10 +426,12 @@ int oracle_batch_decode_paged_kv_mq(const void* Q, int q_dtype, const void* page
                                     int B, int q_len, int H_qo, int H_kv, int D, int P,
                                     int64_t max_pages, int rotary_mode, double rope_scale,
                                     double rope_theta, double sm_scale, double k_scale,
-                                    double v_scale, const double* sink, const uint8_t* mask) {
+                                    double v_scale, int k_rotated, const double* sink,
+                                    const uint8_t* mask) {
   return decode_impl(Q, q_dtype, pages, kv_dtype, indptr, values, length_info, k_rope_pos_offset,
                      q_rope_position, out, lse, B, q_len, H_qo, H_kv, D, P, max_pages, 0,
-                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, sink, mask);
+                     rotary_mode, rope_scale, rope_theta, sm_scale, k_scale, v_scale, k_rotated,
+                     sink, mask);
 }
 
 /* ------------------------------------------------------------------------- */
@@ -460,10 +465,16 @@ void oracle_merge_state(double* V, double* S, const double* V_other, const doubl
 /* Returns the number of slots that were out of range (skipped), or -2.        */
 /* ------------------------------------------------------------------------- */
 
-int oracle_append_paged_kv(void* pages, int kv_dtype, const void* k_new, const void* v_new,
-                           int in_dtype, const int64_t* slot_mapping, int T, int H_kv, int D,
-                           int P, int64_t max_pages, float k_scale, float v_scale) {
-  if (T < 0 || H_kv <= 0 || D <= 0 || P <= 0) return -2;
+/* With RoPE (rotary_mode 1 or 2, positions[t]): the K row is first rotated in fp64   */
+/* at its token's position ([NKI] TKG: RoPE, then the KV cache update), then stored    */
+/* by the same conversion; V is stored as is.                                           */
+static int append_impl(void* pages, int kv_dtype, const void* k_new, const void* v_new,
+                       int in_dtype, const int64_t* slot_mapping, int T, int H_kv, int D, int P,
+                       int64_t max_pages, float k_scale, float v_scale, const int32_t* positions,
+                       int rotary_mode, double rope_scale, double rope_theta) {
+  if (T < 0 || H_kv <= 0 || D <= 0 || P <= 0 || rotary_mode < 0 || rotary_mode > 2) return -2;
+  if (rotary_mode && (!positions || D % 2)) return -2;
+  double* row = (double*)malloc(sizeof(double) * (size_t)D);
   int es_in = elem_size(in_dtype), es_kv = elem_size(kv_dtype);
   int bad = 0;
   for (int t = 0; t < T; ++t) {
@@ -477,12 +488,15 @@ int oracle_append_paged_kv(void* pages, int kv_dtype, const void* k_new, const v
       for (int h = 0; h < H_kv; ++h) {
         size_t si = ((size_t)t * H_kv + h) * D;
         size_t di = ((((size_t)page * 2 + kv) * H_kv + h) * P + off) * D;
-        if (in_dtype == kv_dtype) {
+        const int rot = kv == 0 && rotary_mode;
+        if (in_dtype == kv_dtype && !rot) {
           memcpy((char*)pages + di * es_kv, (const char*)src + si * es_in, (size_t)D * es_kv);
           continue;
         }
+        for (int d = 0; d < D; ++d) row[d] = load_elem(src, in_dtype, si + d);
+        if (rot) apply_rope(rotary_mode, row, D, (double)positions[t], rope_scale, rope_theta);
         for (int d = 0; d < D; ++d) {
-          double x = load_elem(src, in_dtype, si + d);
+          double x = row[d];
           if (kv_dtype == OR_E4M3) {
             float q = (float)x / scale;  /* binary32 division, round-to-nearest */
             ((uint8_t*)pages)[di + d] = oracle_e4m3_encode((double)q);
@@ -493,5 +507,22 @@ int oracle_append_paged_kv(void* pages, int kv_dtype, const void* k_new, const v
       }
     }
   }
+  free(row);
   return bad;
+}
+
+int oracle_append_paged_kv(void* pages, int kv_dtype, const void* k_new, const void* v_new,
+                           int in_dtype, const int64_t* slot_mapping, int T, int H_kv, int D,
+                           int P, int64_t max_pages, float k_scale, float v_scale) {
+  return append_impl(pages, kv_dtype, k_new, v_new, in_dtype, slot_mapping, T, H_kv, D, P,
+                     max_pages, k_scale, v_scale, NULL, 0, 1.0, 1e4);
+}
+
+int oracle_append_paged_kv_rope(void* pages, int kv_dtype, const void* k_new, const void* v_new,
+                                int in_dtype, const int64_t* slot_mapping, int T, int H_kv,
+                                int D, int P, int64_t max_pages, float k_scale, float v_scale,
+                                const int32_t* positions, int rotary_mode, double rope_scale,
+                                double rope_theta) {
+  return append_impl(pages, kv_dtype, k_new, v_new, in_dtype, slot_mapping, T, H_kv, D, P,
+                     max_pages, k_scale, v_scale, positions, rotary_mode, rope_scale, rope_theta);
 }

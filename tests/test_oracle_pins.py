@@ -576,3 +576,56 @@ def test_sink_is_one_merge_with_a_zero_state():
     Vm, Sm = oracle.merge_state(o0, l0, np.zeros_like(o0), np.broadcast_to(sink * LOG2E, l0.shape))
     np.testing.assert_allclose(o1, Vm, rtol=0, atol=1e-12)
     np.testing.assert_allclose(l1, Sm, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------- K rotated at append time
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_append_rope_rows_equal_rotated_then_encoded(mode):
+    """Each appended K row is the pinned RoPE of the input row at its position, then the
+    pinned encoder; V rows are the plain append's."""
+    rng = np.random.default_rng(40 + mode)
+    T, H, D, P, pool = 5, 2, 8, 4, 6
+    pages = oracle.encode(rng.standard_normal((pool, 2, H, P, D)), "bf16")
+    k = oracle.encode(rng.standard_normal((T, H, D)), "bf16")
+    v = oracle.encode(rng.standard_normal((T, H, D)), "bf16")
+    slots = np.array([3, 9, -1, 17, 22], np.int64)
+    pos = np.array([5, 100, 7, 4096, 0], np.int32)
+    got, bad = oracle.append_paged_kv_rope(pages, k, v, slots, pos, in_dtype="bf16",
+                                           kv_dtype="bf16", page_size=P, rotary_mode=mode,
+                                           rope_theta=1e3)
+    plain, _ = oracle.append_paged_kv(pages, k, v, slots, in_dtype="bf16", kv_dtype="bf16",
+                                      page_size=P)
+    assert bad == 0
+    np.testing.assert_array_equal(got[:, 1], plain[:, 1])  # V untouched by RoPE
+    kd = oracle.decode(k, "bf16")
+    for t in range(T):
+        if slots[t] < 0:
+            continue
+        page, off = divmod(int(slots[t]), P)
+        for h in range(H):
+            want = oracle.encode(oracle.rope(kd[t, h], pos[t], 1.0, 1e3, interleaved=mode == 2), "bf16")
+            np.testing.assert_array_equal(got[page, 0, h, off], want)
+
+
+def test_k_rotated_decode_equals_rope_decode_on_exact_values():
+    """A cache whose K rows were rotated beforehand (fp64, stored as f32), decoded with
+    k_rotated, equals the rotating decode of the original cache up to that f32 storage."""
+    rng = np.random.default_rng(44)
+    Q, pages, indptr, values, last, dense = _paged_case(rng, 2, 4, 2, 8, 4, [9, 6])
+    kro = np.array([3, 0], np.int32)
+    qrp = np.array([12, 6], np.int32)
+    kw = dict(q_dtype="f32", kv_dtype="f32", H_kv=2, page_size=4, rotary_mode=1, rope_theta=1e3)
+    o_ref, l_ref, _ = oracle.batch_decode_paged_kv(Q, pages, indptr, values, last, kro, qrp, **kw)
+    rot = pages.copy()
+    for b in range(2):
+        for r in range(int(indptr[b + 1] - indptr[b]) * 4):
+            if r >= [9, 6][b]:
+                break
+            page = values[indptr[b] + r // 4]
+            for h in range(2):
+                rot[page, 0, h, r % 4] = oracle.rope(pages[page, 0, h, r % 4], kro[b] + r, 1.0, 1e3)
+    o_kr, l_kr, _ = oracle.batch_decode_paged_kv(Q, _f32(rot), indptr, values, last, kro, qrp,
+                                                 k_rotated=True, **kw)
+    np.testing.assert_allclose(o_kr, o_ref, rtol=0, atol=1e-5)
+    np.testing.assert_allclose(l_kr, l_ref, rtol=0, atol=1e-5)
