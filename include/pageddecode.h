@@ -81,7 +81,7 @@ typedef struct {
   int32_t max_kv_len_hint;   /* reserved (ignored); set to 0 */
   float k_scale;             /* E4M3 KV only: K = code * k_scale (else ignored) */
   float v_scale;             /* E4M3 KV only: V = code * v_scale (else ignored) */
-  int32_t flags;             /* 0 or PD_DECODE_EARLY_INPUTS (see below) */
+  int32_t flags;             /* 0, or PD_DECODE_EARLY_INPUTS | PD_DECODE_K_ROTATED (below) */
   void* workspace;           /* optional caller workspace (device, 256-byte aligned);
                                 NULL = library-managed */
   size_t workspace_bytes;    /* size of `workspace` */
@@ -109,6 +109,16 @@ typedef struct {
  * runs its start-up (work split scan, page-table and Q loads) under the append.
  */
 #define PD_DECODE_EARLY_INPUTS 1
+
+/*
+ * PD_DECODE_K_ROTATED in desc->flags (with rotary_mode 1 or 2): the cache holds every
+ * K row already rotated at its position, as pd_append_paged_kv_rope writes it ([NKI]
+ * TKG: RoPE, then the KV cache update).  The decode then rotates only Q (at
+ * q_rope_position, per rotary_mode) and uses K as stored: each row is read once
+ * without the per-row rotation, so the RoPE path costs what the plain one does.
+ * k_rope_pos_offset is not read.  Ignored when rotary_mode is 0.
+ */
+#define PD_DECODE_K_ROTATED 2
 
 /*
  * batch_decode_paged_kv — [TVM] `batch_decode_paged_kv`.
@@ -258,6 +268,22 @@ pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
                              const int64_t* slot_mapping, int32_t T, int32_t H_kv, int32_t D,
                              int32_t page_size, int64_t max_pages, int32_t in_dtype,
                              int32_t kv_dtype, float k_scale, float v_scale, pd_stream_t stream);
+
+/*
+ * append_paged_kv_rope — pd_append_paged_kv with each new K row rotated first, at
+ * positions[t] (int32 [T], device), by rotary_mode 1 (rotate-half) or 2 (interleaved)
+ * with the angles of pd_batch_decode_paged_kv's RoPE: the order of [NKI] TKG (RoPE,
+ * then the KV cache update).  The rotation runs in fp32 with angles to fp32 accuracy;
+ * the rotated values are then converted as in pd_append_paged_kv (E4M3: divided by
+ * k_scale, RNE, saturating).  V rows are stored unrotated.  Decode such a cache with
+ * PD_DECODE_K_ROTATED: only Q is rotated then.
+ */
+pd_status pd_append_paged_kv_rope(void* pages, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, const int32_t* positions,
+                                  int32_t T, int32_t H_kv, int32_t D, int32_t page_size,
+                                  int64_t max_pages, int32_t in_dtype, int32_t kv_dtype,
+                                  float k_scale, float v_scale, int32_t rotary_mode,
+                                  float rope_scale, float rope_theta, pd_stream_t stream);
 
 /* Bytes of workspace pd_batch_decode_paged_kv needs for `desc` on the current device
  * (0 on invalid desc).  Host-only apart from reading the device's SM count. */

@@ -7,6 +7,7 @@ PyTorch supplies device memory and streams only.
 from ._lib import (  # noqa: F401
     PDError,
     append_paged_kv,
+    append_paged_kv_rope,
     batch_decode_paged_kv,
     batch_decode_paged_kv_noalloc,
     batch_decode_paged_kv_mq,

@@ -45,6 +45,7 @@ EXPORTS = (
     "pd_batch_decode_paged_kv_noalloc",
     "pd_batch_decode_paged_kv_mq",
     "pd_workspace_size_mq",
+    "pd_append_paged_kv_rope",
     "pd_merge_state_inplace",
     "pd_append_paged_kv",
     "pd_workspace_size",
@@ -114,6 +115,9 @@ def lib():
             L.pd_append_paged_kv.argtypes = [P, P, P, P, i32, i32, i32, i32, i64, i32, i32, f32,
                                              f32, P]
             L.pd_append_paged_kv.restype = i32
+            L.pd_append_paged_kv_rope.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, i32,
+                                                  i32, f32, f32, i32, f32, f32, P]
+            L.pd_append_paged_kv_rope.restype = i32
             L.pd_workspace_size.argtypes = [ctypes.POINTER(DecodeDesc)]
             L.pd_workspace_size.restype = ctypes.c_size_t
             L.pd_workspace_init.argtypes = [P, ctypes.c_size_t, P]
@@ -150,11 +154,12 @@ def _stream(stream) -> ctypes.c_void_p:
 
 
 DECODE_EARLY_INPUTS = 1
+DECODE_K_ROTATED = 2
 
 
 def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_kv_len_hint=0,
               k_scale=1.0, v_scale=1.0, workspace=None, early_inputs=False,
-              sink=None) -> DecodeDesc:
+              sink=None, k_rotated=False) -> DecodeDesc:
     B, H_qo, D = Q.shape
     max_pages, two, H_kv, P, D2 = pages.shape
     if two != 2 or D2 != D:
@@ -165,7 +170,7 @@ def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_k
         sliding_window=int(length_info.dim() == 2), num_splits=int(num_splits),
         max_pages=max_pages, nnz_pages=int(values.numel()) if values is not None else 0,
         max_kv_len_hint=int(max_kv_len_hint), k_scale=float(k_scale), v_scale=float(v_scale),
-        flags=DECODE_EARLY_INPUTS if early_inputs else 0,
+        flags=(DECODE_EARLY_INPUTS if early_inputs else 0) | (DECODE_K_ROTATED if k_rotated else 0),
         workspace=None if workspace is None else workspace.data_ptr(),
         workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
         sink=_sink_ptr(sink, H_qo))
@@ -183,7 +188,7 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
                           k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                           rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                           v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                          early_inputs=False, sink=None, stream=None):
+                          early_inputs=False, sink=None, k_rotated=False, stream=None):
     """pd_batch_decode_paged_kv on device tensors; writes `output` and `lse`.
     early_inputs=True sets PD_DECODE_EARLY_INPUTS: only right after append_paged_kv (or
     another kernel that writes none of Q, the page table, lengths and positions)."""
@@ -192,7 +197,7 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
                      v_scale=v_scale, workspace=workspace, early_inputs=early_inputs,
-                     sink=sink)
+                     sink=sink, k_rotated=k_rotated)
     _check(lib().pd_batch_decode_paged_kv(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -205,14 +210,14 @@ def batch_decode_paged_kv_noalloc(Q, pages, page_table_indptr, page_table_values
                                   length_info, k_rope_pos_offset, q_rope_position, output, lse,
                                   rotary_mode=0, rope_scale=1.0, rope_theta=1e4, sm_scale=None,
                                   *, k_scale=1.0, v_scale=1.0, num_splits=0, max_kv_len_hint=0,
-                                  early_inputs=False, sink=None, stream=None):
+                                  early_inputs=False, sink=None, k_rotated=False, stream=None):
     """pd_batch_decode_paged_kv_noalloc: same result, split scratch in the library's
     static device array (no device allocation)."""
     if sm_scale is None:
         sm_scale = Q.shape[-1] ** -0.5
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
-                     v_scale=v_scale, early_inputs=early_inputs, sink=sink)
+                     v_scale=v_scale, early_inputs=early_inputs, sink=sink, k_rotated=k_rotated)
     _check(lib().pd_batch_decode_paged_kv_noalloc(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -225,7 +230,7 @@ def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, len
                              k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                              rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                              v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                             early_inputs=False, sink=None, stream=None):
+                             early_inputs=False, sink=None, k_rotated=False, stream=None):
     """pd_batch_decode_paged_kv_mq: Q [B, q_len, H_qo, D], output [B, q_len, H_qo, D],
     lse [B, q_len, H_qo]; token t of a sequence sees its rows up to itself."""
     if Q.dim() != 4:
@@ -236,7 +241,8 @@ def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, len
     desc = make_desc(Q[:, 0], pages, page_table_indptr,
                      page_table_values, length_info, output, num_splits=num_splits,
                      max_kv_len_hint=max_kv_len_hint, k_scale=k_scale, v_scale=v_scale,
-                     workspace=workspace, early_inputs=early_inputs, sink=sink)
+                     workspace=workspace, early_inputs=early_inputs, sink=sink,
+                     k_rotated=k_rotated)
     _check(lib().pd_batch_decode_paged_kv_mq(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -276,6 +282,22 @@ def check_device_errors(stream=None) -> str:
 
 def workspace_size(desc: DecodeDesc) -> int:
     return int(lib().pd_workspace_size(ctypes.byref(desc)))
+
+
+def append_paged_kv_rope(pages, k_new, v_new, slot_mapping, positions, rotary_mode=1,
+                         rope_scale=1.0, rope_theta=1e4, k_scale=1.0, v_scale=1.0, stream=None):
+    """pd_append_paged_kv_rope: appends with each K row rotated at positions[t] (int32)."""
+    T, H_kv, D = k_new.shape
+    max_pages, _, H2, P, D2 = pages.shape
+    if v_new.shape != k_new.shape or H2 != H_kv or D2 != D or slot_mapping.dtype != torch.int64:
+        raise ValueError("k_new/v_new [T,H_kv,D] must match pages; slot_mapping int64")
+    if positions.dtype != torch.int32 or positions.numel() != T:
+        raise ValueError("positions must be int32 [T]")
+    _check(lib().pd_append_paged_kv_rope(
+        _ptr(pages), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(positions), T, H_kv, D, P,
+        max_pages, DTYPE_CODES[k_new.dtype], DTYPE_CODES[pages.dtype], float(k_scale),
+        float(v_scale), int(rotary_mode), float(rope_scale), float(rope_theta), _stream(stream)))
+    return pages
 
 
 def workspace_init(ws: torch.Tensor, stream=None):

@@ -52,8 +52,8 @@ struct DeviceState {
   void* ws = nullptr;   // partial (out, lse) of split sequences
   size_t ws_bytes = 0;
   // resident blocks per SM of each kernel variant, queried once:
-  // [mma][q_dtype][kv_dtype][D 64/128/256][rotary 0/1/2][multi-query]; 0 = not yet known
-  int occupancy[2][4][4][3][3][2] = {};
+  // [mma][q_dtype][kv_dtype][D 64/128/256][kernel RoPE mode 0..4][multi-query]; 0 = not yet known
+  int occupancy[2][4][4][3][5][2] = {};
 };
 constexpr int kMaxDevices = 64;
 static DeviceState g_dev[kMaxDevices];
@@ -108,7 +108,8 @@ static pd_status validate_desc(const pd_decode_desc* d) {
   if ((long long)d->max_pages * 2 * d->H_kv > INT_MAX)
     return fail(PD_ERR_UNSUPPORTED, "max_pages * 2 * H_kv exceeds 2^31");
   if (d->num_splits < 0) return fail(PD_ERR_INVALID_ARG, "num_splits < 0");
-  if (d->flags & ~PD_DECODE_EARLY_INPUTS) return fail(PD_ERR_INVALID_ARG, "unknown bits in flags");
+  if (d->flags & ~(PD_DECODE_EARLY_INPUTS | PD_DECODE_K_ROTATED))
+    return fail(PD_ERR_INVALID_ARG, "unknown bits in flags");
   if (d->kv_dtype == kE4M3 && !(d->k_scale > 0.f && d->v_scale > 0.f && std::isfinite(d->k_scale) &&
                                 std::isfinite(d->v_scale)))
     return fail(PD_ERR_INVALID_ARG, "E4M3 KV needs finite positive k_scale and v_scale");
@@ -215,11 +216,13 @@ pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_
   return PD_OK;
 }
 
-static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary, int* ctas,
+// rm: the kernel's RoPE mode: 0 none, 1 / 2 rotate-half / interleaved on Q and K, 3 / 4
+// the same on Q only (the cache holds K rotated).
+static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rm, int* ctas,
                                DeviceState* ds = nullptr, int q_len = 1) {
   const int di = d->D == 64 ? 0 : d->D == 128 ? 1 : 2;
   const int mq = q_len > 1 ? 1 : 0;
-  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rotary == 2 ? 2 : rotary ? 1 : 0][mq]
+  int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rm][mq]
                    : nullptr;
   if (cached && *cached > 0) {
     *ctas = *cached;
@@ -228,7 +231,8 @@ static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rotary
   DecodeParams p{};
   p.D = d->D;
   p.P = d->page_size;
-  p.rotary = rotary;
+  p.rotary = rm > 2 ? rm - 2 : rm;
+  p.k_rotated = rm > 2 ? 1 : 0;
   p.q_len = q_len;
   cudaError_t e;
   int n = 0;
@@ -255,9 +259,9 @@ static size_t workspace_size_q(const pd_decode_desc* desc, int q_len) {
   for (int mma = 0; mma < 2; ++mma) {
     if (mma && !mma_path(desc, nullptr)) continue;
     if (!mma && q_len > 1) continue;  // the multi-query form runs on the tensor-core kernel only
-    for (int rot = 0; rot < 3; ++rot) {
+    for (int rm = 0; rm < 5; ++rm) {
       int ctas = 1;
-      if (occupancy_for(desc, mma != 0, rot, &ctas, ds, q_len) != PD_OK) continue;
+      if (occupancy_for(desc, mma != 0, rm, &ctas, ds, q_len) != PD_OK) continue;
       int mode, grid;
       size_t ws;
       plan_impl(desc, ds->num_sms, ctas, mma ? kMmaWarps : 1, &mode, &grid, &ws, q_len);
@@ -293,8 +297,9 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   if (st != PD_OK) return st;
   const pd_decode_desc& d = *desc;
   if (rotary_mode < 0 || rotary_mode > 2) return fail(PD_ERR_INVALID_ARG, "rotary_mode must be 0, 1 or 2");
-  if (rotary_mode != 0 && (!k_rope_pos_offset || !q_rope_position))
-    return fail(PD_ERR_INVALID_ARG, "RoPE needs k_rope_pos_offset and q_rope_position");
+  if (rotary_mode != 0 && (!q_rope_position ||
+                           (!k_rope_pos_offset && !(desc->flags & PD_DECODE_K_ROTATED))))
+    return fail(PD_ERR_INVALID_ARG, "RoPE needs q_rope_position (and k_rope_pos_offset unless K is rotated)");
   if (rotary_mode != 0 && !(rope_theta > 0.f && std::isfinite(rope_theta) && std::isfinite(rope_scale)))
     return fail(PD_ERR_INVALID_ARG, "rope_theta must be finite and positive");
   if (!std::isfinite(sm_scale)) return fail(PD_ERR_INVALID_ARG, "sm_scale must be finite");
@@ -314,7 +319,8 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
     return fail(PD_ERR_UNSUPPORTED, "multi-query decode runs on the tensor-core kernel only: "
                                     "f16/bf16 (D 64 or 128) or E4M3 (D 128) KV, page size a multiple of 16");
   int ctas = 1;
-  st = occupancy_for(desc, use_mma, rotary_mode, &ctas, ds, q_len);
+  const bool k_rotated = rotary_mode != 0 && (d.flags & PD_DECODE_K_ROTATED);
+  st = occupancy_for(desc, use_mma, rotary_mode + (k_rotated ? 2 : 0), &ctas, ds, q_len);
   if (st != PD_OK) return st;
   int mode = 0, grid_blocks = 0;
   size_t ws_need = 0;
@@ -415,6 +421,7 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   p.out_dtype = d.out_dtype;
   p.out_vec16 = (reinterpret_cast<uintptr_t>(output) % 16) == 0 ? 1 : 0;
   p.early_inputs = (d.flags & PD_DECODE_EARLY_INPUTS) ? 1 : 0;
+  p.k_rotated = k_rotated ? 1 : 0;
   p.sink = d.sink;
   const double log2e = 1.4426950408889634073599246810019;
   const double kdeq = d.kv_dtype == kE4M3 ? (double)d.k_scale : 1.0;
@@ -483,10 +490,20 @@ pd_status pd_merge_state_inplace(void* V, float* S, const void* V_other, const f
   return PD_OK;
 }
 
-pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
+}  // extern "C"
+
+static pd_status append_call(void* pages, const void* k_new, const void* v_new,
                              const int64_t* slot_mapping, int32_t T, int32_t H_kv, int32_t D,
                              int32_t page_size, int64_t max_pages, int32_t in_dtype,
-                             int32_t kv_dtype, float k_scale, float v_scale, pd_stream_t stream) {
+                             int32_t kv_dtype, float k_scale, float v_scale,
+                             const int32_t* positions, int32_t rotary_mode, float rope_scale,
+                             float rope_theta, pd_stream_t stream) {
+  if (rotary_mode < 0 || rotary_mode > 2) return fail(PD_ERR_INVALID_ARG, "rotary_mode must be 0, 1 or 2");
+  if (rotary_mode && (D % 2 || D / 2 > kMaxHalfDim))
+    return fail(PD_ERR_UNSUPPORTED, "RoPE append needs an even head dim of at most 256");
+  if (rotary_mode && !(rope_theta > 0.f && std::isfinite(rope_theta) && std::isfinite(rope_scale)))
+    return fail(PD_ERR_INVALID_ARG, "rope_theta must be finite and positive");
+  if (rotary_mode && T > 0 && !positions) return fail(PD_ERR_INVALID_ARG, "RoPE append needs positions");
   if (T < 0 || H_kv <= 0 || D <= 0 || page_size <= 0 || max_pages <= 0)
     return fail(PD_ERR_INVALID_ARG, "bad T/H_kv/D/page_size/max_pages");
   if (in_dtype != kF32 && in_dtype != kF16 && in_dtype != kBF16)
@@ -500,10 +517,36 @@ pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
   DeviceState* ds = nullptr;
   pd_status st = device_state(&ds);
   if (st != PD_OK) return st;
+  AppendRope rope{};
+  rope.positions = positions;
+  rope.mode = rotary_mode;
+  if (rotary_mode) rope_table(rope_scale, rope_theta, D, rope.F);
   cudaError_t e = launch_append(pages, k_new, v_new, slot_mapping, T, H_kv, D, page_size, max_pages,
-                                in_dtype, kv_dtype, k_scale, v_scale, ds->err, (cudaStream_t)stream);
+                                in_dtype, kv_dtype, k_scale, v_scale, ds->err, rope, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
   return PD_OK;
+}
+
+extern "C" {
+
+pd_status pd_append_paged_kv(void* pages, const void* k_new, const void* v_new,
+                             const int64_t* slot_mapping, int32_t T, int32_t H_kv, int32_t D,
+                             int32_t page_size, int64_t max_pages, int32_t in_dtype,
+                             int32_t kv_dtype, float k_scale, float v_scale, pd_stream_t stream) {
+  return append_call(pages, k_new, v_new, slot_mapping, T, H_kv, D, page_size, max_pages, in_dtype,
+                     kv_dtype, k_scale, v_scale, nullptr, 0, 1.f, 1e4f, stream);
+}
+
+pd_status pd_append_paged_kv_rope(void* pages, const void* k_new, const void* v_new,
+                                  const int64_t* slot_mapping, const int32_t* positions,
+                                  int32_t T, int32_t H_kv, int32_t D, int32_t page_size,
+                                  int64_t max_pages, int32_t in_dtype, int32_t kv_dtype,
+                                  float k_scale, float v_scale, int32_t rotary_mode,
+                                  float rope_scale, float rope_theta, pd_stream_t stream) {
+  if (rotary_mode != 1 && rotary_mode != 2) return fail(PD_ERR_INVALID_ARG, "rotary_mode must be 1 or 2");
+  return append_call(pages, k_new, v_new, slot_mapping, T, H_kv, D, page_size, max_pages, in_dtype,
+                     kv_dtype, k_scale, v_scale, positions, rotary_mode, rope_scale, rope_theta,
+                     stream);
 }
 
 pd_status pd_check_device_errors(pd_stream_t stream) {

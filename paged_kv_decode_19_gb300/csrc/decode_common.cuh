@@ -53,6 +53,7 @@ struct DecodeParams {
   int out_vec16;      // out is 16-byte aligned (vector stores of whole runs)
   int early_inputs;   // Q, page table, lengths and positions may be read before pdl_wait()
   const float* sink;  // [H_qo] learned logit per query head (natural units), or nullptr
+  int k_rotated;      // the cache holds K rotated at append time: only Q is rotated here
   float score_scale;  // raw q.k -> log2 units (sm_scale * log2 e [* k_scale])
   float q_prescale;   // split-operand MMA path: Q is pre-multiplied by this
   float out_scale;    // applied to the final output (v_scale for e4m3 KV)

@@ -76,7 +76,9 @@ struct MinBlocks {
   static constexpr int v = ROPE ? PD_MIN_BLOCKS_ROPE : FP8 ? 3 : PD_MIN_BLOCKS_PLAIN;
 };
 
-template <typename KVT, typename QT, int D, bool ROPE>
+// ROPE: Q is rotated (its hi + lo split keeps the rotation exact); KROT: K is rotated
+// in the kernel too (else the cache holds it rotated, or there is no RoPE).
+template <typename KVT, typename QT, int D, bool ROPE, bool KROT = ROPE>
 struct MmaTraits {
   static constexpr bool kFp8 = sizeof(KVT) == 1;
   using MT = typename std::conditional<std::is_same<KVT, __nv_bfloat16>::value, __nv_bfloat16,
@@ -88,7 +90,7 @@ struct MmaTraits {
   static constexpr bool kQSplit = ROPE || kFp8 || !std::is_same<QT, MT>::value;
   // QK tensor-core type: rotated K is rounded once to f16 (11-bit significand, against
   // bf16's 8), Q is split into f16 hi + lo, so a score keeps about 11 bits of K'
-  using QKT = typename std::conditional<ROPE, __half, MT>::type;
+  using QKT = typename std::conditional<KROT, __half, MT>::type;
   static_assert(kRowBytes == 128 || kRowBytes == 256, "row must be 128 or 256 bytes");
 };
 
@@ -329,12 +331,15 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
   __syncwarp();
 }
 
+// RM: 0 no RoPE; 1 rotate-half, 2 interleaved pairs (Q and K rotated here); 3, 4 the same
+// layouts with K rotated in the cache already (only Q rotated here).
 template <typename KVT, typename QT, int D, int RM, int NW, bool MQ>
-__global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 1)>::v)
+__global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (sizeof(KVT) == 1)>::v)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
-  constexpr bool ROPE = RM != 0;  // RM: 0 no RoPE, 1 rotate-half, 2 interleaved pairs
-  constexpr bool IL = RM == 2;
-  using Tr = MmaTraits<KVT, QT, D, ROPE>;
+  constexpr bool ROPE = RM != 0;               // Q is rotated
+  constexpr bool KROT = RM == 1 || RM == 2;    // K is rotated in the tile loop
+  constexpr bool IL = RM == 2 || RM == 4;      // interleaved pairs (2i, 2i + 1)
+  using Tr = MmaTraits<KVT, QT, D, ROPE, KROT>;
   using MT = typename Tr::MT;
   using QKT = typename Tr::QKT;
   constexpr int NT = NW * 32;
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
   __shared__ int s_msl[NW][32];
   __shared__ long long s_pend[NW][2][4];                    // per-warp deferred merges
   __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
-  __shared__ __align__(16) float2 s_rot8[ROPE ? D / 2 : 2];  // e^(i * 8 * omega_f)
+  __shared__ __align__(16) float2 s_rot8[KROT ? D / 2 : 2];  // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
 
   // Q and the page table are small and needed right after the start-up scan, when the
@@ -364,9 +369,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
     for (int i = threadIdx.x; i < D / 2; i += NT) {
       const unsigned long long F = p.rope_F[i];
       s_ropeF[i] = F;
-      float c8, s8;
-      rope_cos_sin(8, F, c8, s8);
-      s_rot8[i] = make_float2(c8, s8);
+      if (KROT) {
+        float c8, s8;
+        rope_cos_sin(8, F, c8, s8);
+        s_rot8[i] = make_float2(c8, s8);
+      }
     }
   }
   // By default nothing of the caller's is read before the kernel launched before this
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
     lim0 = sg.seq.L - p.q_len + 1 + cc / p.group;
     lim1 = sg.seq.L - p.q_len + 1 + (cc + 1) / p.group;
   }
-  const int kpos0 = ROPE ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
+  const int kpos0 = KROT ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
 
   // ---------------------------------------------------------------- tile stream
   // Pieces [ua, pend) in order.  Entering a piece, the warp prefetches the K and V
@@ -650,7 +657,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
       float qacc[kQChains][4];
 #pragma unroll
       for (int c = 0; c < kQChains; ++c) qacc[c][0] = qacc[c][1] = qacc[c][2] = qacc[c][3] = 0.f;
-      if constexpr (!ROPE) {
+      if constexpr (!KROT) {
 #pragma unroll
         for (int kt = 0; kt < KT; ++kt) {
           uint32_t a[4];
@@ -990,7 +997,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM != 0), (sizeof(KVT) == 
     const int hcount = min(kMaxGroupPerCta, p.ncol - c0);
     // slot rows in flight together: about 16 float4 per lane (4 where registers are
     // tight), for the slice's head count
-    constexpr int kBudget = MinBlocks<ROPE, FP8>::v >= 3 ? 4 : 16;
+    constexpr int kBudget = MinBlocks<KROT, FP8>::v >= 3 ? 4 : 16;
     constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
     if (hcount <= 4)
       warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
@@ -1020,8 +1027,11 @@ static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t s
 // a separate instantiation, so the single-token kernel carries none of it.
 template <typename KVT, typename QT, int D, bool MQ>
 static cudaError_t launch_mma_r(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
-  if (p.rotary == 1) return launch_mma_t<KVT, QT, D, 1, MQ>(p, grid, st, cfg);
-  if (p.rotary == 2) return launch_mma_t<KVT, QT, D, 2, MQ>(p, grid, st, cfg);
+  const int rm = p.rotary ? p.rotary + (p.k_rotated ? 2 : 0) : 0;
+  if (rm == 1) return launch_mma_t<KVT, QT, D, 1, MQ>(p, grid, st, cfg);
+  if (rm == 2) return launch_mma_t<KVT, QT, D, 2, MQ>(p, grid, st, cfg);
+  if (rm == 3) return launch_mma_t<KVT, QT, D, 3, MQ>(p, grid, st, cfg);
+  if (rm == 4) return launch_mma_t<KVT, QT, D, 4, MQ>(p, grid, st, cfg);
   return launch_mma_t<KVT, QT, D, 0, MQ>(p, grid, st, cfg);
 }
 

@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
     for (int e = 0; e < E; ++e) o[j][e] = 0.f;
   }
 
-  const int kpos0 = p.rotary ? p.k_rope_pos_offset[sg.b] : 0;
+  const int kpos0 = p.rotary && !p.k_rotated ? p.k_rope_pos_offset[sg.b] : 0;
   const KT* pages = reinterpret_cast<const KT*>(p.pages);
   const size_t kv_stride = (size_t)p.H_kv * p.P * D;  // K block -> V block of a page
   constexpr int R = 4;  // rows a warp loads before computing them (latency hiding)
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
     }
 #pragma unroll
     for (int u = 0; u < R; ++u) {
-      if (ok[u] && p.rotary) {
+      if (ok[u] && p.rotary && !p.k_rotated) {  // (else the cache holds K rotated)
 #pragma unroll
         for (int e = 0; e < H2; ++e) {
           float c, s;

@@ -41,9 +41,15 @@ void record_error(const char* msg);
 // merge_state_inplace and append_paged_kv
 cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const float* S_other, int N,
                                int H, int D, int v_dtype, cudaStream_t st);
+// RoPE applied to the appended K rows (mode 0: none, 1 rotate-half, 2 interleaved).
+struct AppendRope {
+  const int32_t* positions;                // [T] position of each new token
+  int mode;
+  unsigned long long F[kMaxHalfDim];       // fixed-point turns per frequency
+};
 cudaError_t launch_append(void* pages, const void* k_new, const void* v_new,
                           const int64_t* slot_mapping, int T, int H_kv, int D, int P,
                           long long max_pages, int in_dtype, int kv_dtype, float k_scale,
-                          float v_scale, unsigned* err, cudaStream_t st);
+                          float v_scale, unsigned* err, const AppendRope& rope, cudaStream_t st);
 
 }  // namespace pd

@@ -64,12 +64,25 @@ __device__ __forceinline__ OT convert_elem(IT x, float scale) {
   }
 }
 
+template <typename OT>
+__device__ __forceinline__ OT convert_f32(float x, float scale) {
+  if constexpr (std::is_same<OT, F8>::value) {
+    F8 r;
+    r.v = f32_to_e4m3(x / scale);
+    return r;
+  } else {
+    return from_f32<OT>(x);
+  }
+}
+
 // grid: (T * H_kv) blocks; block threads stride over D.  blockIdx.y: 0 = K, 1 = V.
+// With rope.mode (1 rotate-half, 2 interleaved) each K row is rotated first, in fp32,
+// at positions[t] (angle from the fixed-point turns F[i], to fp32 accuracy).
 template <typename IT, typename OT>
 __global__ void append_kernel(OT* __restrict__ pages, const IT* __restrict__ k_new,
                               const IT* __restrict__ v_new, const int64_t* __restrict__ slots,
                               int T, int H_kv, int D, int P, long long max_pages, float k_scale,
-                              float v_scale, unsigned* err) {
+                              float v_scale, unsigned* err, const __grid_constant__ AppendRope rope) {
   pdl_wait();  // inputs and pages are the previous kernel's to write until it completes
   pdl_release();
   const int th = blockIdx.x;
@@ -85,23 +98,35 @@ __global__ void append_kernel(OT* __restrict__ pages, const IT* __restrict__ k_n
   const IT* src = (kv == 0 ? k_new : v_new) + ((size_t)t * H_kv + h) * D;
   OT* dst = pages + ((((size_t)page * 2 + kv) * H_kv + h) * P + off) * D;
   const float scale = kv == 0 ? k_scale : v_scale;
+  if (kv == 0 && rope.mode) {
+    const int pos = rope.positions[t];
+    for (int i = threadIdx.x; i < D / 2; i += blockDim.x) {
+      const int a = rope.mode == 1 ? i : 2 * i, b = rope.mode == 1 ? i + D / 2 : 2 * i + 1;
+      float c, sn;
+      rope_cos_sin_accurate(pos, rope.F[i], c, sn);
+      const float x = to_f32(src[a]), y = to_f32(src[b]);
+      dst[a] = convert_f32<OT>(x * c - y * sn, scale);
+      dst[b] = convert_f32<OT>(y * c + x * sn, scale);
+    }
+    return;
+  }
   for (int d = threadIdx.x; d < D; d += blockDim.x) dst[d] = convert_elem<IT, OT>(src[d], scale);
 }
 
 template <typename IT>
 static cudaError_t append_in(void* pages, const void* k, const void* v, const int64_t* slots, int T,
                              int H, int D, int P, long long max_pages, int kv_dtype, float ks,
-                             float vs, unsigned* err, cudaStream_t st) {
+                             float vs, unsigned* err, const AppendRope& rope, cudaStream_t st) {
   const dim3 grid((unsigned)T * H, 2);
   const int threads = D < 128 ? D : 128;
   const IT* kk = (const IT*)k;
   const IT* vv = (const IT*)v;
   const dim3 block(threads);
   switch (kv_dtype) {
-    case kF32: return launch_pdl(append_kernel<IT, float>, grid, block, 0, st, (float*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
-    case kF16: return launch_pdl(append_kernel<IT, __half>, grid, block, 0, st, (__half*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
-    case kBF16: return launch_pdl(append_kernel<IT, __nv_bfloat16>, grid, block, 0, st, (__nv_bfloat16*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
-    case kE4M3: return launch_pdl(append_kernel<IT, F8>, grid, block, 0, st, (F8*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err);
+    case kF32: return launch_pdl(append_kernel<IT, float>, grid, block, 0, st, (float*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err, rope);
+    case kF16: return launch_pdl(append_kernel<IT, __half>, grid, block, 0, st, (__half*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err, rope);
+    case kBF16: return launch_pdl(append_kernel<IT, __nv_bfloat16>, grid, block, 0, st, (__nv_bfloat16*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err, rope);
+    case kE4M3: return launch_pdl(append_kernel<IT, F8>, grid, block, 0, st, (F8*)pages, kk, vv, slots, T, H, D, P, max_pages, ks, vs, err, rope);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -109,12 +134,12 @@ static cudaError_t append_in(void* pages, const void* k, const void* v, const in
 cudaError_t launch_append(void* pages, const void* k_new, const void* v_new,
                           const int64_t* slot_mapping, int T, int H_kv, int D, int P,
                           long long max_pages, int in_dtype, int kv_dtype, float k_scale,
-                          float v_scale, unsigned* err, cudaStream_t st) {
+                          float v_scale, unsigned* err, const AppendRope& rope, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   switch (in_dtype) {
-    case kF32: return append_in<float>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, st);
-    case kF16: return append_in<__half>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, st);
-    case kBF16: return append_in<__nv_bfloat16>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, st);
+    case kF32: return append_in<float>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, rope, st);
+    case kF16: return append_in<__half>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, rope, st);
+    case kBF16: return append_in<__nv_bfloat16>(pages, k_new, v_new, slot_mapping, T, H_kv, D, P, max_pages, kv_dtype, k_scale, v_scale, err, rope, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -46,6 +46,7 @@ def test_desc_layout_matches_header():
     assert _lib.DecodeDesc.workspace.offset == 72
     text = open(HEADER).read()
     assert re.search(r"#define PD_DECODE_EARLY_INPUTS (\d+)", text).group(1) == str(_lib.DECODE_EARLY_INPUTS)
+    assert re.search(r"#define PD_DECODE_K_ROTATED (\d+)", text).group(1) == str(_lib.DECODE_K_ROTATED)
 
 
 def _desc(**kw):
@@ -62,13 +63,30 @@ def _desc(**kw):
     (dict(out_dtype=3), "PD_ERR_INVALID_ARG"), (dict(kv_dtype=3, k_scale=0.0), "PD_ERR_INVALID_ARG"),
     (dict(kv_dtype=1), "PD_ERR_UNSUPPORTED"), (dict(num_splits=-2), "PD_ERR_INVALID_ARG"),
     (dict(max_pages=0), "PD_ERR_INVALID_ARG"), (dict(B=-1), "PD_ERR_INVALID_ARG"),
-    (dict(flags=2), "PD_ERR_INVALID_ARG"),
+    (dict(flags=4), "PD_ERR_INVALID_ARG"),
 ])
 def test_decode_validation_without_gpu(L, bad, status):
     d = _desc(**bad)
     st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 0,
                                     1.0, 1e4, 0.1, ctypes.byref(d), None)
     assert _lib.STATUS[st] == status, L.pd_get_last_error_string()
+
+
+def test_unknown_flag_bits_rejected(L):
+    d = _desc(flags=4)
+    st = L.pd_batch_decode_paged_kv(None, None, None, None, None, None, None, None, None, 0,
+                                    1.0, 1e4, 0.1, ctypes.byref(d), None)
+    assert _lib.STATUS[st] == "PD_ERR_INVALID_ARG" and b"flags" in L.pd_get_last_error_string()
+
+
+def test_append_rope_validation_without_gpu(L):
+    f = L.pd_append_paged_kv_rope
+    args = lambda mode, D=64, pos=None: (None, None, None, None, pos, 3, 2, D, 16, 10, 2, 2, 1.0,
+                                         1.0, mode, 1.0, 1e4, None)
+    assert _lib.STATUS[f(*args(0))] == "PD_ERR_INVALID_ARG"
+    assert _lib.STATUS[f(*args(3))] == "PD_ERR_INVALID_ARG"
+    assert _lib.STATUS[f(*args(1))] == "PD_ERR_INVALID_ARG"  # no positions
+    assert _lib.STATUS[f(*args(1, D=63, pos=ctypes.c_void_p(64)))] == "PD_ERR_UNSUPPORTED"
 
 
 def test_decode_rotary_mode_range(L):
