@@ -106,7 +106,8 @@ def _oracle_sample(wl: W.Workload, budget_s: float):
                 Q, pages, ip, vals, li, kro, qrp, q_len=s.q_len, q_dtype=s.q_dtype,
                 kv_dtype=s.kv_dtype, H_kv=s.H_kv, page_size=s.page_size,
                 rotary_mode=s.rotary_mode, rope_scale=s.rope_scale, rope_theta=s.rope_theta,
-                sm_scale=wl.sm_scale, k_scale=wl.k_scale, v_scale=wl.v_scale, mask=mask)
+                sm_scale=wl.sm_scale, k_scale=wl.k_scale, v_scale=wl.v_scale, mask=mask,
+                k_rotated=s.k_rotated)
         else:
             mask = np.zeros((s.B, s.H_qo), bool)
             mask[b] = True
@@ -115,7 +116,7 @@ def _oracle_sample(wl: W.Workload, budget_s: float):
                 H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode,
                 rope_scale=s.rope_scale, rope_theta=s.rope_theta, sm_scale=wl.sm_scale,
                 sliding_window=s.window is not None, k_scale=wl.k_scale, v_scale=wl.v_scale,
-                mask=mask)
+                mask=mask, k_rotated=s.k_rotated)
         nseq += 1
         rows += int(wl.attended[b])
         if time.perf_counter() - t0 >= budget_s:
@@ -242,9 +243,22 @@ def run_ours(args, ws, rank, local):
         wbuf.zero_()
         rbuf.amax()
 
+    # a cache that holds K rotated: the append rotates the new rows at their positions
+    # (attended index, as the decode's RoPE), the decode then rotates only Q
+    kpos = [torch.from_numpy((r[0].k_rope_pos_offset.cpu().numpy()[:, None]
+                              + np.maximum(r[0].attended - s.q_len, 0)[:, None]
+                              + np.arange(s.q_len)[None, :]).reshape(-1).astype(np.int32)).to(dev)
+            for r in reps]
+    kpos_of = {id(r[0]): k for r, k in zip(reps, kpos)}
+
     def append(r):
         w, k_new, v_new, slots = r
-        pd.append_paged_kv(w.pages, k_new, v_new, slots, w.k_scale, w.v_scale)
+        if s.k_rotated:
+            pd.append_paged_kv_rope(w.pages, k_new, v_new, slots, kpos_of[id(w)],
+                                    s.rotary_mode, s.rope_scale, s.rope_theta, w.k_scale,
+                                    w.v_scale)
+        else:
+            pd.append_paged_kv(w.pages, k_new, v_new, slots, w.k_scale, w.v_scale)
 
     def decode(r):
         # the decode follows the append on the stream: its start-up (work split scan,
@@ -252,7 +266,8 @@ def run_ours(args, ws, rank, local):
         w = r[0]
         decode_api(w.Q, w.pages, w.indptr, w.values, w.length_info, w.k_rope_pos_offset,
                    w.q_rope_position, out, lse, s.rotary_mode, s.rope_scale, s.rope_theta,
-                   w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True, **split)
+                   w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
+                   k_rotated=s.k_rotated, **split)
 
     def prefill(n):
         # a spin kernel of about 60 us per step keeps the device busy (at load clocks)
@@ -332,6 +347,8 @@ def run_ours(args, ws, rank, local):
     names = ("Q", "indptr", "values", "length_info", "k_rope_pos_offset", "q_rope_position")
     srcs = {k: getattr(wl, k) for k in names}
     srcs["k_new"], srcs["v_new"], srcs["slots"] = reps[0][1], reps[0][2], reps[0][3]
+    if s.k_rotated:
+        srcs["kpos"] = kpos[0]
     offs, total = {}, 0
     for k, t in srcs.items():
         total = (total + 255) // 256 * 256
@@ -363,11 +380,17 @@ def run_ours(args, ws, rank, local):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         buf.copy_(host_in, non_blocking=True)
-        pd.append_paged_kv(w.pages, di["k_new"], di["v_new"], di["slots"], w.k_scale, w.v_scale)
+        if s.k_rotated:
+            pd.append_paged_kv_rope(w.pages, di["k_new"], di["v_new"], di["slots"], di["kpos"],
+                                    s.rotary_mode, s.rope_scale, s.rope_theta, w.k_scale,
+                                    w.v_scale)
+        else:
+            pd.append_paged_kv(w.pages, di["k_new"], di["v_new"], di["slots"], w.k_scale,
+                               w.v_scale)
         decode_api(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
                    di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e, s.rotary_mode,
                    s.rope_scale, s.rope_theta, w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale,
-                   early_inputs=True, **split)
+                   early_inputs=True, k_rotated=s.k_rotated, **split)
         res_host.copy_(res_dev, non_blocking=True)
         b.record(stream)
         b.synchronize()
@@ -414,7 +437,9 @@ def main():
            "B": spec.B, "H_qo": spec.H_qo, "H_kv": spec.H_kv, "D": spec.D,
            "page_size": spec.page_size, "kv_dtype": spec.kv_dtype, "q_dtype": spec.q_dtype,
            "rotary_mode": spec.rotary_mode, "len_dist": list(spec.len_dist), "q_len": spec.q_len,
-           "step": ("append_paged_kv (1 token/seq) + batch_decode_paged_kv" if spec.q_len == 1 else
+           "step": ("append_paged_kv_rope (1 token/seq, K rotated) + batch_decode_paged_kv "
+                    "(PD_DECODE_K_ROTATED)" if spec.k_rotated else
+                    "append_paged_kv (1 token/seq) + batch_decode_paged_kv" if spec.q_len == 1 else
                     f"append_paged_kv ({spec.q_len} tokens/seq) + batch_decode_paged_kv_mq "
                     f"(q_len={spec.q_len}, causal among the new tokens)"),
            "l2": None,  # filled in below

@@ -15,6 +15,8 @@ CSR page table, ``length_info`` ``[B]`` or ``[3,B]``):
   long_ctx_bf16      B=8,   H 32/8, D=128, P=16, bf16, len U[32768,131072]
   window_sink_f16    B=64,  H 32/4, D=128, P=16, f16, len U[4096,16384], window 4096, sink 4, RoPE 1e4
   fp8_kv_highconc    B=256, H 64/8, D=128, P=32, e4m3 KV (+ bf16 Q), lognormal len, + append
+  llama3_8b_bf16_krot  llama3_8b_bf16 with the cache holding K rotated at append time
+                     (pd_append_paged_kv_rope; the decode rotates only Q)
   spec_decode_bf16   llama3_8b_bf16 with 2 query tokens per sequence (multi-query decode,
                      causal among them: speculative decoding's verification step; the
                      2 x 4 (token, head) columns of a KV head fill one 8-column MMA tile)
@@ -61,6 +63,7 @@ class Spec:
     append: bool = False       # one new token per sequence, written before attention
     max_splits: int = 0        # external split count (long-context chunking)
     q_len: int = 1             # query tokens per sequence (multi-query decode, causal)
+    k_rotated: bool = False    # the cache holds K rotated at append time (decode rotates Q only)
 
 
 SPECS = {
@@ -76,6 +79,9 @@ SPECS = {
                             window=4096, sink=4),
     "fp8_kv_highconc": Spec("fp8_kv_highconc", 256, 64, 8, 128, 32, "bf16", "e4m3", "bf16",
                             ("lognormal", 2048, 0.6, 64, 8192), append=True),
+    "llama3_8b_bf16_krot": Spec("llama3_8b_bf16_krot", 32, 32, 8, 128, 16, "bf16", "bf16",
+                                "bf16", ("uniform", 512, 4096), pool=16384, rotary_mode=1,
+                                rope_theta=500000.0, k_rotated=True),
     "spec_decode_bf16": Spec("spec_decode_bf16", 32, 32, 8, 128, 16, "bf16", "bf16", "bf16",
                              ("uniform", 512, 4096), pool=16384, rotary_mode=1,
                              rope_theta=500000.0, q_len=2),
@@ -90,6 +96,7 @@ REDUCED = {
     "window_sink_f16": dict(B=5, len_dist=("uniform", 200, 900), window=300),
     "fp8_kv_highconc": dict(B=6, len_dist=("lognormal", 300, 0.6, 20, 700)),
     "spec_decode_bf16": dict(B=5, len_dist=("uniform", 17, 700), pool=512),
+    "llama3_8b_bf16_krot": dict(B=5, len_dist=("uniform", 17, 700), pool=512),
 }
 
 

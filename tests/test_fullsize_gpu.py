@@ -46,6 +46,8 @@ def test_fullsize_sampled(name):
     if s.q_len > 1:
         _fullsize_multi_query(wl)
         return
+    if s.k_rotated:  # the synthetic cache stands for K rows rotated at append time
+        kw["k_rotated"] = True
     out, lse = gpu_decode(wl, **kw)
     assert pd.check_device_errors() == "PD_OK"
     # properties of every output: finite; each output element is a convex combination
@@ -55,7 +57,7 @@ def test_fullsize_sampled(name):
     assert out.float().abs().max().item() <= vmax * (1 + 1e-2)
     assert (lse > -5e4).all()
     mask = _sample_mask(wl)
-    ro, rl, st = oracle_decode(wl, pages=ref_pages, mask=mask)
+    ro, rl, st = oracle_decode(wl, pages=ref_pages, mask=mask, k_rotated=s.k_rotated)
     assert st == 0
     compare(kind_of(wl), out, lse, ro, rl, mask=mask)
 
