@@ -94,6 +94,13 @@ struct MmaTraits {
   static_assert(kRowBytes == 128 || kRowBytes == 256, "row must be 128 or 256 bytes");
 };
 
+// Slot of frequency f in the shared RoPE tables: two spare 8-byte words after every 16
+// frequencies, so that the four quad lanes, which read frequencies 8 apart (rotate-half)
+// or 4 apart (interleaved), hit different banks; slots stay even (16-byte reads of
+// s_rot8 at an even f stay aligned).
+__device__ __forceinline__ int rope_slot(int f) { return f + 2 * (f >> 4); }
+constexpr int rope_slots(int D) { return D / 2 + 2 * (D / 32); }
+
 // Dim of A-fragment element (k-tile kt, half 0: k-pos 2q..2q+1 / half 1: 2q+8..2q+9,
 // element e) for thread quad index q4: thread q4 owns 16-byte chunks 4c + q4 of a row.
 template <bool FP8>
@@ -355,8 +362,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   __shared__ float s_mw[NW][34][kMaxGroupPerCta];           // per-warp merge scratch
   __shared__ int s_msl[NW][32];
   __shared__ long long s_pend[NW][2][4];                    // per-warp deferred merges
-  __shared__ unsigned long long s_ropeF[ROPE ? D / 2 : 1];  // RoPE frequencies (fixed point)
-  __shared__ __align__(16) float2 s_rot8[KROT ? D / 2 : 2];  // e^(i * 8 * omega_f)
+  __shared__ unsigned long long s_ropeF[ROPE ? rope_slots(D) : 1];  // frequencies (fixed point)
+  __shared__ __align__(16) float2 s_rot8[KROT ? rope_slots(D) : 2];  // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
 
   // Q and the page table are small and needed right after the start-up scan, when the
@@ -368,11 +375,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   if (ROPE) {
     for (int i = threadIdx.x; i < D / 2; i += NT) {
       const unsigned long long F = p.rope_F[i];
-      s_ropeF[i] = F;
+      s_ropeF[rope_slot(i)] = F;
       if (KROT) {
         float c8, s8;
         rope_cos_sin(8, F, c8, s8);
-        s_rot8[i] = make_float2(c8, s8);
+        s_rot8[rope_slot(i)] = make_float2(c8, s8);
       }
     }
   }
@@ -596,7 +603,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             float c, sn;
-            rope_cos_sin(qpos, s_ropeF[frag_dim<FP8>(kt, h, e, q4)], c, sn);
+            rope_cos_sin(qpos, s_ropeF[rope_slot(frag_dim<FP8>(kt, h, e, q4))], c, sn);
             const float x = qv[0][h][e], y = qv[1][h][e];
             qv[0][h][e] = x * c - y * sn;
             qv[1][h][e] = y * c + x * sn;
@@ -608,7 +615,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             float c, sn;
-            rope_cos_sin(qpos, s_ropeF[frag_dim<FP8>(kt + u * (KT / 2), h, 0, q4) >> 1], c, sn);
+            rope_cos_sin(qpos, s_ropeF[rope_slot(frag_dim<FP8>(kt + u * (KT / 2), h, 0, q4) >> 1)], c, sn);
             const float x = qv[u][h][0], y = qv[u][h][1];
             qv[u][h][0] = x * c - y * sn;
             qv[u][h][1] = y * c + x * sn;
@@ -702,8 +709,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
           for (int half = 0; half < 2; ++half) {
             const int f = frag_dim<FP8>(kt, half, 0, q4) >> 1;
             float c0, s0;
-            rope_cos_sin(pos0, s_ropeF[f], c0, s0);
-            const float2 r8 = s_rot8[f];  // (cos, sin) of 8 positions
+            rope_cos_sin(pos0, s_ropeF[rope_slot(f)], c0, s0);
+            const float2 r8 = s_rot8[rope_slot(f)];  // (cos, sin) of 8 positions
             const float2 cc = make_float2(c0, c0 * r8.x - s0 * r8.y);
             const float2 ss = make_float2(s0, s0 * r8.x + c0 * r8.y);
             const float2 a0 = unpack2<MT>(araw[2 * half]);      // row g_id: (2i, 2i + 1)
@@ -730,9 +737,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
             // rows g_id (direct) and g_id + 8 (rotated by 8 positions)
             const int f = frag_dim<FP8>(kt, half, 0, q4);
             float2 cs_c[2], cs_s[2];  // [row] (cos f, cos f+1), (sin f, sin f+1)
-            rope_cos_sin(pos0, s_ropeF[f], cs_c[0].x, cs_s[0].x);
-            rope_cos_sin(pos0, s_ropeF[f + 1], cs_c[0].y, cs_s[0].y);
-            const float4 r8 = *reinterpret_cast<const float4*>(&s_rot8[f]);  // (c8, s8) of f, f+1
+            rope_cos_sin(pos0, s_ropeF[rope_slot(f)], cs_c[0].x, cs_s[0].x);
+            rope_cos_sin(pos0, s_ropeF[rope_slot(f) + 1], cs_c[0].y, cs_s[0].y);
+            const float4 r8 = *reinterpret_cast<const float4*>(&s_rot8[rope_slot(f)]);  // (c8, s8) of f, f+1
             const float2 r8c = make_float2(r8.x, r8.z), r8s = make_float2(r8.y, r8.w);
             cs_c[1] = sub_f2(mul_f2(cs_c[0], r8c), mul_f2(cs_s[0], r8s));
             cs_s[1] = fma_f2(cs_s[0], r8c, mul_f2(cs_c[0], r8s));
