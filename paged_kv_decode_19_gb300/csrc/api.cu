@@ -1,6 +1,7 @@
 // Host side of libpageddecode: argument validation, the split planner, workspace
-// and error-word management and kernel dispatch.  Every
-// entry point of include/pageddecode.h is defined here.
+// and error-word management and kernel dispatch.  Every entry point of
+// include/pageddecode.h is defined here, except pd_batch_decode_paged_kv_noalloc
+// (decode_noalloc.cu), which calls pd_batch_decode_paged_kv.
 #include <algorithm>
 #include <climits>
 #include <cmath>

@@ -34,11 +34,14 @@
 // tile loop is kept nearly branch-free (its instruction fetch and branch stalls
 // measurably limit it): the next piece comes from a per-lane cache by shuffles, the
 // Q-packing mode is a compile-time parameter, and only partial tiles take a branch.
-// RoPE (rotate-half) is applied to K in registers before the MMA; rotated K is rounded
-// once to f16 (11 significant bits; a score error of about 2^-12 of |q| |k| sqrt(D)
-// scale) and multiplied with Q split into f16 hi + lo parts, one MMA per k-tile when
-// the hi and lo parts share the n dimension (<= 4 heads).  The rotated K of a bf16
-// cache must stay inside the f16 range (|k| < 46000).  FP8 codes
+// RoPE (rotate-half pairs (d, d + D/2) or interleaved pairs (2i, 2i + 1)) is applied to
+// K in registers before the MMA; rotated K is rounded once to f16 (11 significant bits;
+// a score error of about 2^-12 of |q| |k| sqrt(D) scale) and multiplied with Q split
+// into f16 hi + lo parts, one MMA per k-tile when the hi and lo parts share the n
+// dimension (<= 4 columns).  The rotated K of a bf16 cache must stay inside the f16
+// range (|k| < 46000).  A cache that holds K rotated at append time skips the K
+// rotation (RoPE modes 3 and 4: Q only).  The frequency tables sit in shared memory
+// padded against bank conflicts (rope_slot).  FP8 codes
 // become f16 in registers (exact); k_scale folds into the score scale, v_scale into
 // the output.
 //

@@ -7,6 +7,8 @@
 //   [max_pages, 2, H_kv, P, D]; FP8 encode per the NKI Attention Block TKG reference
 //   (per-tensor k_scale / v_scale, OCP e4m3fn): IEEE fp32 division, then the hardware
 //   round-to-nearest-even saturating conversion.  A negative slot skips the token.
+//   With RoPE (append_paged_kv_rope) each K row is rotated at its token's position
+//   before the conversion, the order of the NKI TKG block (RoPE, then the cache update).
 #include "common.cuh"
 #include "kernels.h"
 
