@@ -61,3 +61,34 @@ def test_traffic_record_only_for_matching_sources(tmp_path, monkeypatch):
     assert bench._measured_traffic("cfgA", 4) == 1234
     assert bench._measured_traffic("cfgB", 4) is None   # taken on other sources
     assert bench._measured_traffic("cfgA", 8) is None   # another batch size
+
+
+def test_append_inputs_cover_the_last_q_len_rows():
+    """The step's append writes each sequence's last q_len rows (its new tokens): the
+    slot of row r is page_table[r // P] * P + r % P; a row before the sequence start
+    is skipped (-1)."""
+    import numpy as np
+    from paged_kv_decode_19_gb300 import workloads as W
+    for q_len in (1, 2, 3):
+        wl = W.make("llama3_8b_bf16", seed=5, reduced=True, device="cpu", q_len=q_len,
+                    len_dist=("uniform", 1, 40), B=6)
+        k, v, slots = bench._append_inputs(wl, "cpu")
+        s = wl.spec
+        assert k.shape == (s.B * q_len, s.H_kv, s.D) and v.shape == k.shape
+        ip, vals, P = wl.indptr.numpy(), wl.values.numpy(), s.page_size
+        got = slots.numpy().reshape(s.B, q_len)
+        for b in range(s.B):
+            for j in range(q_len):
+                r = int(wl.seq_len[b]) - q_len + j
+                want = -1 if r < 0 else int(vals[ip[b] + r // P]) * P + r % P
+                assert got[b, j] == want, (q_len, b, j)
+
+
+def test_spec_decode_workload_shapes_and_positions():
+    from paged_kv_decode_19_gb300 import workloads as W
+    wl = W.make("spec_decode_bf16", seed=6, reduced=True, device="cpu")
+    s = wl.spec
+    assert s.q_len == 2 and wl.Q.shape == (s.B, 2, s.H_qo, s.D)
+    # token t of a sequence sits at its own row's position: L - q_len + t
+    assert (wl.q_rope_position.numpy() == (wl.attended - 2).clip(min=0)).all()
+    assert wl.io_bytes() == 2 * W.make("llama3_8b_bf16", seed=6, reduced=True, device="cpu").io_bytes()
