@@ -174,3 +174,23 @@ def test_multi_query_validation_without_gpu(L):
     # the desc is validated as for the single-token entry point
     assert _lib.STATUS[L.pd_batch_decode_paged_kv_mq(*args(2, _desc(D=96)))] == "PD_ERR_UNSUPPORTED"
     assert L.pd_batch_decode_paged_kv_mq(*args(2, _desc(B=0))) == 0
+
+
+def test_plain_c_caller(L, tmp_path):
+    # the boundary is a C ABI: a C program compiled against include/pageddecode.h and
+    # linked with the library sees the same planner and validation results
+    import subprocess
+    so = _lib._LIB_PATH
+    exe = tmp_path / "abi_check"
+    subprocess.check_call(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "c", "abi_check.c"), so, "-o", str(exe),
+                           "-Wl,-rpath," + os.path.dirname(so)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
+    invalid = {v: k for k, v in _lib.STATUS.items()}["PD_ERR_INVALID_ARG"]
+    lines = out.strip().splitlines()
+    assert lines[0] == f"version {L.pd_version()}"
+    mode, grid, ws = _lib.plan(_desc(B=32, H_qo=32, H_kv=8, nnz_pages=4608, max_pages=16384), 152, 2)
+    assert lines[1] == f"plan 0 schedule {mode} grid {grid} workspace {ws}"
+    assert lines[2].startswith(f"bad heads {invalid} ") and "H_kv" in lines[2]
+    assert lines[3] == f"bad flags {invalid}"
+    assert lines[4] == f"bad q_len {invalid}"
