@@ -183,3 +183,47 @@ def test_mq_sink_logits(splits):
         H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode, rope_scale=s.rope_scale,
         rope_theta=s.rope_theta, sm_scale=wl.sm_scale, sink=sk.cpu().numpy())
     compare("bf16", out, lse, ro, rl)
+
+
+@pytest.mark.parametrize("splits", [0, 3])
+def test_mq_fp8_interleaved_with_sinks(splits):
+    # the next-row features together: E4M3 cache, 2 query tokens, interleaved RoPE,
+    # per-head sinks, internal splits
+    q_len = 2
+    wl, Q = _mq("fp8_kv_highconc", 69, q_len, rotary_mode=2, rope_theta=1e4)
+    s = wl.spec
+    g = torch.Generator(device=DEV)
+    g.manual_seed(70)
+    sk = (torch.randn(s.H_qo, generator=g, device=DEV) * 3).float()
+    kw = dict(num_splits=splits, max_kv_len_hint=int(wl.attended.max())) if splits else {}
+    out, lse = _gpu(wl, Q, sink=sk, **kw)
+    assert pd.check_device_errors() == "PD_OK"
+    ro, rl, _ = oracle.batch_decode_paged_kv_mq(
+        W.bits(Q), W.bits(wl.pages), wl.indptr.cpu().numpy(), wl.values.cpu().numpy(),
+        wl.length_info.cpu().numpy(), wl.k_rope_pos_offset.cpu().numpy(),
+        wl.q_rope_position.cpu().numpy(), q_len=q_len, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
+        H_kv=s.H_kv, page_size=s.page_size, rotary_mode=2, rope_scale=s.rope_scale,
+        rope_theta=s.rope_theta, sm_scale=wl.sm_scale, k_scale=wl.k_scale, v_scale=wl.v_scale,
+        sink=sk.cpu().numpy())
+    compare("e4m3", out, lse, ro, rl)
+
+
+def test_mq_k_rotated_cache_with_sinks_and_early_inputs():
+    # K rotated in the cache (Q-only RoPE), sinks, two tokens, the decode started under
+    # the previous kernel: the synthetic cache stands for already-rotated K rows
+    q_len = 2
+    wl, Q = _mq("llama3_8b_bf16", 71, q_len)
+    s = wl.spec
+    g = torch.Generator(device=DEV)
+    g.manual_seed(72)
+    sk = (torch.randn(s.H_qo, generator=g, device=DEV) * 3).float()
+    out, lse = _gpu(wl, Q, sink=sk, k_rotated=True, early_inputs=True)
+    torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    ro, rl, _ = oracle.batch_decode_paged_kv_mq(
+        W.bits(Q), W.bits(wl.pages), wl.indptr.cpu().numpy(), wl.values.cpu().numpy(),
+        wl.length_info.cpu().numpy(), None, wl.q_rope_position.cpu().numpy(), q_len=q_len,
+        q_dtype=s.q_dtype, kv_dtype=s.kv_dtype, H_kv=s.H_kv, page_size=s.page_size,
+        rotary_mode=1, rope_scale=s.rope_scale, rope_theta=s.rope_theta, sm_scale=wl.sm_scale,
+        sink=sk.cpu().numpy(), k_rotated=True)
+    compare("bf16", out, lse, ro, rl)
