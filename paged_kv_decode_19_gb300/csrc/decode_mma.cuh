@@ -802,21 +802,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
 #pragma unroll
         for (int i = 0; i < 4; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], 2);
       }
-      // K registers are free: start the next tile's K loads
-      // next tile's K (after the last tile: this tile's block again, never used), then the
-      // L2 prefetch when a new piece starts
+      // K registers are free: start the next tile's K loads (after the last tile: this
+      // tile's block again, never used)
       const uint8_t* nk = nxt.kblk ? nxt.kblk : cur.kblk;
       const int nt = nxt.kblk ? nxt.t : cur.t;
       load_k(nk, nt);
-      {
-        const int jpf = nxt.piece + kPrefetchPieces;
-        const bool pf = nxt.kblk && nxt.piece != cur.piece && jpf < pend && jpf < pb_base + 32;
-        const int pg = __shfl_sync(0xffffffffu, pb_page, min(max(jpf - pb_base, 0), 31));
-        if (pf && pg >= 0 && lane == 0) {
-          prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
-          prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
-        }
-      }
       // ------------------------------------------------------------ online softmax (log2)
       float sc[4];
       sc[0] = v0 ? acc[0] * post_scale : -INFINITY;  // row g_id, heads 2q, 2q+1
@@ -913,6 +903,18 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
         Mma<MT>::run(oacc[mt], a, pb0, pb1);
       }
       load_v(nk, nt);
+      // The L2 prefetch of the page kPrefetchPieces ahead goes out when a new piece starts,
+      // behind the next tile's K and V loads so that it does not delay them
+      // (llama3 decode 65.4 -> 63.7 us, window 108.9 -> 106.7 us, alternating replicas).
+      {
+        const int jpf = nxt.piece + kPrefetchPieces;
+        const bool pf = nxt.kblk && nxt.piece != cur.piece && jpf < pend && jpf < pb_base + 32;
+        const int pg = __shfl_sync(0xffffffffu, pb_page, min(max(jpf - pb_base, 0), 31));
+        if (pf && pg >= 0 && lane == 0) {
+          prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
+          prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
+        }
+      }
       cur = nxt;
     }
   };
