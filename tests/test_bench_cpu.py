@@ -92,3 +92,26 @@ def test_spec_decode_workload_shapes_and_positions():
     # token t of a sequence sits at its own row's position: L - q_len + t
     assert (wl.q_rope_position.numpy() == (wl.attended - 2).clip(min=0)).all()
     assert wl.io_bytes() == 2 * W.make("llama3_8b_bf16", seed=6, reduced=True, device="cpu").io_bytes()
+
+
+def test_oracle_samples_single_and_threaded_cover_whole_sequences():
+    """Both CPU-baseline samples decode whole sequences: with an ample budget every
+    sequence is done exactly once and the attended rows add up; with no budget the
+    single-thread sample stops after one sequence and the threaded one after its first
+    wave (one sequence per thread)."""
+    from paged_kv_decode_19_gb300 import workloads as W
+    wl = W.make("llama3_8b_bf16", seed=7, reduced=True, device="cpu", B=5,
+                len_dist=("uniform", 1, 60))
+    total = int(wl.attended.sum())
+    _, n1, r1 = bench._oracle_sample(wl, 1e9)
+    _, n3, r3 = bench._oracle_sample_threads(wl, 1e9, 3)
+    assert (n1, r1) == (5, total) and (n3, r3) == (5, total)
+    _, n1, r1 = bench._oracle_sample(wl, 0.0)
+    assert (n1, r1) == (1, int(wl.attended[0]))
+    _, n3, r3 = bench._oracle_sample_threads(wl, 0.0, 3)
+    assert (n3, r3) == (3, int(wl.attended[:3].sum()))  # the first wave, nothing after it
+    line = bench._cpu_baseline(wl, 1e9)
+    assert line["kind"] == "oracle" and line["cores"] == 1 and line["value"] > 0
+    if bench._host_cores() > 1:
+        assert line["all_cores"]["cores"] == bench._host_cores()
+        assert line["all_cores"]["value"] > 0
