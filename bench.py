@@ -264,6 +264,45 @@ def _append_inputs(wl: W.Workload, device):
     return k, v, torch.from_numpy(slots.astype(np.int64)).to(device)
 
 
+def _external_split(w: "W.Workload", nsplit: int, dev):
+    """Inputs of the multi-stage form of a long-context decode: each sequence's page list
+    cut into nsplit page-aligned chunks, decoded as nsplit * B pseudo-sequences (chunk
+    j of sequence b at j * B + b, Q repeated) into fp32 partial states."""
+    s = w.spec
+    ipc, valc, lastc, roff = W.split_chunks_padded(w.indptr.cpu().numpy(),
+                                                   w.values.cpu().numpy(), w.seq_len,
+                                                   s.page_size, nsplit)
+    kro = np.tile(w.k_rope_pos_offset.cpu().numpy(), nsplit) + roff
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)
+    n = nsplit * s.B
+    return {"Q": w.Q.repeat(nsplit, 1, 1).contiguous(), "indptr": t(ipc), "values": t(valc),
+            "length_info": t(lastc), "k_rope_pos_offset": t(kro),
+            "q_rope_position": w.q_rope_position.repeat(nsplit).contiguous(),
+            "out": torch.empty((n, s.H_qo, s.D), dtype=torch.float32, device=dev),
+            "lse": torch.empty((n, s.H_qo), dtype=torch.float32, device=dev)}
+
+
+def _merge_tree(out, lse, nsplit: int, B: int, merge):
+    """log2(nsplit) rounds of the pairwise merge: the first half of the chunk-major
+    partial states absorbs the second half, so sequence b ends in row b."""
+    half = nsplit
+    while half > 1:
+        half //= 2
+        n = half * B
+        merge(out[:n], lse[:n], out[n:2 * n], lse[n:2 * n])
+    return out[:B], lse[:B]
+
+
+def run_external_split(pd, w, x, nsplit: int):
+    """The multi-stage decode of one workload: chunk decode, then the merge tree."""
+    s = w.spec
+    pd.batch_decode_paged_kv(x["Q"], w.pages, x["indptr"], x["values"], x["length_info"],
+                             x["k_rope_pos_offset"], x["q_rope_position"], x["out"], x["lse"],
+                             s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
+                             k_scale=w.k_scale, v_scale=w.v_scale, num_splits=1)
+    return _merge_tree(x["out"], x["lse"], nsplit, s.B, pd.merge_state_inplace)
+
+
 def run_ours(args, ws, rank, local):
     import paged_kv_decode_19_gb300 as pd
 
@@ -395,6 +434,39 @@ def run_ours(args, ws, rank, local):
     # the same steps after a flush of L2 (for comparison; not the reported value)
     _, dec_flushed_ms, _ = timed_steps(max(args.steps // 2, 3), flush=True, breakdown=True)
 
+    # the multi-stage form of the same decode (for comparison; not the reported value):
+    # page-aligned chunks decoded as pseudo-sequences into fp32 partials, then the
+    # pairwise merge tree; one event pair around each stage, replicas alternating
+    ext = None
+    nsplit = s.max_splits
+    if nsplit > 1 and s.window is None and s.q_len == 1 and not s.k_rotated:
+        assert nsplit & (nsplit - 1) == 0, "the merge tree halves the chunk count"
+        xs = [_external_split(r[0], nsplit, dev) for r in reps]
+        for i in range(2):
+            run_external_split(pd, reps[i][0], xs[i], nsplit)
+        n = max(args.steps // 2, 3)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        prefill(n)
+        for i in range(n):
+            w, x = reps[i % 2][0], xs[i % 2]
+            if not alternate:
+                flush_l2()
+            ev[i][0].record(stream)
+            pd.batch_decode_paged_kv(x["Q"], w.pages, x["indptr"], x["values"],
+                                     x["length_info"], x["k_rope_pos_offset"],
+                                     x["q_rope_position"], x["out"], x["lse"], s.rotary_mode,
+                                     s.rope_scale, s.rope_theta, w.sm_scale, k_scale=w.k_scale,
+                                     v_scale=w.v_scale, num_splits=1)
+            ev[i][1].record(stream)
+            _merge_tree(x["out"], x["lse"], nsplit, s.B, pd.merge_state_inplace)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        assert pd.check_device_errors() == "PD_OK"
+        ext = {"nsplit": nsplit,
+               "decode_us": statistics.mean(e[0].elapsed_time(e[1]) for e in ev) * 1e3,
+               "merge_tree_us": statistics.mean(e[1].elapsed_time(e[2]) for e in ev) * 1e3}
+        del xs
+
     # end-to-end through the public API from pinned host memory: every step copies its
     # inputs (one pinned staging buffer holding Q, the page table, length_info, the RoPE
     # positions and the new tokens' K/V and slots) to the device, runs append + decode on
@@ -456,7 +528,8 @@ def run_ours(args, ws, rank, local):
                dec_med=statistics.median(dec_ms), app=statistics.mean(app_ms),
                dec_flushed=statistics.mean(dec_flushed_ms),
                e2e=statistics.mean(e2e_ms), launches=launches, variant=variant,
-               clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h, alternate=alternate, l2=l2)
+               clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h, alternate=alternate, l2=l2,
+               ext=ext)
     return res
 
 
@@ -576,6 +649,17 @@ def main():
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
     }
+    if res["ext"]:
+        e = res["ext"]
+        line["multi_stage"] = {
+            "chunks": e["nsplit"], "decode_us": round(e["decode_us"], 2),
+            "merge_tree_us": round(e["merge_tree_us"], 2),
+            "total_us": round(e["decode_us"] + e["merge_tree_us"], 2),
+            "what": (f"each sequence cut into {e['nsplit']} page-aligned chunks, decoded as "
+                     f"{e['nsplit']} x B pseudo-sequences into fp32 partial states (one "
+                     f"launch), then {e['nsplit'].bit_length() - 1} rounds of "
+                     "merge_state_inplace; compare decode_us (the split merged inside the "
+                     "decode launch)")}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(wl, args.cpu_budget)
     print(json.dumps(line))

@@ -288,3 +288,35 @@ def split_chunks(indptr: np.ndarray, values: np.ndarray, seq_len: np.ndarray, pa
             owner.append(b)
     return (np.array(ip, np.int32), np.array(vals, np.int32), np.array(last, np.int32),
             np.array(koff, np.int32), np.array(owner, np.int64))
+
+
+def split_chunks_padded(indptr: np.ndarray, values: np.ndarray, seq_len: np.ndarray,
+                        page_size: int, nsplit: int):
+    """The same page-aligned split, laid out chunk-major and padded: pseudo-sequence
+    j * B + b is chunk j of sequence b (pages [j*per, (j+1)*per) of its list, per =
+    ceil(npages / nsplit)), and a chunk past the end of the list has no pages.  An empty
+    pseudo-sequence decodes to the merge identity (out 0, lse -5e4), so a pairwise merge
+    of the first half of the chunks with the second, halving log2(nsplit) times, leaves
+    each sequence's result in pseudo-sequence b.  A pure re-indexing of the page table.
+
+    Returns (indptr_c [nsplit*B+1], values_c, last_c [nsplit*B], row_off_c [nsplit*B]):
+    row_off_c is the chunk's first row in its sequence.
+    """
+    P = page_size
+    B = len(seq_len)
+    npg = (indptr[1:] - indptr[:-1]).astype(np.int64)
+    per = np.maximum(1, -(-npg // nsplit))
+    ip, vals = [0], []
+    last = np.zeros(nsplit * B, np.int32)
+    roff = np.zeros(nsplit * B, np.int32)
+    for j in range(nsplit):
+        for b in range(B):
+            p0 = min(int(npg[b]), j * int(per[b]))
+            p1 = min(int(npg[b]), p0 + int(per[b]))
+            vals.extend(values[indptr[b] + p0: indptr[b] + p1].tolist())
+            ip.append(len(vals))
+            if p1 > p0:
+                rows = min(int(seq_len[b]), p1 * P) - p0 * P
+                last[j * B + b] = rows - (p1 - p0 - 1) * P
+                roff[j * B + b] = p0 * P
+    return np.array(ip, np.int32), np.array(vals, np.int32), last, roff

@@ -115,3 +115,61 @@ def test_oracle_samples_single_and_threaded_cover_whole_sequences():
     if bench._host_cores() > 1:
         assert line["all_cores"]["cores"] == bench._host_cores()
         assert line["all_cores"]["value"] > 0
+
+
+def test_padded_chunk_split_layout():
+    """Chunk j of sequence b sits at j * B + b; the chunks of a sequence hold its page
+    list once, in order, and their rows add up to its length; a chunk past the end of
+    the list has no pages."""
+    import numpy as np
+    from paged_kv_decode_19_gb300 import workloads as W
+    wl = W.make("long_ctx_bf16", seed=2, reduced=True, device="cpu")
+    ip, vals, B = wl.indptr.numpy(), wl.values.numpy(), wl.spec.B
+    for nsplit in (1, 4, 32):
+        ipc, valc, lastc, roff = W.split_chunks_padded(ip, vals, wl.seq_len, 16, nsplit)
+        assert len(ipc) == nsplit * B + 1 and len(lastc) == len(roff) == nsplit * B
+        for b in range(B):
+            sel = [j * B + b for j in range(nsplit)]
+            got = np.concatenate([valc[ipc[i]:ipc[i + 1]] for i in sel])
+            assert np.array_equal(got, vals[ip[b]:ip[b + 1]])
+            rows, start = 0, 0
+            for i in sel:
+                n = ipc[i + 1] - ipc[i]
+                if n == 0:
+                    continue
+                assert roff[i] == start and 1 <= lastc[i] <= 16
+                start += n * 16
+                rows += (n - 1) * 16 + lastc[i]
+            assert rows == wl.seq_len[b]
+
+
+def test_multi_stage_flow_equals_unsplit_decode_in_the_oracle():
+    """The bench's multi-stage flow, run with the oracle on both stages (chunk decode of
+    the padded pseudo-sequences with RoPE offsets, then the halving merge tree), equals
+    the oracle's unsplit decode: the re-indexing and the tree drop or repeat no row."""
+    import numpy as np
+    import oracle
+    from paged_kv_decode_19_gb300 import workloads as W
+    wl = W.make("llama3_8b_bf16", seed=8, reduced=True, device="cpu", B=3,
+                len_dist=("uniform", 1, 150))
+    s, nsplit = wl.spec, 8
+    x = bench._external_split(wl, nsplit, "cpu")
+    kw = dict(q_dtype=s.q_dtype, kv_dtype=s.kv_dtype, H_kv=s.H_kv, page_size=s.page_size,
+              rotary_mode=s.rotary_mode, rope_scale=s.rope_scale, rope_theta=s.rope_theta,
+              sm_scale=wl.sm_scale)
+    out, lse, st = oracle.batch_decode_paged_kv(
+        W.bits(x["Q"]), W.bits(wl.pages), x["indptr"].numpy(), x["values"].numpy(),
+        x["length_info"].numpy(), x["k_rope_pos_offset"].numpy(),
+        x["q_rope_position"].numpy(), **kw)
+    assert st == 0
+
+    def merge(V, S, Vo, So):
+        V[...], S[...] = oracle.merge_state(V, S, Vo, So)
+
+    got_o, got_l = bench._merge_tree(out, lse, nsplit, s.B, merge)
+    ro, rl, st = oracle.batch_decode_paged_kv(
+        W.bits(wl.Q), W.bits(wl.pages), wl.indptr.numpy(), wl.values.numpy(),
+        wl.length_info.numpy(), wl.k_rope_pos_offset.numpy(), wl.q_rope_position.numpy(), **kw)
+    assert st == 0
+    np.testing.assert_allclose(got_o, ro, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got_l, rl, rtol=0, atol=1e-12)

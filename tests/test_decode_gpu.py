@@ -89,6 +89,20 @@ def test_long_context_external_split_merge_tree():
     compare("bf16", out[first], lse[first], ro, rl)
 
 
+def test_long_context_multi_stage_flow_of_the_bench():
+    """The multi-stage flow the benchmark times beside the fused decode (32 padded
+    chunk-major pseudo-sequences, fp32 partials, 5 halving merge rounds) against the
+    oracle's unsplit decode."""
+    import bench
+    wl = _wl("long_ctx_bf16", 3)
+    x = bench._external_split(wl, 32, DEV)
+    out, lse = bench.run_external_split(pd, wl, x, 32)
+    assert pd.check_device_errors() == "PD_OK"
+    ro, rl, st = oracle_decode(wl)
+    assert st == 0
+    compare("bf16", out, lse, ro, rl)
+
+
 @pytest.mark.parametrize("seed", [0, 5])
 def test_window_sink_f16(seed):
     _check(_wl("window_sink_f16", seed), "mma")

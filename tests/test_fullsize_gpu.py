@@ -88,3 +88,22 @@ def _fullsize_multi_query(wl):
         rope_theta=s.rope_theta, sm_scale=wl.sm_scale, mask=mask)
     assert st == 0
     compare(kind_of(wl), out, lse, ro, rl, mask=mask)
+
+
+def test_fullsize_multi_stage_long_ctx():
+    """The benchmark's multi-stage form of the long-context decode at full size: sampled
+    outputs against the oracle, and every output against the fused decode."""
+    import bench
+    wl = W.make("long_ctx_bf16", seed=SEED, device=DEV)
+    s = wl.spec
+    x = bench._external_split(wl, s.max_splits, DEV)
+    out, lse = bench.run_external_split(pd, wl, x, s.max_splits)
+    assert pd.check_device_errors() == "PD_OK"
+    fo, fl = gpu_decode(wl)
+    assert pd.check_device_errors() == "PD_OK"
+    assert (out - fo.float()).abs().max().item() <= 2e-2
+    assert (lse - fl).abs().max().item() <= 2e-3
+    mask = _sample_mask(wl)
+    ro, rl, st = oracle_decode(wl, mask=mask)
+    assert st == 0
+    compare("bf16", out, lse, ro, rl, mask=mask)
