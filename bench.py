@@ -13,10 +13,16 @@ that fit in L2: the L2 is flushed before every timed step (a 2x-L2 buffer writte
 then another read, leaving it cold and clean) and each step has its own events.  A
 second pass of the same steps puts events between the kernels, which times each
 kernel alone (decode_us, append_us and the roofline).  The flushed decode time of the
-large workloads is reported as well (decode_us_l2_flushed).  `e2e` re-times the step through the public API from pinned
-host buffers (H2D of the step's inputs and D2H of out + lse inside the timed region).
+large workloads is reported as well (decode_us_l2_flushed).  `e2e` re-times the step
+through the public API from pinned host buffers (H2D of the step's inputs and D2H of out + lse inside the timed region).
 Before each timed pass a spin kernel keeps the device busy while the host enqueues the
 pass, so device-side times carry no host launch gaps.
+
+A workload with an external split count (the long-context one) also reports
+`multi_stage`: the same decode as page-aligned chunks decoded into fp32 partial states,
+then a tree of merge_state_inplace calls, each stage timed with its own events.  The
+`cpu_baseline` holds the fp64 oracle timed on one thread and, as `all_cores`, on one
+thread per host core.
 
 --impl reference times the fp64 oracle (the CPU baseline) on a bounded sample.
 Under torchrun every rank runs its own replica of the workload (no collective on the
