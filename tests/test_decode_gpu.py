@@ -276,6 +276,30 @@ def test_edge_rope_short_rows_large_positions(dt):
         assert rms <= 6e-4, rms
 
 
+@pytest.mark.parametrize("P", [1, 3, 32, 48, 64, 128, 256])
+@pytest.mark.parametrize("rope", [0, 1])
+def test_page_size_sweep(P, rope):
+    """Page sizes across the accepted range [1, 256]: multiples of 16 run on the
+    tensor-core kernel (several 16-row tiles per page, a partial last tile), the others
+    on the SIMT kernel; lengths of one row, a full page, a page plus one row, several
+    pages, and empty; whole sequences and forced splits."""
+    lens = [1, P, P + 1, 2 * P + 3, 5 * P - 1, 0, 7]
+    wl = _custom(lens, P=P, rope=rope, seed=P)
+    want = "mma" if P % 16 == 0 else "simt"
+    _check(wl, want)
+    _check(wl, want, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+
+
+@pytest.mark.parametrize("P", [48, 256])
+def test_page_size_window_sink(P):
+    """Sliding window and sink rows on pages of several tiles: the window start falls
+    inside a page and inside a tile."""
+    lens = [3 * P + 5, 2 * P, P + 40]
+    wl = _custom(lens, P=P, window=P + 21, sink=4, dt="f16", rope=1, seed=P + 1)
+    _check(wl, "mma")
+    _check(wl, "mma", num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+
+
 def test_edge_more_chunks_than_pages():
     wl = _custom([33, 5, 70])
     _check(wl, num_splits=64, max_kv_len_hint=70)

@@ -82,6 +82,15 @@ def test_mq_group_sweep(kv, D, group, q_len):
     _check(wl, Q, num_splits=4, max_kv_len_hint=300)
 
 
+@pytest.mark.parametrize("P,q_len", [(64, 3), (256, 5)])
+def test_mq_large_pages(P, q_len):
+    """Multi-query decode on pages of several 16-row tiles (the causal limit of the
+    new tokens then falls inside a tile of the last page)."""
+    wl, Q = _mq("llama3_8b_bf16", 50 + P, q_len, page_size=P, pool="fit")
+    _check(wl, Q)
+    _check(wl, Q, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+
+
 def test_mq_q_len_one_is_the_decode():
     wl, Q = _mq("llama3_8b_bf16", 61, 1)
     out1, lse1 = _gpu(wl, Q)
