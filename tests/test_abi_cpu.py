@@ -63,7 +63,11 @@ def _desc(**kw):
     (dict(out_dtype=3), "PD_ERR_INVALID_ARG"), (dict(kv_dtype=3, k_scale=0.0), "PD_ERR_INVALID_ARG"),
     (dict(kv_dtype=1), "PD_ERR_UNSUPPORTED"), (dict(num_splits=-2), "PD_ERR_INVALID_ARG"),
     (dict(max_pages=0), "PD_ERR_INVALID_ARG"), (dict(B=-1), "PD_ERR_INVALID_ARG"),
-    (dict(flags=4), "PD_ERR_INVALID_ARG"),
+    (dict(flags=4), "PD_ERR_INVALID_ARG"), (dict(page_size=257), "PD_ERR_INVALID_ARG"),
+    (dict(H_kv=0), "PD_ERR_INVALID_ARG"), (dict(nnz_pages=-1), "PD_ERR_INVALID_ARG"),
+    (dict(max_pages=1 << 30, H_kv=2, H_qo=8), "PD_ERR_UNSUPPORTED"),
+    (dict(kv_dtype=3, v_scale=float("inf")), "PD_ERR_INVALID_ARG"),
+    (dict(kv_dtype=3, k_scale=float("nan")), "PD_ERR_INVALID_ARG"),
 ])
 def test_decode_validation_without_gpu(L, bad, status):
     d = _desc(**bad)
