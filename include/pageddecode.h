@@ -63,7 +63,10 @@ typedef struct {
   int32_t H_qo;              /* query heads; must be a multiple of H_kv */
   int32_t H_kv;              /* KV heads; Q head h reads KV head h / (H_qo/H_kv) */
   int32_t D;                 /* head dim: 64, 128 or 256 */
-  int32_t page_size;         /* rows per page, P */
+  int32_t page_size;         /* rows per page, P: 1 to 256.  The tensor-core kernel runs
+                                P a multiple of 16 with F16/BF16 KV (D 64 or 128) or
+                                E4M3 KV (D 128, 16-bit Q); every other accepted shape
+                                runs on the SIMT kernel (pd_last_decode_variant) */
   int32_t q_dtype;           /* pd_dtype of Q: F32, F16 or BF16 */
   int32_t kv_dtype;          /* pd_dtype of pages: F32, F16, BF16 or E4M3 */
   int32_t out_dtype;         /* pd_dtype of output: F32, F16 or BF16 */
