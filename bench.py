@@ -182,7 +182,8 @@ def _cpu_baseline(wl: W.Workload, budget_s: float):
     line = {"value": round(us_per_call, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"fp64 oracle (single thread) on {nseq} of {wl.spec.B} sequences, all "
                       f"{wl.spec.H_qo} heads ({rows} of {total_rows} attended rows) in "
-                      f"{secs:.1f} s, scaled to the full batch by attended rows"}
+                      f"{secs:.1f} s, scaled to the full batch by attended rows (the decode; "
+                      f"the step's append is not timed)"}
     cores = _host_cores()
     if cores > 1:
         secs, nseq, rows = _oracle_sample_threads(wl, budget_s, cores)
@@ -599,7 +600,8 @@ def main():
                                  "kind": "oracle",
                                  "sample": "fp64 oracle, single thread: each step decodes one "
                                            "sequence (all heads) and is scaled to the batch by "
-                                           "attended rows"},
+                                           "attended rows; the step's append (one row per "
+                                           "sequence) is not timed"},
                 "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))

@@ -173,3 +173,24 @@ def test_multi_stage_flow_equals_unsplit_decode_in_the_oracle():
     assert st == 0
     np.testing.assert_allclose(got_o, ro, rtol=0, atol=1e-12)
     np.testing.assert_allclose(got_l, rl, rtol=0, atol=1e-12)
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` needs no GPU: it times the fp64 oracle and prints one
+    JSON line with the arm's metric, unit and config, marked as the reference."""
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl",
+                        "reference", "--config", "tiny_fp32", "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=600, cwd=bench.ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["higher_is_better"] is False and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["config"]["workload"].startswith("tiny_fp32:")
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
