@@ -64,6 +64,13 @@ class Spec:
     max_splits: int = 0        # external split count (long-context chunking)
     q_len: int = 1             # query tokens per sequence (multi-query decode, causal)
     k_rotated: bool = False    # the cache holds K rotated at append time (decode rotates Q only)
+    # Score-shaping stress inputs (both default off): every cached K row at sequence
+    # offset o is multiplied by 1 + k_ramp * o / (len - 1), so scores grow along the
+    # sequence and the running maximum of an online softmax keeps moving; Q is
+    # multiplied by q_gain (a peaked softmax).  Pure input scaling, applied before the
+    # cast to the cache / query type.
+    k_ramp: float = 0.0
+    q_gain: float = 1.0
 
 
 SPECS = {
@@ -183,6 +190,19 @@ def _cast_pool(x: torch.Tensor, dtype: str, scale: float) -> torch.Tensor:
     return x.to(TORCH_DTYPES[dtype])
 
 
+def _ramp_factors(values, indptr, seq_len, pool, P, ramp) -> torch.Tensor:
+    """[pool, P] float32 row factors: 1 + ramp * o / (len - 1) for the row at sequence
+    offset o of the sequence owning the page, 1 for rows of unused pages."""
+    f = np.ones((pool, P), np.float32)
+    for b in range(len(seq_len)):
+        n = int(indptr[b + 1] - indptr[b])
+        if n == 0:
+            continue
+        o = np.arange(n * P, dtype=np.float64).reshape(n, P)
+        f[values[indptr[b]:indptr[b + 1]]] = 1.0 + ramp * o / max(int(seq_len[b]) - 1, 1)
+    return torch.from_numpy(f)
+
+
 def make(name: str, seed: int = 0, reduced: bool = False, device="cpu", **overrides) -> Workload:
     """Draw the workload `name` with `seed` on `device` (torch generator of that device)."""
     s = spec(name, reduced, **overrides)
@@ -219,6 +239,8 @@ def make(name: str, seed: int = 0, reduced: bool = False, device="cpu", **overri
     gen = torch.Generator(device=device)
     gen.manual_seed(seed)
     x = _randn((pool, 2, s.H_kv, P, s.D), gen, device)
+    if s.k_ramp:
+        x[:, 0] *= _ramp_factors(values, indptr, seq_len, pool, P, s.k_ramp).to(device)[:, None, :, None]
     k_scale = v_scale = 1.0
     if s.kv_dtype == "e4m3":
         k_scale = float(x[:, 0].abs().max()) / E4M3_MAX
@@ -230,7 +252,10 @@ def make(name: str, seed: int = 0, reduced: bool = False, device="cpu", **overri
         pages = x.to(TORCH_DTYPES[s.kv_dtype])
     del x
     qshape = (s.B, s.H_qo, s.D) if s.q_len == 1 else (s.B, s.q_len, s.H_qo, s.D)
-    Q = _randn(qshape, gen, device).to(TORCH_DTYPES[s.q_dtype])
+    Q = _randn(qshape, gen, device)
+    if s.q_gain != 1.0:
+        Q *= s.q_gain
+    Q = Q.to(TORCH_DTYPES[s.q_dtype])
     k_new = v_new = slot_mapping = None
     if s.append:
         in_dt = TORCH_DTYPES[s.q_dtype]

@@ -57,3 +57,30 @@ def test_external_split_covers_every_page_once():
         assert np.array_equal(got, vals[ip[b]:ip[b + 1]])
         rows = sum((ipc[j + 1] - ipc[j] - 1) * 16 + lastc[j] for j in sel)
         assert rows == wl.seq_len[b]
+
+
+def test_stress_inputs_move_the_running_max():
+    """The score-shaping inputs do what the rescale tests rely on: along most (sequence,
+    head) rows, some later score exceeds the maximum of the first 16 rows by more than
+    2^8 (8 in log2 units), so an online softmax must rescale a non-empty state."""
+    l2e = 1.4426950408889634
+    for over in (dict(k_ramp=8.0), dict(q_gain=8.0), dict(k_ramp=4.0)):
+        wl = W.make("llama3_8b_bf16", seed=201, reduced=True, rotary_mode=0, H_kv=2, H_qo=8,
+                    **over)
+        s = wl.spec
+        Q = wl.Q.float().numpy()
+        pages = wl.pages.float().numpy()
+        ip, vals = wl.indptr.numpy(), wl.values.numpy()
+        moved = total = 0
+        for b in range(s.B):
+            L = int(wl.seq_len[b])
+            if L <= 16:
+                continue
+            rows = np.arange(L)
+            pg = vals[ip[b] + rows // s.page_size]
+            for h in range(s.H_qo):
+                K = pages[pg, 0, h // (s.H_qo // s.H_kv), rows % s.page_size]
+                sc = (K @ Q[b, h]) * wl.sm_scale * l2e
+                total += 1
+                moved += int(sc[16:].max() - sc[:16].max() > 8.0)
+        assert moved >= 0.5 * total, (over, moved, total)
