@@ -47,6 +47,9 @@ import torch  # noqa: E402
 
 from paged_kv_decode_19_gb300 import workloads as W  # noqa: E402
 
+# the five serving loads; one bench run times each of them (the headline is --config)
+PER_CONFIG = ("tiny_fp32", "llama3_8b_bf16", "long_ctx_bf16", "window_sink_f16",
+              "fp8_kv_highconc")
 METRIC = "paged decode attention µs/call and KV-read GB/s as % of GB300 HBM peak"
 UNIT = "us/call"
 
@@ -310,9 +313,11 @@ def run_external_split(pd, w, x, nsplit: int):
     return _merge_tree(x["out"], x["lse"], nsplit, s.B, pd.merge_state_inplace)
 
 
-def run_ours(args, ws, rank, local):
+def run_ours(args, ws, rank, local, config=None):
     import paged_kv_decode_19_gb300 as pd
 
+    config = config or args.config
+    over = args.over if config == args.config else {}
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     # Two replicas of the workload (same seed, separate device memory) alternate step by
@@ -322,7 +327,7 @@ def run_ours(args, ws, rank, local):
     # read: cold and clean).
     reps = []
     for _ in range(2):
-        wl = W.make(args.config, seed=1000 + rank, device=dev, **args.over)
+        wl = W.make(config, seed=1000 + rank, device=dev, **over)
         reps.append((wl,) + _append_inputs(wl, dev))
     wl = reps[0][0]
     s = wl.spec
@@ -333,7 +338,7 @@ def run_ours(args, ws, rank, local):
     lse = torch.empty(qdims + (s.H_qo,), dtype=torch.float32, device=dev)
     # q_len query tokens per sequence: the multi-query entry point
     decode_api = pd.batch_decode_paged_kv if s.q_len == 1 else pd.batch_decode_paged_kv_mq
-    split = dict(num_splits=1) if args.config == "tiny_fp32" else {}
+    split = dict(num_splits=1) if config == "tiny_fp32" else {}
     stream = torch.cuda.current_stream(dev)
     wbuf = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     rbuf = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.float32, device=dev)
@@ -560,6 +565,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time the --config workload alone (no per_config block)")
     ap.add_argument("--B", type=int, default=None,
                     help="override the batch size (smaller cases for profiling)")
     args = ap.parse_args()
@@ -587,10 +594,12 @@ def main():
         wl = W.make(args.config, seed=1000, **args.over)
         for _ in range(args.warmup):
             _oracle_sample(wl, 0.0)
-        times = []
+        times, secs_timed, rows_timed = [], 0.0, 0
         for _ in range(args.steps):
             secs, nseq, rows = _oracle_sample(wl, 0.0)  # one sequence per step
             times.append(secs * 1e6 * int(wl.attended.sum()) / max(rows, 1))
+            secs_timed += secs
+            rows_timed += rows
         v = statistics.mean(times)
         line = {"metric": METRIC, "value": round(v, 1), "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(v / 1e3, 3),
@@ -603,45 +612,91 @@ def main():
                                            "attended rows; the step's append (one row per "
                                            "sequence) is not timed"},
                 "e2e": {"value": round(v, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
-                        "d2h_bytes_per_step": 0}}
+                        "d2h_bytes_per_step": 0},
+                # the value is not a measured whole call: each step times one sequence and
+                # scales it to the batch by attended rows
+                "value_is_scaled": True,
+                "scaling_of_value": {"rows_per_call": int(wl.attended.sum()),
+                                     "rows_timed_per_step": round(rows_timed / max(args.steps, 1), 1),
+                                     "seconds_timed_per_step": round(secs_timed / max(args.steps, 1), 3)}}
         print(json.dumps(line))
         return
 
     if ws > 1:
         torch.distributed.init_process_group("nccl")
     res = run_ours(args, ws, rank, local)
-    step_us = _max_over_ranks(res["step"] * 1e3, ws)
-    dec_us = _max_over_ranks(res["dec"] * 1e3, ws)
-    e2e_us = _max_over_ranks(res["e2e"] * 1e3, ws)
+    head = _summarise(res, args.config, spec, ws)
+    # the other serving loads, each in its own pass (their own replicas, warm-up and
+    # timed steps), reported beside the headline in `per_config`
+    per = {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            if name == args.config:
+                continue
+            torch.cuda.empty_cache()
+            r = run_ours(args, ws, rank, local, config=name)
+            per[name] = _summarise(r, name, W.spec(name), ws)
+            del r
     if rank != 0:
         torch.distributed.destroy_process_group() if ws > 1 else None
         return
     wl = res["wl"]
-    cfg["l2"] = (f"inputs larger than L2 ({wl.kv_bytes_attended() / 1e6:.0f} MB attended KV vs "
-                 f"{res['l2'] / 1e6:.0f} MB L2): two replicas alternate, no flush; the "
-                 "steps run back to back between one pair of events"
-                 if res["alternate"] else
-                 "flushed before every timed step: 2x L2 written, then 2x L2 read (cold, clean L2)")
+    cfg["l2"] = head.pop("l2")
     cfg["timing"] = ("CUDA events on the launching stream; each timed pass is enqueued "
                      "behind a spin kernel, so it runs without host launch gaps")
-    kv_bytes = wl.kv_bytes_attended()
-    alg_bytes = kv_bytes + wl.io_bytes()
-    peak, peak_kind = _peaks()
-    achieved = alg_bytes / (dec_us * 1e-6) / 1e9
     line = {
         "metric": METRIC,
-        "value": round(step_us / ws, 2),
+        # per-call time of the step (append + decode), the slowest replica's: every rank
+        # decodes its own full batch, so the time per call does not shrink with N
+        "value": head["step_us"],
         "unit": UNIT,
         "n_gpus": ws,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(step_us / 1e3, 5),
+        "ms_per_step": round(head["step_us"] / 1e3, 5),
         "higher_is_better": False,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": spec.kv_dtype,
         "data": "synthetic",
         "config": cfg,
+        "decode_us": head["decode_us"],
+        "decode_us_l2_flushed": head["decode_us_l2_flushed"],
+        "append_us": head["append_us"],
+        "kv_read_gbs": head["kv_read_gbs"],
+        "decode_variant": head["decode_variant"],
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": res["launches"] + sum(p["gpu_launches"] for p in per.values()),
+        "clocks": head["clocks"],
+    }
+    if ws > 1:
+        line["aggregate_calls_per_s"] = round(ws * 1e6 / head["step_us"], 1)
+    if "multi_stage" in head:
+        line["multi_stage"] = head["multi_stage"]
+    if per:
+        line["per_config"] = per
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = _cpu_baseline(wl, args.cpu_budget)
+    print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def _summarise(res, config: str, spec, ws: int) -> dict:
+    """The bench numbers of one workload's pass (times are the maximum over ranks)."""
+    step_us = _max_over_ranks(res["step"] * 1e3, ws)
+    dec_us = _max_over_ranks(res["dec"] * 1e3, ws)
+    e2e_us = _max_over_ranks(res["e2e"] * 1e3, ws)
+    wl = res["wl"]
+    kv_bytes = wl.kv_bytes_attended()
+    alg_bytes = kv_bytes + wl.io_bytes()
+    peak, peak_kind = _peaks()
+    achieved = alg_bytes / (dec_us * 1e-6) / 1e9
+    out = {
+        "workload": f"{config}: B={spec.B}, H_qo={spec.H_qo}, H_kv={spec.H_kv}, D={spec.D}, "
+                    f"page_size={spec.page_size}, {spec.kv_dtype} KV",
+        "step_us": round(step_us, 2),
         "decode_us": round(dec_us, 2),
         "decode_us_l2_flushed": round(res["dec_flushed"] * 1e3, 2),
         "append_us": round(res["app"] * 1e3, 2),
@@ -649,17 +704,22 @@ def main():
         "decode_variant": res["variant"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "traffic": _measured_traffic(args.config, spec.B),
+                     "traffic": _measured_traffic(config, spec.B),
                      "kernel": f"decode_{res['variant']}_kernel",
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
-        "e2e": {"value": round(e2e_us / ws, 2), "unit": UNIT,
+        "e2e": {"value": round(e2e_us, 2), "unit": UNIT,
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
+        "l2": (f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB attended KV vs "
+               f"{res['l2'] / 1e6:.0f} MB L2): two replicas alternate, no flush; the "
+               "steps run back to back between one pair of events"
+               if res["alternate"] else
+               "flushed before every timed step: 2x L2 written, then 2x L2 read (cold, clean L2)"),
     }
     if res["ext"]:
         e = res["ext"]
-        line["multi_stage"] = {
+        out["multi_stage"] = {
             "chunks": e["nsplit"], "decode_us": round(e["decode_us"], 2),
             "merge_tree_us": round(e["merge_tree_us"], 2),
             "total_us": round(e["decode_us"] + e["merge_tree_us"], 2),
@@ -668,11 +728,7 @@ def main():
                      f"launch), then {e['nsplit'].bit_length() - 1} rounds of "
                      "merge_state_inplace; compare decode_us (the split merged inside the "
                      "decode launch)")}
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = _cpu_baseline(wl, args.cpu_budget)
-    print(json.dumps(line))
-    if ws > 1:
-        torch.distributed.destroy_process_group()
+    return out
 
 
 if __name__ == "__main__":

@@ -18,13 +18,27 @@ def _free_port():
         return s.getsockname()[1]
 
 
+def _fake_res(step_ms, dec_ms):
+    """A pass result as run_ours returns it, for a small CPU workload."""
+    from paged_kv_decode_19_gb300 import workloads as W
+    wl = W.make("llama3_8b_bf16", seed=3, reduced=True, device="cpu", B=2,
+                len_dist=("uniform", 5, 20))
+    return dict(step=step_ms, dec=dec_ms, dec_med=dec_ms, app=0.005, dec_flushed=dec_ms,
+                e2e=2 * step_ms, launches=40, variant="mma", clocks=None, wl=wl, h2d=10,
+                d2h=20, alternate=True, l2=1 << 27, ext=None)
+
+
 def _rank_main(rank, ws, port, q):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
                       WORLD_SIZE=str(ws))
     dist.init_process_group("gloo", rank=rank, world_size=ws)
     try:
         # each replica reports its own time; every rank learns the slowest
-        q.put((rank, bench._max_over_ranks(10.0 + 5.0 * rank, ws), bench._dist()))
+        mx = bench._max_over_ranks(10.0 + 5.0 * rank, ws)
+        # replicas: the per-call times are the slowest rank's, not divided by the ranks
+        res = _fake_res(0.060 + 0.004 * rank, 0.050 + 0.004 * rank)
+        summ = bench._summarise(res, "llama3_8b_bf16", res["wl"].spec, ws)
+        q.put((rank, mx, bench._dist(), summ["step_us"], summ["decode_us"], summ["e2e"]["value"]))
     finally:
         dist.destroy_process_group()
 
@@ -42,10 +56,24 @@ def test_max_over_ranks_two_gloo_ranks():
         assert p.exitcode == 0
     assert [g[1] for g in got] == [15.0, 15.0]
     assert [g[2][:2] for g in got] == [(2, 0), (2, 1)]  # (world size, rank) from the env
+    for g in got:
+        assert g[3] == 64.0 and g[4] == 54.0 and g[5] == 128.0
 
 
 def test_single_rank_is_identity():
     assert bench._max_over_ranks(3.5, 1) == 3.5
+
+
+def test_summary_of_one_pass():
+    """Per-call times in microseconds from the pass's milliseconds; the roofline divides
+    the algorithmic bytes (attended K + V, Q, out, lse) by the decode time."""
+    res = _fake_res(0.060, 0.050)
+    s = bench._summarise(res, "llama3_8b_bf16", res["wl"].spec, 1)
+    assert s["step_us"] == 60.0 and s["decode_us"] == 50.0 and s["e2e"]["value"] == 120.0
+    alg = res["wl"].kv_bytes_attended() + res["wl"].io_bytes()
+    assert s["roofline"]["algorithmic_bytes"] == alg
+    assert abs(s["roofline"]["achieved"] - alg / 50e-6 / 1e9) < 0.1
+    assert "multi_stage" not in s and s["l2"].startswith("inputs larger than L2")
 
 
 def test_traffic_record_only_for_matching_sources(tmp_path, monkeypatch):
@@ -194,3 +222,5 @@ def test_reference_arm_prints_the_contract_line():
     assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    assert d["value_is_scaled"] is True
+    assert d["scaling_of_value"]["rows_per_call"] > d["scaling_of_value"]["rows_timed_per_step"] > 0
