@@ -162,10 +162,17 @@ typedef struct {
  * once to f16, so a bf16 cache must keep |k| below 46000.  f32 caches run an fp32
  * kernel without tensor cores.
  * Workspace: desc->workspace if non-NULL (at least pd_workspace_size(desc) bytes,
- * 256-byte aligned, zero-filled before its first use — see pd_workspace_init),
- * otherwise a per-device buffer the library allocates on first use and grows as
- * needed (allocation happens on the calling thread; do the first call of a given
- * size outside CUDA-graph capture).
+ * 256-byte aligned, zero-filled before its first use — see pd_workspace_init; the
+ * caller must not let two calls that share it overlap on the GPU), otherwise the
+ * library's workspace for `stream`: one arena per stream (per process-unique stream
+ * id) on the current device, allocated stream-ordered (cudaMallocAsync) on the first
+ * split call on that stream and grown stream-ordered when a larger batch needs more
+ * (the new buffer is allocated first, the old one released with cudaFreeAsync on the
+ * stream, after the work already enqueued there).  So decodes in flight on different
+ * streams never share split scratch, and any host threads may call concurrently; a
+ * per-device lock is held from the arena's hand-out until the kernel is enqueued.  Do
+ * the first call of a given size on a stream outside CUDA-graph capture.  An arena
+ * lives until pd_release_stream_workspace(stream) or process exit.
  * Returns PD_OK once the work is enqueued.
  */
 pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
@@ -287,6 +294,15 @@ pd_status pd_append_paged_kv_rope(void* pages, const void* k_new, const void* v_
                                   int64_t max_pages, int32_t in_dtype, int32_t kv_dtype,
                                   float k_scale, float v_scale, int32_t rotary_mode,
                                   float rope_scale, float rope_theta, pd_stream_t stream);
+
+/*
+ * Releases the library-managed decode workspace of `stream` on the current device
+ * (stream-ordered: cudaFreeAsync on `stream`, after the work already enqueued there).
+ * A later split decode on the stream allocates a new one.  Call it before destroying a
+ * stream that ran split decodes with desc->workspace == NULL, if the process keeps
+ * creating streams.  No arena for the stream: PD_OK, nothing is done.
+ */
+pd_status pd_release_stream_workspace(pd_stream_t stream);
 
 /* Bytes of workspace pd_batch_decode_paged_kv needs for `desc` on the current device
  * (0 on invalid desc).  Host-only apart from reading the device's SM count. */

@@ -16,6 +16,7 @@ from ._lib import (  # noqa: F401
     make_desc,
     merge_state_inplace,
     plan,
+    release_stream_workspace,
     version,
     workspace_init,
     workspace_size,

@@ -50,6 +50,7 @@ EXPORTS = (
     "pd_append_paged_kv",
     "pd_workspace_size",
     "pd_workspace_init",
+    "pd_release_stream_workspace",
     "pd_plan",
     "pd_check_device_errors",
     "pd_last_decode_variant",
@@ -122,6 +123,8 @@ def lib():
             L.pd_workspace_size.restype = ctypes.c_size_t
             L.pd_workspace_init.argtypes = [P, ctypes.c_size_t, P]
             L.pd_workspace_init.restype = i32
+            L.pd_release_stream_workspace.argtypes = [P]
+            L.pd_release_stream_workspace.restype = i32
             L.pd_plan.argtypes = [ctypes.POINTER(DecodeDesc), i32, i32, ctypes.POINTER(i32),
                                   ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_size_t)]
             L.pd_plan.restype = i32
@@ -298,6 +301,12 @@ def append_paged_kv_rope(pages, k_new, v_new, slot_mapping, positions, rotary_mo
         max_pages, DTYPE_CODES[k_new.dtype], DTYPE_CODES[pages.dtype], float(k_scale),
         float(v_scale), int(rotary_mode), float(rope_scale), float(rope_theta), _stream(stream)))
     return pages
+
+
+def release_stream_workspace(stream=None):
+    """pd_release_stream_workspace: frees the library-managed workspace of `stream`
+    (stream-ordered)."""
+    _check(lib().pd_release_stream_workspace(_stream(stream)))
 
 
 def workspace_init(ws: torch.Tensor, stream=None):

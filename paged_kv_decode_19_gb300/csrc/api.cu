@@ -10,6 +10,7 @@
 #include <mutex>
 #include <string>
 
+#include "arena.h"
 #include "kernels.h"
 #include "pageddecode.h"
 
@@ -48,10 +49,10 @@ struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   unsigned* err = nullptr;
-  void* cnt = nullptr;  // split arrival counters (kept at zero between calls)
-  size_t cnt_bytes = 0;
-  void* ws = nullptr;   // partial (out, lse) of split sequences
-  size_t ws_bytes = 0;
+  // library-managed workspace: one arena per stream (arena.h); ws_mu is held from an
+  // arena's hand-out until the kernel that uses it is enqueued
+  std::mutex ws_mu;
+  ArenaTable arenas;
   // resident blocks per SM of each kernel variant, queried once:
   // [mma][q_dtype][kv_dtype][D 64/128/256][kernel RoPE mode 0..4][multi-query]; 0 = not yet known
   int occupancy[2][4][4][3][5][2] = {};
@@ -89,6 +90,16 @@ static int elem_bytes(int dt) {
 }
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Stream-ordered allocator operations of the per-stream workspace arenas.
+static int arena_alloc(void*, void** p, size_t bytes, void* st) {
+  return (int)cudaMallocAsync(p, bytes, (cudaStream_t)st);
+}
+static int arena_release(void*, void* p, void* st) { return (int)cudaFreeAsync(p, (cudaStream_t)st); }
+static int arena_zero(void*, void* p, size_t bytes, void* st) {
+  return (int)cudaMemsetAsync(p, 0, bytes, (cudaStream_t)st);
+}
+static const ArenaOps kCudaArenaOps = {nullptr, arena_alloc, arena_release, arena_zero};
 
 // ---------------------------------------------------------------------------- validation
 static pd_status validate_desc(const pd_decode_desc* d) {
@@ -337,6 +348,7 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   const size_t lse_bytes = align_up((size_t)2 * grid_blocks * wpb * kMaxGroupPerCta * sizeof(float), kWsAlign);
   int* counters = nullptr;
   char* partials = nullptr;
+  std::unique_lock<std::mutex> ws_lock;  // library workspace: held until the launch
   if (ws_need) {
     if (d.workspace) {
       // caller workspace: [counters][partial lse][partial out]; the counter prefix is
@@ -349,39 +361,20 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
       cudaError_t e = cudaMemsetAsync(counters, 0, cnt_bytes, s);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(counters)");
     } else {
-      // library workspace: counters live in their own buffer, zeroed when it grows and
-      // left at zero by every completed call (the last block of a sequence resets its
-      // counter); partial results live in a second buffer.
-      std::lock_guard<std::mutex> lk(g_mu);
-      if (ds->cnt_bytes < cnt_bytes) {
-        if (ds->cnt) {
-          cudaError_t e = cudaFree(ds->cnt);
-          ds->cnt = nullptr;
-          ds->cnt_bytes = 0;
-          if (e != cudaSuccess) return cuda_fail(e, "cudaFree(counters)");
-        }
-        const size_t bytes = align_up(cnt_bytes * 2, 4096);
-        cudaError_t e = cudaMalloc(&ds->cnt, bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(counters)");
-        e = cudaMemset(ds->cnt, 0, bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(counters)");
-        ds->cnt_bytes = bytes;
-      }
-      const size_t part_bytes = ws_need - cnt_bytes;
-      if (ds->ws_bytes < part_bytes) {
-        if (ds->ws) {
-          cudaError_t e = cudaFree(ds->ws);
-          ds->ws = nullptr;
-          ds->ws_bytes = 0;
-          if (e != cudaSuccess) return cuda_fail(e, "cudaFree(workspace)");
-        }
-        const size_t bytes = align_up(part_bytes + part_bytes / 4, 1 << 20);
-        cudaError_t e = cudaMalloc(&ds->ws, bytes);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-        ds->ws_bytes = bytes;
-      }
-      counters = (int*)ds->cnt;
-      partials = (char*)ds->ws;
+      // library workspace: the arena of this stream (counters in one buffer, zero
+      // between calls; partial results in another), grown stream-ordered; the device's
+      // workspace lock stays held until the kernel is enqueued
+      unsigned long long sid = 0;
+      cudaError_t e = cudaStreamGetId(s, &sid);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
+      ws_lock = std::unique_lock<std::mutex>(ds->ws_mu);
+      void* cnt = nullptr;
+      void* part = nullptr;
+      const int rc = ds->arenas.acquire(sid, (void*)s, cnt_bytes, ws_need - cnt_bytes, kCudaArenaOps,
+                                        &cnt, &part);
+      if (rc) return cuda_fail((cudaError_t)rc, "library workspace (stream-ordered allocation)");
+      counters = (int*)cnt;
+      partials = (char*)part;
     }
   }
 
@@ -548,6 +541,19 @@ pd_status pd_append_paged_kv_rope(void* pages, const void* k_new, const void* v_
   return append_call(pages, k_new, v_new, slot_mapping, T, H_kv, D, page_size, max_pages, in_dtype,
                      kv_dtype, k_scale, v_scale, positions, rotary_mode, rope_scale, rope_theta,
                      stream);
+}
+
+pd_status pd_release_stream_workspace(pd_stream_t stream) {
+  DeviceState* ds = nullptr;
+  pd_status st = device_state(&ds);
+  if (st != PD_OK) return st;
+  unsigned long long sid = 0;
+  cudaError_t e = cudaStreamGetId((cudaStream_t)stream, &sid);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
+  std::lock_guard<std::mutex> lk(ds->ws_mu);
+  const int rc = ds->arenas.release(sid, (void*)stream, kCudaArenaOps);
+  if (rc) return cuda_fail((cudaError_t)rc, "cudaFreeAsync (stream workspace)");
+  return PD_OK;
 }
 
 pd_status pd_check_device_errors(pd_stream_t stream) {

@@ -198,3 +198,18 @@ def test_plain_c_caller(L, tmp_path):
     assert lines[2].startswith(f"bad heads {invalid} ") and "H_kv" in lines[2]
     assert lines[3] == f"bad flags {invalid}"
     assert lines[4] == f"bad q_len {invalid}"
+
+
+def test_stream_workspace_arena_bookkeeping(tmp_path):
+    # the per-stream arenas of the library-managed workspace, with fake stream-ordered
+    # allocator calls (tests/c/arena_check.cpp): separate buffers per stream, growth
+    # that allocates first and releases the old buffer on its stream, zeroed counters,
+    # unchanged arena after a failed allocation, release of both buffers once
+    import subprocess
+    exe = tmp_path / "arena_check"
+    subprocess.check_call(["g++", "-std=c++17", "-Wall", "-Werror", "-I",
+                           os.path.join(ROOT, "paged_kv_decode_19_gb300", "csrc"),
+                           os.path.join(ROOT, "tests", "c", "arena_check.cpp"), "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stderr
+    assert out.stdout.strip() == "arena bookkeeping ok"

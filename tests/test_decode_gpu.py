@@ -453,3 +453,53 @@ def test_sink_empty_sequence_and_noalloc():
                                      s.rotary_mode, s.rope_scale, s.rope_theta, wl.sm_scale,
                                      sink=sk)
     assert torch.equal(out2, out) and torch.equal(lse2, lse)
+
+
+# ----------------------------------------------------------------------------- workspace per stream
+
+def test_library_workspace_two_streams_concurrently():
+    """Split decodes of two different workloads in flight at once on two streams, both
+    with the library-managed workspace: each stream has its own arena, so neither sees
+    the other's arrival counters or partial slots; each matches the oracle."""
+    a = _wl("long_ctx_bf16", 300)
+    b = _wl("window_sink_f16", 301, B=16)
+    ra, rb = oracle_decode(a), oracle_decode(b)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    outs = []
+    for rep in range(3):
+        with torch.cuda.stream(sa):
+            oa, la = gpu_decode(a, stream=sa, num_splits=16, max_kv_len_hint=int(a.attended.max()))
+        with torch.cuda.stream(sb):
+            ob, lb = gpu_decode(b, stream=sb, num_splits=5, max_kv_len_hint=int(b.attended.max()))
+        outs.append((oa, la, ob, lb))
+    torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    for oa, la, ob, lb in outs:
+        compare("bf16", oa, la, ra[0], ra[1])
+        compare("f16", ob, lb, rb[0], rb[1])
+    for st in (sa, sb):
+        pd.release_stream_workspace(st)
+    pd.release_stream_workspace(torch.cuda.Stream())  # no arena: nothing to do
+
+
+def test_library_workspace_grows_behind_work_in_flight():
+    """A small split decode, then at once a much larger one on the same stream: the
+    arena grows while the first kernel may still run (the old buffer is released
+    stream-ordered, after it); both results match the oracle."""
+    st = torch.cuda.Stream()
+    pd.release_stream_workspace(st)
+    small = _wl("llama3_8b_bf16", 302, B=2)
+    big = _wl("llama3_8b_bf16", 303, B=40, len_dist=("uniform", 100, 900), pool=3000)
+    rs, rb = oracle_decode(small), oracle_decode(big)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(st):
+        o1, l1 = gpu_decode(small, stream=st, num_splits=3, max_kv_len_hint=700)
+        o2, l2 = gpu_decode(big, stream=st, num_splits=24, max_kv_len_hint=900)
+        o3, l3 = gpu_decode(small, stream=st, num_splits=3, max_kv_len_hint=700)
+    st.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    compare("bf16", o1, l1, rs[0], rs[1])
+    compare("bf16", o2, l2, rb[0], rb[1])
+    compare("bf16", o3, l3, rs[0], rs[1])
+    pd.release_stream_workspace(st)
