@@ -1,11 +1,13 @@
 """pd_batch_decode_paged_kv_noalloc — the decode entry point for callers that cannot
 allocate device memory (its split scratch is a static array inside the library).
 
-Called straight through the C ABI (ctypes), twice in a row, and compared with the
-regular pd_batch_decode_paged_kv on the same inputs, within the bf16 decode
-tolerance (max |out| error 2e-2, max |lse| error 2e-3).  This file is collected last
-so that a failure here stops a -x run only after every other test has run; it also
-passes on its own in a fresh process.
+Called straight through the C ABI (ctypes), twice in a row, and compared both with the
+fp64 oracle and with the regular pd_batch_decode_paged_kv on the same inputs, within
+the bf16 decode tolerance (max |out| error 2e-2, max |lse| error 2e-3).  The device's
+free memory must not change across the calls after the first (the first may load the
+library's device code, which holds the static array).  This file is collected last so
+that a failure here stops a -x run only after every other test has run; it also passes
+on its own in a fresh process.
 """
 import ctypes
 
@@ -15,6 +17,7 @@ import torch
 
 from paged_kv_decode_19_gb300 import _lib
 from paged_kv_decode_19_gb300 import workloads as W
+from tests._util import compare, oracle_decode
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -47,12 +50,23 @@ def test_noalloc_matches_regular_entry_point_twice():
     assert L.pd_workspace_size(ctypes.byref(desc)) > 0
     assert _call(L.pd_batch_decode_paged_kv, wl, ref_out, ref_lse, desc) == 0
     assert L.pd_check_device_errors(None) == 0
-    for _ in range(2):
-        out = torch.full(shape, float("nan"), dtype=torch.bfloat16, device=DEV)
-        lse = torch.full((s.B, s.H_qo), float("nan"), dtype=torch.float32, device=DEV)
+    ro, rl, st = oracle_decode(wl)
+    assert st == 0
+    # outputs of the calls below allocated up front: nothing else allocates meanwhile
+    outs = [torch.full(shape, float("nan"), dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    lses = [torch.full((s.B, s.H_qo), float("nan"), dtype=torch.float32, device=DEV)
+            for _ in range(3)]
+    torch.cuda.synchronize()
+    free = []
+    for out, lse in zip(outs, lses):
         st = _call(L.pd_batch_decode_paged_kv_noalloc, wl, out, lse, desc)
         assert st == 0, L.pd_get_last_error_string()
         assert L.pd_check_device_errors(None) == 0
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
+    assert free[1:] == free[:1] * (len(free) - 1), free
+    for out, lse in zip(outs, lses):
+        compare("bf16", out, lse, ro, rl)
         eo = (out.float() - ref_out.float()).abs().max().item()
         el = (lse - ref_lse).abs().max().item()
         assert np.isfinite(eo) and eo <= 2e-2, eo
