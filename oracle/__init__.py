@@ -69,6 +69,8 @@ def lib():
             L.oracle_batch_decode_paged_kv.restype = i32
             L.oracle_merge_state.argtypes = [P, P, P, P, i32, i32, i32]
             L.oracle_merge_state.restype = None
+            L.oracle_merge_states.argtypes = [P, P, P, P, i32, i32, i32, i32]
+            L.oracle_merge_states.restype = None
             L.oracle_append_paged_kv.argtypes = [
                 P, i32, P, P, i32, P, i32, i32, i32, i32, i64, ctypes.c_float, ctypes.c_float]
             L.oracle_append_paged_kv.restype = i32
@@ -244,6 +246,18 @@ def merge_state(V, S, V_other, S_other):
     So = _c(S_other, np.float64)
     N, H, D = V.shape
     lib().oracle_merge_state(_ptr(V), _ptr(S), _ptr(Vo), _ptr(So), N, H, D)
+    return V, S
+
+
+def merge_states(V_parts, S_parts):
+    """fp64 merge of R attention states at once: V_parts [R,N,H,D], S_parts [R,N,H] (log2);
+    returns (V [N,H,D], S [N,H]).  All partners empty (S <= -5e4): V = 0, S = -5e4."""
+    Vp = _c(V_parts, np.float64)
+    Sp = _c(S_parts, np.float64)
+    R, N, H, D = Vp.shape
+    V = np.zeros((N, H, D), np.float64)
+    S = np.zeros((N, H), np.float64)
+    lib().oracle_merge_states(_ptr(Vp), _ptr(Sp), _ptr(V), _ptr(S), R, N, H, D)
     return V, S
 
 

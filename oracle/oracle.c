@@ -456,6 +456,46 @@ void oracle_merge_state(double* V, double* S, const double* V_other, const doubl
 }
 
 /* ------------------------------------------------------------------------- */
+/* merge of R states at once: the [TVM] merge formula over R partners (the     */
+/* pairwise form is R = 2; the module docstring's multi-stage decoding and the */
+/* distributed KV-transfer path combine the (V, S) states of R partial         */
+/* decodes).  For every (n, h):                                                */
+/*   M = max_r S_r;  w_r = 2^(S_r - M);  V = sum_r w_r V_r / sum_r w_r;         */
+/*   S = log2(sum_r w_r) + M.                                                   */
+/* If every partner is the empty state (S_r <= -5e4: the decode's sentinel of  */
+/* a sequence with no row), the result is the empty state itself: V = 0,       */
+/* S = -5e4 (reading R4 applied to the merged set of rows, which is empty).    */
+/* V_parts [R,N,H,D], S_parts [R,N,H]; V_out [N,H,D], S_out [N,H].             */
+/* ------------------------------------------------------------------------- */
+
+void oracle_merge_states(const double* V_parts, const double* S_parts, double* V_out,
+                         double* S_out, int R, int N, int H, int D) {
+  const size_t rows = (size_t)N * H;
+  for (size_t i = 0; i < rows; ++i) {
+    double M = -INFINITY;
+    for (int r = 0; r < R; ++r) {
+      double s = S_parts[(size_t)r * rows + i];
+      if (s > M) M = s;
+    }
+    double* v = V_out + i * D;
+    for (int d = 0; d < D; ++d) v[d] = 0.0;
+    if (!(M > -5e4)) {
+      S_out[i] = -5e4;
+      continue;
+    }
+    double den = 0.0;
+    for (int r = 0; r < R; ++r) {
+      double w = exp2(S_parts[(size_t)r * rows + i] - M);
+      den += w;
+      const double* vr = V_parts + ((size_t)r * rows + i) * D;
+      for (int d = 0; d < D; ++d) v[d] += w * vr[d];
+    }
+    for (int d = 0; d < D; ++d) v[d] /= den;
+    S_out[i] = log2(den) + M;
+  }
+}
+
+/* ------------------------------------------------------------------------- */
 /* append_paged_kv: [VLLM] `reshape_and_cache` on the TVM page layout.         */
 /* For token t with slot s >= 0: page = s / P, off = s % P;                    */
 /*   pages[page,0,h,off,:] = conv(k[t,h,:]),  pages[page,1,h,off,:] = conv(v). */

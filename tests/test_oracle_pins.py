@@ -629,3 +629,86 @@ def test_k_rotated_decode_equals_rope_decode_on_exact_values():
                                                  k_rotated=True, **kw)
     np.testing.assert_allclose(o_kr, o_ref, rtol=0, atol=1e-5)
     np.testing.assert_allclose(l_kr, l_ref, rtol=0, atol=1e-5)
+
+
+# --------------------------------------------------------------------------- merge of R states
+
+def _chunk_decodes(rng, lens, R, P=4, rope=True):
+    """Each sequence decoded whole, and as R page-aligned chunks (chunk r: pages
+    [r per, (r+1) per), per = ceil(npages / R); a chunk past the end of the page list is
+    empty), each chunk a pseudo-sequence whose RoPE positions start at its first row."""
+    B, H_qo, H_kv, D = len(lens), 4, 2, 8
+    Q, pages, indptr, values, last, _ = _paged_case(rng, B, H_qo, H_kv, D, P, lens)
+    kw = dict(rotary_mode=1 if rope else 0, rope_theta=50.0, rope_scale=1.0, sm_scale=0.35,
+              q_dtype="f32", kv_dtype="f32", H_kv=H_kv, page_size=P)
+    qpos = np.array(lens, np.int32)
+    full = oracle.batch_decode_paged_kv(Q, pages, indptr, values, last, np.zeros(B, np.int32),
+                                        qpos, **kw)
+    Vp, Sp = [], []
+    for r in range(R):
+        ip, vals, li, koff = [0], [], [], []
+        for b in range(B):
+            npg = int(indptr[b + 1] - indptr[b])
+            per = -(-npg // R) if npg else 1
+            p0, p1 = min(npg, r * per), min(npg, (r + 1) * per)
+            vals.extend(values[indptr[b] + p0: indptr[b] + p1])
+            ip.append(len(vals))
+            rows = min(lens[b], p1 * P) - p0 * P if p1 > p0 else 0
+            li.append(rows - (p1 - p0 - 1) * P if p1 > p0 else 0)
+            koff.append(p0 * P)
+        o, l, st = oracle.batch_decode_paged_kv(
+            Q, pages, np.array(ip, np.int32), np.array(vals if vals else [0], np.int32),
+            np.array(li, np.int32), np.array(koff, np.int32), qpos, **kw)
+        assert st == 0
+        Vp.append(o)
+        Sp.append(l)
+    return full, np.stack(Vp), np.stack(Sp)
+
+
+@pytest.mark.parametrize("R", [2, 3, 8])
+def test_merge_states_of_chunks_equals_unsplit(R):
+    # sequences shorter than R pages leave some chunks empty (their state is the
+    # empty sentinel, which must add nothing); an empty sequence stays empty
+    rng = np.random.default_rng(40 + R)
+    lens = [21, 14, 9, 3, 0, 33]
+    (fo, fl, _), Vp, Sp = _chunk_decodes(rng, lens, R)
+    assert (Sp == -5e4).any()
+    mo, ml = oracle.merge_states(Vp, Sp)
+    np.testing.assert_allclose(mo, fo, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(ml, fl, rtol=0, atol=1e-12)
+    assert np.all(mo[4] == 0) and np.all(ml[4] == -5e4)
+
+
+def test_merge_states_is_the_pairwise_fold_and_order_free():
+    rng = np.random.default_rng(50)
+    R, N, H, D = 5, 3, 4, 6
+    Vp = rng.standard_normal((R, N, H, D))
+    Sp = rng.uniform(-6, 6, (R, N, H))
+    mo, ml = oracle.merge_states(Vp, Sp)
+    fo, fl = Vp[0], Sp[0]
+    for r in range(1, R):
+        fo, fl = oracle.merge_state(fo, fl, Vp[r], Sp[r])
+    np.testing.assert_allclose(mo, fo, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(ml, fl, rtol=0, atol=1e-13)
+    perm = rng.permutation(R)
+    po, pl = oracle.merge_states(Vp[perm], Sp[perm])
+    np.testing.assert_allclose(po, mo, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(pl, ml, rtol=0, atol=1e-13)
+    # closed form of one row
+    w = 2.0 ** Sp[:, 1, 2]
+    np.testing.assert_allclose(mo[1, 2], (w[:, None] * Vp[:, 1, 2]).sum(0) / w.sum(), rtol=1e-13, atol=1e-14)
+
+
+def test_merge_states_empty_partners():
+    rng = np.random.default_rng(51)
+    Vp = rng.standard_normal((3, 2, 2, 4))
+    Sp = rng.uniform(-3, 3, (3, 2, 2))
+    Vp[1], Sp[1] = 0.0, -5e4                 # an empty partner adds nothing
+    mo, ml = oracle.merge_states(Vp, Sp)
+    ro, rl = oracle.merge_states(Vp[[0, 2]], Sp[[0, 2]])
+    np.testing.assert_allclose(mo, ro, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(ml, rl, rtol=0, atol=1e-13)
+    Sp[:, 0, 1] = -5e4                       # every partner empty: the empty state
+    Vp[:, 0, 1] = 0.0
+    mo, ml = oracle.merge_states(Vp, Sp)
+    assert np.all(mo[0, 1] == 0) and ml[0, 1] == -5e4
