@@ -262,6 +262,55 @@ pd_status pd_merge_state_inplace(void* V, float* S, const void* V_other, const f
                                  pd_stream_t stream);
 
 /*
+ * merge_states — the [TVM] `merge_state_inplace` formula over R partners at once, the
+ * combine step of a decode split across R ranks (context parallelism, [NKI] `CP`: each
+ * rank decodes its slice of the context to a partial (out, lse), the partials are
+ * exchanged and combined) or across R chunks of one GPU's multi-stage decode.
+ * For every (n, h):  M = max_r S_r;  w_r = 2^(S_r - M);
+ *   V_out[n,h,:] = sum_r w_r V_r[n,h,:] / sum_r w_r;  S_out[n,h] = log2(sum_r w_r) + M.
+ * If every partner is empty (S_r <= -5e4, the decode's empty-sequence state), V_out = 0
+ * and S_out = -5e4.  Arithmetic in fp32.
+ * Arguments (device pointers):
+ *   V_parts  float32 partner outputs; partner r's [N, H, D] rows at V_parts + r * v_rank_stride.
+ *   S_parts  float32 partner lse (log2); partner r's [N, H] at S_parts + r * s_rank_stride.
+ *   Two layouts are accepted: separate arrays [R,N,H,D] / [R,N,H] (v_rank_stride = N*H*D,
+ *   s_rank_stride = N*H), or one packed block [N*H*D outputs | N*H lse] per partner, as an
+ *   all-gather of each rank's packed partial delivers it (v_rank_stride = s_rank_stride =
+ *   N*H*(D+1), S_parts = V_parts + N*H*D); anything else is PD_ERR_INVALID_ARG.
+ *   V_out    [N, H, D] of out_dtype (F32, F16 or BF16);  S_out [N, H] float32.
+ * The outputs must not overlap the partners.
+ */
+pd_status pd_merge_states(void* V_out, float* S_out, const float* V_parts, const float* S_parts,
+                          int64_t v_rank_stride, int64_t s_rank_stride, int32_t R, int32_t N,
+                          int32_t H, int32_t D, int32_t out_dtype, pd_stream_t stream);
+
+/*
+ * cp_shard_plan — host-only (no CUDA call): the page table of one rank's slice of the
+ * context for a decode split across `world` ranks ([NKI] `CP`: each rank holds an
+ * S_ctx/CP slice of the prior KV cache), cut at page boundaries (TVM multi-stage
+ * decoding's chunks are valid pseudo-sequences): sequence b's npages pages are cut
+ * into `world` chunks of per = ceil(npages / world) pages, and rank `rank` takes pages
+ * [rank * per, min((rank + 1) * per, npages)); a rank past the end of the list gets an
+ * empty chunk (no pages, its decode gives the empty state, which the merge ignores).
+ * The chunk is a sequence of its own: rows = min(L, p1 P) - p0 P, last page length
+ * rows - (p1 - p0 - 1) P, and RoPE positions that start at k_rope_pos_offset[b] + p0 P,
+ * so that every K row keeps its position.  Decode the rank's chunk with
+ * pd_batch_decode_paged_kv (fp32 output) into a partial (out, lse), exchange the
+ * partials, and combine them with pd_merge_states: the result equals the unsplit decode.
+ * No sliding window (length_info is [B] last_page_len).
+ * Arguments (HOST pointers): indptr [B+1], values [indptr[B]], length_info [B],
+ * k_rope_pos_offset [B] or NULL (0); outputs shard_indptr [B+1], shard_values (room for
+ * shard_values_capacity entries; at most ceil(npages/world) per sequence),
+ * shard_length_info [B], shard_k_rope_pos_offset [B].  The page ids are the global
+ * table's; a deployment whose ranks hold only their own slice maps them to its pool.
+ */
+pd_status pd_cp_shard_plan(const int32_t* indptr, const int32_t* values, const int32_t* length_info,
+                           const int32_t* k_rope_pos_offset, int32_t B, int32_t page_size,
+                           int32_t world, int32_t rank, int32_t* shard_indptr,
+                           int32_t* shard_values, int64_t shard_values_capacity,
+                           int32_t* shard_length_info, int32_t* shard_k_rope_pos_offset);
+
+/*
  * append_paged_kv — [VLLM] `reshape_and_cache`, on the [TVM] page layout.
  * For token t with slot_mapping[t] = s >= 0:  page = s / P, off = s % P;
  *   pages[page, 0, h, off, :] = conv(k_new[t, h, :]);  pages[page, 1, h, off, :] = conv(v_new[t, h, :]).

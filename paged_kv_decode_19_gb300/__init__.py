@@ -15,6 +15,9 @@ from ._lib import (  # noqa: F401
     last_decode_variant,
     make_desc,
     merge_state_inplace,
+    merge_states,
+    merge_states_packed,
+    cp_shard_plan,
     plan,
     release_stream_workspace,
     version,

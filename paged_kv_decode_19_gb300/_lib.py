@@ -47,6 +47,8 @@ EXPORTS = (
     "pd_workspace_size_mq",
     "pd_append_paged_kv_rope",
     "pd_merge_state_inplace",
+    "pd_merge_states",
+    "pd_cp_shard_plan",
     "pd_append_paged_kv",
     "pd_workspace_size",
     "pd_workspace_init",
@@ -113,6 +115,10 @@ def lib():
             L.pd_workspace_size_mq.restype = ctypes.c_size_t
             L.pd_merge_state_inplace.argtypes = [P, P, P, P, i32, i32, i32, i32, P]
             L.pd_merge_state_inplace.restype = i32
+            L.pd_merge_states.argtypes = [P, P, P, P, i64, i64, i32, i32, i32, i32, i32, P]
+            L.pd_merge_states.restype = i32
+            L.pd_cp_shard_plan.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, i64, P, P]
+            L.pd_cp_shard_plan.restype = i32
             L.pd_append_paged_kv.argtypes = [P, P, P, P, i32, i32, i32, i32, i64, i32, i32, f32,
                                              f32, P]
             L.pd_append_paged_kv.restype = i32
@@ -262,6 +268,56 @@ def merge_state_inplace(V, S, V_other, S_other, stream=None):
     _check(lib().pd_merge_state_inplace(_ptr(V), _ptr(S), _ptr(V_other), _ptr(S_other), N, H, D,
                                         DTYPE_CODES[V.dtype], _stream(stream)))
     return V, S
+
+
+def merge_states(V_out, S_out, V_parts, S_parts, stream=None):
+    """pd_merge_states: V_parts [R,N,H,D] float32, S_parts [R,N,H] float32 -> V_out [N,H,D]
+    (F32/F16/BF16), S_out [N,H] float32."""
+    R, N, H, D = V_parts.shape
+    if V_parts.dtype != torch.float32 or S_parts.dtype != torch.float32 or S_parts.shape != (R, N, H):
+        raise ValueError("merge_states: V_parts [R,N,H,D] and S_parts [R,N,H] must be float32")
+    if V_out.shape != (N, H, D) or S_out.shape != (N, H) or S_out.dtype != torch.float32:
+        raise ValueError("merge_states: V_out [N,H,D], S_out [N,H] float32")
+    _check(lib().pd_merge_states(_ptr(V_out), _ptr(S_out), _ptr(V_parts), _ptr(S_parts),
+                                 N * H * D, N * H, R, N, H, D, DTYPE_CODES[V_out.dtype],
+                                 _stream(stream)))
+    return V_out, S_out
+
+
+def merge_states_packed(V_out, S_out, packed, stream=None):
+    """pd_merge_states on R packed partials: packed [R, N*H*D + N*H] float32, each row a
+    partner's outputs followed by its lse (the layout an all-gather of packed partials
+    gives)."""
+    N, H, D = V_out.shape
+    R, width = packed.shape
+    if packed.dtype != torch.float32 or width != N * H * (D + 1) or not packed.is_contiguous():
+        raise ValueError("merge_states_packed: packed must be float32 [R, N*H*(D+1)]")
+    base = packed.data_ptr()
+    _check(lib().pd_merge_states(_ptr(V_out), _ptr(S_out), ctypes.c_void_p(base),
+                                 ctypes.c_void_p(base + 4 * N * H * D), width, width, R, N, H, D,
+                                 DTYPE_CODES[V_out.dtype], _stream(stream)))
+    return V_out, S_out
+
+
+def cp_shard_plan(indptr, values, length_info, k_rope_pos_offset, page_size, world, rank):
+    """pd_cp_shard_plan on host int32 arrays: returns (indptr, values, length_info,
+    k_rope_pos_offset) of rank `rank`'s page-aligned slice, as numpy int32 arrays."""
+    import numpy as np
+    ip = np.ascontiguousarray(indptr, np.int32)
+    vals = np.ascontiguousarray(values, np.int32)
+    li = np.ascontiguousarray(length_info, np.int32)
+    B = len(li)
+    ko = None if k_rope_pos_offset is None else np.ascontiguousarray(k_rope_pos_offset, np.int32)
+    npg = ip[1:] - ip[:-1]
+    cap = int(np.sum(-(-npg // world))) if B and world >= 1 else 0
+    o_ip = np.zeros(B + 1, np.int32)
+    o_vals = np.zeros(max(cap, 1), np.int32)
+    o_li = np.zeros(B, np.int32)
+    o_ko = np.zeros(B, np.int32)
+    p = lambda a: None if a is None else ctypes.c_void_p(a.ctypes.data)
+    _check(lib().pd_cp_shard_plan(p(ip), p(vals), p(li), p(ko), B, int(page_size), int(world),
+                                  int(rank), p(o_ip), p(o_vals), cap, p(o_li), p(o_ko)))
+    return o_ip, o_vals[:o_ip[-1]], o_li, o_ko
 
 
 def append_paged_kv(pages, k_new, v_new, slot_mapping, k_scale=1.0, v_scale=1.0, stream=None):

@@ -484,6 +484,68 @@ pd_status pd_merge_state_inplace(void* V, float* S, const void* V_other, const f
   return PD_OK;
 }
 
+pd_status pd_merge_states(void* V_out, float* S_out, const float* V_parts, const float* S_parts,
+                          int64_t v_rank_stride, int64_t s_rank_stride, int32_t R, int32_t N,
+                          int32_t H, int32_t D, int32_t out_dtype, pd_stream_t stream) {
+  if (R < 1 || N < 0 || H < 0 || D <= 0) return fail(PD_ERR_INVALID_ARG, "bad R/N/H/D");
+  if (out_dtype != kF32 && out_dtype != kF16 && out_dtype != kBF16)
+    return fail(PD_ERR_INVALID_ARG, "out_dtype must be F32, F16 or BF16");
+  const long long rows = (long long)N * H;
+  if (rows == 0) return PD_OK;
+  if (rows > INT_MAX || (long long)R * rows > INT_MAX) return fail(PD_ERR_UNSUPPORTED, "R * N * H exceeds 2^31");
+  if (!V_out || !S_out || !V_parts || !S_parts) return fail(PD_ERR_INVALID_ARG, "NULL device pointer");
+  if (v_rank_stride != rows * D || s_rank_stride != rows) {
+    // strided partners (one packed buffer per rank): the kernel reads partner r at
+    // V_parts + r * v_rank_stride; it is given contiguous strides below, so only the
+    // packed layout [R][N*H*D + N*H] of the exchange and the plain [R,N,H,D] are taken
+    if (!(v_rank_stride == s_rank_stride && v_rank_stride == rows * D + rows &&
+          S_parts == V_parts + rows * D))
+      return fail(PD_ERR_INVALID_ARG,
+                  "partner strides must be [R,N,H,D] / [R,N,H], or one packed [out | lse] block per partner");
+  }
+  cudaError_t e = launch_merge_states(V_out, S_out, V_parts, S_parts, R, (int)N, H, D, out_dtype,
+                                      v_rank_stride, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "merge_states launch");
+  return PD_OK;
+}
+
+pd_status pd_cp_shard_plan(const int32_t* indptr, const int32_t* values, const int32_t* length_info,
+                           const int32_t* k_rope_pos_offset, int32_t B, int32_t page_size,
+                           int32_t world, int32_t rank, int32_t* shard_indptr,
+                           int32_t* shard_values, int64_t shard_values_capacity,
+                           int32_t* shard_length_info, int32_t* shard_k_rope_pos_offset) {
+  if (B < 0 || page_size <= 0 || world < 1 || rank < 0 || rank >= world)
+    return fail(PD_ERR_INVALID_ARG, "bad B / page_size / world / rank");
+  if (!shard_indptr || (B > 0 && (!indptr || !length_info || !shard_length_info || !shard_k_rope_pos_offset)))
+    return fail(PD_ERR_INVALID_ARG, "NULL host pointer");
+  shard_indptr[0] = 0;
+  long long n = 0;
+  for (int b = 0; b < B; ++b) {
+    const long long npg = (long long)indptr[b + 1] - indptr[b];
+    if (npg < 0) return fail(PD_ERR_INVALID_ARG, "page_table_indptr decreases");
+    const long long per = npg > 0 ? (npg + world - 1) / world : 1;
+    const long long p0 = std::min(npg, rank * per), p1 = std::min(npg, (rank + 1) * per);
+    const long long L = npg > 0 ? (npg - 1) * page_size + length_info[b] : 0;
+    if (npg > 0 && (length_info[b] < 1 || length_info[b] > page_size))
+      return fail(PD_ERR_INVALID_ARG, "last_page_len outside [1, page_size]");
+    if (p1 > p0) {
+      if (!values || !shard_values) return fail(PD_ERR_INVALID_ARG, "NULL page table");
+      if (n + (p1 - p0) > shard_values_capacity)
+        return fail(PD_ERR_INVALID_ARG, "shard_values_capacity too small");
+      for (long long j = p0; j < p1; ++j) shard_values[n++] = values[indptr[b] + j];
+      const long long rows = std::min(L, p1 * page_size) - p0 * page_size;
+      shard_length_info[b] = (int32_t)(rows - (p1 - p0 - 1) * page_size);
+    } else {
+      shard_length_info[b] = 0;
+    }
+    if (n > INT_MAX) return fail(PD_ERR_UNSUPPORTED, "shard page table exceeds 2^31 entries");
+    shard_indptr[b + 1] = (int32_t)n;
+    shard_k_rope_pos_offset[b] =
+        (int32_t)((k_rope_pos_offset ? (long long)k_rope_pos_offset[b] : 0) + p0 * page_size);
+  }
+  return PD_OK;
+}
+
 }  // extern "C"
 
 static pd_status append_call(void* pages, const void* k_new, const void* v_new,

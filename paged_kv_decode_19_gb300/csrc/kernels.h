@@ -41,6 +41,12 @@ void record_error(const char* msg);
 // merge_state_inplace and append_paged_kv
 cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const float* S_other, int N,
                                int H, int D, int v_dtype, cudaStream_t st);
+// R-way merge of fp32 partial states into out (out_dtype) and S_out; partner r's rows
+// at V_parts + r * rstride (rstride = N*H*D: [R,N,H,D] with S [R,N,H]; or N*H*(D+1):
+// one packed [out | lse] block per partner, S_parts = V_parts + N*H*D).
+cudaError_t launch_merge_states(void* out, float* S_out, const float* V_parts, const float* S_parts,
+                                int R, int N, int H, int D, int out_dtype, long long rstride,
+                                cudaStream_t st);
 // RoPE applied to the appended K rows (mode 0: none, 1 rotate-half, 2 interleaved).
 struct AppendRope {
   const int32_t* positions;                // [T] position of each new token

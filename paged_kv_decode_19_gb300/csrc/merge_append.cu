@@ -1,5 +1,7 @@
 // merge_state_inplace and append_paged_kv kernels.
 //
+// merge_states: the same formula over R partners at once (the combine step of a
+//   decode split across ranks); fp32 partial rows in, the output type out.
 // merge: Apache TVM `_decode_kernels.py`, `merge_state_inplace` — one warp per
 //   (n, h) row: both log-sum-exps are read, the row of V is rescaled and summed in
 //   fp32, and S is written last (after the warp's reads).
@@ -50,6 +52,65 @@ cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const flo
   if (v_dtype == kF16)
     return launch_pdl(merge_state_kernel<__half>, grid, dim3(threads), 0, st, (__half*)V, S,
                       (const __half*)V_other, S_other, rows, D);
+  return cudaErrorInvalidValue;
+}
+
+// merge_states: the merge formula over R partners at once (one warp per (n, h) row): the
+// R log-sum-exps are read by the lanes (r = lane, lane + 32, ...), M and the weight sum
+// come from warp reductions, then each lane accumulates its dims over the R fp32
+// partial rows and writes the output type.  All partners empty: out 0, lse -5e4.
+template <typename OT>
+__global__ void merge_states_kernel(OT* __restrict__ out, float* __restrict__ S_out,
+                                    const float* __restrict__ Vp, const float* __restrict__ Sp,
+                                    int R, int rows, int D, long long rstride) {
+  pdl_wait();
+  pdl_release();
+  const int warps = blockDim.x >> 5;
+  const int row = blockIdx.x * warps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float M = kEmptyM;
+  // partner r: S at Sp + r * sstride, V rows at Vp + r * rstride (rstride = rows * D, or
+  // one packed [out | lse] block per partner: rstride = sstride = rows * (D + 1))
+  const long long sstride = rstride == (long long)rows * D ? rows : rstride;
+  for (int r = lane; r < R; r += 32) M = fmaxf(M, Sp[r * sstride + row]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  OT* o = out + (size_t)row * D;
+  if (!(M > kEmptyM)) {
+    for (int d = lane; d < D; d += 32) o[d] = from_f32<OT>(0.f);
+    if (lane == 0) S_out[row] = kEmptyM;
+    return;
+  }
+  float den = 0.f;
+  for (int r = lane; r < R; r += 32) den += exp2f(Sp[r * sstride + row] - M);
+  den = warp_sum(den);
+  const float inv = 1.f / den;
+  for (int d = lane; d < D; d += 32) {
+    float acc = 0.f;
+    for (int r = 0; r < R; ++r)
+      acc = fmaf(exp2f(Sp[r * sstride + row] - M), Vp[r * rstride + (long long)row * D + d], acc);
+    o[d] = from_f32<OT>(acc * inv);
+  }
+  if (lane == 0) S_out[row] = M + log2f(den);
+}
+
+cudaError_t launch_merge_states(void* out, float* S_out, const float* V_parts, const float* S_parts,
+                                int R, int N, int H, int D, int out_dtype, long long rstride,
+                                cudaStream_t st) {
+  const int rows = N * H;
+  if (rows == 0) return cudaSuccess;
+  const int threads = 256, per = threads / 32;
+  const dim3 grid((rows + per - 1) / per);
+  if (out_dtype == kF32)
+    return launch_pdl(merge_states_kernel<float>, grid, dim3(threads), 0, st, (float*)out, S_out,
+                      V_parts, S_parts, R, rows, D, rstride);
+  if (out_dtype == kBF16)
+    return launch_pdl(merge_states_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st,
+                      (__nv_bfloat16*)out, S_out, V_parts, S_parts, R, rows, D, rstride);
+  if (out_dtype == kF16)
+    return launch_pdl(merge_states_kernel<__half>, grid, dim3(threads), 0, st, (__half*)out, S_out,
+                      V_parts, S_parts, R, rows, D, rstride);
   return cudaErrorInvalidValue;
 }
 
