@@ -366,14 +366,20 @@ def run_ours(args, ws, rank, local, config=None):
         else:
             pd.append_paged_kv(w.pages, k_new, v_new, slots, w.k_scale, w.v_scale)
 
+    # host copies of each replica's page-table offsets and lengths (the serving
+    # scheduler's own arrays): the decode plans its split from them on the host
+    metas = {id(r[0]): pd._lib.host_meta_of(r[0].indptr, r[0].length_info) for r in reps}
+    use_host_plan = [True]
+
     def decode(r):
-        # the decode follows the append on the stream: its start-up (work split scan,
-        # page table, Q) may run under the append (PD_DECODE_EARLY_INPUTS)
+        # the decode follows the append on the stream: its start-up (page table, Q) may
+        # run under the append (PD_DECODE_EARLY_INPUTS)
         w = r[0]
         decode_api(w.Q, w.pages, w.indptr, w.values, w.length_info, w.k_rope_pos_offset,
                    w.q_rope_position, out, lse, s.rotary_mode, s.rope_scale, s.rope_theta,
                    w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
-                   k_rotated=s.k_rotated, **split)
+                   k_rotated=s.k_rotated, host_meta=metas[id(w)] if use_host_plan[0] else None,
+                   **split)
 
     def prefill(n):
         # a spin kernel of about 60 us per step keeps the device busy (at load clocks)
@@ -445,6 +451,11 @@ def run_ours(args, ws, rank, local, config=None):
     launches = 2 * args.steps
     # the same steps after a flush of L2 (for comparison; not the reported value)
     _, dec_flushed_ms, _ = timed_steps(max(args.steps // 2, 3), flush=True, breakdown=True)
+    # the decode planning its split on the device instead (a scan of the device
+    # indptr / length_info at the kernel's start), for comparison
+    use_host_plan[0] = False
+    _, dec_devplan_ms, _ = timed_steps(args.steps, flush=not alternate, breakdown=True)
+    use_host_plan[0] = True
 
     # the multi-stage form of the same decode (for comparison; not the reported value):
     # page-aligned chunks decoded as pseudo-sequences into fp32 partials, then the
@@ -529,7 +540,8 @@ def run_ours(args, ws, rank, local, config=None):
         decode_api(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
                    di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e, s.rotary_mode,
                    s.rope_scale, s.rope_theta, w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale,
-                   early_inputs=True, k_rotated=s.k_rotated, **split)
+                   early_inputs=True, k_rotated=s.k_rotated, host_meta=metas[id(reps[0][0])],
+                   **split)
         res_host.copy_(res_dev, non_blocking=True)
         b.record(stream)
         b.synchronize()
@@ -539,6 +551,7 @@ def run_ours(args, ws, rank, local, config=None):
     res = dict(step=statistics.mean(step_ms), dec=statistics.mean(dec_ms),
                dec_med=statistics.median(dec_ms), app=statistics.mean(app_ms),
                dec_flushed=statistics.mean(dec_flushed_ms),
+               dec_devplan=statistics.mean(dec_devplan_ms),
                e2e=statistics.mean(e2e_ms), launches=launches, variant=variant,
                clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h, alternate=alternate, l2=l2,
                ext=ext)
@@ -569,8 +582,15 @@ def main():
                     help="time the --config workload alone (no per_config block)")
     ap.add_argument("--B", type=int, default=None,
                     help="override the batch size (smaller cases for profiling)")
+    ap.add_argument("--page-size", type=int, default=None,
+                    help="override the page size (the pool keeps its row count)")
     args = ap.parse_args()
     args.over = {} if args.B is None else {"B": args.B}
+    if args.page_size is not None:
+        base = W.spec(args.config)
+        args.over["page_size"] = args.page_size
+        if isinstance(base.pool, int):
+            args.over["pool"] = base.pool * base.page_size // args.page_size
     args.warmup = max(args.warmup, 3)
     ws, rank, local = _dist()
     spec = W.spec(args.config, **args.over)
@@ -662,6 +682,7 @@ def main():
         "config": cfg,
         "decode_us": head["decode_us"],
         "decode_us_l2_flushed": head["decode_us_l2_flushed"],
+        "decode_us_device_plan": head["decode_us_device_plan"],
         "append_us": head["append_us"],
         "kv_read_gbs": head["kv_read_gbs"],
         "decode_variant": head["decode_variant"],
@@ -699,6 +720,7 @@ def _summarise(res, config: str, spec, ws: int) -> dict:
         "step_us": round(step_us, 2),
         "decode_us": round(dec_us, 2),
         "decode_us_l2_flushed": round(res["dec_flushed"] * 1e3, 2),
+        "decode_us_device_plan": round(_max_over_ranks(res["dec_devplan"] * 1e3, ws), 2),
         "append_us": round(res["app"] * 1e3, 2),
         "kv_read_gbs": round(kv_bytes / (dec_us * 1e-6) / 1e9, 1),
         "decode_variant": res["variant"],

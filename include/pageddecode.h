@@ -94,6 +94,17 @@ typedef struct {
                                 row -- out = sum_r e^(t_r) v_r / (e^sink + sum_r e^(t_r)),
                                 t_r = sm_scale q.k_r, and lse includes it (an empty
                                 sequence gives out = 0, lse = sink * log2(e)) */
+  const int32_t* host_indptr;       /* optional HOST copy of page_table_indptr [B+1], or NULL */
+  const int32_t* host_length_info;  /* optional HOST copy of length_info ([B] or [3,B]), or NULL.
+                                 Both or neither.  When given (and 2(B+1) plus the length_info
+                                 entries fit in 1024 ints), the decode uses these instead of
+                                 the device arrays: the split is planned on the host and the
+                                 sequences' lengths and page-table offsets travel inside the
+                                 kernel launch, so no kernel reads page_table_indptr or
+                                 length_info and the start-up scan of them is skipped (the
+                                 serving scheduler that builds these arrays holds them on the
+                                 host anyway).  Read during the call only.  Page-table reads
+                                 stay bounds-checked against nnz_pages. */
 } pd_decode_desc;
 
 /*

@@ -89,6 +89,8 @@ class DecodeDesc(ctypes.Structure):
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
         ("sink", ctypes.c_void_p),
+        ("host_indptr", ctypes.c_void_p),
+        ("host_length_info", ctypes.c_void_p),
     ]
 
 
@@ -168,7 +170,9 @@ DECODE_K_ROTATED = 2
 
 def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_kv_len_hint=0,
               k_scale=1.0, v_scale=1.0, workspace=None, early_inputs=False,
-              sink=None, k_rotated=False) -> DecodeDesc:
+              sink=None, k_rotated=False, host_meta=None) -> DecodeDesc:
+    """host_meta: optional (indptr, length_info) numpy int32 host copies (the caller keeps
+    them alive for the call)."""
     B, H_qo, D = Q.shape
     max_pages, two, H_kv, P, D2 = pages.shape
     if two != 2 or D2 != D:
@@ -182,7 +186,23 @@ def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_k
         flags=(DECODE_EARLY_INPUTS if early_inputs else 0) | (DECODE_K_ROTATED if k_rotated else 0),
         workspace=None if workspace is None else workspace.data_ptr(),
         workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
-        sink=_sink_ptr(sink, H_qo))
+        sink=_sink_ptr(sink, H_qo),
+        host_indptr=None if host_meta is None else _host_i32(host_meta[0], B + 1),
+        host_length_info=None if host_meta is None else _host_i32(host_meta[1], length_info.numel()))
+
+
+def _host_i32(a, n):
+    import numpy as np
+    if not isinstance(a, np.ndarray) or a.dtype != np.int32 or not a.flags.c_contiguous or a.size != n:
+        raise ValueError(f"host copies must be contiguous numpy int32 arrays of {n} entries")
+    return a.ctypes.data
+
+
+def host_meta_of(indptr, length_info):
+    """Host copies (numpy int32) of a page table's indptr and length_info, for host_meta."""
+    import numpy as np
+    return (np.ascontiguousarray(indptr.cpu().numpy(), dtype=np.int32),
+            np.ascontiguousarray(length_info.cpu().numpy(), dtype=np.int32).reshape(-1))
 
 
 def _sink_ptr(sink, H_qo):
@@ -197,8 +217,11 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
                           k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                           rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                           v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                          early_inputs=False, sink=None, k_rotated=False, stream=None):
+                          early_inputs=False, sink=None, k_rotated=False, host_meta=None,
+                          stream=None):
     """pd_batch_decode_paged_kv on device tensors; writes `output` and `lse`.
+    host_meta=(indptr, length_info) numpy int32 host copies: the split is planned on the
+    host (desc->host_indptr / host_length_info).
     early_inputs=True sets PD_DECODE_EARLY_INPUTS: only right after append_paged_kv (or
     another kernel that writes none of Q, the page table, lengths and positions)."""
     if sm_scale is None:
@@ -206,7 +229,7 @@ def batch_decode_paged_kv(Q, pages, page_table_indptr, page_table_values, length
     desc = make_desc(Q, pages, page_table_indptr, page_table_values, length_info, output,
                      num_splits=num_splits, max_kv_len_hint=max_kv_len_hint, k_scale=k_scale,
                      v_scale=v_scale, workspace=workspace, early_inputs=early_inputs,
-                     sink=sink, k_rotated=k_rotated)
+                     sink=sink, k_rotated=k_rotated, host_meta=host_meta)
     _check(lib().pd_batch_decode_paged_kv(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),
@@ -239,7 +262,8 @@ def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, len
                              k_rope_pos_offset, q_rope_position, output, lse, rotary_mode=0,
                              rope_scale=1.0, rope_theta=1e4, sm_scale=None, *, k_scale=1.0,
                              v_scale=1.0, num_splits=0, max_kv_len_hint=0, workspace=None,
-                             early_inputs=False, sink=None, k_rotated=False, stream=None):
+                             early_inputs=False, sink=None, k_rotated=False, host_meta=None,
+                             stream=None):
     """pd_batch_decode_paged_kv_mq: Q [B, q_len, H_qo, D], output [B, q_len, H_qo, D],
     lse [B, q_len, H_qo]; token t of a sequence sees its rows up to itself."""
     if Q.dim() != 4:
@@ -251,7 +275,7 @@ def batch_decode_paged_kv_mq(Q, pages, page_table_indptr, page_table_values, len
                      page_table_values, length_info, output, num_splits=num_splits,
                      max_kv_len_hint=max_kv_len_hint, k_scale=k_scale, v_scale=v_scale,
                      workspace=workspace, early_inputs=early_inputs, sink=sink,
-                     k_rotated=k_rotated)
+                     k_rotated=k_rotated, host_meta=host_meta)
     _check(lib().pd_batch_decode_paged_kv_mq(
         _ptr(Q), _ptr(pages), _ptr(page_table_indptr), _ptr(page_table_values),
         _ptr(length_info), _ptr(k_rope_pos_offset), _ptr(q_rope_position), _ptr(output),

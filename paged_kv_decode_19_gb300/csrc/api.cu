@@ -194,6 +194,34 @@ static cudaError_t mma_dispatch(const DecodeParams& p, int q_dtype, int kv_dtype
   return launch_mma_fp8(p, q_dtype, grid, st, cfg);
 }
 
+// Host plan: copy the caller's host indptr / length_info into the launch, with the
+// prefix over the sequences of (work units + segment cost) that places the workers
+// (the device's units_of on the same fields).  False when they do not fit.
+static bool fill_host_plan(const pd_decode_desc& d, DecodeParams& p) {
+  const int B = d.B;
+  const long long li_n = d.sliding_window ? 3ll * B : (long long)B;
+  if (2ll * (B + 1) + li_n > kHostPlanInts) return false;
+  const int32_t* ip = d.host_indptr;
+  const int32_t* li = d.host_length_info;
+  p.hp_ptr = B + 1;
+  p.hp_li = 2 * (B + 1);
+  long long acc = 0;
+  p.hp[0] = 0;
+  for (int b = 0; b < B; ++b) {
+    const long long off = d.sliding_window ? li[B + b] : 0, sk = d.sliding_window ? li[2 * B + b] : 0;
+    bool bad = false;
+    const SeqInfo s = seq_from(ip[b], ip[b + 1], li[b], off, sk, d.page_size, d.sliding_window != 0, bad);
+    acc += units_of(s, d.page_size) + p.seg_cost;
+    if (acc > INT_MAX) return false;
+    p.hp[b + 1] = (int32_t)acc;
+    p.hp[p.hp_ptr + b] = ip[b];
+  }
+  p.hp[p.hp_ptr + B] = ip[B];
+  for (long long i = 0; i < li_n; ++i) p.hp[p.hp_li + i] = li[i];
+  p.hp_B = B;
+  return true;
+}
+
 // Fixed-point RoPE frequencies: F_i = 2^64 * frac(rope_scale / rope_theta^(2i/D) / (2 pi)).
 static void rope_table(float rope_scale, float rope_theta, int D, unsigned long long* F) {
   const double two_pi = 6.283185307179586476925286766559;
@@ -212,7 +240,7 @@ using namespace pd;
 
 extern "C" {
 
-int32_t pd_version(void) { return 10000; }
+int32_t pd_version(void) { return 10100; }
 
 const char* pd_get_last_error_string(void) { return t_last_error.c_str(); }
 
@@ -319,6 +347,14 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   if (!Q || !pages || !page_table_indptr || !length_info || !output || !lse)
     return fail(PD_ERR_INVALID_ARG, "NULL device pointer");
   if (d.nnz_pages > 0 && !page_table_values) return fail(PD_ERR_INVALID_ARG, "page_table_values is NULL");
+  if (!d.host_indptr != !d.host_length_info)
+    return fail(PD_ERR_INVALID_ARG, "host_indptr and host_length_info go together");
+  if (d.host_indptr) {
+    if (d.host_indptr[0] < 0 || d.host_indptr[d.B] > d.nnz_pages)
+      return fail(PD_ERR_INVALID_ARG, "host_indptr outside [0, nnz_pages]");
+    for (int b = 0; b < d.B; ++b)
+      if (d.host_indptr[b + 1] < d.host_indptr[b]) return fail(PD_ERR_INVALID_ARG, "host_indptr decreases");
+  }
   // both kernels read Q and K/V rows with vector accesses of up to 16 bytes
   if ((reinterpret_cast<uintptr_t>(pages) % 16) != 0 || (reinterpret_cast<uintptr_t>(Q) % 16) != 0)
     return fail(PD_ERR_INVALID_ARG, "Q and pages must be 16-byte aligned");
@@ -423,6 +459,7 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   p.q_prescale = p.score_scale;
   p.out_scale = d.kv_dtype == kE4M3 ? d.v_scale : 1.f;
   if (rotary_mode) rope_table(rope_scale, rope_theta, d.D, p.rope_F);
+  if (d.host_indptr && d.host_length_info) fill_host_plan(d, p);
 
   const dim3 grid((unsigned)grid_blocks);
   cudaError_t e;

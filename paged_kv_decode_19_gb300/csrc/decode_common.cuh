@@ -18,6 +18,8 @@ constexpr int kMaxGroupPerCta = 8;  // query heads one block serves at a time (a
 constexpr int kMaxHalfDim = 128;    // D <= 256
 constexpr int kMmaWarps = 4;        // warps (independent workers) per tensor-core block
 constexpr int kStartCacheB = 1024;  // batch sizes whose start-up scan runs in shared memory
+// Host plan: ints of sequence metadata the launch itself may carry (see DecodeParams::hp)
+constexpr int kHostPlanInts = 1024;
 
 // Block schedules (DecodeParams::mode)
 enum : int {
@@ -58,6 +60,14 @@ struct DecodeParams {
   float q_prescale;   // split-operand MMA path: Q is pre-multiplied by this
   float out_scale;    // applied to the final output (v_scale for e4m3 KV)
   unsigned long long rope_F[kMaxHalfDim];  // fixed-point turns/position per frequency
+  // Host plan: when hp_B > 0 the caller gave host copies of page_table_indptr and
+  // length_info, and the launch carries them: hp[0 .. B] = prefix sums over the
+  // sequences of (work units + seg_cost), hp[hp_ptr ..] = indptr [B+1],
+  // hp[hp_li ..] = length_info [B] or [3,B].  The kernels then read a sequence's
+  // lengths and page-table offset from here, and each worker finds its first segment
+  // by a binary search over the prefix, without the start-up scan of device memory.
+  int hp_B, hp_ptr, hp_li;
+  int32_t hp[kHostPlanInts];
 };
 
 // Attended length and row mapping of one sequence (length_info reading: no window
@@ -99,44 +109,67 @@ __device__ __forceinline__ SinkAdj apply_sink(const DecodeParams& p, int h, floa
   return {a / den, m + log2f(den)};
 }
 
-__device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
-  // every load is issued up front (one round trip), then the fields are checked
-  const int i0 = __ldg(p.indptr + b), i1 = __ldg(p.indptr + b + 1);
-  const long long last = __ldg(p.length_info + b);
-  long long off = 0, sk = 0;
-  if (p.window) {
-    off = __ldg(p.length_info + p.B + b);
-    sk = __ldg(p.length_info + 2 * p.B + b);
-  }
+// SeqInfo from a sequence's raw fields (page-table offsets i0, i1; last page length;
+// window start and sink length); an inconsistent sequence is treated as empty and sets
+// `bad`.  Shared by the kernels and the host planner, so both count the same work.
+__host__ __device__ __forceinline__ SeqInfo seq_from(long long i0, long long i1, long long last,
+                                                     long long off, long long sk, int P,
+                                                     bool window, bool& bad) {
   SeqInfo s;
-  s.page_begin = i0;
-  s.npages = i1 - i0;
+  s.page_begin = (int)i0;
+  s.npages = (int)(i1 - i0);
   s.L = 0;
   s.sink = 0;
   s.win_off = 0;
   if (s.npages <= 0) {
-    if (s.npages < 0) set_error(p.err, kErrBadLength);
+    if (s.npages < 0) bad = true;
     s.npages = 0;
     return s;
   }
   long long L;
-  if (!p.window) {
-    L = (long long)(s.npages - 1) * p.P + last;
-    s.sink = (int)min(max(L, 0ll), (long long)INT32_MAX);
+  if (!window) {
+    L = (long long)(s.npages - 1) * P + last;
+    s.sink = (int)(L < 0 ? 0 : L > (long long)INT32_MAX ? (long long)INT32_MAX : L);
   } else {
-    L = (long long)(s.npages - 1) * p.P + last - off + sk;
+    L = (long long)(s.npages - 1) * P + last - off + sk;
     if (sk < 0 || off < sk) {  // inconsistent window: sequence treated as empty
-      set_error(p.err, kErrBadLength);
+      bad = true;
       L = 0;
     }
     s.sink = (int)sk;
     s.win_off = (int)off;
   }
   if (L < 0 || L > (long long)INT32_MAX) {
-    set_error(p.err, kErrBadLength);
+    bad = true;
     L = 0;
   }
   s.L = (int)L;
+  return s;
+}
+
+__device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
+  long long i0, i1, last, off = 0, sk = 0;
+  if (p.hp_B) {  // the launch carries the host copies
+    i0 = p.hp[p.hp_ptr + b];
+    i1 = p.hp[p.hp_ptr + b + 1];
+    last = p.hp[p.hp_li + b];
+    if (p.window) {
+      off = p.hp[p.hp_li + p.B + b];
+      sk = p.hp[p.hp_li + 2 * p.B + b];
+    }
+  } else {
+    // every load is issued up front (one round trip), then the fields are checked
+    i0 = __ldg(p.indptr + b);
+    i1 = __ldg(p.indptr + b + 1);
+    last = __ldg(p.length_info + b);
+    if (p.window) {
+      off = __ldg(p.length_info + p.B + b);
+      sk = __ldg(p.length_info + 2 * p.B + b);
+    }
+  }
+  bool bad = false;
+  const SeqInfo s = seq_from(i0, i1, last, off, sk, p.P, p.window != 0, bad);
+  if (bad) set_error(p.err, kErrBadLength);
   return s;
 }
 
@@ -147,14 +180,17 @@ __device__ __forceinline__ SeqInfo load_seq(const DecodeParams& p, int b) {
 struct Pieces {
   int ra0, ra1, ob0, ob1, shift;  // run A rows [ra0,ra1) (offset = row); run B offsets [ob0,ob1)
   int pa, na, pb, nb;             // first page and count of each run
-  __device__ __forceinline__ int count() const { return na + nb; }
+  __host__ __device__ __forceinline__ int count() const { return na + nb; }
 };
 
-__device__ __forceinline__ Pieces make_pieces(int r0, int r1, const SeqInfo& s, int P) {
+__host__ __device__ __forceinline__ int imin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int imax(int a, int b) { return a > b ? a : b; }
+
+__host__ __device__ __forceinline__ Pieces make_pieces(int r0, int r1, const SeqInfo& s, int P) {
   Pieces c;
   c.ra0 = r0;
-  c.ra1 = max(r0, min(r1, s.sink));
-  const int rb0 = max(r0, s.sink), rb1 = max(rb0, r1);
+  c.ra1 = imax(r0, imin(r1, s.sink));
+  const int rb0 = imax(r0, s.sink), rb1 = imax(rb0, r1);
   c.shift = s.win_off - s.sink;
   c.ob0 = rb0 + c.shift;
   c.ob1 = rb1 + c.shift;
@@ -193,13 +229,13 @@ __device__ __forceinline__ Piece get_piece(const Pieces& c, int i, int P) {
 
 // Work units of a sequence: its pieces, or one (empty) unit when it has none, so that
 // an empty sequence still gets its output written (out = 0, lse = -5e4).
-__device__ __forceinline__ int units_of(const SeqInfo& s, int P) {
+__host__ __device__ __forceinline__ int units_of(const SeqInfo& s, int P) {
   return s.L > 0 ? make_pieces(0, s.L, s, P).count() : 1;
 }
 
 // Physical page of piece page index `pidx` (or -1 when out of range -> error bit).
 __device__ __forceinline__ int lookup_page(const DecodeParams& p, const SeqInfo& s, int pidx) {
-  if (pidx < 0 || pidx >= s.npages) {
+  if (pidx < 0 || pidx >= s.npages || (long long)s.page_begin + pidx >= p.nnz_pages) {
     set_error(p.err, kErrBadPage);
     return -1;
   }
@@ -362,6 +398,40 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
   const int C = p.seg_cost;
   const long long W = (long long)gridDim.x * WPB;
   const long long w_first = (long long)blockIdx.x * WPB;
+  if (p.hp_B && p.mode == kSchedBalanced) {
+    // host plan: the sequences' cost-line prefix is in the launch; each worker finds the
+    // sequence holding its first position by a binary search over it
+    if (tid < WPB) {
+      const int32_t* pre = p.hp;  // [B+1], strictly increasing (every sequence >= 1 unit)
+      const long long U = (long long)pre[p.B] * HZ;
+      const long long w = w_first + tid;
+      WorkerStart s;
+      s.U = U;
+      s.x0 = w * U / W;
+      s.x1 = (w + 1) * U / W;
+      s.b = -1;
+      s.hz = 0;
+      s.off = 0;
+      if (s.x0 < s.x1) {
+        int lo = 0, hi = p.B - 1;  // last b with pre[b] * HZ <= x0
+        while (lo < hi) {
+          const int mid = (lo + hi + 1) >> 1;
+          if ((long long)pre[mid] * HZ <= s.x0) lo = mid;
+          else hi = mid - 1;
+        }
+        const long long first = (long long)pre[lo] * HZ;
+        const int n = pre[lo + 1] - pre[lo];
+        s.b = lo;
+        s.hz = (int)((s.x0 - first) / n);
+        s.off = first + (long long)s.hz * n;
+      } else {
+        s.x1 = s.x0;
+      }
+      s_ws[tid] = s;
+    }
+    __syncthreads();
+    return;
+  }
   if (p.mode != kSchedBalanced) {
     if (tid < WPB) {
       const long long w = w_first + tid;

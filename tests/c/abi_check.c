@@ -1,6 +1,7 @@
 /* A plain C caller of libpageddecode: includes the public header, links the shared
  * library and exercises its host-only paths (no GPU needed): version, the split
  * planner, argument validation and the last-error string. */
+#include <stddef.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -43,5 +44,22 @@ int main(void) {
   st = pd_batch_decode_paged_kv_mq(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 0,
                                    1.0f, 1e4f, 0.1f, &d, NULL);
   printf("bad q_len %d\n", (int)st);
+  /* host copies of the page table: one without the other, or a decreasing indptr */
+  {
+    int32_t ip[3] = {0, 2, 1}, li[2] = {5, 5};
+    d = desc();
+    d.B = 2;
+    d.nnz_pages = 2;
+    d.host_indptr = ip;
+    st = pd_batch_decode_paged_kv((void*)16, (void*)16, (int32_t*)16, (int32_t*)16, (int32_t*)16, NULL,
+                                  NULL, (void*)16, (float*)16, 0, 1.0f, 1e4f, 0.1f, &d, NULL);
+    printf("host alone %d\n", (int)st);
+    d.host_length_info = li;
+    st = pd_batch_decode_paged_kv((void*)16, (void*)16, (int32_t*)16, (int32_t*)16, (int32_t*)16, NULL,
+                                  NULL, (void*)16, (float*)16, 0, 1.0f, 1e4f, 0.1f, &d, NULL);
+    printf("host decreasing %d\n", (int)st);
+  }
+  printf("desc %zu %zu %zu\n", sizeof(pd_decode_desc), offsetof(pd_decode_desc, host_indptr),
+         offsetof(pd_decode_desc, host_length_info));
   return 0;
 }

@@ -34,13 +34,16 @@ def test_header_declares_the_binding_exports():
 def test_library_exports_every_declared_symbol(L):
     for name in declared_functions():
         assert hasattr(L, name), name
-    assert L.pd_version() == 10000
+    assert L.pd_version() == 10100
 
 
 def test_desc_layout_matches_header():
-    # int32 x10, int64 x2, int32, float x2, int32, void*, size_t, const float*
-    assert ctypes.sizeof(_lib.DecodeDesc) == 96
+    # int32 x10, int64 x2, int32, float x2, int32, void*, size_t, const float*,
+    # const int32_t* x2
+    assert ctypes.sizeof(_lib.DecodeDesc) == 112
     assert _lib.DecodeDesc.sink.offset == 88
+    assert _lib.DecodeDesc.host_indptr.offset == 96
+    assert _lib.DecodeDesc.host_length_info.offset == 104
     assert _lib.DecodeDesc.max_pages.offset == 40
     assert _lib.DecodeDesc.flags.offset == 68
     assert _lib.DecodeDesc.workspace.offset == 72
@@ -198,6 +201,11 @@ def test_plain_c_caller(L, tmp_path):
     assert lines[2].startswith(f"bad heads {invalid} ") and "H_kv" in lines[2]
     assert lines[3] == f"bad flags {invalid}"
     assert lines[4] == f"bad q_len {invalid}"
+    assert lines[5] == f"host alone {invalid}"
+    assert lines[6] == f"host decreasing {invalid}"
+    # the C compiler's layout of the descriptor is the binding's
+    assert lines[7] == (f"desc {ctypes.sizeof(_lib.DecodeDesc)} {_lib.DecodeDesc.host_indptr.offset} "
+                        f"{_lib.DecodeDesc.host_length_info.offset}")
 
 
 def test_stream_workspace_arena_bookkeeping(tmp_path):

@@ -24,6 +24,7 @@ def _fake_res(step_ms, dec_ms):
     wl = W.make("llama3_8b_bf16", seed=3, reduced=True, device="cpu", B=2,
                 len_dist=("uniform", 5, 20))
     return dict(step=step_ms, dec=dec_ms, dec_med=dec_ms, app=0.005, dec_flushed=dec_ms,
+                dec_devplan=dec_ms,
                 e2e=2 * step_ms, launches=40, variant="mma", clocks=None, wl=wl, h2d=10,
                 d2h=20, alternate=True, l2=1 << 27, ext=None)
 
