@@ -4,10 +4,13 @@
 // kernel does not take (page size not a multiple of 16, D = 256).
 //
 // A block walks its share of (sequence, KV head, slice of <= 8 query heads) segments
-// (see block_range); its warps take 32-row tiles of the share in turn.  Within a tile
-// the lanes first own ROWS: lane i gathers row i's page, reads its K row in chunks,
-// rotates it (RoPE) and computes the scores of all the slice's heads with Q read from
-// shared memory (no cross-lane reduction per row).  The base-2 online softmax of the
+// (see block_range); its warps take tiles of the share's rows in turn (32 rows, fewer
+// for rows above 256 bytes).  A tile's K and V rows are gathered through the page table
+// into the warp's shared-memory stage with cp.async (every row of the tile in flight at
+// once; the next tile's page-table entries are read meanwhile).  The lanes then own
+// ROWS (one, two or four lanes per row): each reads its share of its K row, rotates it
+// (RoPE) and computes the scores of all the slice's heads with Q read from shared
+// memory (no reduction across the warp per row).  The base-2 online softmax of the
 // TVM `batch_decode_paged_kv` kernel (running max m, sum d, output O) then needs one
 // warp maximum per head per tile; each lane keeps its own rows' share of d.  For P.V
 // the lanes own DIMS: each lane accumulates its D/32 output dims over the tile's rows,
@@ -20,38 +23,32 @@
 
 namespace pd {
 
-// N consecutive elements of a row as floats, loaded with the widest vector accesses
-// their byte count allows (the chunk starts at a multiple of its own size).
+// N consecutive elements of a row in shared memory as floats (the chunk starts at a
+// multiple of its own size, at most 16 bytes apart from it).
 template <typename T, int N>
-__device__ __forceinline__ void load_row_f32(const T* src, float (&dst)[N]) {
+__device__ __forceinline__ void load_smem_f32(const T* src, float (&dst)[N]) {
   constexpr int kBytes = N * ElemBytes<T>::v;
-  if constexpr (kBytes < 4) {  // 1 or 2 bytes (E4M3 rows at D = 32, 64)
-#pragma unroll
-    for (int k = 0; k < N; ++k) dst[k] = to_f32(src[k]);
-  } else if constexpr (kBytes % 16 == 0) {
+  if constexpr (kBytes >= 16 && kBytes % 16 == 0) {
 #pragma unroll
     for (int i = 0; i < kBytes / 16; ++i) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      const uint4 v = reinterpret_cast<const uint4*>(src)[i];
       const T* e = reinterpret_cast<const T*>(&v);
 #pragma unroll
       for (int k = 0; k < 16 / (int)ElemBytes<T>::v; ++k) dst[i * (16 / ElemBytes<T>::v) + k] = to_f32(e[k]);
     }
-  } else if constexpr (kBytes % 8 == 0) {
+  } else if constexpr (kBytes == 8) {
+    const uint2 v = *reinterpret_cast<const uint2*>(src);
+    const T* e = reinterpret_cast<const T*>(&v);
 #pragma unroll
-    for (int i = 0; i < kBytes / 8; ++i) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(src) + i);
-      const T* e = reinterpret_cast<const T*>(&v);
+    for (int k = 0; k < N; ++k) dst[k] = to_f32(e[k]);
+  } else if constexpr (kBytes == 4) {
+    const unsigned v = *reinterpret_cast<const unsigned*>(src);
+    const T* e = reinterpret_cast<const T*>(&v);
 #pragma unroll
-      for (int k = 0; k < 8 / (int)ElemBytes<T>::v; ++k) dst[i * (8 / ElemBytes<T>::v) + k] = to_f32(e[k]);
-    }
+    for (int k = 0; k < N; ++k) dst[k] = to_f32(e[k]);
   } else {
 #pragma unroll
-    for (int i = 0; i < kBytes / 4; ++i) {
-      const unsigned v = __ldg(reinterpret_cast<const unsigned*>(src) + i);
-      const T* e = reinterpret_cast<const T*>(&v);
-#pragma unroll
-      for (int k = 0; k < 4 / (int)ElemBytes<T>::v; ++k) dst[i * (4 / ElemBytes<T>::v) + k] = to_f32(e[k]);
-    }
+    for (int k = 0; k < N; ++k) dst[k] = to_f32(src[k]);
   }
 }
 
@@ -67,22 +64,58 @@ __device__ __forceinline__ float exp2_kv(float x) {
   else return fast_exp2(x);
 }
 
-constexpr int kSimtChunk = 16;  // K dims (per half, with RoPE) a lane reads at a time
+// cp.async: 16 bytes global -> shared, through L2 only (completion: cp_async_wait_all)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Tile geometry of the SIMT kernel for rows of RB bytes: TR rows per warp tile (each
+// row's K and V copied into the warp's shared-memory stage), LPR = 32 / TR lanes per row
+// in the K.Q phase; a stage is about 8 KB of K plus 8 KB of V.
+template <int RB>
+struct SimtTile {
+  static constexpr int TR = RB <= 256 ? 32 : RB == 512 ? 16 : 8;
+  static constexpr int LPR = 32 / TR;
+  static constexpr int KS = RB + 16;  // K row stride in shared memory (16 bytes apart per row:
+                                      // the lanes' 16-byte reads of 8 rows cover all banks)
+  static constexpr int kStage = TR * (KS + RB);
+};
+
+template <typename KT, int D, int NW>
+struct SimtSmem {
+  static constexpr int RB = D * ElemBytes<KT>::v;
+  using Tl = SimtTile<RB>;
+  static constexpr int G8 = kMaxGroupPerCta;
+  // [Q rows G8 x D f32][probabilities NW x 32 x G8 f32][row offsets NW x 32 i64][stages NW]
+  static constexpr int kQ = 0;
+  static constexpr int kP = kQ + G8 * D * 4;
+  static constexpr int kRow = kP + NW * 32 * G8 * 4;
+  static constexpr int kStage = kRow + NW * 32 * 8;
+  static constexpr int kBytes = kStage + NW * Tl::kStage;
+  // the warps' final states [NW][G8][D] f32 reuse the space from the start
+  static_assert(NW * G8 * D * 4 <= kBytes, "state overlay");
+};
 
 template <typename KT, typename QT, int D, int NW>
-__global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NT = NW * 32;
   constexpr int E = D / 32;  // output dims per lane in P.V
   constexpr int G8 = kMaxGroupPerCta;
-  // The tile loop's Q rows and probabilities share their space with the warps' final
-  // states (a block barrier separates the two uses).
-  static_assert(G8 * D + NW * 32 * G8 <= NW * G8 * D, "shared layout");
-  __shared__ __align__(16) float s_buf[NW * G8 * D];
-  float (*s_q)[D] = reinterpret_cast<float (*)[D]>(s_buf);                 // [G8][D] Q rows (rotated, log2-scaled)
-  float (*s_p)[32][G8] = reinterpret_cast<float (*)[32][G8]>(s_buf + G8 * D);  // [NW][32][G8] probabilities
-  float* sm_o = s_buf;                                                       // [NW][G8][D] warp states
-  __shared__ long long s_row[NW][32];                // element offset of each tile row's K row, -1: none
-  __shared__ unsigned long long s_F[D / 2];          // RoPE turns per position, per frequency
+  using SM = SimtSmem<KT, D, NW>;
+  using Tl = typename SM::Tl;
+  constexpr int RB = SM::RB, TR = Tl::TR, LPR = Tl::LPR, KS = Tl::KS;
+  constexpr int FP = (D / 2) / LPR;  // RoPE frequencies (pairs) per lane of a row
+  constexpr int CH = FP < 8 ? FP : 8;
+  extern __shared__ __align__(16) unsigned char s_dyn[];
+  float (*s_q)[D] = reinterpret_cast<float (*)[D]>(s_dyn + SM::kQ);
+  float (*s_p)[32][G8] = reinterpret_cast<float (*)[32][G8]>(s_dyn + SM::kP);
+  long long (*s_row)[32] = reinterpret_cast<long long (*)[32]>(s_dyn + SM::kRow);
+  float* sm_o = reinterpret_cast<float*>(s_dyn);  // [NW][G8][D] after the tiles
+  __shared__ unsigned long long s_F[D / 2];       // RoPE turns per position, per frequency
   __shared__ float sm_m[NW * G8], sm_d[NW * G8];
 
   pdl_wait();  // nothing of the caller's is read before the previous kernel completes
@@ -92,10 +125,14 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
   const BlockRange br = block_range<NT>(p);
   if (br.x0 >= br.x1) return;  // no units for this block
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int trow = lane / LPR, part = lane % LPR;  // K.Q phase: this lane's row and part
+  unsigned char* stage = s_dyn + SM::kStage + warp * Tl::kStage;
+  unsigned char* st_k = stage;                  // [TR][KS]
+  unsigned char* st_v = stage + TR * KS;        // [TR][RB]
   const bool il = p.rotary == 2;
   const bool krot = p.rotary && !p.k_rotated;
-  const KT* pages = reinterpret_cast<const KT*>(p.pages);
-  const size_t kv_stride = (size_t)p.H_kv * p.P * D;  // K block -> V block of a page
+  const unsigned char* pages = reinterpret_cast<const unsigned char*>(p.pages);
+  const size_t kv_stride = (size_t)p.H_kv * p.P * RB;  // K block -> V block of a page (bytes)
 
   // The block walks the segments (sequence, head slice) its unit range [x0, x1) touches;
   // its share of a segment, pieces [ua, pend), is the contiguous attended-row range [r0, r1).
@@ -154,79 +191,84 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
     for (int e = 0; e < E; ++e) o[j][e] = 0.f;
   }
 
+  // byte offset in the pages of row r's K row (-1: no row / bad page)
+  auto row_offset = [&](int r) -> long long {
+    if (r >= r1) return -1;
+    const int so = r < wseq.sink ? r : r - wseq.sink + wseq.win_off;
+    const int page = lookup_page(p, wseq, so / p.P);
+    if (page < 0) return -1;
+    return ((((long long)page * 2 * p.H_kv + hk) * p.P) + (so % p.P)) * RB;
+  };
+
   // the tile loop for slices of at most HM heads (4 or 8: the scores' registers)
   auto tiles = [&](auto hm_tag) {
     constexpr int HM = decltype(hm_tag)::value;
-    for (int rb = r0 + warp * 32; rb < r1; rb += NW * 32) {
-      // ---- rows on lanes: gather, K . Q for every head
-      const int r = rb + lane;
-      long long off = -1;
-      if (r < r1) {
-        const int so = r < wseq.sink ? r : r - wseq.sink + wseq.win_off;
-        const int page = lookup_page(p, wseq, so / p.P);
-        if (page >= 0) off = ((((long long)page * 2 * p.H_kv + hk) * p.P) + (so % p.P)) * D;
+    int rb = r0 + warp * TR;
+    long long off = rb < r1 ? row_offset(rb + trow) : -1;  // this lane's row of the tile
+    for (; rb < r1; rb += NW * TR) {
+      // ---- the tile's K and V rows -> this warp's stage (each row by its LPR lanes)
+      if (part == 0) s_row[warp][trow] = off;
+      if (off >= 0) {
+#pragma unroll
+        for (int k = 0; k < RB / (16 * LPR); ++k) {
+          const int c = (k * LPR + part) * 16;
+          cp_async16(st_k + trow * KS + c, pages + off + c);
+          cp_async16(st_v + trow * RB + c, pages + off + kv_stride + c);
+        }
       }
-      s_row[warp][lane] = off;
+      // the next tile's page-table entries are read while this one streams in
+      const int rn = rb + NW * TR;
+      const long long off_next = rn < r1 ? row_offset(rn + trow) : -1;
+      cp_async_wait_all();
+      __syncwarp();
+      // ---- rows on lanes: K . Q over this lane's share of the row, summed over the row's lanes
       float sc[HM];
 #pragma unroll
       for (int j = 0; j < HM; ++j) sc[j] = 0.f;
       if (off >= 0) {
-        const KT* krow = pages + off;
-        if (!krot) {
-#pragma unroll 2
-          for (int c = 0; c < D; c += kSimtChunk) {
-            float k[kSimtChunk];
-            load_row_f32<KT, kSimtChunk>(krow + c, k);
+        const KT* krow = reinterpret_cast<const KT*>(st_k + trow * KS);
+        const int pos = kpos0 + rb + trow;
 #pragma unroll
-            for (int j = 0; j < HM; ++j) {
+        for (int c0 = 0; c0 < FP; c0 += CH) {
+          const int f0 = part * FP + c0;  // first frequency of this chunk
+          float kx[CH], ky[CH];
+          if (!il) {
+            load_smem_f32<KT, CH>(krow + f0, kx);
+            load_smem_f32<KT, CH>(krow + D / 2 + f0, ky);
+          } else {
+            float a[2 * CH];
+            load_smem_f32<KT, 2 * CH>(krow + 2 * f0, a);
 #pragma unroll
-              for (int e = 0; e < kSimtChunk; e += 4) {
-                const float4 q = *reinterpret_cast<const float4*>(&s_q[j][c + e]);
-                sc[j] = fmaf(q.x, k[e], sc[j]);
-                sc[j] = fmaf(q.y, k[e + 1], sc[j]);
-                sc[j] = fmaf(q.z, k[e + 2], sc[j]);
-                sc[j] = fmaf(q.w, k[e + 3], sc[j]);
-              }
+            for (int e = 0; e < CH; ++e) {
+              kx[e] = a[2 * e];
+              ky[e] = a[2 * e + 1];
             }
           }
-        } else {
-          // RoPE pairs: frequency i rotates (i, i + D/2), or (2i, 2i + 1) interleaved
-          const int pos = kpos0 + r;
-#pragma unroll 1
-          for (int c = 0; c < D / 2; c += kSimtChunk) {
-            float kx[kSimtChunk], ky[kSimtChunk];
-            if (!il) {
-              load_row_f32<KT, kSimtChunk>(krow + c, kx);
-              load_row_f32<KT, kSimtChunk>(krow + D / 2 + c, ky);
-            } else {
-              float a[2 * kSimtChunk];
-              load_row_f32<KT, 2 * kSimtChunk>(krow + 2 * c, a);
+          if (krot) {
 #pragma unroll
-              for (int e = 0; e < kSimtChunk; ++e) {
-                kx[e] = a[2 * e];
-                ky[e] = a[2 * e + 1];
-              }
-            }
-#pragma unroll
-            for (int e = 0; e < kSimtChunk; ++e) {
+            for (int e = 0; e < CH; ++e) {
               float cs, sn;
-              rope_cs<KT>(pos, s_F[c + e], cs, sn);
+              rope_cs<KT>(pos, s_F[f0 + e], cs, sn);
               const float x = kx[e], y = ky[e];
               kx[e] = x * cs - y * sn;
               ky[e] = y * cs + x * sn;
             }
+          }
 #pragma unroll
-            for (int j = 0; j < HM; ++j) {
+          for (int j = 0; j < HM; ++j) {
 #pragma unroll
-              for (int e = 0; e < kSimtChunk; ++e) {
-                const int dx = il ? 2 * (c + e) : c + e, dy = il ? dx + 1 : c + e + D / 2;
-                sc[j] = fmaf(s_q[j][dx], kx[e], sc[j]);
-                sc[j] = fmaf(s_q[j][dy], ky[e], sc[j]);
-              }
+            for (int e = 0; e < CH; ++e) {
+              const int dx = il ? 2 * (f0 + e) : f0 + e, dy = il ? dx + 1 : f0 + e + D / 2;
+              sc[j] = fmaf(s_q[j][dx], kx[e], sc[j]);
+              sc[j] = fmaf(s_q[j][dy], ky[e], sc[j]);
             }
           }
         }
       }
+#pragma unroll
+      for (int j = 0; j < HM; ++j)
+#pragma unroll
+        for (int k = 1; k < LPR; k <<= 1) sc[j] += __shfl_xor_sync(0xffffffffu, sc[j], k);
       // ---- online softmax: one warp maximum per head per tile
 #pragma unroll
       for (int j = 0; j < HM; ++j) {
@@ -241,18 +283,19 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
         for (int e = 0; e < E; ++e) o[j][e] *= a;
         m[j] = mn;
         const float pr = off >= 0 ? exp2_kv<KT>(s - mn) : 0.f;
-        dl[j] += pr;
-        s_p[warp][lane][j] = pr;
+        if (part == 0) {
+          dl[j] += pr;
+          s_p[warp][trow][j] = pr;
+        }
       }
       __syncwarp();
       // ---- dims on lanes: O[:, lane's dims] += p[:, row] v[row, lane's dims]
-      const int nrow = min(32, r1 - rb);
+      const int nrow = min(TR, r1 - rb);
 #pragma unroll 4
       for (int i = 0; i < nrow; ++i) {
-        const long long ro = s_row[warp][i];
-        if (ro < 0) continue;  // bad page: the row is skipped (error recorded)
+        if (s_row[warp][i] < 0) continue;  // no row (bad page: error recorded)
         float v[E];
-        load_row_f32<KT, E>(pages + ro + kv_stride + lane * E, v);
+        load_smem_f32<KT, E>(reinterpret_cast<const KT*>(st_v + i * RB) + lane * E, v);
         float pj[HM];
 #pragma unroll
         for (int j = 0; j < HM; j += 4) {
@@ -267,14 +310,15 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
 #pragma unroll
           for (int e = 0; e < E; ++e) o[j][e] = fmaf(pj[j], v[e], o[j][e]);
       }
-      __syncwarp();  // s_p / s_row are rewritten by the next tile
+      __syncwarp();  // the stage, s_p and s_row are rewritten by the next tile
+      off = off_next;
     }
   };
   if (hcount <= 4) tiles(std::integral_constant<int, 4>{});
   else tiles(std::integral_constant<int, 8>{});
 
   // warp states -> shared memory (unnormalised O, m, d = the lanes' shares summed), over
-  // the Q rows and probabilities, once every warp is done with them
+  // the Q rows, probabilities and stages, once every warp is done with them
   __syncthreads();
 #pragma unroll
   for (int j = 0; j < G8; ++j) {
@@ -297,9 +341,21 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
 template <typename KT, typename QT, int D>
 static cudaError_t launch_simt_d(const DecodeParams& p, dim3 grid, cudaStream_t st, int* ctas) {
   constexpr int NW = 4;
+  constexpr int smem = SimtSmem<KT, D, NW>::kBytes;
   auto kern = decode_simt_kernel<KT, QT, D, NW>;
-  if (ctas) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, NW * 32, 0);
-  return launch_pdl(kern, grid, dim3(NW * 32), 0, st, p);
+  // the dynamic shared memory above the default 48 KB is opted into once per device
+  static bool opted[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!opted[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    opted[dev] = true;
+  }
+  if (ctas) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, kern, NW * 32, smem);
+  return launch_pdl(kern, grid, dim3(NW * 32), smem, st, p);
 }
 
 template <typename KT, typename QT>
