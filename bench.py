@@ -368,7 +368,8 @@ def run_ours(args, ws, rank, local, config=None):
 
     # host copies of each replica's page-table offsets and lengths (the serving
     # scheduler's own arrays): the decode plans its split from them on the host
-    metas = {id(r[0]): pd._lib.host_meta_of(r[0].indptr, r[0].length_info) for r in reps}
+    metas = {id(r[0]): pd._lib.host_meta_of(r[0].indptr, r[0].length_info, r[0].values)
+             for r in reps}
     use_host_plan = [True]
 
     def decode(r):
@@ -584,8 +585,12 @@ def main():
                     help="override the batch size (smaller cases for profiling)")
     ap.add_argument("--page-size", type=int, default=None,
                     help="override the page size (the pool keeps its row count)")
+    ap.add_argument("--q-len", type=int, default=None,
+                    help="override the query tokens per sequence (multi-query decode)")
     args = ap.parse_args()
     args.over = {} if args.B is None else {"B": args.B}
+    if args.q_len is not None:
+        args.over["q_len"] = args.q_len
     if args.page_size is not None:
         base = W.spec(args.config)
         args.over["page_size"] = args.page_size

@@ -105,6 +105,12 @@ typedef struct {
                                  serving scheduler that builds these arrays holds them on the
                                  host anyway).  Read during the call only.  Page-table reads
                                  stay bounds-checked against nnz_pages. */
+  const int32_t* host_values;       /* optional HOST copy of page_table_values [nnz_pages], or
+                                 NULL; only with host_indptr / host_length_info.  Used on the
+                                 host to find each worker's first page, which the tensor-core
+                                 kernel prefetches into L2 at its first instruction (a hint:
+                                 the kernel still reads page_table_values itself).  Read
+                                 during the call only. */
 } pd_decode_desc;
 
 /*

@@ -19,7 +19,7 @@ constexpr int kMaxHalfDim = 128;    // D <= 256
 constexpr int kMmaWarps = 4;        // warps (independent workers) per tensor-core block
 constexpr int kStartCacheB = 1024;  // batch sizes whose start-up scan runs in shared memory
 // Host plan: ints of sequence metadata the launch itself may carry (see DecodeParams::hp)
-constexpr int kHostPlanInts = 1024;
+constexpr int kHostPlanInts = 4096;
 
 // Block schedules (DecodeParams::mode)
 enum : int {
@@ -44,6 +44,10 @@ struct DecodeParams {
   long long max_pages;
   long long nnz_pages;  // entries of the page table (page_table_values)
   int B, H_qo, H_kv, D, P, group, n_z;
+  int zg;             // 1, or n_z (2 or 4): the n_z slices of a (sequence, KV head) run on
+                      // n_z adjacent warps of one block, which walk the same pages together
+                      // (the cost line then holds (sequence, KV head) groups, one position per
+                      // page, and every group of n_z warps takes one share of it)
   int q_len;          // query tokens per sequence (multi-query decode; 1 = plain decode)
   int ncol;           // query columns per KV head: q_len * group, in slices of <= 8
   int window, rotary;
@@ -66,7 +70,10 @@ struct DecodeParams {
   // hp[hp_li ..] = length_info [B] or [3,B].  The kernels then read a sequence's
   // lengths and page-table offset from here, and each worker finds its first segment
   // by a binary search over the prefix, without the start-up scan of device memory.
-  int hp_B, hp_ptr, hp_li;
+  // With the host copy of page_table_values too, hp[hp_first + w] (w < hp_nw) is the
+  // (page, K, KV head) block index of worker w's first tile, or -1: each worker
+  // prefetches that block and its V block into L2 at its first instruction.
+  int hp_B, hp_ptr, hp_li, hp_first, hp_nw;
   int32_t hp[kHostPlanInts];
 };
 
@@ -205,7 +212,7 @@ struct Piece {
   int page_idx, s_lo, s_hi, r_lo;
 };
 
-__device__ __forceinline__ Piece get_piece(const Pieces& c, int i, int P) {
+__host__ __device__ __forceinline__ Piece get_piece(const Pieces& c, int i, int P) {
   Piece q;
   int lo, hi, shift;
   if (i < c.na) {
@@ -356,22 +363,30 @@ __device__ BlockRange block_range(const DecodeParams& p) {
 __device__ __forceinline__ bool next_segment(const DecodeParams& p, Segment& s, int extra = 0) {
   const int HZ = p.H_kv * p.n_z;
   s.off += s.n + extra;
-  if (s.hz + 1 < HZ) {
-    ++s.hz;
+  if (s.hz + p.zg < HZ) {  // the next KV head's slice of this warp (zg = 1: next slice)
+    s.hz += p.zg;
     return true;
   }
   if (s.b + 1 >= p.B) return false;
   ++s.b;
-  s.hz = 0;
+  s.hz = s.hz % p.zg;
   s.seq = load_seq(p, s.b);
   s.n = units_of(s.seq, p.P);
   return true;
 }
 
+// floor(a / b) for 0 <= a, 0 < b: the hardware-friendly 32-bit division when both fit in
+// 32 bits (the usual case: cost-line positions times worker counts), else the 64-bit one.
+__device__ __forceinline__ long long div_floor(long long a, long long b) {
+  if (((unsigned long long)a | (unsigned long long)b) < (1ull << 32))
+    return (long long)((unsigned)a / (unsigned)b);
+  return a / b;
+}
+
 // Share (block or worker) whose balanced range holds global unit x, with G shares:
 // floor(((x+1) G - 1) / U).
 __device__ __forceinline__ long long share_of(long long x, long long U, long long G) {
-  return ((x + 1) * G - 1) / U;
+  return div_floor((x + 1) * G - 1, U);
 }
 
 // ---------------------------------------------------------------------------- workers
@@ -394,9 +409,13 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
   __shared__ long long s_warp[NT / 32];
   __shared__ long long s_hit[WPB][2];
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int HZ = p.H_kv * p.n_z;
   const int C = p.seg_cost;
-  const long long W = (long long)gridDim.x * WPB;
+  // grouped slices (zg > 1): the line holds (sequence, KV head) groups and each group of
+  // zg adjacent workers takes one share of it; worker i of the block is line worker
+  // (w_first + i) / zg, slice (w_first + i) % zg of each group
+  const int zg = p.mode == kSchedBalanced ? p.zg : 1;
+  const int HZ = p.H_kv * p.n_z / zg;
+  const long long W = (long long)gridDim.x * WPB / zg;
   const long long w_first = (long long)blockIdx.x * WPB;
   if (p.hp_B && p.mode == kSchedBalanced) {
     // host plan: the sequences' cost-line prefix is in the launch; each worker finds the
@@ -404,11 +423,11 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
     if (tid < WPB) {
       const int32_t* pre = p.hp;  // [B+1], strictly increasing (every sequence >= 1 unit)
       const long long U = (long long)pre[p.B] * HZ;
-      const long long w = w_first + tid;
+      const long long w = (w_first + tid) / zg;
       WorkerStart s;
       s.U = U;
-      s.x0 = w * U / W;
-      s.x1 = (w + 1) * U / W;
+      s.x0 = div_floor(w * U, W);
+      s.x1 = div_floor((w + 1) * U, W);
       s.b = -1;
       s.hz = 0;
       s.off = 0;
@@ -424,6 +443,7 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
         s.b = lo;
         s.hz = (int)((s.x0 - first) / n);
         s.off = first + (long long)s.hz * n;
+        s.hz = s.hz * zg + (int)((w_first + tid) % zg);
       } else {
         s.x1 = s.x0;
       }
@@ -484,7 +504,7 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
       const long long hi = lo + (long long)(s_units[b] + C) * HZ;
 #pragma unroll
       for (int i = 0; i < WPB; ++i) {
-        const long long t = (w_first + i) * U / W;
+        const long long t = ((w_first + i) / zg) * U / W;
         if (t >= lo && t < hi) {
           s_hit[i][0] = b;
           s_hit[i][1] = lo;  // = HZ * (units of the sequences before b)
@@ -534,7 +554,7 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
       const long long lo = base + incl - n, hi = base + incl;
 #pragma unroll
       for (int i = 0; i < WPB; ++i) {
-        const long long t = (w_first + i) * U / W;
+        const long long t = ((w_first + i) / zg) * U / W;
         if (b < p.B && t >= lo && t < hi) {
           s_hit[i][0] = b;
           s_hit[i][1] = lo;
@@ -545,7 +565,7 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
     }
   }
   if (tid < WPB) {
-    const long long w = w_first + tid;
+    const long long w = (w_first + tid) / zg;
     WorkerStart s;
     s.U = U;
     s.x0 = w * U / W;
@@ -560,6 +580,7 @@ __device__ void worker_starts(const DecodeParams& p, WorkerStart* s_ws, int* s_u
       const int n = C + (s.b < kStartCacheB && p.B <= kStartCacheB ? s_units[s.b] : units_of(load_seq(p, s.b), p.P));
       s.hz = (int)((s.x0 - s_hit[tid][1]) / n);
       s.off = s_hit[tid][1] + (long long)s.hz * n;
+      s.hz = s.hz * zg + (int)((w_first + tid) % zg);
     }
     s_ws[tid] = s;
   }
@@ -582,9 +603,16 @@ __device__ __forceinline__ void store_out(const DecodeParams& p, size_t idx, flo
 // or -1 when block cc's range is empty (it wrote nothing).
 __device__ __forceinline__ long long share_slot(long long cc, long long off, long long U,
                                                 long long G) {
-  const long long x0 = cc * U / G;
-  if ((cc + 1) * U / G <= x0) return -1;
+  const long long x0 = div_floor(cc * U, G);
+  if (div_floor((cc + 1) * U, G) <= x0) return -1;
   return (2 * cc + (off <= x0 ? 0 : 1)) * kMaxGroupPerCta;
+}
+// The same for line worker cc of a grouped schedule: its slice-z worker is cc * zg + z.
+__device__ __forceinline__ long long share_slot_z(long long cc, long long off, long long U,
+                                                  long long G, int zg, int z) {
+  const long long x0 = div_floor(cc * U, G);
+  if (div_floor((cc + 1) * U, G) <= x0) return -1;
+  return (2 * (cc * zg + z) + (off <= x0 ? 0 : 1)) * kMaxGroupPerCta;
 }
 
 // Combine the partial states of every block holding units of segment `sg` into the

@@ -157,7 +157,7 @@ __device__ __forceinline__ void store_run(const DecodeParams& p, size_t idx, con
 template <int D, int HMAX, int BATCH, bool MQ>
 __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, int seg_c, int seg_n,
                            long long U, long long W, int hk, int c0, int hcount,
-                           float (*s_w)[kMaxGroupPerCta], int* s_sl) {
+                           float (*s_w)[kMaxGroupPerCta], int* s_sl, int zg, int zw) {
   constexpr int G8 = kMaxGroupPerCta;
   constexpr int D4 = D / 4;
   constexpr int kV = (HMAX * D4 + 31) / 32;  // float4 outputs per lane
@@ -165,7 +165,8 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
   const int lane = threadIdx.x & 31;
   const long long w0 = share_of(seg_off + seg_c, U, W);
   const int ns = (int)(share_of(seg_off + seg_c + seg_n - 1, U, W) - w0 + 1);
-  const long long sl0 = share_slot(w0, seg_off, U, W);  // worker w0 always holds units
+  // line worker w's slot for this slice: worker w * zg + zw (zg = 1: w itself)
+  const long long sl0 = share_slot_z(w0, seg_off, U, W, zg, zw);  // worker w0 always holds units
   float* s_M = s_w[32];
   float* s_den = s_w[33];
   float4 acc[kV];
@@ -207,7 +208,7 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
 #pragma unroll
     for (int j = 0; j < HMAX; ++j) v[j] = kEmptyM;
     if (lane < ns) {
-      sl = share_slot(w0 + lane, seg_off, U, W);
+      sl = share_slot_z(w0 + lane, seg_off, U, W, zg, zw);
       if (sl >= 0) {
 #pragma unroll
         for (int q = 0; q < HMAX / 4; ++q) {
@@ -254,7 +255,7 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
       den[j] = 0.f;
     }
     for (int s = lane; s < ns; s += 32) {
-      const long long sl = share_slot(w0 + s, seg_off, U, W);
+      const long long sl = share_slot_z(w0 + s, seg_off, U, W, zg, zw);
       if (sl < 0) continue;
 #pragma unroll
       for (int j = 0; j < HMAX; ++j) M[j] = fmaxf(M[j], j < hcount ? __ldcg(p.part_lse + sl + j) : kEmptyM);
@@ -265,7 +266,7 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
       for (int off = 16; off > 0; off >>= 1) M[j] = fmaxf(M[j], __shfl_xor_sync(0xffffffffu, M[j], off));
     for (int base = 0; base < ns; base += 32) {
       const int s = base + lane;
-      const long long sl = s < ns ? share_slot(w0 + s, seg_off, U, W) : -1;
+      const long long sl = s < ns ? share_slot_z(w0 + s, seg_off, U, W, zg, zw) : -1;
 #pragma unroll
       for (int j = 0; j < HMAX; ++j) {
         const float w = (sl >= 0 && j < hcount) ? merge_exp2(p, __ldcg(p.part_lse + sl + j) - M[j]) : 0.f;
@@ -369,6 +370,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   __shared__ __align__(16) float2 s_rot8[KROT ? rope_slots(D) : 2];  // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
 
+  // the host plan's first-tile hint: this worker's first K and V blocks start coming into
+  // L2 now, while the set-up below runs
+  if (p.hp_nw && (threadIdx.x & 31) == 0) {
+    const int w = blockIdx.x * NW + (threadIdx.x >> 5);
+    const int blk = w < p.hp_nw ? p.hp[p.hp_first + w] : -1;
+    if (blk >= 0) {
+      const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.pages) + (size_t)blk * p.P * Tr::kRowBytes;
+      prefetch_l2_bulk(kb, (uint32_t)(p.P * Tr::kRowBytes));
+      prefetch_l2_bulk(kb + (size_t)p.H_kv * p.P * Tr::kRowBytes, (uint32_t)(p.P * Tr::kRowBytes));
+    }
+  }
   // Q and the page table are small and needed right after the start-up scan, when the
   // first tiles of every worker flood HBM: each block prefetches its share into L2 now
   if (threadIdx.x == 0) {
@@ -404,7 +416,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   const uint8_t* kv_base = reinterpret_cast<const uint8_t*>(p.pages);
   const size_t block_bytes = (size_t)P * RB;          // one (page, K|V, head) block
   const size_t v_off = (size_t)p.H_kv * block_bytes;  // K block -> V block
-  const long long Wn = (long long)gridDim.x * NW;
+  // line workers (grouped slices: zg adjacent warps share one) and this warp's slice
+  const int zg = p.mode == kSchedBalanced ? p.zg : 1;
+  const long long Wn = (long long)gridDim.x * NW / zg;
   const long long wid = (long long)blockIdx.x * NW + warp;
 
   Segment sg;
@@ -1015,9 +1029,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
     constexpr int kBudget = MinBlocks<KROT, FP8>::v >= 3 ? 4 : 16;
     constexpr int kV4 = (4 * (D / 4) + 31) / 32, kV8 = (8 * (D / 4) + 31) / 32;
     if (hcount <= 4)
-      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
+      warp_merge<D, 4, (kBudget / kV4 > 1 ? kBudget / kV4 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp], zg, (int)(wid % zg));
     else
-      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp]);
+      warp_merge<D, 8, (kBudget / kV8 > 1 ? kBudget / kV8 : 1), MQ>(p, (int)b, off, C, n, ws.U, Wn, hk, c0, hcount, s_mw[warp], s_msl[warp], zg, (int)(wid % zg));
   }
 }
 

@@ -4,11 +4,11 @@
 // kernel does not take (page size not a multiple of 16, D = 256).
 //
 // A block walks its share of (sequence, KV head, slice of <= 8 query heads) segments
-// (see block_range); its warps take tiles of the share's rows in turn (32 rows, fewer
-// for rows above 256 bytes).  A tile's K and V rows are gathered through the page table
+// (see block_range); its warps take tiles of the share's rows in turn (4 KB of K rows
+// per tile: 32 rows of 128 bytes down to 4 rows of 1 KB).  A tile's K and V rows are gathered through the page table
 // into the warp's shared-memory stage with cp.async (every row of the tile in flight at
 // once; the next tile's page-table entries are read meanwhile).  The lanes then own
-// ROWS (one, two or four lanes per row): each reads its share of its K row, rotates it
+// ROWS (one to eight lanes per row): each reads its share of its K row, rotates it
 // (RoPE) and computes the scores of all the slice's heads with Q read from shared
 // memory (no reduction across the warp per row).  The base-2 online softmax of the
 // TVM `batch_decode_paged_kv` kernel (running max m, sum d, output O) then needs one
@@ -75,10 +75,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
 
 // Tile geometry of the SIMT kernel for rows of RB bytes: TR rows per warp tile (each
 // row's K and V copied into the warp's shared-memory stage), LPR = 32 / TR lanes per row
-// in the K.Q phase; a stage is about 8 KB of K plus 8 KB of V.
+// in the K.Q phase; a stage is about 4 KB of K plus 4 KB of V, so that three blocks of
+// four warps fit on an SM with the RoPE tables.
 template <int RB>
 struct SimtTile {
-  static constexpr int TR = RB <= 256 ? 32 : RB == 512 ? 16 : 8;
+  static constexpr int TR = RB <= 128 ? 32 : RB == 256 ? 16 : RB == 512 ? 8 : 4;
   static constexpr int LPR = 32 / TR;
   static constexpr int KS = RB + 16;  // K row stride in shared memory (16 bytes apart per row:
                                       // the lanes' 16-byte reads of 8 rows cover all banks)
@@ -91,17 +92,21 @@ struct SimtSmem {
   using Tl = SimtTile<RB>;
   static constexpr int G8 = kMaxGroupPerCta;
   // [Q rows G8 x D f32][probabilities NW x 32 x G8 f32][row offsets NW x 32 i64][stages NW]
+  // and, with RoPE on K, [per-warp Q rows NW x G8 x D f32][row rotations TR x D/2 float2]
   static constexpr int kQ = 0;
   static constexpr int kP = kQ + G8 * D * 4;
   static constexpr int kRow = kP + NW * 32 * G8 * 4;
   static constexpr int kStage = kRow + NW * 32 * 8;
   static constexpr int kBytes = kStage + NW * Tl::kStage;
+  static constexpr int kQW = kBytes;
+  static constexpr int kRT = kQW + NW * G8 * D * 4;
+  static constexpr int kBytesRope = kRT + Tl::TR * (D / 2) * 8;
   // the warps' final states [NW][G8][D] f32 reuse the space from the start
   static_assert(NW * G8 * D * 4 <= kBytes, "state overlay");
 };
 
 template <typename KT, typename QT, int D, int NW>
-__global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NT = NW * 32;
   constexpr int E = D / 32;  // output dims per lane in P.V
   constexpr int G8 = kMaxGroupPerCta;
@@ -114,6 +119,11 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
   float (*s_q)[D] = reinterpret_cast<float (*)[D]>(s_dyn + SM::kQ);
   float (*s_p)[32][G8] = reinterpret_cast<float (*)[32][G8]>(s_dyn + SM::kP);
   long long (*s_row)[32] = reinterpret_cast<long long (*)[32]>(s_dyn + SM::kRow);
+  // RoPE on K: a tile's rows sit at positions base + t (t = 0 .. TR-1); K row t is turned
+  // by t positions (s_rt, the same for every tile) and each warp's Q rows by -base
+  // (s_qw), since R(qpos) q . R(base + t) k = R(qpos - base) q . R(t) k
+  float (*s_qw)[G8][D] = reinterpret_cast<float (*)[G8][D]>(s_dyn + SM::kQW);
+  float2 (*s_rt)[D / 2] = reinterpret_cast<float2 (*)[D / 2]>(s_dyn + SM::kRT);
   float* sm_o = reinterpret_cast<float*>(s_dyn);  // [NW][G8][D] after the tiles
   __shared__ unsigned long long s_F[D / 2];       // RoPE turns per position, per frequency
   __shared__ float sm_m[NW * G8], sm_d[NW * G8];
@@ -122,9 +132,15 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
   pdl_release();
   if (p.rotary)
     for (int i = threadIdx.x; i < D / 2; i += NT) s_F[i] = p.rope_F[i];
-  const BlockRange br = block_range<NT>(p);
+  const BlockRange br = block_range<NT>(p);  // (its barriers also publish s_F)
   if (br.x0 >= br.x1) return;  // no units for this block
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (p.rotary && !p.k_rotated)  // published by the barrier after the first Q build
+    for (int it = tid; it < TR * (D / 2); it += NT) {
+      float c, sn;
+      rope_cs<KT>(it / (D / 2), s_F[it % (D / 2)], c, sn);
+      s_rt[it / (D / 2)][it % (D / 2)] = make_float2(c, sn);
+    }
   const int trow = lane / LPR, part = lane % LPR;  // K.Q phase: this lane's row and part
   unsigned char* stage = s_dyn + SM::kStage + warp * Tl::kStage;
   unsigned char* st_k = stage;                  // [TR][KS]
@@ -182,14 +198,6 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
   __syncthreads();
 
   const int kpos0 = krot ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
-  float m[G8], dl[G8], o[G8][E];
-#pragma unroll
-  for (int j = 0; j < G8; ++j) {
-    m[j] = kEmptyM;
-    dl[j] = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) o[j][e] = 0.f;
-  }
 
   // byte offset in the pages of row r's K row (-1: no row / bad page)
   auto row_offset = [&](int r) -> long long {
@@ -203,9 +211,31 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
   // the tile loop for slices of at most HM heads (4 or 8: the scores' registers)
   auto tiles = [&](auto hm_tag) {
     constexpr int HM = decltype(hm_tag)::value;
+    float m[HM], dl[HM], o[HM][E];  // this warp's state of the slice's (first HM) heads
+#pragma unroll
+    for (int j = 0; j < HM; ++j) {
+      m[j] = kEmptyM;
+      dl[j] = 0.f;
+#pragma unroll
+      for (int e = 0; e < E; ++e) o[j][e] = 0.f;
+    }
     int rb = r0 + warp * TR;
     long long off = rb < r1 ? row_offset(rb + trow) : -1;  // this lane's row of the tile
     for (; rb < r1; rb += NW * TR) {
+      if (krot) {  // this tile's Q rows, turned by -(position of its row 0)
+        const int base = kpos0 + rb;
+        for (int i = lane; i < D / 2; i += 32) {
+          float c, sn;
+          rope_cs<KT>(-base, s_F[i], c, sn);
+          const int dx = il ? 2 * i : i, dy = il ? 2 * i + 1 : i + D / 2;
+#pragma unroll
+          for (int j = 0; j < HM; ++j) {
+            const float x = s_q[j][dx], y = s_q[j][dy];
+            s_qw[warp][j][dx] = x * c - y * sn;
+            s_qw[warp][j][dy] = y * c + x * sn;
+          }
+        }
+      }
       // ---- the tile's K and V rows -> this warp's stage (each row by its LPR lanes)
       if (part == 0) s_row[warp][trow] = off;
       if (off >= 0) {
@@ -227,7 +257,7 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
       for (int j = 0; j < HM; ++j) sc[j] = 0.f;
       if (off >= 0) {
         const KT* krow = reinterpret_cast<const KT*>(st_k + trow * KS);
-        const int pos = kpos0 + rb + trow;
+        const float* qbase = krot ? &s_qw[warp][0][0] : &s_q[0][0];
 #pragma unroll
         for (int c0 = 0; c0 < FP; c0 += CH) {
           const int f0 = part * FP + c0;  // first frequency of this chunk
@@ -247,20 +277,35 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
           if (krot) {
 #pragma unroll
             for (int e = 0; e < CH; ++e) {
-              float cs, sn;
-              rope_cs<KT>(pos, s_F[f0 + e], cs, sn);
+              const float2 cs = s_rt[trow][f0 + e];
               const float x = kx[e], y = ky[e];
-              kx[e] = x * cs - y * sn;
-              ky[e] = y * cs + x * sn;
+              kx[e] = x * cs.x - y * cs.y;
+              ky[e] = y * cs.x + x * cs.y;
             }
           }
 #pragma unroll
           for (int j = 0; j < HM; ++j) {
+            float qx[CH], qy[CH];  // Q of the chunk's pairs, read as 16-byte vectors
+            const float* qj = qbase + j * D;
+            if (!il) {
+#pragma unroll
+              for (int e = 0; e < CH; e += 4) {
+                const float4 a = *reinterpret_cast<const float4*>(qj + f0 + e);
+                const float4 b = *reinterpret_cast<const float4*>(qj + D / 2 + f0 + e);
+                qx[e] = a.x; qx[e + 1] = a.y; qx[e + 2] = a.z; qx[e + 3] = a.w;
+                qy[e] = b.x; qy[e + 1] = b.y; qy[e + 2] = b.z; qy[e + 3] = b.w;
+              }
+            } else {
+#pragma unroll
+              for (int e = 0; e < CH; e += 2) {
+                const float4 a = *reinterpret_cast<const float4*>(qj + 2 * (f0 + e));
+                qx[e] = a.x; qy[e] = a.y; qx[e + 1] = a.z; qy[e + 1] = a.w;
+              }
+            }
 #pragma unroll
             for (int e = 0; e < CH; ++e) {
-              const int dx = il ? 2 * (f0 + e) : f0 + e, dy = il ? dx + 1 : f0 + e + D / 2;
-              sc[j] = fmaf(s_q[j][dx], kx[e], sc[j]);
-              sc[j] = fmaf(s_q[j][dy], ky[e], sc[j]);
+              sc[j] = fmaf(qx[e], kx[e], sc[j]);
+              sc[j] = fmaf(qy[e], ky[e], sc[j]);
             }
           }
         }
@@ -313,23 +358,23 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
       __syncwarp();  // the stage, s_p and s_row are rewritten by the next tile
       off = off_next;
     }
+    // warp states -> shared memory (unnormalised O, m, d = the lanes' shares summed),
+    // over the Q rows, probabilities and stages, once every warp is done with them
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < G8; ++j) {
+      const float d = j < HM ? warp_sum(dl[j < HM ? j : 0]) : 0.f;
+      if (lane == 0) {
+        sm_m[warp * G8 + j] = j < HM ? m[j < HM ? j : 0] : kEmptyM;
+        sm_d[warp * G8 + j] = d;
+      }
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        sm_o[(warp * G8 + j) * D + lane * E + e] = j < HM ? o[j < HM ? j : 0][e] : 0.f;
+    }
   };
   if (hcount <= 4) tiles(std::integral_constant<int, 4>{});
   else tiles(std::integral_constant<int, 8>{});
-
-  // warp states -> shared memory (unnormalised O, m, d = the lanes' shares summed), over
-  // the Q rows, probabilities and stages, once every warp is done with them
-  __syncthreads();
-#pragma unroll
-  for (int j = 0; j < G8; ++j) {
-    const float d = warp_sum(dl[j]);
-    if (lane == 0) {
-      sm_m[warp * G8 + j] = m[j];
-      sm_d[warp * G8 + j] = d;
-    }
-#pragma unroll
-    for (int e = 0; e < E; ++e) sm_o[(warp * G8 + j) * D + lane * E + e] = o[j][e];
-  }
   __syncthreads();
   finish_share<NT, NW>(p, br, sg, ua, ub, hq0, hcount, sm_m, sm_d, sm_o);
   if (sg.off + sg.n >= br.x1 || !next_segment(p, sg)) break;
@@ -341,7 +386,8 @@ __global__ void __launch_bounds__(NW * 32) decode_simt_kernel(const __grid_const
 template <typename KT, typename QT, int D>
 static cudaError_t launch_simt_d(const DecodeParams& p, dim3 grid, cudaStream_t st, int* ctas) {
   constexpr int NW = 4;
-  constexpr int smem = SimtSmem<KT, D, NW>::kBytes;
+  using SM = SimtSmem<KT, D, NW>;
+  const int smem = p.rotary && !p.k_rotated ? SM::kBytesRope : SM::kBytes;
   auto kern = decode_simt_kernel<KT, QT, D, NW>;
   // the dynamic shared memory above the default 48 KB is opted into once per device
   static bool opted[64];
@@ -350,7 +396,7 @@ static cudaError_t launch_simt_d(const DecodeParams& p, dim3 grid, cudaStream_t 
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!opted[dev]) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SM::kBytesRope);
     if (e != cudaSuccess) return e;
     opted[dev] = true;
   }

@@ -72,9 +72,12 @@ def test_mq_matches_oracle(name, over, q_len):
 
 @pytest.mark.parametrize("kv", ["bf16", "f16"])
 @pytest.mark.parametrize("D", [64, 128])
-@pytest.mark.parametrize("group,q_len", [(1, 4), (2, 3), (4, 2), (8, 2), (12, 3)])
+@pytest.mark.parametrize("group,q_len", [(1, 4), (2, 3), (4, 2), (8, 2), (12, 3), (4, 4), (2, 8),
+                                         (8, 4), (4, 8), (16, 2), (8, 3)])
 def test_mq_group_sweep(kv, D, group, q_len):
-    # columns = q_len x group per KV head, cut into slices of <= 8 (packed below 5)
+    # columns = q_len x group per KV head, cut into slices of <= 8 (packed below 5); 16 and
+    # 32 columns (two or four slices) run as grouped slices whose warps walk the same pages
+    # side by side, 24 and 36 columns as separate segments
     wl, Q = _mq("llama3_8b_bf16", 50 + group, q_len, q_dtype=kv, kv_dtype=kv, out_dtype=kv, D=D,
                 H_kv=2, H_qo=2 * group, B=3, len_dist=("uniform", 1, 300), pool=200,
                 rotary_mode=int(group % 2 == 0))
