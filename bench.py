@@ -368,8 +368,7 @@ def run_ours(args, ws, rank, local, config=None):
 
     # host copies of each replica's page-table offsets and lengths (the serving
     # scheduler's own arrays): the decode plans its split from them on the host
-    metas = {id(r[0]): pd._lib.host_meta_of(r[0].indptr, r[0].length_info, r[0].values)
-             for r in reps}
+    metas = {id(r[0]): pd._lib.host_meta_of(r[0].indptr, r[0].length_info) for r in reps}
     use_host_plan = [True]
 
     def decode(r):

@@ -91,7 +91,6 @@ class DecodeDesc(ctypes.Structure):
         ("sink", ctypes.c_void_p),
         ("host_indptr", ctypes.c_void_p),
         ("host_length_info", ctypes.c_void_p),
-        ("host_values", ctypes.c_void_p),
     ]
 
 
@@ -172,8 +171,8 @@ DECODE_K_ROTATED = 2
 def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_kv_len_hint=0,
               k_scale=1.0, v_scale=1.0, workspace=None, early_inputs=False,
               sink=None, k_rotated=False, host_meta=None) -> DecodeDesc:
-    """host_meta: optional (indptr, length_info[, values]) numpy int32 host copies (the
-    caller keeps them alive for the call)."""
+    """host_meta: optional (indptr, length_info) numpy int32 host copies (the caller keeps
+    them alive for the call)."""
     B, H_qo, D = Q.shape
     max_pages, two, H_kv, P, D2 = pages.shape
     if two != 2 or D2 != D:
@@ -189,9 +188,7 @@ def make_desc(Q, pages, indptr, values, length_info, out, *, num_splits=0, max_k
         workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
         sink=_sink_ptr(sink, H_qo),
         host_indptr=None if host_meta is None else _host_i32(host_meta[0], B + 1),
-        host_length_info=None if host_meta is None else _host_i32(host_meta[1], length_info.numel()),
-        host_values=None if host_meta is None or len(host_meta) < 3 or host_meta[2] is None
-        else _host_i32(host_meta[2], values.numel()))
+        host_length_info=None if host_meta is None else _host_i32(host_meta[1], length_info.numel()))
 
 
 def _host_i32(a, n):
@@ -201,15 +198,11 @@ def _host_i32(a, n):
     return a.ctypes.data
 
 
-def host_meta_of(indptr, length_info, values=None):
-    """Host copies (numpy int32) of a page table's indptr, length_info and (optionally)
-    values, for host_meta."""
+def host_meta_of(indptr, length_info):
+    """Host copies (numpy int32) of a page table's indptr and length_info, for host_meta."""
     import numpy as np
-    meta = (np.ascontiguousarray(indptr.cpu().numpy(), dtype=np.int32),
+    return (np.ascontiguousarray(indptr.cpu().numpy(), dtype=np.int32),
             np.ascontiguousarray(length_info.cpu().numpy(), dtype=np.int32).reshape(-1))
-    if values is not None:
-        meta += (np.ascontiguousarray(values.cpu().numpy(), dtype=np.int32),)
-    return meta
 
 
 def _sink_ptr(sink, H_qo):

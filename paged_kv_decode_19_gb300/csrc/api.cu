@@ -176,7 +176,7 @@ static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int
 // Tensor-core variant eligibility (pages == nullptr: ignore the pointer's alignment).
 static bool mma_path(const pd_decode_desc* d, const void* pages) {
   if ((reinterpret_cast<uintptr_t>(pages) & 15) != 0) return false;
-  if (d->page_size % 16 != 0) return false;
+  if (d->page_size % 8 != 0) return false;
   if (d->kv_dtype == kBF16 || d->kv_dtype == kF16) return d->D == 64 || d->D == 128;
   if (d->kv_dtype == kE4M3) return d->D == 128 && (d->q_dtype == kBF16 || d->q_dtype == kF16);
   return false;
@@ -196,12 +196,8 @@ static cudaError_t mma_dispatch(const DecodeParams& p, int q_dtype, int kv_dtype
 
 // Host plan: copy the caller's host indptr / length_info into the launch, with the
 // prefix over the sequences of (work units + segment cost) that places the workers
-// (the device's units_of on the same fields).  With host values and `workers` > 0 (the
-// tensor-core kernel's balanced schedule), also each worker's first-tile block hint,
-// found with the device's own arithmetic (worker_starts, first_tile_from).  False when
-// the plan does not fit.
-static long long host_div_floor(long long a, long long b) { return a / b; }
-static bool fill_host_plan(const pd_decode_desc& d, DecodeParams& p, long long workers = 0) {
+// (the device's units_of on the same fields).  False when they do not fit.
+static bool fill_host_plan(const pd_decode_desc& d, DecodeParams& p) {
   const int B = d.B;
   const long long li_n = d.sliding_window ? 3ll * B : (long long)B;
   if (2ll * (B + 1) + li_n > kHostPlanInts) return false;
@@ -223,51 +219,6 @@ static bool fill_host_plan(const pd_decode_desc& d, DecodeParams& p, long long w
   p.hp[p.hp_ptr + B] = ip[B];
   for (long long i = 0; i < li_n; ++i) p.hp[p.hp_li + i] = li[i];
   p.hp_B = B;
-  p.hp_first = 0;
-  p.hp_nw = 0;
-  const long long used = p.hp_li + li_n;
-  if (d.host_values && workers > 0 && p.mode == kSchedBalanced && used + workers <= kHostPlanInts) {
-    // grouped slices: zg adjacent workers form one line worker (worker_starts)
-    const int zg = p.zg;
-    const int HZ = d.H_kv * p.n_z / zg;
-    const long long U = (long long)p.hp[B] * HZ, Wl = workers / zg;
-    const int C = p.seg_cost;
-    for (long long w = 0; w < workers; ++w) {
-      int32_t hint = -1;
-      const long long lw = w / zg;
-      const long long x0 = host_div_floor(lw * U, Wl), x1 = host_div_floor((lw + 1) * U, Wl);
-      if (x0 < x1) {
-        int lo = 0, hi = B - 1;  // last b with prefix[b] * HZ <= x0
-        while (lo < hi) {
-          const int mid = (lo + hi + 1) >> 1;
-          if ((long long)p.hp[mid] * HZ <= x0) lo = mid;
-          else hi = mid - 1;
-        }
-        const long long first = (long long)p.hp[lo] * HZ;
-        const int n = p.hp[lo + 1] - p.hp[lo];
-        const int hz = (int)((x0 - first) / n);
-        const long long off = first + (long long)hz * n;
-        const long long off_b = d.sliding_window ? li[B + lo] : 0, sk_b = d.sliding_window ? li[2 * B + lo] : 0;
-        bool bad = false;
-        const SeqInfo s = seq_from(ip[lo], ip[lo + 1], li[lo], off_b, sk_b, d.page_size,
-                                   d.sliding_window != 0, bad);
-        const Pieces pcs = make_pieces(0, s.L, s, d.page_size);
-        const long long ua = std::max(x0 - off - C, 0ll);
-        if (s.L > 0 && ua < pcs.count()) {
-          const Piece pc = get_piece(pcs, (int)ua, d.page_size);
-          const long long e = (long long)ip[lo] + pc.page_idx;
-          if (pc.page_idx < s.npages && e < d.nnz_pages) {
-            const int32_t page = d.host_values[e];
-            if (page >= 0 && page < d.max_pages)
-              hint = (int32_t)(((long long)page * 2) * d.H_kv + hz * zg / p.n_z);
-          }
-        }
-      }
-      p.hp[used + w] = hint;
-    }
-    p.hp_first = (int)used;
-    p.hp_nw = (int)workers;
-  }
   return true;
 }
 
@@ -398,8 +349,6 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   if (d.nnz_pages > 0 && !page_table_values) return fail(PD_ERR_INVALID_ARG, "page_table_values is NULL");
   if (!d.host_indptr != !d.host_length_info)
     return fail(PD_ERR_INVALID_ARG, "host_indptr and host_length_info go together");
-  if (d.host_values && !d.host_indptr)
-    return fail(PD_ERR_INVALID_ARG, "host_values needs host_indptr and host_length_info");
   if (d.host_indptr) {
     if (d.host_indptr[0] < 0 || d.host_indptr[d.B] > d.nnz_pages)
       return fail(PD_ERR_INVALID_ARG, "host_indptr outside [0, nnz_pages]");
@@ -416,7 +365,7 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   const bool use_mma = mma_path(desc, pages);
   if (q_len > 1 && !use_mma)
     return fail(PD_ERR_UNSUPPORTED, "multi-query decode runs on the tensor-core kernel only: "
-                                    "f16/bf16 (D 64 or 128) or E4M3 (D 128) KV, page size a multiple of 16");
+                                    "f16/bf16 (D 64 or 128) or E4M3 (D 128) KV, page size a multiple of 8");
   int ctas = 1;
   const bool k_rotated = rotary_mode != 0 && (d.flags & PD_DECODE_K_ROTATED);
   st = occupancy_for(desc, use_mma, rotary_mode + (k_rotated ? 2 : 0), &ctas, ds, q_len);
@@ -513,8 +462,7 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   p.q_prescale = p.score_scale;
   p.out_scale = d.kv_dtype == kE4M3 ? d.v_scale : 1.f;
   if (rotary_mode) rope_table(rope_scale, rope_theta, d.D, p.rope_F);
-  if (d.host_indptr && d.host_length_info)
-    fill_host_plan(d, p, use_mma ? (long long)grid_blocks * kMmaWarps : 0);
+  if (d.host_indptr && d.host_length_info) fill_host_plan(d, p);
 
   const dim3 grid((unsigned)grid_blocks);
   cudaError_t e;

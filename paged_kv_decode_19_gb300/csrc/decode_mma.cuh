@@ -45,7 +45,8 @@
 // become f16 in registers (exact); k_scale folds into the score scale, v_scale into
 // the output.
 //
-// Limits: head dim 64/128 for 16-bit KV, 128 for FP8; page size a multiple of 16.
+// Limits: head dim 64/128 for 16-bit KV, 128 for FP8; page size a multiple of 8 (a page
+// of 8 rows is a half-filled 16-row tile).
 #pragma once
 
 #include <type_traits>
@@ -370,17 +371,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   __shared__ __align__(16) float2 s_rot8[KROT ? rope_slots(D) : 2];  // e^(i * 8 * omega_f)
   __shared__ WorkerStart s_start[NW];
 
-  // the host plan's first-tile hint: this worker's first K and V blocks start coming into
-  // L2 now, while the set-up below runs
-  if (p.hp_nw && (threadIdx.x & 31) == 0) {
-    const int w = blockIdx.x * NW + (threadIdx.x >> 5);
-    const int blk = w < p.hp_nw ? p.hp[p.hp_first + w] : -1;
-    if (blk >= 0) {
-      const uint8_t* kb = reinterpret_cast<const uint8_t*>(p.pages) + (size_t)blk * p.P * Tr::kRowBytes;
-      prefetch_l2_bulk(kb, (uint32_t)(p.P * Tr::kRowBytes));
-      prefetch_l2_bulk(kb + (size_t)p.H_kv * p.P * Tr::kRowBytes, (uint32_t)(p.P * Tr::kRowBytes));
-    }
-  }
   // Q and the page table are small and needed right after the start-up scan, when the
   // first tiles of every worker flood HBM: each block prefetches its share into L2 now
   if (threadIdx.x == 0) {
@@ -562,12 +552,16 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   };
   uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
   uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
+  // A page whose size is not a multiple of 16 ends in a half tile: its rows past the
+  // page are not loaded (zero), and the softmax and P.V masks drop them.
   auto load_k = [&](const uint8_t* kblk, int t) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const uint8_t* row = kblk + (size_t)(t * 16 + g_id + 8 * rr) * RB;
+      const int row_in_page = t * 16 + g_id + 8 * rr;
+      const uint8_t* row = kblk + (size_t)row_in_page * RB;
 #pragma unroll
-      for (int ch = 0; ch < KCH; ++ch) kr[rr][ch] = ldg_stream(row + (4 * ch + q4) * 16);
+      for (int ch = 0; ch < KCH; ++ch)
+        kr[rr][ch] = row_in_page < P ? ldg_stream(row + (4 * ch + q4) * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
   auto load_v = [&](const uint8_t* kblk, int t) {
@@ -576,7 +570,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
       const int row_in_page = t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
       const uint8_t* row = kblk + v_off + (size_t)row_in_page * RB;
 #pragma unroll
-      for (int j = 0; j < VCH; ++j) vr[i][j] = ldg_stream(row + (g_id + 8 * j) * 16);
+      for (int j = 0; j < VCH; ++j)
+        vr[i][j] = row_in_page < P ? ldg_stream(row + (g_id + 8 * j) * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
 

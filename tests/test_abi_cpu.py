@@ -39,12 +39,11 @@ def test_library_exports_every_declared_symbol(L):
 
 def test_desc_layout_matches_header():
     # int32 x10, int64 x2, int32, float x2, int32, void*, size_t, const float*,
-    # const int32_t* x3
-    assert ctypes.sizeof(_lib.DecodeDesc) == 120
+    # const int32_t* x2
+    assert ctypes.sizeof(_lib.DecodeDesc) == 112
     assert _lib.DecodeDesc.sink.offset == 88
     assert _lib.DecodeDesc.host_indptr.offset == 96
     assert _lib.DecodeDesc.host_length_info.offset == 104
-    assert _lib.DecodeDesc.host_values.offset == 112
     assert _lib.DecodeDesc.max_pages.offset == 40
     assert _lib.DecodeDesc.flags.offset == 68
     assert _lib.DecodeDesc.workspace.offset == 72

@@ -41,9 +41,13 @@ def test_llama3_bf16_rope_mma(seed):
     _check(_wl("llama3_8b_bf16", seed), "mma")
 
 
-def test_llama3_bf16_rope_simt_page8():
-    """Page size 8 is outside the tensor-core variant: the SIMT kernel serves it."""
-    _check(_wl("llama3_8b_bf16", 4, page_size=8, pool=1200), "simt")
+def test_llama3_bf16_rope_page8_and_page4():
+    """Page size 8 runs on the tensor-core kernel as half-filled 16-row tiles; page size 4
+    is outside it and the SIMT kernel serves it."""
+    _check(_wl("llama3_8b_bf16", 4, page_size=8, pool=1200), "mma")
+    _check(_wl("llama3_8b_bf16", 4, page_size=8, pool=1200), "mma", num_splits=5,
+           max_kv_len_hint=700)
+    _check(_wl("llama3_8b_bf16", 5, page_size=4, pool=2400), "simt")
 
 
 @pytest.mark.parametrize("seed", [0, 1])
@@ -163,7 +167,9 @@ def test_fp8_f16_query_and_simt_variant():
     wl = _wl("fp8_kv_highconc", 8, q_dtype="f16", out_dtype="f16")
     _check(wl, "mma")
     wl2 = _wl("fp8_kv_highconc", 9, page_size=8)
-    _check(wl2, "simt")
+    _check(wl2, "mma")
+    wl3 = _wl("fp8_kv_highconc", 9, page_size=4)
+    _check(wl3, "simt")
 
 
 @pytest.mark.parametrize("kv", ["bf16", "f16"])
@@ -276,21 +282,21 @@ def test_edge_rope_short_rows_large_positions(dt):
         assert rms <= 6e-4, rms
 
 
-@pytest.mark.parametrize("P", [1, 3, 32, 48, 64, 128, 256])
+@pytest.mark.parametrize("P", [1, 3, 8, 24, 32, 48, 64, 128, 256])
 @pytest.mark.parametrize("rope", [0, 1])
 def test_page_size_sweep(P, rope):
-    """Page sizes across the accepted range [1, 256]: multiples of 16 run on the
-    tensor-core kernel (several 16-row tiles per page, a partial last tile), the others
-    on the SIMT kernel; lengths of one row, a full page, a page plus one row, several
+    """Page sizes across the accepted range [1, 256]: multiples of 8 run on the
+    tensor-core kernel (several 16-row tiles per page, a partial last tile; 8 and 24 end
+    every page in a half tile), the others on the SIMT kernel; lengths of one row, a full page, a page plus one row, several
     pages, and empty; whole sequences and forced splits."""
     lens = [1, P, P + 1, 2 * P + 3, 5 * P - 1, 0, 7]
     wl = _custom(lens, P=P, rope=rope, seed=P)
-    want = "mma" if P % 16 == 0 else "simt"
+    want = "mma" if P % 8 == 0 else "simt"
     _check(wl, want)
     _check(wl, want, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
 
 
-@pytest.mark.parametrize("P", [48, 256])
+@pytest.mark.parametrize("P", [8, 24, 48, 256])
 def test_page_size_window_sink(P):
     """Sliding window and sink rows on pages of several tiles: the window start falls
     inside a page and inside a tile."""
@@ -408,7 +414,8 @@ def test_rope_interleaved_fp8_and_window():
 def test_rope_interleaved_simt(D):
     wl = W.make("tiny_fp32", seed=92 + D, D=D, rotary_mode=2, rope_theta=1e4).to(DEV)
     _check(wl, "simt")
-    _check(_wl("llama3_8b_bf16", 93, page_size=8, pool=1200, rotary_mode=2), "simt")
+    _check(_wl("llama3_8b_bf16", 93, page_size=4, pool=2400, rotary_mode=2), "simt")
+    _check(_wl("llama3_8b_bf16", 93, page_size=8, pool=1200, rotary_mode=2), "mma")
 
 
 # ----------------------------------------------------------------------------- learned sinks

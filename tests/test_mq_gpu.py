@@ -85,7 +85,7 @@ def test_mq_group_sweep(kv, D, group, q_len):
     _check(wl, Q, num_splits=4, max_kv_len_hint=300)
 
 
-@pytest.mark.parametrize("P,q_len", [(64, 3), (256, 5)])
+@pytest.mark.parametrize("P,q_len", [(8, 3), (24, 2), (64, 3), (256, 5)])
 def test_mq_large_pages(P, q_len):
     """Multi-query decode on pages of several 16-row tiles (the causal limit of the
     new tokens then falls inside a tile of the last page)."""
