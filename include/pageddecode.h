@@ -64,7 +64,7 @@ typedef struct {
   int32_t H_kv;              /* KV heads; Q head h reads KV head h / (H_qo/H_kv) */
   int32_t D;                 /* head dim: 64, 128 or 256 */
   int32_t page_size;         /* rows per page, P: 1 to 256.  The tensor-core kernel runs
-                                P a multiple of 8 with F16/BF16 KV (D 64 or 128) or
+                                P = 8 or a multiple of 16 with F16/BF16 KV (D 64 or 128) or
                                 E4M3 KV (D 128, 16-bit Q); every other accepted shape
                                 runs on the SIMT kernel (pd_last_decode_variant) */
   int32_t q_dtype;           /* pd_dtype of Q: F32, F16 or BF16 */
@@ -246,7 +246,7 @@ pd_status pd_batch_decode_paged_kv_noalloc(const void* Q, const void* pages,
  * The work unit is (sequence, KV head, slice of <= 8 query columns), a column being
  * one (token, head) of the KV head's group, so each KV page is read once for all
  * tokens and heads of a slice.  Runs on the tensor-core kernel only: f16/bf16 KV
- * (D 64 or 128) or E4M3 KV (D 128), page size a multiple of 8; otherwise
+ * (D 64 or 128) or E4M3 KV (D 128), page size a multiple of 16; otherwise
  * PD_ERR_UNSUPPORTED, as is desc->sliding_window != 0.  A caller workspace must hold
  * pd_workspace_size_mq(desc, q_len) bytes.
  */
@@ -381,7 +381,7 @@ pd_status pd_workspace_init(void* workspace, size_t bytes, pd_stream_t stream);
  * slice)), the number of blocks (*grid_blocks) and the workspace bytes (per-segment
  * arrival counters plus two partial (out, lse) slots per worker; 0 when nothing is
  * split).  Workers per block: 4 (warps) when desc selects the tensor-core kernel
- * (16-bit or E4M3 KV, page_size % 8 == 0, D = 64/128, D = 128 for E4M3), else 1.
+ * (16-bit or E4M3 KV, page_size 8 or % 16 == 0, D = 64/128, D = 128 for E4M3), else 1.
  * Used by the library and exposed for tests.
  */
 pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_sm,

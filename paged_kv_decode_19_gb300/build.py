@@ -21,7 +21,8 @@ LIB = os.path.join(BUILD, "libpageddecode.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "decode_simt.cu", "decode_mma_bf16.cu", "decode_mma_f16.cu",
            "decode_mma_fp8.cu", "decode_mma_mq_bf16.cu", "decode_mma_mq_f16.cu",
-           "decode_mma_mq_fp8.cu", "merge_append.cu", "decode_noalloc.cu"]
+           "decode_mma_mq_fp8.cu", "decode_mma_pair_bf16.cu", "decode_mma_pair_f16.cu",
+           "decode_mma_pair_fp8.cu", "merge_append.cu", "decode_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -54,8 +54,9 @@ struct DeviceState {
   std::mutex ws_mu;
   ArenaTable arenas;
   // resident blocks per SM of each kernel variant, queried once:
-  // [mma][q_dtype][kv_dtype][D 64/128/256][kernel RoPE mode 0..4][multi-query]; 0 = not yet known
-  int occupancy[2][4][4][3][5][2] = {};
+  // [mma][q_dtype][kv_dtype][D 64/128/256][kernel RoPE mode 0..4][single / multi-query /
+  // pages of 8 rows]; 0 = not yet known
+  int occupancy[2][4][4][3][5][3] = {};
 };
 constexpr int kMaxDevices = 64;
 static DeviceState g_dev[kMaxDevices];
@@ -176,7 +177,7 @@ static void plan_impl(const pd_decode_desc* d, int num_sms, int ctas_per_sm, int
 // Tensor-core variant eligibility (pages == nullptr: ignore the pointer's alignment).
 static bool mma_path(const pd_decode_desc* d, const void* pages) {
   if ((reinterpret_cast<uintptr_t>(pages) & 15) != 0) return false;
-  if (d->page_size % 8 != 0) return false;
+  if (d->page_size % 16 != 0 && d->page_size != 8) return false;
   if (d->kv_dtype == kBF16 || d->kv_dtype == kF16) return d->D == 64 || d->D == 128;
   if (d->kv_dtype == kE4M3) return d->D == 128 && (d->q_dtype == kBF16 || d->q_dtype == kF16);
   return false;
@@ -188,6 +189,11 @@ static cudaError_t mma_dispatch(const DecodeParams& p, int q_dtype, int kv_dtype
     if (kv_dtype == kBF16) return launch_mma_mq_bf16(p, q_dtype, grid, st, cfg);
     if (kv_dtype == kF16) return launch_mma_mq_f16(p, q_dtype, grid, st, cfg);
     return launch_mma_mq_fp8(p, q_dtype, grid, st, cfg);
+  }
+  if (p.P == 8) {  // pages of 8 rows: two pages per 16-row tile
+    if (kv_dtype == kBF16) return launch_mma_pair_bf16(p, q_dtype, grid, st, cfg);
+    if (kv_dtype == kF16) return launch_mma_pair_f16(p, q_dtype, grid, st, cfg);
+    return launch_mma_pair_fp8(p, q_dtype, grid, st, cfg);
   }
   if (kv_dtype == kBF16) return launch_mma_bf16(p, q_dtype, grid, st, cfg);
   if (kv_dtype == kF16) return launch_mma_f16(p, q_dtype, grid, st, cfg);
@@ -261,7 +267,7 @@ pd_status pd_plan(const pd_decode_desc* desc, int32_t num_sms, int32_t ctas_per_
 static pd_status occupancy_for(const pd_decode_desc* d, bool use_mma, int rm, int* ctas,
                                DeviceState* ds = nullptr, int q_len = 1) {
   const int di = d->D == 64 ? 0 : d->D == 128 ? 1 : 2;
-  const int mq = q_len > 1 ? 1 : 0;
+  const int mq = q_len > 1 ? 1 : (use_mma && d->page_size == 8 ? 2 : 0);
   int* cached = ds ? &ds->occupancy[use_mma ? 1 : 0][d->q_dtype & 3][d->kv_dtype & 3][di][rm][mq]
                    : nullptr;
   if (cached && *cached > 0) {
@@ -363,9 +369,9 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
   st = device_state(&ds);
   if (st != PD_OK) return st;
   const bool use_mma = mma_path(desc, pages);
-  if (q_len > 1 && !use_mma)
+  if (q_len > 1 && (!use_mma || d.page_size % 16 != 0))
     return fail(PD_ERR_UNSUPPORTED, "multi-query decode runs on the tensor-core kernel only: "
-                                    "f16/bf16 (D 64 or 128) or E4M3 (D 128) KV, page size a multiple of 8");
+                                    "f16/bf16 (D 64 or 128) or E4M3 (D 128) KV, page size a multiple of 16");
   int ctas = 1;
   const bool k_rotated = rotary_mode != 0 && (d.flags & PD_DECODE_K_ROTATED);
   st = occupancy_for(desc, use_mma, rotary_mode + (k_rotated ? 2 : 0), &ctas, ds, q_len);

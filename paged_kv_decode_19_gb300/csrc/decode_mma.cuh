@@ -45,8 +45,8 @@
 // become f16 in registers (exact); k_scale folds into the score scale, v_scale into
 // the output.
 //
-// Limits: head dim 64/128 for 16-bit KV, 128 for FP8; page size a multiple of 8 (a page
-// of 8 rows is a half-filled 16-row tile).
+// Limits: head dim 64/128 for 16-bit KV, 128 for FP8; page size a multiple of 16, or 8
+// (PAIR: two pages per 16-row tile).
 #pragma once
 
 #include <type_traits>
@@ -345,7 +345,9 @@ __device__ void warp_merge(const DecodeParams& p, int seg_b, long long seg_off, 
 
 // RM: 0 no RoPE; 1 rotate-half, 2 interleaved pairs (Q and K rotated here); 3, 4 the same
 // layouts with K rotated in the cache already (only Q rotated here).
-template <typename KVT, typename QT, int D, int RM, int NW, bool MQ>
+// PAIR: pages of 8 rows; a 16-row tile takes two consecutive pages (rows 0-7 from the
+// first, rows 8-15 from the second) when their attended rows follow each other, else one.
+template <typename KVT, typename QT, int D, int RM, int NW, bool MQ, bool PAIR = false>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (sizeof(KVT) == 1)>::v)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   constexpr bool ROPE = RM != 0;               // Q is rotated
@@ -482,6 +484,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   struct Tile {
     int piece, t, s_lo, s_hi, r_lo;
     const uint8_t* kblk;  // K block of (page, hk); nullptr = no more tiles
+    // PAIR: the second page's K block (rows 8-15; nullptr: none) and its slot range
+    const uint8_t* kblk2;
+    int s_lo2, s_hi2;
   };
   // This warp's pieces come 32 at a time: lane i holds piece base + i (its physical
   // page or -1, its slot range, its first row), handed out with shuffles, so moving to
@@ -511,8 +516,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   auto first_tile_from = [&](int j) -> Tile {  // first tile of piece j or later
     Tile tl;
     tl.kblk = nullptr;  // no more tiles (the other fields stay defined)
+    tl.kblk2 = nullptr;
     tl.piece = pend;
-    tl.t = tl.s_lo = tl.s_hi = tl.r_lo = 0;
+    tl.t = tl.s_lo = tl.s_hi = tl.r_lo = tl.s_lo2 = tl.s_hi2 = 0;
     for (; j < pend; ++j) {
       if (j >= pb_base + 32) load_batch(j);
       const int src = j - pb_base;
@@ -525,6 +531,21 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
       tl.t = tl.s_lo >> 4;
       tl.r_lo = __shfl_sync(0xffffffffu, pb_row, src);
       tl.kblk = kblock(pg);
+      if constexpr (PAIR) {
+        // the next piece joins as rows 8-15 when it is in this batch, has a valid page
+        // and its attended rows continue this page's (row 8 + s of the tile = its slot s)
+        const int j2 = j + 1, src2 = min(j2 - pb_base, 31);
+        const int pg2 = __shfl_sync(0xffffffffu, pb_page, src2);
+        const int sl2 = __shfl_sync(0xffffffffu, pb_slots, src2);
+        const int rl2 = __shfl_sync(0xffffffffu, pb_row, src2);
+        if (j2 < pend && j2 - pb_base < 32 && pg2 >= 0 &&
+            rl2 - (sl2 & 0xffff) == tl.r_lo - tl.s_lo + 8) {
+          tl.kblk2 = kblock(pg2);
+          tl.s_lo2 = sl2 & 0xffff;
+          tl.s_hi2 = sl2 >> 16;
+          tl.piece = j2;  // the tile ends with piece j2
+        }
+      }
       break;
     }
     return tl;
@@ -533,6 +554,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   // the next piece when it is in the current batch and has a valid page; anything else
   // (a batch reload, a bad page id, the end) takes the slow path.
   auto next_tile = [&](const Tile& c) -> Tile {
+    if constexpr (PAIR) return first_tile_from(c.piece + 1);
     const bool same = (c.t + 1) * 16 < c.s_hi;
     const int j = c.piece + 1;
     const int src = min(max(j - pb_base, 0), 31);
@@ -548,30 +570,36 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
     n.t = same ? c.t + 1 : ((sl & 0xffff) >> 4);
     n.r_lo = same ? c.r_lo : rl;
     n.kblk = same ? c.kblk : kblock(pg);
+    n.kblk2 = nullptr;
+    n.s_lo2 = n.s_hi2 = 0;
     return n;
   };
   uint4 kr[2][KCH];      // K rows t*16 + g_id (+8): chunks 4c + q4
   uint4 vr[4][VCH];      // V rows t*16 + 2q4, +1, +8, +9: chunks g_id + 8j
-  // A page whose size is not a multiple of 16 ends in a half tile: its rows past the
-  // page are not loaded (zero), and the softmax and P.V masks drop them.
-  auto load_k = [&](const uint8_t* kblk, int t) {
+  // PAIR: rows 8-15 come from the tile's second page, at slots 0-7, or are zero (no second
+  // page); the softmax and P.V masks drop them then.
+  auto load_k = [&](const Tile& c) {
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
-      const int row_in_page = t * 16 + g_id + 8 * rr;
-      const uint8_t* row = kblk + (size_t)row_in_page * RB;
+      const int row_in_page = PAIR ? g_id : c.t * 16 + g_id + 8 * rr;
+      const uint8_t* blk = PAIR && rr ? c.kblk2 : c.kblk;
+      const bool ok = !PAIR || rr == 0 || c.kblk2 != nullptr;
+      const uint8_t* row = blk + (size_t)row_in_page * RB;
 #pragma unroll
       for (int ch = 0; ch < KCH; ++ch)
-        kr[rr][ch] = row_in_page < P ? ldg_stream(row + (4 * ch + q4) * 16) : make_uint4(0u, 0u, 0u, 0u);
+        kr[rr][ch] = ok ? ldg_stream(row + (4 * ch + q4) * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
-  auto load_v = [&](const uint8_t* kblk, int t) {
+  auto load_v = [&](const Tile& c) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const int row_in_page = t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
-      const uint8_t* row = kblk + v_off + (size_t)row_in_page * RB;
+      const int row_in_page = PAIR ? 2 * q4 + (i & 1) : c.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
+      const uint8_t* blk = PAIR && (i >> 1) ? c.kblk2 : c.kblk;
+      const bool ok = !PAIR || (i >> 1) == 0 || c.kblk2 != nullptr;
+      const uint8_t* row = blk + v_off + (size_t)row_in_page * RB;
 #pragma unroll
       for (int j = 0; j < VCH; ++j)
-        vr[i][j] = row_in_page < P ? ldg_stream(row + (g_id + 8 * j) * 16) : make_uint4(0u, 0u, 0u, 0u);
+        vr[i][j] = ok ? ldg_stream(row + (g_id + 8 * j) * 16) : make_uint4(0u, 0u, 0u, 0u);
     }
   };
 
@@ -588,8 +616,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
     pdl_release();
   }
   if (cur.kblk) {
-    load_k(cur.kblk, cur.t);
-    load_v(cur.kblk, cur.t);
+    load_k(cur);
+    load_v(cur);
   }
 
   // ---------------------------------------------------------------- Q^T B fragments
@@ -670,7 +698,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
       const Tile nxt = next_tile(cur);
       const int slot0 = cur.t * 16 + g_id, slot1 = slot0 + 8;
       const bool v0 = slot0 >= cur.s_lo && slot0 < cur.s_hi;
-      const bool v1 = slot1 >= cur.s_lo && slot1 < cur.s_hi;
+      const bool v1 = PAIR ? (cur.kblk2 != nullptr && g_id >= cur.s_lo2 && g_id < cur.s_hi2)
+                           : (slot1 >= cur.s_lo && slot1 < cur.s_hi);
       // ------------------------------------------------------------ S^T = K Q^T
       // independent accumulators shorten the dependent MMA chain; summed after
       // spread over kQChains independent accumulators: the products of one tile would
@@ -813,9 +842,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
       }
       // K registers are free: start the next tile's K loads (after the last tile: this
       // tile's block again, never used)
-      const uint8_t* nk = nxt.kblk ? nxt.kblk : cur.kblk;
-      const int nt = nxt.kblk ? nxt.t : cur.t;
-      load_k(nk, nt);
+      const Tile& ntile = nxt.kblk ? nxt : cur;
+      load_k(ntile);
       // ------------------------------------------------------------ online softmax (log2)
       float sc[4];
       sc[0] = v0 ? acc[0] * post_scale : -INFINITY;  // row g_id, heads 2q, 2q+1
@@ -877,7 +905,18 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
       // rows outside the piece may hold anything (even NaN): in a partial tile (the first
       // or last of a piece; warp-uniform test) this thread's V rows 2q, 2q+1, 2q+8, 2q+9
       // that fall outside are zeroed in the registers, so full tiles need no masking
-      if (cur.t * 16 < cur.s_lo || cur.t * 16 + 16 > cur.s_hi) {
+      if constexpr (PAIR) {  // rows 0-7: the first page's slots; rows 8-15: the second's
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 2 * q4 + (i & 1);
+          const bool ok = (i >> 1) ? (cur.kblk2 != nullptr && r >= cur.s_lo2 && r < cur.s_hi2)
+                                   : (r >= cur.s_lo && r < cur.s_hi);
+          if (!ok) {
+#pragma unroll
+            for (int j = 0; j < VCH; ++j) vr[i][j] = make_uint4(0u, 0u, 0u, 0u);
+          }
+        }
+      } else if (cur.t * 16 < cur.s_lo || cur.t * 16 + 16 > cur.s_hi) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = cur.t * 16 + 2 * q4 + (i & 1) + 8 * (i >> 1);
@@ -911,7 +950,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
         }
         Mma<MT>::run(oacc[mt], a, pb0, pb1);
       }
-      load_v(nk, nt);
+      load_v(ntile);
       // The L2 prefetch of the page kPrefetchPieces ahead goes out when a new piece starts,
       // behind the next tile's K and V loads so that it does not delay them
       // (llama3 decode 65.4 -> 63.7 us, window 108.9 -> 106.7 us, alternating replicas).
@@ -922,6 +961,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
         if (pf && pg >= 0 && lane == 0) {
           prefetch_l2_bulk(kblock(pg), (uint32_t)block_bytes);
           prefetch_l2_bulk(kblock(pg) + v_off, (uint32_t)block_bytes);
+        }
+        if constexpr (PAIR) {  // a tile spans two pages: the one after jpf as well
+          const int j2 = jpf + 1;
+          const int pg2 = __shfl_sync(0xffffffffu, pb_page, min(max(j2 - pb_base, 0), 31));
+          if (pf && j2 < pend && j2 < pb_base + 32 && pg2 >= 0 && lane == 0) {
+            prefetch_l2_bulk(kblock(pg2), (uint32_t)block_bytes);
+            prefetch_l2_bulk(kblock(pg2) + v_off, (uint32_t)block_bytes);
+          }
         }
       }
       cur = nxt;
@@ -1030,11 +1077,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<(RM == 1 || RM == 2), (size
   }
 }
 
-template <typename KVT, typename QT, int D, int RM, bool MQ>
+template <typename KVT, typename QT, int D, int RM, bool MQ, bool PAIR = false>
 static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
   constexpr int NW = kMmaWarps;
   constexpr int dyn = 0;
-  auto kern = decode_mma_kernel<KVT, QT, D, RM, NW, MQ>;
+  auto kern = decode_mma_kernel<KVT, QT, D, RM, NW, MQ, PAIR>;
   if (cfg) {
     cfg->threads = NW * 32;
     cfg->smem_bytes = dyn;
@@ -1049,14 +1096,14 @@ static cudaError_t launch_mma_t(const DecodeParams& p, dim3 grid, cudaStream_t s
 
 // MQ: the multi-query form (query columns = tokens x heads, causal among the tokens);
 // a separate instantiation, so the single-token kernel carries none of it.
-template <typename KVT, typename QT, int D, bool MQ>
+template <typename KVT, typename QT, int D, bool MQ, bool PAIR = false>
 static cudaError_t launch_mma_r(const DecodeParams& p, dim3 grid, cudaStream_t st, MmaConfig* cfg) {
   const int rm = p.rotary ? p.rotary + (p.k_rotated ? 2 : 0) : 0;
-  if (rm == 1) return launch_mma_t<KVT, QT, D, 1, MQ>(p, grid, st, cfg);
-  if (rm == 2) return launch_mma_t<KVT, QT, D, 2, MQ>(p, grid, st, cfg);
-  if (rm == 3) return launch_mma_t<KVT, QT, D, 3, MQ>(p, grid, st, cfg);
-  if (rm == 4) return launch_mma_t<KVT, QT, D, 4, MQ>(p, grid, st, cfg);
-  return launch_mma_t<KVT, QT, D, 0, MQ>(p, grid, st, cfg);
+  if (rm == 1) return launch_mma_t<KVT, QT, D, 1, MQ, PAIR>(p, grid, st, cfg);
+  if (rm == 2) return launch_mma_t<KVT, QT, D, 2, MQ, PAIR>(p, grid, st, cfg);
+  if (rm == 3) return launch_mma_t<KVT, QT, D, 3, MQ, PAIR>(p, grid, st, cfg);
+  if (rm == 4) return launch_mma_t<KVT, QT, D, 4, MQ, PAIR>(p, grid, st, cfg);
+  return launch_mma_t<KVT, QT, D, 0, MQ, PAIR>(p, grid, st, cfg);
 }
 
 }  // namespace pd

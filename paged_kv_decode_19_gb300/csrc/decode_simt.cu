@@ -1,7 +1,7 @@
 // SIMT decode kernel: any element type (fp32 / f16 / bf16 / e4m3 KV), head dim
 // 64/128/256, any page size, any GQA group.  Used for fp32 (where the 16-bit tensor
 // path would lose the 1e-5 accuracy the fp32 path keeps) and for shapes the MMA
-// kernel does not take (page size not a multiple of 16, D = 256).
+// kernel does not take (page sizes other than 8 and multiples of 16, D = 256).
 //
 // A block walks its share of (sequence, KV head, slice of <= 8 query heads) segments
 // (see block_range); its warps take tiles of the share's rows in turn (4 KB of K rows
@@ -106,7 +106,7 @@ struct SimtSmem {
 };
 
 template <typename KT, typename QT, int D, int NW>
-__global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_constant__ DecodeParams p) {
   constexpr int NT = NW * 32;
   constexpr int E = D / 32;  // output dims per lane in P.V
   constexpr int G8 = kMaxGroupPerCta;
@@ -128,6 +128,13 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
   __shared__ unsigned long long s_F[D / 2];       // RoPE turns per position, per frequency
   __shared__ float sm_m[NW * G8], sm_d[NW * G8];
 
+  // Q and the page table are needed right after the start-up: each block prefetches its
+  // share into L2 while it waits for the previous kernel (a prefetch reads nothing into
+  // the program, and L2 sees that kernel's writes)
+  if (threadIdx.x == 0) {
+    prefetch_l2_share(p.Q, (size_t)p.B * p.H_qo * D * sizeof(QT), blockIdx.x, gridDim.x);
+    if (p.values) prefetch_l2_share(p.values, (size_t)p.nnz_pages * sizeof(int32_t), blockIdx.x, gridDim.x);
+  }
   pdl_wait();  // nothing of the caller's is read before the previous kernel completes
   pdl_release();
   if (p.rotary)
@@ -385,7 +392,10 @@ __global__ void __launch_bounds__(NW * 32, 2) decode_simt_kernel(const __grid_co
 // Launch, or (ctas != nullptr) report how many blocks of the variant fit on one SM.
 template <typename KT, typename QT, int D>
 static cudaError_t launch_simt_d(const DecodeParams& p, dim3 grid, cudaStream_t st, int* ctas) {
-  constexpr int NW = 4;
+  // 8 warps per block: a sequence's rows spread over twice the warps when each block
+  // serves one (sequence, head slice) whole (no split), and one block of 8 warps holds
+  // an SM like two of 4 would (registers)
+  constexpr int NW = 8;
   using SM = SimtSmem<KT, D, NW>;
   const int smem = p.rotary && !p.k_rotated ? SM::kBytesRope : SM::kBytes;
   auto kern = decode_simt_kernel<KT, QT, D, NW>;

@@ -27,6 +27,13 @@ cudaError_t launch_mma_f16(const DecodeParams& p, int q_dtype, dim3 grid, cudaSt
                            MmaConfig* cfg);
 cudaError_t launch_mma_fp8(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
                            MmaConfig* cfg);
+// The same for pages of 8 rows (single token): two pages per 16-row tile.
+cudaError_t launch_mma_pair_bf16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                                 MmaConfig* cfg);
+cudaError_t launch_mma_pair_f16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                                MmaConfig* cfg);
+cudaError_t launch_mma_pair_fp8(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
+                                MmaConfig* cfg);
 // The same for the multi-query form (p.q_len > 1).
 cudaError_t launch_mma_mq_bf16(const DecodeParams& p, int q_dtype, dim3 grid, cudaStream_t st,
                                MmaConfig* cfg);

@@ -42,8 +42,8 @@ def test_llama3_bf16_rope_mma(seed):
 
 
 def test_llama3_bf16_rope_page8_and_page4():
-    """Page size 8 runs on the tensor-core kernel as half-filled 16-row tiles; page size 4
-    is outside it and the SIMT kernel serves it."""
+    """Page size 8 runs on the tensor-core kernel with two pages per 16-row tile; page
+    size 4 is outside it and the SIMT kernel serves it."""
     _check(_wl("llama3_8b_bf16", 4, page_size=8, pool=1200), "mma")
     _check(_wl("llama3_8b_bf16", 4, page_size=8, pool=1200), "mma", num_splits=5,
            max_kv_len_hint=700)
@@ -285,13 +285,13 @@ def test_edge_rope_short_rows_large_positions(dt):
 @pytest.mark.parametrize("P", [1, 3, 8, 24, 32, 48, 64, 128, 256])
 @pytest.mark.parametrize("rope", [0, 1])
 def test_page_size_sweep(P, rope):
-    """Page sizes across the accepted range [1, 256]: multiples of 8 run on the
-    tensor-core kernel (several 16-row tiles per page, a partial last tile; 8 and 24 end
-    every page in a half tile), the others on the SIMT kernel; lengths of one row, a full page, a page plus one row, several
+    """Page sizes across the accepted range [1, 256]: multiples of 16 run on the
+    tensor-core kernel (several 16-row tiles per page, a partial last tile), and 8 as two
+    pages per tile; the others on the SIMT kernel; lengths of one row, a full page, a page plus one row, several
     pages, and empty; whole sequences and forced splits."""
     lens = [1, P, P + 1, 2 * P + 3, 5 * P - 1, 0, 7]
     wl = _custom(lens, P=P, rope=rope, seed=P)
-    want = "mma" if P % 8 == 0 else "simt"
+    want = "mma" if P % 16 == 0 or P == 8 else "simt"
     _check(wl, want)
     _check(wl, want, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
 
@@ -302,8 +302,9 @@ def test_page_size_window_sink(P):
     inside a page and inside a tile."""
     lens = [3 * P + 5, 2 * P, P + 40]
     wl = _custom(lens, P=P, window=P + 21, sink=4, dt="f16", rope=1, seed=P + 1)
-    _check(wl, "mma")
-    _check(wl, "mma", num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+    want = "mma" if P % 16 == 0 or P == 8 else "simt"
+    _check(wl, want)
+    _check(wl, want, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
 
 
 def test_edge_more_chunks_than_pages():
