@@ -279,6 +279,23 @@ __device__ BlockRange block_range(const DecodeParams& p) {
   const int HZ = p.H_kv * p.n_z;
   const long long G = gridDim.x;
   BlockRange r;
+  if (p.mode != kSchedBalanced) {
+    // per-segment: block c takes segment c = (sequence c / HZ, slice c % HZ) whole, on a
+    // private range; no scan (the barrier publishes what the block wrote before the call)
+    __syncthreads();
+    const long long c = blockIdx.x;
+    r.U = (long long)p.B * HZ;
+    r.x0 = r.x1 = 0;
+    if (c >= r.U) return r;
+    Segment& sg = r.seg;
+    sg.b = (int)(c / HZ);
+    sg.hz = (int)(c - (long long)sg.b * HZ);
+    sg.seq = load_seq(p, sg.b);
+    sg.n = units_of(sg.seq, p.P);
+    sg.off = 0;
+    r.x1 = sg.n;
+    return r;
+  }
   // pass 1: U
   long long total = 0;
   for (int start = 0; start < p.B; start += NT) {

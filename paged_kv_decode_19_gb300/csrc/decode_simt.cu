@@ -64,22 +64,27 @@ __device__ __forceinline__ float exp2_kv(float x) {
   else return fast_exp2(x);
 }
 
-// cp.async: 16 bytes global -> shared, through L2 only (completion: cp_async_wait_all)
+// cp.async: 16 bytes global -> shared, through L2 only.  A thread's copies since its
+// last commit form a group; cp_async_wait<N> returns once all but its N most recent
+// groups have landed.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Tile geometry of the SIMT kernel for rows of RB bytes: TR rows per warp tile (each
-// row's K and V copied into the warp's shared-memory stage), LPR = 32 / TR lanes per row
-// in the K.Q phase; a stage is about 4 KB of K plus 4 KB of V, so that three blocks of
-// four warps fit on an SM with the RoPE tables.
-template <int RB>
+// row's K and V copied into one of the warp's two shared-memory stages), LPR = 32 / TR
+// lanes per row in the K.Q phase; a stage is about 4 KB of K plus 4 KB of V (2 KB each
+// at D = 256, where the per-warp Q rows take the room).
+template <int RB, int D>
 struct SimtTile {
-  static constexpr int TR = RB <= 128 ? 32 : RB == 256 ? 16 : RB == 512 ? 8 : 4;
+  static constexpr int kKBytes = D >= 256 ? 2048 : 4096;
+  static constexpr int TR = RB * 32 <= kKBytes ? 32 : kKBytes / RB;
   static constexpr int LPR = 32 / TR;
   static constexpr int KS = RB + 16;  // K row stride in shared memory (16 bytes apart per row:
                                       // the lanes' 16-byte reads of 8 rows cover all banks)
@@ -89,20 +94,24 @@ struct SimtTile {
 template <typename KT, int D, int NW>
 struct SimtSmem {
   static constexpr int RB = D * ElemBytes<KT>::v;
-  using Tl = SimtTile<RB>;
+  using Tl = SimtTile<RB, D>;
   static constexpr int G8 = kMaxGroupPerCta;
-  // [Q rows G8 x D f32][probabilities NW x 32 x G8 f32][row offsets NW x 32 i64][stages NW]
-  // and, with RoPE on K, [per-warp Q rows NW x G8 x D f32][row rotations TR x D/2 float2]
+  // [Q rows G8 x D f32][probabilities NW x 32 x G8 f32][row offsets 2 x NW x 32 i64]
+  // [stages 2 x NW] and, with RoPE on K, [per-warp Q rows NW x G8 x D f32][row rotations
+  // TR x D/2 float2]; stage b of warp w is at kStage + (b NW + w) Tl::kStage
   static constexpr int kQ = 0;
   static constexpr int kP = kQ + G8 * D * 4;
   static constexpr int kRow = kP + NW * 32 * G8 * 4;
-  static constexpr int kStage = kRow + NW * 32 * 8;
-  static constexpr int kBytes = kStage + NW * Tl::kStage;
+  static constexpr int kStage = kRow + 2 * NW * 32 * 8;
+  static constexpr int kBytes = kStage + 2 * NW * Tl::kStage;
   static constexpr int kQW = kBytes;
   static constexpr int kRT = kQW + NW * G8 * D * 4;
   static constexpr int kBytesRope = kRT + Tl::TR * (D / 2) * 8;
   // the warps' final states [NW][G8][D] f32 reuse the space from the start
   static_assert(NW * G8 * D * 4 <= kBytes, "state overlay");
+  // with the kernel's static shared memory (12 KB, start-up scan and merge scratch), within
+  // the 227 KB a block may hold
+  static_assert(kBytesRope + 16 * 1024 <= 227 * 1024, "shared memory");
 };
 
 template <typename KT, typename QT, int D, int NW>
@@ -118,7 +127,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
   extern __shared__ __align__(16) unsigned char s_dyn[];
   float (*s_q)[D] = reinterpret_cast<float (*)[D]>(s_dyn + SM::kQ);
   float (*s_p)[32][G8] = reinterpret_cast<float (*)[32][G8]>(s_dyn + SM::kP);
-  long long (*s_row)[32] = reinterpret_cast<long long (*)[32]>(s_dyn + SM::kRow);
+  long long (*s_row)[NW][32] = reinterpret_cast<long long (*)[NW][32]>(s_dyn + SM::kRow);
   // RoPE on K: a tile's rows sit at positions base + t (t = 0 .. TR-1); K row t is turned
   // by t positions (s_rt, the same for every tile) and each warp's Q rows by -base
   // (s_qw), since R(qpos) q . R(base + t) k = R(qpos - base) q . R(t) k
@@ -149,9 +158,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
       s_rt[it / (D / 2)][it % (D / 2)] = make_float2(c, sn);
     }
   const int trow = lane / LPR, part = lane % LPR;  // K.Q phase: this lane's row and part
-  unsigned char* stage = s_dyn + SM::kStage + warp * Tl::kStage;
-  unsigned char* st_k = stage;                  // [TR][KS]
-  unsigned char* st_v = stage + TR * KS;        // [TR][RB]
+  // this warp's two stages: K rows [TR][KS], then V rows [TR][RB]
+  auto stage_k = [&](int buf) { return s_dyn + SM::kStage + (buf * NW + warp) * Tl::kStage; };
+  auto stage_v = [&](int buf) { return stage_k(buf) + TR * KS; };
   const bool il = p.rotary == 2;
   const bool krot = p.rotary && !p.k_rotated;
   const unsigned char* pages = reinterpret_cast<const unsigned char*>(p.pages);
@@ -178,25 +187,85 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
   }
   const SeqInfo wseq = sg.seq;
 
+  // A row's page-table entry is loaded first (row_entry) and used later (row_offset), so
+  // that the load is in flight during other work; so < 0: no row.
+  struct RowRef {
+    int page, so;
+  };
+  auto row_entry = [&](int r) -> RowRef {
+    RowRef e{-1, -1};
+    if (r >= r1) return e;
+    e.so = r < wseq.sink ? r : r - wseq.sink + wseq.win_off;
+    const int pidx = e.so / p.P;
+    if (pidx < 0 || pidx >= wseq.npages || (long long)wseq.page_begin + pidx >= p.nnz_pages)
+      set_error(p.err, kErrBadPage);  // page stays -1
+    else
+      e.page = __ldg(p.values + wseq.page_begin + pidx);
+    return e;
+  };
+  // byte offset in the pages of the row's K row (-1: no row / bad page, error recorded)
+  auto row_offset = [&](const RowRef& e) -> long long {
+    if (e.so < 0) return -1;
+    if (e.page < 0 || (long long)e.page >= p.max_pages) {
+      set_error(p.err, kErrBadPage);
+      return -1;
+    }
+    return ((((long long)e.page * 2 * p.H_kv + hk) * p.P) + (e.so % p.P)) * RB;
+  };
+  // a tile's K and V rows -> stage `buf` of this warp (each row by its LPR lanes), as
+  // one cp.async group of this thread
+  auto issue_tile = [&](int buf, long long off) {
+    if (part == 0) s_row[buf][warp][trow] = off;
+    if (off >= 0) {
+#pragma unroll
+      for (int k = 0; k < RB / (16 * LPR); ++k) {
+        const int c = (k * LPR + part) * 16;
+        cp_async16(stage_k(buf) + trow * KS + c, pages + off + c);
+        cp_async16(stage_v(buf) + trow * RB + c, pages + off + kv_stride + c);
+      }
+    }
+    cp_async_commit();
+  };
+
   // Q rows of the slice -> shared memory, rotated at q_rope_position and scaled to log2
-  // units; heads beyond the slice are zero.  Thread t takes (head, RoPE pair) items.
+  // units; heads beyond the slice are zero.  Thread t takes (head, RoPE pair) items.  The
+  // raw Q elements and the page-table entries of this warp's first two tiles are loaded
+  // together; the first tile's gather then streams in while Q is rotated and stored.
+  const int rb_first = r0 + warp * TR;
+  const RowRef e_first = row_entry(rb_first + trow);
+  const RowRef e_second = row_entry(rb_first + NW * TR + trow);
+  long long off_first;
   {
+    constexpr int kQI = (G8 * (D / 2) + NT - 1) / NT;  // items per thread
+    float qx[kQI], qy[kQI];
     const int qpos = p.rotary ? __ldg(p.q_rope_position + sg.b) : 0;
-    for (int it = tid; it < G8 * (D / 2); it += NT) {
+#pragma unroll
+    for (int k = 0; k < kQI; ++k) {
+      const int it = tid + k * NT;
       const int j = it / (D / 2), i = it - j * (D / 2);
       const int dx = il ? 2 * i : i, dy = il ? 2 * i + 1 : i + D / 2;  // the pair of frequency i
-      float x = 0.f, y = 0.f;
-      if (j < hcount) {
+      qx[k] = qy[k] = 0.f;
+      if (it < G8 * (D / 2) && j < hcount) {
         const QT* qrow = reinterpret_cast<const QT*>(p.Q) + ((size_t)sg.b * p.H_qo + hq0 + j) * D;
-        x = to_f32(qrow[dx]);
-        y = to_f32(qrow[dy]);
-        if (p.rotary) {
-          float c, s;
-          rope_cs<KT>(qpos, s_F[i], c, s);
-          const float xr = x * c - y * s, yr = y * c + x * s;
-          x = xr;
-          y = yr;
-        }
+        qx[k] = to_f32(qrow[dx]);
+        qy[k] = to_f32(qrow[dy]);
+      }
+    }
+    off_first = row_offset(e_first);
+    issue_tile(0, off_first);
+#pragma unroll
+    for (int k = 0; k < kQI; ++k) {
+      const int it = tid + k * NT;
+      if (it >= G8 * (D / 2)) break;
+      const int j = it / (D / 2), i = it - j * (D / 2);
+      const int dx = il ? 2 * i : i, dy = il ? 2 * i + 1 : i + D / 2;
+      float x = qx[k], y = qy[k];
+      if (p.rotary && j < hcount) {
+        float c, sn;
+        rope_cs<KT>(qpos, s_F[i], c, sn);
+        const float xr = x * c - y * sn, yr = y * c + x * sn;
+        x = xr;
+        y = yr;
       }
       s_q[j][dx] = x * p.score_scale;
       s_q[j][dy] = y * p.score_scale;
@@ -205,15 +274,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
   __syncthreads();
 
   const int kpos0 = krot ? __ldg(p.k_rope_pos_offset + sg.b) : 0;
-
-  // byte offset in the pages of row r's K row (-1: no row / bad page)
-  auto row_offset = [&](int r) -> long long {
-    if (r >= r1) return -1;
-    const int so = r < wseq.sink ? r : r - wseq.sink + wseq.win_off;
-    const int page = lookup_page(p, wseq, so / p.P);
-    if (page < 0) return -1;
-    return ((((long long)page * 2 * p.H_kv + hk) * p.P) + (so % p.P)) * RB;
-  };
 
   // the tile loop for slices of at most HM heads (4 or 8: the scores' registers)
   auto tiles = [&](auto hm_tag) {
@@ -226,9 +286,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
 #pragma unroll
       for (int e = 0; e < E; ++e) o[j][e] = 0.f;
     }
-    int rb = r0 + warp * TR;
-    long long off = rb < r1 ? row_offset(rb + trow) : -1;  // this lane's row of the tile
-    for (; rb < r1; rb += NW * TR) {
+    // Two stages per warp: tile i computes from stage i & 1 while tile i + 1 streams into
+    // the other, and the page-table entries of tile i + 2 are loaded meanwhile.
+    long long off = off_first;  // this lane's row of the current tile
+    RowRef e_next = e_second;             // ... of the next tile
+    int buf = 0;
+    for (int rb = rb_first; rb < r1; rb += NW * TR, buf ^= 1) {
       if (krot) {  // this tile's Q rows, turned by -(position of its row 0)
         const int base = kpos0 + rb;
         for (int i = lane; i < D / 2; i += 32) {
@@ -243,21 +306,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
           }
         }
       }
-      // ---- the tile's K and V rows -> this warp's stage (each row by its LPR lanes)
-      if (part == 0) s_row[warp][trow] = off;
-      if (off >= 0) {
-#pragma unroll
-        for (int k = 0; k < RB / (16 * LPR); ++k) {
-          const int c = (k * LPR + part) * 16;
-          cp_async16(st_k + trow * KS + c, pages + off + c);
-          cp_async16(st_v + trow * RB + c, pages + off + kv_stride + c);
-        }
-      }
-      // the next tile's page-table entries are read while this one streams in
-      const int rn = rb + NW * TR;
-      const long long off_next = rn < r1 ? row_offset(rn + trow) : -1;
-      cp_async_wait_all();
+      // the next tile's rows -> the other stage (read by the previous tile, whose last
+      // __syncwarp has passed); an empty group past the last tile
+      const long long off_next = row_offset(e_next);
+      issue_tile(buf ^ 1, off_next);
+      e_next = row_entry(rb + 2 * NW * TR + trow);
+      cp_async_wait<1>();  // this tile's rows have landed
       __syncwarp();
+      const unsigned char* st_k = stage_k(buf);
+      const unsigned char* st_v = stage_v(buf);
       // ---- rows on lanes: K . Q over this lane's share of the row, summed over the row's lanes
       float sc[HM];
 #pragma unroll
@@ -345,7 +402,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
       const int nrow = min(TR, r1 - rb);
 #pragma unroll 4
       for (int i = 0; i < nrow; ++i) {
-        if (s_row[warp][i] < 0) continue;  // no row (bad page: error recorded)
+        if (s_row[buf][warp][i] < 0) continue;  // no row (bad page: error recorded)
         float v[E];
         load_smem_f32<KT, E>(reinterpret_cast<const KT*>(st_v + i * RB) + lane * E, v);
         float pj[HM];
@@ -362,7 +419,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_simt_kernel(const __grid_co
 #pragma unroll
           for (int e = 0; e < E; ++e) o[j][e] = fmaf(pj[j], v[e], o[j][e]);
       }
-      __syncwarp();  // the stage, s_p and s_row are rewritten by the next tile
+      __syncwarp();  // s_p is rewritten by the next tile, this stage by the one after
       off = off_next;
     }
     // warp states -> shared memory (unnormalised O, m, d = the lanes' shares summed),
