@@ -13,7 +13,9 @@ that fit in L2: the L2 is flushed before every timed step (a 2x-L2 buffer writte
 then another read, leaving it cold and clean) and each step has its own events.  A
 second pass of the same steps puts events between the kernels, which times each
 kernel alone (decode_us, append_us and the roofline).  The flushed decode time of the
-large workloads is reported as well (decode_us_l2_flushed).  `e2e` re-times the step
+large workloads is reported as well (decode_us_l2_flushed), and so is their decode
+launched K times back to back between one pair of events (decode_us_back_to_back: each
+launch's start-up under the tail of the one before).  `e2e` re-times the step
 through the public API from pinned host buffers (H2D of the step's inputs and D2H of out + lse inside the timed region).
 Before each timed pass a spin kernel keeps the device busy while the host enqueues the
 pass, so device-side times carry no host launch gaps.
@@ -463,6 +465,20 @@ def run_ours(args, ws, rank, local, config=None):
     use_host_plan[0] = False
     _, dec_devplan_ms, _ = timed_steps(args.steps, flush=not alternate, breakdown=True)
     use_host_plan[0] = True
+    # the decode alone, K launches back to back between one event pair (replicas
+    # alternating; only where the inputs exceed L2): each launch's start-up (work split,
+    # page table, Q) runs under the tail of the one before, as between the kernels of a
+    # serving loop.  Reported beside the per-launch time, which stays the roofline's.
+    dec_b2b_ms = None
+    if alternate:
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        prefill(args.steps)
+        a.record(stream)
+        for i in range(args.steps):
+            decode(reps[i % 2])
+        b.record(stream)
+        torch.cuda.synchronize()
+        dec_b2b_ms = a.elapsed_time(b) / args.steps
 
     # the multi-stage form of the same decode (for comparison; not the reported value):
     # page-aligned chunks decoded as pseudo-sequences into fp32 partials, then the
@@ -558,7 +574,7 @@ def run_ours(args, ws, rank, local, config=None):
     res = dict(step=statistics.mean(step_ms), dec=statistics.mean(dec_ms),
                dec_med=statistics.median(dec_ms), app=statistics.mean(app_ms),
                dec_flushed=statistics.mean(dec_flushed_ms),
-               dec_devplan=statistics.mean(dec_devplan_ms),
+               dec_devplan=statistics.mean(dec_devplan_ms), dec_b2b=dec_b2b_ms,
                e2e=statistics.mean(e2e_ms), launches=launches, variant=variant,
                clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h, alternate=alternate, l2=l2,
                ext=ext)
@@ -694,6 +710,7 @@ def main():
         "decode_us": head["decode_us"],
         "decode_us_l2_flushed": head["decode_us_l2_flushed"],
         "decode_us_device_plan": head["decode_us_device_plan"],
+        "decode_us_back_to_back": head["decode_us_back_to_back"],
         "append_us": head["append_us"],
         "kv_read_gbs": head["kv_read_gbs"],
         "decode_variant": head["decode_variant"],
@@ -732,6 +749,8 @@ def _summarise(res, config: str, spec, ws: int) -> dict:
         "decode_us": round(dec_us, 2),
         "decode_us_l2_flushed": round(res["dec_flushed"] * 1e3, 2),
         "decode_us_device_plan": round(_max_over_ranks(res["dec_devplan"] * 1e3, ws), 2),
+        "decode_us_back_to_back": (None if res.get("dec_b2b") is None else
+                                   round(_max_over_ranks(res["dec_b2b"] * 1e3, ws), 2)),
         "append_us": round(res["app"] * 1e3, 2),
         "kv_read_gbs": round(kv_bytes / (dec_us * 1e-6) / 1e9, 1),
         "decode_variant": res["variant"],

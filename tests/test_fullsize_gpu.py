@@ -62,6 +62,13 @@ def test_fullsize_sampled(name):
     compare(kind_of(wl), out, lse, ro, rl, mask=mask)
 
 
+@pytest.mark.parametrize("q_len", [4, 8])
+def test_fullsize_multi_query_grouped_slices(q_len):
+    """Speculative verification at full size with 4 or 8 query tokens (16 or 32 columns of
+    a KV head): grouped slices whose warps share each K tile's rotation."""
+    _fullsize_multi_query(W.make("spec_decode_bf16", seed=SEED, device=DEV, q_len=q_len))
+
+
 def _fullsize_multi_query(wl):
     """Multi-query workload: the same properties, and sampled (sequence, token, head)
     outputs against the oracle's multi-query form."""

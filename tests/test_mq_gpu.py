@@ -85,6 +85,15 @@ def test_mq_group_sweep(kv, D, group, q_len):
     _check(wl, Q, num_splits=4, max_kv_len_hint=300)
 
 
+@pytest.mark.parametrize("q_len", [2, 4])
+def test_mq_fp8_rope_grouped_slices(q_len):
+    """FP8 KV with rotate-half RoPE at group 8: 16 or 32 query columns run as grouped
+    slices whose warps each rotate a share of every K tile and exchange the rest."""
+    wl, Q = _mq("fp8_kv_highconc", 70 + q_len, q_len, rotary_mode=1, rope_theta=1e4)
+    _check(wl, Q)
+    _check(wl, Q, num_splits=3, max_kv_len_hint=int(wl.attended.max()))
+
+
 @pytest.mark.parametrize("P,q_len", [(64, 3), (256, 5)])
 def test_mq_large_pages(P, q_len):
     """Multi-query decode on pages of several 16-row tiles (the causal limit of the
