@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     batch_decode_paged_kv_noalloc,
     batch_decode_paged_kv_mq,
     check_device_errors,
+    host_meta_of,
     last_decode_variant,
     make_desc,
     merge_state_inplace,

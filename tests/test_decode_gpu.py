@@ -163,6 +163,35 @@ def test_early_inputs_decode_starts_under_append(name):
     compare(kind_of(wl), out, lse, ro, rl)
 
 
+@pytest.mark.parametrize("name", ["llama3_8b_bf16", "window_sink_f16", "tiny_fp32"])
+def test_back_to_back_decodes_with_early_inputs(name):
+    # Decodes launched one after another with PD_DECODE_EARLY_INPUTS (as the bench's
+    # back-to-back timing runs them): each one's start-up runs under the previous one's
+    # tail, on the same stream workspace and the same out / lse; every result must stand.
+    wls = [_wl(name, 40 + i) for i in range(3)]
+    s = wls[0].spec
+    host = [pd.host_meta_of(w.indptr, w.length_info) for w in wls]
+    outs = [torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=DEV) for _ in wls]
+    lses = [torch.empty((s.B, s.H_qo), dtype=torch.float32, device=DEV) for _ in wls]
+    shared_out = torch.empty_like(outs[0])
+    shared_lse = torch.empty_like(lses[0])
+    for rep in range(2):
+        for i, w in enumerate(wls):
+            o, l = (outs[i], lses[i]) if rep == 0 else (shared_out, shared_lse)
+            pd.batch_decode_paged_kv(w.Q, w.pages, w.indptr, w.values, w.length_info,
+                                     w.k_rope_pos_offset, w.q_rope_position, o, l,
+                                     s.rotary_mode, s.rope_scale, s.rope_theta, w.sm_scale,
+                                     k_scale=w.k_scale, v_scale=w.v_scale, early_inputs=True,
+                                     host_meta=host[i] if i != 1 else None)
+    torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    for i, w in enumerate(wls):
+        ro, rl, _ = oracle_decode(w)
+        compare(kind_of(w), outs[i], lses[i], ro, rl)
+    ro, rl, _ = oracle_decode(wls[-1])
+    compare(kind_of(wls[-1]), shared_out, shared_lse, ro, rl)
+
+
 def test_fp8_f16_query_and_simt_variant():
     wl = _wl("fp8_kv_highconc", 8, q_dtype="f16", out_dtype="f16")
     _check(wl, "mma")
