@@ -5,16 +5,18 @@
 //
 // A block walks its share of (sequence, KV head, slice of <= 8 query heads) segments
 // (see block_range); its warps take tiles of the share's rows in turn (4 KB of K rows
-// per tile: 32 rows of 128 bytes down to 4 rows of 1 KB).  A tile's K and V rows are gathered through the page table
-// into the warp's shared-memory stage with cp.async (every row of the tile in flight at
-// once; the next tile's page-table entries are read meanwhile).  The lanes then own
-// ROWS (one to eight lanes per row): each reads its share of its K row, rotates it
-// (RoPE) and computes the scores of all the slice's heads with Q read from shared
-// memory (no reduction across the warp per row).  The base-2 online softmax of the
-// TVM `batch_decode_paged_kv` kernel (running max m, sum d, output O) then needs one
-// warp maximum per head per tile; each lane keeps its own rows' share of d.  For P.V
-// the lanes own DIMS: each lane accumulates its D/32 output dims over the tile's rows,
-// with the probabilities and row addresses read back from shared memory as broadcasts.
+// per tile, 2 KB at D = 256: 32 rows of 128 bytes down to 2 rows of 1 KB).  Each warp has
+// two shared-memory stages: while it computes a tile from one, the next tile's K and V
+// rows are gathered through the page table into the other with cp.async (every row of
+// the tile in flight at once), and the page-table entries of the tile after that are
+// loaded.  The lanes then own ROWS (one to sixteen lanes per row): each reads its share
+// of its K row, rotates it (RoPE) and computes the scores of all the slice's heads with
+// Q read from shared memory (no reduction across the warp per row).  The base-2 online
+// softmax of the TVM `batch_decode_paged_kv` kernel (running max m, sum d, output O)
+// then needs one warp maximum per head per tile; each lane keeps its own rows' share of
+// d.  For P.V the lanes own DIMS: each lane accumulates its D/32 output dims over the
+// tile's rows, with the probabilities and row addresses read back from shared memory as
+// broadcasts.
 // The warps' states are merged at the end (same formula as `merge_state_inplace`).
 #include <type_traits>
 
