@@ -571,11 +571,66 @@ def run_ours(args, ws, rank, local, config=None):
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
 
+    # The same step replayed from a CUDA graph, as a serving loop runs it: captured once
+    # per replica (the H2D copy, append, decode and D2H copy), the split planned on the
+    # device so that the graph reads whatever page table the copy brought; each timed step
+    # is one graph launch, the copies still inside the timed region.
+    def e2e_step_body(j):
+        w, di, buf = reps[j][0], dv[j], dev_in[j]
+        buf.copy_(host_in, non_blocking=True)
+        if s.k_rotated:
+            pd.append_paged_kv_rope(w.pages, di["k_new"], di["v_new"], di["slots"], di["kpos"],
+                                    s.rotary_mode, s.rope_scale, s.rope_theta, w.k_scale,
+                                    w.v_scale)
+        else:
+            pd.append_paged_kv(w.pages, di["k_new"], di["v_new"], di["slots"], w.k_scale,
+                               w.v_scale)
+        decode_api(di["Q"], w.pages, di["indptr"], di["values"], di["length_info"],
+                   di["k_rope_pos_offset"], di["q_rope_position"], out_e, lse_e, s.rotary_mode,
+                   s.rope_scale, s.rope_theta, w.sm_scale, k_scale=w.k_scale, v_scale=w.v_scale,
+                   early_inputs=True, k_rotated=s.k_rotated, **split)
+        res_host.copy_(res_dev, non_blocking=True)
+
+    e2e_graph_ms, graph_error = [], None
+    try:
+        cap = torch.cuda.Stream()
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for j in range(2):  # warm-up on the capture stream (its workspace arena)
+                e2e_step_body(j)
+        cap.synchronize()
+        graphs = []
+        for j in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                e2e_step_body(j)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        for i in range(args.warmup + args.steps):
+            if not alternate:
+                flush_l2()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            graphs[i % 2].replay()
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e2e_graph_ms.append(a.elapsed_time(b))
+        del graphs
+    except Exception as ex:  # a capture the runtime refuses: reported in the line (graph_error)
+        graph_error = f"{type(ex).__name__}: {ex}"[:200]
+        e2e_graph_ms = []
+        torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+
     res = dict(step=statistics.mean(step_ms), dec=statistics.mean(dec_ms),
                dec_med=statistics.median(dec_ms), app=statistics.mean(app_ms),
                dec_flushed=statistics.mean(dec_flushed_ms),
                dec_devplan=statistics.mean(dec_devplan_ms), dec_b2b=dec_b2b_ms,
-               e2e=statistics.mean(e2e_ms), launches=launches, variant=variant,
+               e2e=statistics.mean(e2e_ms),
+               e2e_graph=statistics.mean(e2e_graph_ms) if e2e_graph_ms else None,
+               graph_error=graph_error,
+               launches=launches, variant=variant,
                clocks=clk.result, wl=wl, h2d=h2d, d2h=d2h, alternate=alternate, l2=l2,
                ext=ext)
     return res
@@ -760,7 +815,10 @@ def _summarise(res, config: str, spec, ws: int) -> dict:
                      "kernel": f"decode_{res['variant']}_kernel",
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(e2e_us, 2), "unit": UNIT,
-                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"]},
+                "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
+                "graph_replayed": (None if res.get("e2e_graph") is None else
+                                   round(_max_over_ranks(res["e2e_graph"] * 1e3, ws), 2))},
+        **({"graph_error": res["graph_error"]} if res.get("graph_error") else {}),
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
         "l2": (f"inputs larger than L2 ({kv_bytes / 1e6:.0f} MB attended KV vs "

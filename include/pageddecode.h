@@ -181,9 +181,18 @@ typedef struct {
  * (the new buffer is allocated first, the old one released with cudaFreeAsync on the
  * stream, after the work already enqueued there).  So decodes in flight on different
  * streams never share split scratch, and any host threads may call concurrently; a
- * per-device lock is held from the arena's hand-out until the kernel is enqueued.  Do
- * the first call of a given size on a stream outside CUDA-graph capture.  An arena
- * lives until pd_release_stream_workspace(stream) or process exit.
+ * per-device lock is held from the arena's hand-out until the kernel is enqueued.
+ * CUDA-graph capture: while `stream` is being captured the library allocates nothing;
+ * it hands out the arena that the same stream handle last used outside capture, which
+ * must already be large enough (make the same call, or a larger one, on the stream once
+ * before capturing), else the call returns PD_ERR_WORKSPACE without enqueuing anything.
+ * The graph keeps those buffers: replay it only while the stream's arena is neither
+ * released nor grown, and replays must not overlap one another or other split decodes
+ * on that stream's arena.  A caller workspace (desc->workspace) has no such conditions
+ * beyond its own.  The split is planned on the device unless the host copies of the
+ * page table are given, in which case the plan (and the lengths) are fixed in the
+ * captured launch.  An arena lives until pd_release_stream_workspace(stream) or
+ * process exit.
  * Returns PD_OK once the work is enqueued.
  */
 pd_status pd_batch_decode_paged_kv(const void* Q, const void* pages,
@@ -360,7 +369,8 @@ pd_status pd_append_paged_kv_rope(void* pages, const void* k_new, const void* v_
  * (stream-ordered: cudaFreeAsync on `stream`, after the work already enqueued there).
  * A later split decode on the stream allocates a new one.  Call it before destroying a
  * stream that ran split decodes with desc->workspace == NULL, if the process keeps
- * creating streams.  No arena for the stream: PD_OK, nothing is done.
+ * creating streams.  No arena for the stream: PD_OK, nothing is done.  A stream being
+ * captured into a CUDA graph: PD_ERR_INVALID_ARG, nothing is done.
  */
 pd_status pd_release_stream_workspace(pd_stream_t stream);
 

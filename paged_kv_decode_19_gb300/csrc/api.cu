@@ -405,16 +405,31 @@ static pd_status decode_call(const void* Q, const void* pages, const int32_t* pa
     } else {
       // library workspace: the arena of this stream (counters in one buffer, zero
       // between calls; partial results in another), grown stream-ordered; the device's
-      // workspace lock stays held until the kernel is enqueued
+      // workspace lock stays held until the kernel is enqueued.  While the stream is
+      // being captured into a graph its arena must already be large enough (nothing is
+      // allocated behind the graph's back; a capturing stream's id cannot be queried).
+      cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing(s, &cap);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
       unsigned long long sid = 0;
-      cudaError_t e = cudaStreamGetId(s, &sid);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
+      if (cap == cudaStreamCaptureStatusNone) {
+        e = cudaStreamGetId(s, &sid);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
+      }
       ws_lock = std::unique_lock<std::mutex>(ds->ws_mu);
       void* cnt = nullptr;
       void* part = nullptr;
-      const int rc = ds->arenas.acquire(sid, (void*)s, cnt_bytes, ws_need - cnt_bytes, kCudaArenaOps,
-                                        &cnt, &part);
-      if (rc) return cuda_fail((cudaError_t)rc, "library workspace (stream-ordered allocation)");
+      if (cap != cudaStreamCaptureStatusNone) {
+        if (ds->arenas.acquire_captured((void*)s, cnt_bytes, ws_need - cnt_bytes, &cnt, &part))
+          return fail(PD_ERR_WORKSPACE,
+                      "stream capture: the stream's library workspace is missing or too small; "
+                      "make the same call on the stream once before capturing, or pass "
+                      "desc->workspace");
+      } else {
+        const int rc = ds->arenas.acquire(sid, (void*)s, cnt_bytes, ws_need - cnt_bytes,
+                                          kCudaArenaOps, &cnt, &part);
+        if (rc) return cuda_fail((cudaError_t)rc, "library workspace (stream-ordered allocation)");
+      }
       counters = (int*)cnt;
       partials = (char*)part;
     }
@@ -655,8 +670,13 @@ pd_status pd_release_stream_workspace(pd_stream_t stream) {
   DeviceState* ds = nullptr;
   pd_status st = device_state(&ds);
   if (st != PD_OK) return st;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(PD_ERR_INVALID_ARG, "the workspace of a stream is not released while it is being captured");
   unsigned long long sid = 0;
-  cudaError_t e = cudaStreamGetId((cudaStream_t)stream, &sid);
+  e = cudaStreamGetId((cudaStream_t)stream, &sid);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
   std::lock_guard<std::mutex> lk(ds->ws_mu);
   const int rc = ds->arenas.release(sid, (void*)stream, kCudaArenaOps);

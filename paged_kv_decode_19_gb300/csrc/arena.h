@@ -18,6 +18,12 @@
 // The caller serialises acquire/release and the enqueue of the kernel that uses the
 // returned buffers (one mutex per device), so no other host thread can retire a
 // buffer between its hand-out and the launch that uses it.
+//
+// Stream capture (CUDA graphs): a capturing stream's id cannot be queried, and memory
+// must not be allocated or freed behind the graph's back, so acquire_captured finds the
+// arena by the stream handle that last used it outside capture and hands out its
+// buffers as they are; it never allocates.  The graph then owns references to those
+// buffers: they stay valid until the stream's arena is released or grows.
 #pragma once
 
 #include <stddef.h>
@@ -37,6 +43,7 @@ struct ArenaOps {
 
 struct Arena {
   unsigned long long key;  // stream id
+  void* handle = nullptr;  // the stream handle of its last acquire (null: superseded)
   void* cnt = nullptr;     // arrival counters (zero between calls)
   size_t cnt_bytes = 0;
   void* part = nullptr;    // partial (lse, out) slots
@@ -60,6 +67,11 @@ class ArenaTable {
       a = &arenas_.back();
       a->key = key;
     }
+    // a handle names one live stream at a time: an older arena that saw it (a destroyed
+    // stream whose handle came back) is no longer found by it
+    for (Arena& o : arenas_)
+      if (&o != a && o.handle == stream) o.handle = nullptr;
+    a->handle = stream;
     if (a->cnt_bytes < cnt_need) {
       const size_t bytes = round_up(cnt_need * 2, kCntGrain);
       void* p = nullptr;
@@ -100,6 +112,20 @@ class ArenaTable {
     return 0;
   }
 
+  // During stream capture: the buffers of the arena last acquired with `stream`, if it
+  // holds cnt_need / part_need bytes; else kNoRoom (nothing is allocated).
+  static constexpr int kNoRoom = -1;
+  int acquire_captured(void* stream, size_t cnt_need, size_t part_need, void** cnt,
+                       void** part) const {
+    for (const Arena& a : arenas_) {
+      if (a.handle != stream || !stream) continue;
+      if (a.cnt_bytes < cnt_need || a.part_bytes < part_need) return kNoRoom;
+      *cnt = a.cnt;
+      *part = a.part;
+      return 0;
+    }
+    return kNoRoom;
+  }
   // Releases the arena of stream `key` (stream-ordered) and forgets it; no arena: 0.
   int release(unsigned long long key, void* stream, const ArenaOps& ops) {
     for (size_t i = 0; i < arenas_.size(); ++i) {

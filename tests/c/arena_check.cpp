@@ -2,7 +2,9 @@
 // with fake stream-ordered operations that log every call: streams get separate
 // buffers; growth allocates the new buffer before it releases the old one, releases it
 // on the same stream, and zero-fills new counters; a failed allocation leaves the arena
-// as it was; release frees both buffers once.
+// as it was; release frees both buffers once; during stream capture the arena is found
+// by the stream handle that last used it, handed out without any call, and a handle that
+// came back with a new stream finds the new stream's arena.
 #include <stdio.h>
 #include <stdlib.h>
 
@@ -101,6 +103,23 @@ int main() {
   CHECK(f.log.size() == n1 + 3 && f.log[n1].op == "alloc" && f.log[n1 + 1].op == "zero" &&
         f.log[n1 + 1].id == f.log[n1].id && f.log[n1 + 2].op == "release" &&
         f.log[n1 + 2].id == id_of(&f, cA));
+  // stream capture: the arena last used by the handle, handed out as it is (no calls);
+  // a need beyond its size, or a handle never seen, gives kNoRoom
+  {
+    const size_t nc = f.log.size();
+    void *cc = nullptr, *pc = nullptr;
+    CHECK(t.acquire_captured(sA, 1 << 16, 1 << 22, &cc, &pc) == 0 && cc == c4 && pc == p3);
+    CHECK(t.acquire_captured(sA, 1 << 16, 1 << 27, &cc, &pc) == pd::ArenaTable::kNoRoom);
+    CHECK(t.acquire_captured((void*)0x99, 16, 16, &cc, &pc) == pd::ArenaTable::kNoRoom);
+    CHECK(t.acquire_captured(nullptr, 16, 16, &cc, &pc) == pd::ArenaTable::kNoRoom);
+    CHECK(f.log.size() == nc);
+    // a new stream (id 11) that got stream B's handle back: the handle now finds its arena
+    void *c11, *p11;
+    CHECK(t.acquire(11, sB, 1000, 5000, ops, &c11, &p11) == 0 && c11 != cB);
+    CHECK(t.acquire_captured(sB, 16, 16, &cc, &pc) == 0 && cc == c11 && pc == p11);
+    CHECK(t.release(11, sB, ops) == 0);
+    CHECK(t.acquire_captured(sB, 16, 16, &cc, &pc) == pd::ArenaTable::kNoRoom);
+  }
   // a failed allocation while growing: error returned, the arena keeps its buffers
   f.fail_next_alloc = 1;
   void *c5 = nullptr, *p5 = nullptr;
