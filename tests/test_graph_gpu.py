@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from paged_kv_decode_19_gb300 import workloads as W
 from tests._util import compare, kind_of, oracle_decode
 
@@ -38,7 +39,20 @@ def _variant(wl, seed):
                                length_info=torch.from_numpy(li).to(DEV))
 
 
-@pytest.mark.parametrize("name", ["llama3_8b_bf16", "fp8_kv_highconc", "tiny_fp32"])
+def _oracle_of(v):
+    s = v.spec
+    if s.q_len == 1:
+        return oracle_decode(v)
+    return oracle.batch_decode_paged_kv_mq(
+        W.bits(v.Q), W.bits(v.pages), v.indptr.cpu().numpy(), v.values.cpu().numpy(),
+        v.length_info.cpu().numpy(), v.k_rope_pos_offset.cpu().numpy(),
+        v.q_rope_position.cpu().numpy(), q_len=s.q_len, q_dtype=s.q_dtype, kv_dtype=s.kv_dtype,
+        H_kv=s.H_kv, page_size=s.page_size, rotary_mode=s.rotary_mode, rope_scale=s.rope_scale,
+        rope_theta=s.rope_theta, sm_scale=v.sm_scale)
+
+
+@pytest.mark.parametrize("name", ["llama3_8b_bf16", "fp8_kv_highconc", "tiny_fp32",
+                                  "spec_decode_bf16"])
 def test_decode_replayed_from_cuda_graph(name):
     wl = W.make(name, seed=90, reduced=True).to(DEV)
     s = wl.spec
@@ -46,16 +60,17 @@ def test_decode_replayed_from_cuda_graph(name):
     # the step's device buffers, refilled before each replay
     buf = {k: getattr(wl, k).clone() for k in ("Q", "pages", "indptr", "values", "length_info",
                                                "k_rope_pos_offset", "q_rope_position")}
-    out = torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=DEV)
-    lse = torch.empty((s.B, s.H_qo), dtype=torch.float32, device=DEV)
+    qd = (s.B,) if s.q_len == 1 else (s.B, s.q_len)
+    out = torch.empty(qd + (s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=DEV)
+    lse = torch.empty(qd + (s.H_qo,), dtype=torch.float32, device=DEV)
     kw = dict(num_splits=1) if name == "tiny_fp32" else {}
+    api = pd.batch_decode_paged_kv if s.q_len == 1 else pd.batch_decode_paged_kv_mq
 
     def step():
-        pd.batch_decode_paged_kv(buf["Q"], buf["pages"], buf["indptr"], buf["values"],
-                                 buf["length_info"], buf["k_rope_pos_offset"],
-                                 buf["q_rope_position"], out, lse, s.rotary_mode, s.rope_scale,
-                                 s.rope_theta, wl.sm_scale, k_scale=wl.k_scale,
-                                 v_scale=wl.v_scale, **kw)
+        api(buf["Q"], buf["pages"], buf["indptr"], buf["values"], buf["length_info"],
+            buf["k_rope_pos_offset"], buf["q_rope_position"], out, lse, s.rotary_mode,
+            s.rope_scale, s.rope_theta, wl.sm_scale, k_scale=wl.k_scale, v_scale=wl.v_scale,
+            **kw)
 
     cap = torch.cuda.Stream()
     cap.wait_stream(torch.cuda.current_stream())
@@ -74,7 +89,7 @@ def test_decode_replayed_from_cuda_graph(name):
         graph.replay()
         torch.cuda.synchronize()
         assert pd.check_device_errors() == "PD_OK"
-        ro, rl, st = oracle_decode(v)
+        ro, rl, st = _oracle_of(v)
         assert st == 0
         compare(kind_of(v), out, lse, ro, rl)
 
