@@ -151,17 +151,19 @@ def _check(status: int):
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    """Device address of a contiguous tensor (the C functions take it as void*)."""
     if t is None:
         return None
     if not t.is_contiguous():
         raise ValueError("tensors must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream) -> int:
+    """cudaStream_t of `stream` (a torch stream or a raw handle); None: the current stream."""
     if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
 
 
 DECODE_EARLY_INPUTS = 1
@@ -195,7 +197,7 @@ def _host_i32(a, n):
     import numpy as np
     if not isinstance(a, np.ndarray) or a.dtype != np.int32 or not a.flags.c_contiguous or a.size != n:
         raise ValueError(f"host copies must be contiguous numpy int32 arrays of {n} entries")
-    return a.ctypes.data
+    return a.__array_interface__["data"][0]
 
 
 def host_meta_of(indptr, length_info):
