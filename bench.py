@@ -636,6 +636,66 @@ def run_ours(args, ws, rank, local, config=None):
     return res
 
 
+def run_cp(args, local, world: int) -> dict:
+    """The context-parallel step of the headline load on this GPU, rank by rank: each of
+    the `world` ranks' page-aligned slices (pd_cp_shard_plan) decoded into its row of the
+    buffer an all-gather would fill (each decode bracketed by its own events), then the
+    R-way merge of the gathered partials (pd_merge_states).  Two replicas alternate as in
+    the main pass.  The all-gather itself needs `world` GPUs and is not timed."""
+    import paged_kv_decode_19_gb300 as pd
+    from paged_kv_decode_19_gb300 import cp
+
+    dev = torch.device("cuda", local)
+    reps = [W.make(args.config, seed=1000, device=dev, **args.over) for _ in range(2)]
+    s = reps[0].spec
+    if s.q_len != 1:
+        raise ValueError("--cp-ranks: single-token loads only")
+    shards = [[cp.shard(w.indptr, w.values, w.length_info, w.k_rope_pos_offset, s.page_size,
+                        world, r, dev) for r in range(world)] for w in reps]
+    gathered = [torch.empty((world, cp.packed_width(s.B, s.H_qo, s.D)), dtype=torch.float32,
+                            device=dev) for _ in reps]
+    out = torch.empty((s.B, s.H_qo, s.D), dtype=W.TORCH_DTYPES[s.out_dtype], device=dev)
+    lse = torch.empty((s.B, s.H_qo), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step(i, ev=None):
+        w, sh, g = reps[i % 2], shards[i % 2], gathered[i % 2]
+        for r in range(world):
+            if ev is not None:
+                ev[r][0].record(stream)
+            cp.decode_partial(w.Q, w.pages, sh[r], w.q_rope_position, g[r], s.rotary_mode,
+                              s.rope_scale, s.rope_theta, w.sm_scale, k_scale=w.k_scale,
+                              v_scale=w.v_scale)
+            if ev is not None:
+                ev[r][1].record(stream)
+        if ev is not None:
+            ev[world][0].record(stream)
+        cp.combine(g, out, lse)
+        if ev is not None:
+            ev[world][1].record(stream)
+
+    for i in range(args.warmup):
+        one_step(i)
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(world + 1)]
+           for _ in range(args.steps)]
+    if hasattr(torch.cuda, "_sleep"):
+        torch.cuda._sleep(int(args.steps * world * 100e-6 * 2.0e9))
+    for i in range(args.steps):
+        one_step(i, evs[i])
+    torch.cuda.synchronize()
+    assert pd.check_device_errors() == "PD_OK"
+    rank_us = [statistics.mean(e[r][0].elapsed_time(e[r][1]) for e in evs) * 1e3
+               for r in range(world)]
+    merge_us = statistics.mean(e[world][0].elapsed_time(e[world][1]) for e in evs) * 1e3
+    return {"world": world, "rank_decode_us": [round(x, 2) for x in rank_us],
+            "slowest_rank_decode_us": round(max(rank_us), 2), "merge_us": round(merge_us, 2),
+            "exchange_bytes_per_rank": cp.packed_width(s.B, s.H_qo, s.D) * 4,
+            "what": ("each rank's slice decoded on this GPU in turn (one launch each, events "
+                     "around it), then pd_merge_states over the gathered partials; the "
+                     "all-gather between GPUs is not timed")}
+
+
 def _max_over_ranks(x: float, ws: int) -> float:
     """Max of x over the ranks of the default process group (the replicas' times)."""
     if ws == 1:
@@ -664,6 +724,9 @@ def main():
                     help="override the page size (the pool keeps its row count)")
     ap.add_argument("--q-len", type=int, default=None,
                     help="override the query tokens per sequence (multi-query decode)")
+    ap.add_argument("--cp-ranks", type=int, default=0,
+                    help="also time the context-parallel step of the headline load for this "
+                         "many ranks, rank by rank on this GPU (field context_parallel)")
     args = ap.parse_args()
     args.over = {} if args.B is None else {"B": args.B}
     if args.q_len is not None:
@@ -780,6 +843,8 @@ def main():
         line["multi_stage"] = head["multi_stage"]
     if per:
         line["per_config"] = per
+    if args.cp_ranks > 1 and ws == 1:
+        line["context_parallel"] = run_cp(args, local, args.cp_ranks)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = _cpu_baseline(wl, args.cpu_budget)
     print(json.dumps(line))

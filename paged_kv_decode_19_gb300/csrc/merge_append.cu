@@ -59,7 +59,7 @@ cudaError_t launch_merge_state(void* V, float* S, const void* V_other, const flo
 // R log-sum-exps are read by the lanes (r = lane, lane + 32, ...), M and the weight sum
 // come from warp reductions, then each lane accumulates its dims over the R fp32
 // partial rows and writes the output type.  All partners empty: out 0, lse -5e4.
-template <typename OT>
+template <typename OT, int DPL>
 __global__ void merge_states_kernel(OT* __restrict__ out, float* __restrict__ S_out,
                                     const float* __restrict__ Vp, const float* __restrict__ Sp,
                                     int R, int rows, int D, long long rstride) {
@@ -69,11 +69,13 @@ __global__ void merge_states_kernel(OT* __restrict__ out, float* __restrict__ S_
   const int row = blockIdx.x * warps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
-  float M = kEmptyM;
   // partner r: S at Sp + r * sstride, V rows at Vp + r * rstride (rstride = rows * D, or
   // one packed [out | lse] block per partner: rstride = sstride = rows * (D + 1))
   const long long sstride = rstride == (long long)rows * D ? rows : rstride;
-  for (int r = lane; r < R; r += 32) M = fmaxf(M, Sp[r * sstride + row]);
+  // lane r holds S_r of the first 32 partners (the common case: one load per lane)
+  const float s_lane = lane < R ? Sp[lane * sstride + row] : kEmptyM;
+  float M = s_lane;
+  for (int r = lane + 32; r < R; r += 32) M = fmaxf(M, Sp[r * sstride + row]);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   OT* o = out + (size_t)row * D;
@@ -82,17 +84,58 @@ __global__ void merge_states_kernel(OT* __restrict__ out, float* __restrict__ S_
     if (lane == 0) S_out[row] = kEmptyM;
     return;
   }
-  float den = 0.f;
-  for (int r = lane; r < R; r += 32) den += exp2f(Sp[r * sstride + row] - M);
+  // the partners' weights 2^(S_r - M), each computed once: lane r's for r < 32
+  const float w_lane = lane < R ? exp2f(s_lane - M) : 0.f;
+  float den = w_lane;
+  for (int r = lane + 32; r < R; r += 32) den += exp2f(Sp[r * sstride + row] - M);
   den = warp_sum(den);
   const float inv = 1.f / den;
-  for (int d = lane; d < D; d += 32) {
-    float acc = 0.f;
-    for (int r = 0; r < R; ++r)
-      acc = fmaf(exp2f(Sp[r * sstride + row] - M), Vp[r * rstride + (long long)row * D + d], acc);
-    o[d] = from_f32<OT>(acc * inv);
+  // each lane owns DPL dims of a chunk of 32 DPL (d = d0 + lane + 32 e); the rows of four
+  // partners are requested before any is accumulated, so the loads overlap instead of
+  // queueing one L2 round trip behind another
+  for (int d0 = 0; d0 < D; d0 += 32 * DPL) {
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+    const float* vrow = Vp + (long long)row * D + d0 + lane;
+    for (int r0 = 0; r0 < R; r0 += 4) {
+      float v[4][DPL];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < DPL; ++e)
+          v[u][e] = r0 + u < R && d0 + lane + 32 * e < D ? vrow[(r0 + u) * rstride + 32 * e] : 0.f;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int r = r0 + u;
+        float w = __shfl_sync(0xffffffffu, w_lane, r & 31);
+        if (r >= 32) w = r < R ? exp2f(Sp[r * sstride + row] - M) : 0.f;
+        if (r >= R) w = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] = fmaf(w, v[u][e], acc[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < DPL; ++e)
+      if (d0 + lane + 32 * e < D) o[d0 + lane + 32 * e] = from_f32<OT>(acc[e] * inv);
   }
   if (lane == 0) S_out[row] = M + log2f(den);
+}
+
+template <typename OT>
+static cudaError_t launch_merge_states_t(dim3 grid, dim3 block, cudaStream_t st, OT* out,
+                                         float* S_out, const float* V_parts,
+                                         const float* S_parts, int R, int rows, int D,
+                                         long long rstride) {
+  // dims per lane and chunk: D = 64 and 128 in one chunk, anything larger in chunks of 256
+  if (D <= 64)
+    return launch_pdl(merge_states_kernel<OT, 2>, grid, block, 0, st, out, S_out, V_parts,
+                      S_parts, R, rows, D, rstride);
+  if (D <= 128)
+    return launch_pdl(merge_states_kernel<OT, 4>, grid, block, 0, st, out, S_out, V_parts,
+                      S_parts, R, rows, D, rstride);
+  return launch_pdl(merge_states_kernel<OT, 8>, grid, block, 0, st, out, S_out, V_parts,
+                    S_parts, R, rows, D, rstride);
 }
 
 cudaError_t launch_merge_states(void* out, float* S_out, const float* V_parts, const float* S_parts,
@@ -103,14 +146,14 @@ cudaError_t launch_merge_states(void* out, float* S_out, const float* V_parts, c
   const int threads = 256, per = threads / 32;
   const dim3 grid((rows + per - 1) / per);
   if (out_dtype == kF32)
-    return launch_pdl(merge_states_kernel<float>, grid, dim3(threads), 0, st, (float*)out, S_out,
-                      V_parts, S_parts, R, rows, D, rstride);
+    return launch_merge_states_t(grid, dim3(threads), st, (float*)out, S_out, V_parts, S_parts,
+                                 R, rows, D, rstride);
   if (out_dtype == kBF16)
-    return launch_pdl(merge_states_kernel<__nv_bfloat16>, grid, dim3(threads), 0, st,
-                      (__nv_bfloat16*)out, S_out, V_parts, S_parts, R, rows, D, rstride);
+    return launch_merge_states_t(grid, dim3(threads), st, (__nv_bfloat16*)out, S_out, V_parts,
+                                 S_parts, R, rows, D, rstride);
   if (out_dtype == kF16)
-    return launch_pdl(merge_states_kernel<__half>, grid, dim3(threads), 0, st, (__half*)out, S_out,
-                      V_parts, S_parts, R, rows, D, rstride);
+    return launch_merge_states_t(grid, dim3(threads), st, (__half*)out, S_out, V_parts, S_parts,
+                                 R, rows, D, rstride);
   return cudaErrorInvalidValue;
 }
 

@@ -61,12 +61,15 @@ def test_context_parallel_short_and_empty_sequences():
         assert torch.all(lse[torch.from_numpy(empty).to(DEV)] == -5e4)
 
 
-@pytest.mark.parametrize("R", [1, 2, 5, 33, 70])
+@pytest.mark.parametrize("R,D", [(1, 128), (2, 128), (5, 128), (33, 128), (70, 128), (3, 64),
+                                 (6, 256), (4, 96), (7, 320), (35, 40)])
 @pytest.mark.parametrize("odt", ["f32", "bf16", "f16"])
-def test_merge_states_matches_oracle(R, odt):
+def test_merge_states_matches_oracle(R, D, odt):
+    # partner counts below, at and above a warp (the lanes hold the first 32 weights), and
+    # head dims of one chunk per lane, ragged ones and more than 256 (several chunks)
     g = torch.Generator(device=DEV)
-    g.manual_seed(R)
-    N, H, D = 5, 6, 128
+    g.manual_seed(R * 1000 + D)
+    N, H = 5, 6
     Vp = torch.randn((R, N, H, D), generator=g, device=DEV)
     Sp = torch.rand((R, N, H), generator=g, device=DEV) * 20 - 10
     Sp[0, 1] = -5e4                     # an empty partner
