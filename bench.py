@@ -696,6 +696,14 @@ def run_cp(args, local, world: int) -> dict:
                      "all-gather between GPUs is not timed")}
 
 
+def _max_or_none(ms, ws: int):
+    """Max over ranks of a time in ms (as µs), None where no rank has one.  Every rank
+    takes part in the reduction whether or not it has a value, so that a rank without
+    one (a graph capture its runtime refused) cannot leave the others waiting."""
+    v = _max_over_ranks(ms * 1e3 if ms is not None else -1.0, ws)
+    return None if v < 0 else round(v, 2)
+
+
 def _max_over_ranks(x: float, ws: int) -> float:
     """Max of x over the ranks of the default process group (the replicas' times)."""
     if ws == 1:
@@ -881,8 +889,7 @@ def _summarise(res, config: str, spec, ws: int) -> dict:
                      "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"},
         "e2e": {"value": round(e2e_us, 2), "unit": UNIT,
                 "h2d_bytes_per_step": res["h2d"], "d2h_bytes_per_step": res["d2h"],
-                "graph_replayed": (None if res.get("e2e_graph") is None else
-                                   round(_max_over_ranks(res["e2e_graph"] * 1e3, ws), 2))},
+                "graph_replayed": _max_or_none(res.get("e2e_graph"), ws)},
         **({"graph_error": res["graph_error"]} if res.get("graph_error") else {}),
         "gpu_launches": res["launches"],
         "clocks": res["clocks"],
