@@ -38,8 +38,12 @@ def _rank_main(rank, ws, port, q):
         mx = bench._max_over_ranks(10.0 + 5.0 * rank, ws)
         # replicas: the per-call times are the slowest rank's, not divided by the ranks
         res = _fake_res(0.060 + 0.004 * rank, 0.050 + 0.004 * rank)
+        # rank 1 has no graph-replayed time (its capture refused): no rank may hang on it
+        res["e2e_graph"] = 0.070 if rank == 0 else None
+        res["dec_b2b"] = 0.045 + 0.002 * rank
         summ = bench._summarise(res, "llama3_8b_bf16", res["wl"].spec, ws)
-        q.put((rank, mx, bench._dist(), summ["step_us"], summ["decode_us"], summ["e2e"]["value"]))
+        q.put((rank, mx, bench._dist(), summ["step_us"], summ["decode_us"], summ["e2e"]["value"],
+               summ["e2e"]["graph_replayed"], summ["decode_us_back_to_back"]))
     finally:
         dist.destroy_process_group()
 
@@ -59,6 +63,7 @@ def test_max_over_ranks_two_gloo_ranks():
     assert [g[2][:2] for g in got] == [(2, 0), (2, 1)]  # (world size, rank) from the env
     for g in got:
         assert g[3] == 64.0 and g[4] == 54.0 and g[5] == 128.0
+        assert g[6] == 70.0 and g[7] == 47.0
 
 
 def test_single_rank_is_identity():
